@@ -1,0 +1,269 @@
+/*
+ * qg_oracle.c -- plain fp64 CPU oracle for the int4 affine dequant-GEMV decode path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker the CUDA library is compared with.
+ * Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg may load it.  It shares
+ * no code, header, table or constant with the CUDA library (moe_int4_affine_gb300/csrc), and
+ * neither side includes or links the other.
+ *
+ * Everything here is the plain definition, written out: decode the stored values exactly into
+ * double, unpack each nibble, dequantise each weight on its own, multiply, and sum in index
+ * order.  No blocking, no factoring of the group sum, no fusion.
+ *
+ * Sources (web pages; they carry no section numbers, so each citation names the page and the
+ * commit or paragraph that states the fact):
+ *   [FFAI#14]  thewafflehaus/FFAI pull request #14, "feat(everything-bagel): clean migration
+ *              of PR #9 + #10 onto updated dev"
+ *   [FFAI#9]   thewafflehaus/FFAI pull request #9, "Everything Bagel"
+ *   [ds4#844]  antirez/ds4 pull request #844, "Ornith 1.5 + Qwen 3.8 27B hybrid runtime +
+ *              DFlash speculative decoding on Metal"
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_EINVAL (-1)
+
+/* x / activation element types accepted by the oracle */
+#define ORC_X_BF16 0
+#define ORC_X_F32 1
+
+/* ---------------------------------------------------------------------------------------
+ * Stored-value decode.
+ * bf16 is the upper 16 bits of an IEEE-754 binary32; widening to binary32 is exact, and
+ * binary32 -> binary64 is exact.  Scales and biases are bf16 ([FFAI#9] "affine-quant ...
+ * u32-packed ... the dtype must be derived from the scales tensor"; [ds4#844] Q4_64A commit:
+ * "BF16 scale/bias").
+ * ------------------------------------------------------------------------------------- */
+double orc_bf16_to_f64(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static double load_x(const void *x, int xtype, int64_t j) {
+  if (xtype == ORC_X_BF16) return orc_bf16_to_f64(((const uint16_t *)x)[j]);
+  return (double)((const float *)x)[j];
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Nibble unpack.
+ * Weight tensor is u32 words, [out][in/8] ([FFAI#14] commit "moeRouterTopK /
+ * dequantGemvInt4ExpertIndexed": stacked "[nExperts, outDim, inDim/8] u32"; [FFAI#14]
+ * "batchedQkvQ*Fast ... derive in_dim from wQ.shape[1] * 8").  Within a word, element
+ * 8*w + i sits in bits 4i..4i+3 (low nibble first).
+ * ------------------------------------------------------------------------------------- */
+unsigned orc_nibble(const uint32_t *packed, int64_t in, int64_t row, int64_t j) {
+  uint32_t word = packed[row * (in / 8) + j / 8];
+  return (unsigned)((word >> (4 * (j % 8))) & 0xFu);
+}
+
+void orc_unpack_rows(const uint32_t *packed, int64_t in, int64_t r0, int64_t r1, uint8_t *q) {
+  for (int64_t r = r0; r < r1; ++r)
+    for (int64_t j = 0; j < in; ++j) q[(r - r0) * in + j] = (uint8_t)orc_nibble(packed, in, r, j);
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Affine group dequantisation: w[r][j] = scale[r][j/gs] * q[r][j] + bias[r][j/gs].
+ * Scales and biases are [out][in/gs] ([FFAI#14] "(weight, scales, biases, input, output)";
+ * group_size = 64 in every fast-path precondition of [FFAI#14]).  No zero-point is
+ * subtracted: the bias carries the offset ([ds4#844] Q4_64A "scale/bias").
+ * ------------------------------------------------------------------------------------- */
+double orc_dequant(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases, int64_t in,
+                   int64_t gs, int64_t row, int64_t j) {
+  int64_t g = j / gs, ng = in / gs;
+  double s = orc_bf16_to_f64(scales[row * ng + g]);
+  double b = orc_bf16_to_f64(biases[row * ng + g]);
+  return s * (double)orc_nibble(packed, in, row, j) + b;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Dequant-GEMV, M = 1:  y[r] = sum_j w[r][j] * x[j]  for rows r0 <= r < r1, summed in j
+ * order in double ([FFAI#14] "dequant_gemv_int4_*", CPU-truth "build packed weights +
+ * scales + biases + expected GEMV output").
+ * absref[r] = sum_j |w[r][j] * x[j]| is the scale of the acceptance bound.
+ * y and absref are indexed r - r0.  absref may be NULL.
+ * ------------------------------------------------------------------------------------- */
+int orc_qgemv_rows(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases, int64_t out,
+                   int64_t in, int64_t gs, const void *x, int xtype, int64_t r0, int64_t r1, double *y,
+                   double *absref) {
+  if (gs <= 0 || in <= 0 || in % gs != 0 || in % 8 != 0 || r0 < 0 || r1 > out || r0 > r1) return ORC_EINVAL;
+  if (xtype != ORC_X_BF16 && xtype != ORC_X_F32) return ORC_EINVAL;
+  for (int64_t r = r0; r < r1; ++r) {
+    double acc = 0.0, aacc = 0.0;
+    for (int64_t j = 0; j < in; ++j) {
+      double t = orc_dequant(packed, scales, biases, in, gs, r, j) * load_x(x, xtype, j);
+      acc += t;
+      aacc += fabs(t);
+    }
+    y[r - r0] = acc;
+    if (absref) absref[r - r0] = aacc;
+  }
+  return ORC_OK;
+}
+
+/* Same product with a double-precision input vector (used for the MoE down projection, whose
+ * input h is kept in double by the oracle). */
+int orc_qgemv_rows_f64x(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases, int64_t out,
+                        int64_t in, int64_t gs, const double *x, int64_t r0, int64_t r1, double *y,
+                        double *absref) {
+  if (gs <= 0 || in <= 0 || in % gs != 0 || in % 8 != 0 || r0 < 0 || r1 > out || r0 > r1) return ORC_EINVAL;
+  for (int64_t r = r0; r < r1; ++r) {
+    double acc = 0.0, aacc = 0.0;
+    for (int64_t j = 0; j < in; ++j) {
+      double t = orc_dequant(packed, scales, biases, in, gs, r, j) * x[j];
+      acc += t;
+      aacc += fabs(t);
+    }
+    y[r - r0] = acc;
+    if (absref) absref[r - r0] = aacc;
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * SwiGLU: h = silu(g) * u = g / (1 + exp(-g)) * u, unclamped ([FFAI#14] fused MoE down
+ * commit: "inner[k] = silu(gate[k]) * up[k]"; [ds4#844] "unclamped SwiGLU").
+ * ------------------------------------------------------------------------------------- */
+double orc_silu(double g) { return g / (1.0 + exp(-g)); }
+
+void orc_swiglu(const double *g, const double *u, int64_t n, double *h) {
+  for (int64_t i = 0; i < n; ++i) h[i] = orc_silu(g[i]) * u[i];
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Router top-K ([FFAI#14] commit "moeRouterTopK": logits [nExperts] -> k u32 indices + k
+ * weights; test "top-K of (1, 5, 3, 4) at k=2 picks indices {1, 3}; weights sum to 1.0";
+ * [FFAI#9] partial-sort commit: order is (value desc, index asc)).
+ * Selection: k rounds of "take the not-yet-taken expert with the largest logit; on equal
+ * logits the smaller index".  Weights: renorm=1 -> softmax over the k selected logits
+ * (sums to 1); renorm=0 -> the full softmax over all n experts, read at the selected ones.
+ * The slot order of the output is the selection order.
+ * ------------------------------------------------------------------------------------- */
+int orc_router_topk(const float *logits, int n, int k, int renorm, uint32_t *idx, double *p) {
+  if (n <= 0 || k <= 0 || k > n) return ORC_EINVAL;
+  char *taken = (char *)calloc((size_t)n, 1);
+  if (!taken) return ORC_EINVAL;
+  for (int s = 0; s < k; ++s) {
+    int best = -1;
+    for (int e = 0; e < n; ++e) {
+      if (taken[e]) continue;
+      if (best < 0 || logits[e] > logits[best]) best = e; /* strict '>' keeps the lower index on ties */
+    }
+    taken[best] = 1;
+    idx[s] = (uint32_t)best;
+  }
+  free(taken);
+  double m = (double)logits[idx[0]];
+  if (renorm) {
+    double z = 0.0;
+    for (int s = 0; s < k; ++s) z += exp((double)logits[idx[s]] - m);
+    for (int s = 0; s < k; ++s) p[s] = exp((double)logits[idx[s]] - m) / z;
+  } else {
+    double z = 0.0;
+    for (int e = 0; e < n; ++e) z += exp((double)logits[e] - m); /* idx[0] holds the global max */
+    for (int s = 0; s < k; ++s) p[s] = exp((double)logits[idx[s]] - m) / z;
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Scalar-weighted chain accumulate with residual:
+ *   y[i] = r[i] + sum_{k<K} p[k] * v[k][i]
+ * ([FFAI#14] scalar-FMA commit: "scalarFMAChain8 ... exact 8-way fused dispatch",
+ * "out[i] = base[i] + scalar[0] * value[i]"; residual folded in as in
+ * "sigmoidScalarFMAResidual ... post-MoE residual add folded in").
+ * absref[i] = |r[i]| + sum_k |p[k] * v[k][i]|.  Indices i0 <= i < i1; outputs indexed i - i0.
+ * r is bf16; v is fp32 [K][n].
+ * ------------------------------------------------------------------------------------- */
+void orc_chain_residual(const double *p, int K, const float *v, const uint16_t *r, int64_t n, int64_t i0,
+                        int64_t i1, double *y, double *absref) {
+  for (int64_t i = i0; i < i1; ++i) {
+    double rv = orc_bf16_to_f64(r[i]);
+    double acc = rv, aacc = fabs(rv);
+    for (int k = 0; k < K; ++k) {
+      double t = p[k] * (double)v[(int64_t)k * n + i];
+      acc += t;
+      aacc += fabs(t);
+    }
+    y[i - i0] = acc;
+    if (absref) absref[i - i0] = aacc;
+  }
+}
+
+/* ---------------------------------------------------------------------------------------
+ * MoE top-K gather decode step ([FFAI#14] commits "moeRouterTopK / dequantGemvInt4ExpertIndexed"
+ * and "ffai_moe_down_swiglu_accum_int4_chain8"):
+ *   for each slot k:  e = idx[k];  g = Wg[e] x;  u = Wu[e] x;  h = silu(g) * u;  d = Wd[e] h
+ *   y[i] = r[i] + sum_k p[k] * d_k[i]
+ * The expert slab e of a stacked weight is the e-th [rows][in/8] block (and the e-th
+ * [rows][in/gs] block of its scales and biases).  h stays in double.  A slot whose index is
+ * >= n_experts contributes nothing and sets the returned flag bit (1 << k).
+ * absref[i] = |r[i]| + sum_k |p[k]| * sum_j |Wd[e][i][j] * h_k[j]|.
+ * Shapes: gate/up [n_experts][inter][hidden/8], down [n_experts][hidden][inter/8].
+ * ------------------------------------------------------------------------------------- */
+int orc_moe(const uint32_t *gq, const uint16_t *gs_, const uint16_t *gb, const uint32_t *uq, const uint16_t *us,
+            const uint16_t *ub, const uint32_t *dq, const uint16_t *ds, const uint16_t *db, int64_t n_experts,
+            int64_t hidden, int64_t inter, int64_t gsz, const uint32_t *idx, const double *p, int K,
+            const uint16_t *x, const uint16_t *resid, double *y, double *absref) {
+  if (hidden % gsz || inter % gsz || hidden % 8 || inter % 8) return ORC_EINVAL;
+  double *g = (double *)malloc(sizeof(double) * (size_t)inter);
+  double *u = (double *)malloc(sizeof(double) * (size_t)inter);
+  double *h = (double *)malloc(sizeof(double) * (size_t)inter);
+  double *d = (double *)malloc(sizeof(double) * (size_t)hidden);
+  double *da = (double *)malloc(sizeof(double) * (size_t)hidden);
+  if (!g || !u || !h || !d || !da) return ORC_EINVAL;
+  int flags = 0;
+  for (int64_t i = 0; i < hidden; ++i) {
+    y[i] = orc_bf16_to_f64(resid[i]);
+    if (absref) absref[i] = fabs(y[i]);
+  }
+  const int64_t gu_words = inter * (hidden / 8), gu_groups = inter * (hidden / gsz);
+  const int64_t d_words = hidden * (inter / 8), d_groups = hidden * (inter / gsz);
+  for (int k = 0; k < K; ++k) {
+    int64_t e = (int64_t)idx[k];
+    if (e < 0 || e >= n_experts) {
+      flags |= 1 << k;
+      continue;
+    }
+    orc_qgemv_rows(gq + e * gu_words, gs_ + e * gu_groups, gb + e * gu_groups, inter, hidden, gsz, x, ORC_X_BF16,
+                   0, inter, g, NULL);
+    orc_qgemv_rows(uq + e * gu_words, us + e * gu_groups, ub + e * gu_groups, inter, hidden, gsz, x, ORC_X_BF16,
+                   0, inter, u, NULL);
+    orc_swiglu(g, u, inter, h);
+    orc_qgemv_rows_f64x(dq + e * d_words, ds + e * d_groups, db + e * d_groups, hidden, inter, gsz, h, 0, hidden, d,
+                        da);
+    for (int64_t i = 0; i < hidden; ++i) {
+      y[i] += p[k] * d[i];
+      if (absref) absref[i] += fabs(p[k]) * da[i];
+    }
+  }
+  free(g);
+  free(u);
+  free(h);
+  free(d);
+  free(da);
+  return flags;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Dequant-GEMM for T > 1:  Y[t][r] = sum_j w[r][j] * X[t][j]  ([FFAI#9] "Ops.dequantGemmDynamicM:
+ * host-side T-padding driver ... Pads T -> ceil(T/32)*32 with zero rows, dispatches, slices the
+ * first T rows back").  Padding rows contribute nothing to the first T rows, so the oracle
+ * computes exactly T rows.  X is bf16 [T][in].  Rows r0 <= r < r1; Y and absref are
+ * [T][r1 - r0].
+ * ------------------------------------------------------------------------------------- */
+int orc_qgemm_rows(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases, int64_t out, int64_t in,
+                   int64_t gs, const uint16_t *X, int64_t T, int64_t r0, int64_t r1, double *Y, double *absref) {
+  if (T <= 0) return ORC_EINVAL;
+  int64_t w = r1 - r0;
+  for (int64_t t = 0; t < T; ++t) {
+    int rc = orc_qgemv_rows(packed, scales, biases, out, in, gs, X + t * in, ORC_X_BF16, r0, r1, Y + t * w,
+                            absref ? absref + t * w : NULL);
+    if (rc) return rc;
+  }
+  return ORC_OK;
+}

@@ -1,0 +1,381 @@
+"""Pins for the fp64 oracle: values the pages print, closed forms, invariants and exact-rational
+brute force.  Each check is built so that a plausible slip in the oracle (a dropped bias term, a
+wrong group or nibble index, a transposed operand, a missing renormalisation, a wrong SiLU sign,
+a dropped residual) fails at least one of them.  CPU only."""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from moe_int4_affine_gb300 import inputs as I
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    d = {}
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, *v = line.split()
+            d[k] = v
+    return d
+
+
+# ---------------------------------------------------------------- bf16 decode
+def _bf16_fraction(bits: int) -> Fraction:
+    """bf16 value from its fields (sign, 8-bit exponent, 7-bit fraction), as an exact rational."""
+    sign = -1 if bits & 0x8000 else 1
+    e = (bits >> 7) & 0xFF
+    f = bits & 0x7F
+    assert e != 0xFF
+    if e == 0:
+        return sign * Fraction(f, 128) * Fraction(2) ** (-126)
+    return sign * (1 + Fraction(f, 128)) * Fraction(2) ** (e - 127)
+
+
+@pytest.mark.parametrize("bits,val", [(0x3F80, 1.0), (0xC000, -2.0), (0x3F81, 1 + 2 ** -7), (0x0000, 0.0),
+                                      (0x8000, -0.0), (0x0001, 2.0 ** -133), (0x7F7F, (2 - 2 ** -7) * 2.0 ** 127),
+                                      (0x3D80, 0.0625), (0xBE80, -0.25)])
+def test_bf16_decode_known_values(bits, val):
+    assert oracle.bf16_to_f64(bits) == val
+    assert float(_bf16_fraction(bits)) == val
+
+
+def test_bf16_decode_all_finite_patterns_match_fields():
+    for bits in list(range(0, 0x7F80, 97)) + list(range(0x8000, 0xFF80, 89)):
+        assert oracle.bf16_to_f64(bits) == float(_bf16_fraction(bits)), hex(bits)
+
+
+# ---------------------------------------------------------------- nibble unpack
+def test_unpack_known_words():
+    w = np.array([[0x76543210, 0xFEDCBA98]], dtype=np.uint32)
+    q = oracle.unpack(w, 16)
+    assert q.tolist() == [list(range(16))]
+
+
+def test_unpack_every_value_every_position():
+    for pos in range(8):
+        for v in range(16):
+            w = np.array([[v << (4 * pos)]], dtype=np.uint32)
+            q = oracle.unpack(w, 8)[0]
+            exp = [0] * 8
+            exp[pos] = v
+            assert q.tolist() == exp, (pos, v)
+
+
+def test_unpack_random_words_vs_base16_digits():
+    g = np.random.default_rng(5)
+    words = g.integers(0, 2 ** 32, size=(7, 12), dtype=np.uint64).astype(np.uint32)
+    q = oracle.unpack(words, 96)
+    for r in range(7):
+        for w in range(12):
+            n = int(words[r, w])
+            digits = []
+            for _ in range(8):  # little-endian base-16 digits
+                n, d = divmod(n, 16)
+                digits.append(d)
+            assert q[r, 8 * w:8 * w + 8].tolist() == digits
+
+
+def test_generator_packing_roundtrip_through_oracle_unpack():
+    d = I.int4_weight(0, 99, 5, 192, keep_codes=True)
+    assert np.array_equal(oracle.unpack(d["packed"], 192), d["codes"])
+
+
+# ---------------------------------------------------------------- worked example (golden)
+def test_qgemv_worked_example():
+    g = _read_golden("qgemv_worked_example.txt")
+    out, in_dim = int(g["out"][0]), int(g["in"][0])
+    packed = np.array([[int(h, 16) for h in g[f"row{r}_words"]] for r in range(out)], dtype=np.uint32)
+    scales = np.array([int(h, 16) for h in g["scales"]], dtype=np.uint16).reshape(out, in_dim // 64)
+    biases = np.array([int(h, 16) for h in g["biases"]], dtype=np.uint16).reshape(out, in_dim // 64)
+    x = np.array([int(g["x_even"][0], 16) if j % 2 == 0 else int(g["x_odd"][0], 16) for j in range(in_dim)],
+                 dtype=np.uint16)
+    y, a = oracle.qgemv(packed, scales, biases, x)
+    assert y.tolist() == [float(v) for v in g["y"]]
+    assert a.tolist() == [float(v) for v in g["absref"]]
+
+
+# ---------------------------------------------------------------- closed forms
+def _weight(out=6, in_dim=256, seed=3):
+    return I.int4_weight(seed, 1, out, in_dim, keep_codes=True)
+
+
+def test_all_zero_codes_gives_bias_times_group_sum():
+    d = _weight()
+    packed = np.zeros_like(d["packed"])
+    x = I.bf16_normal(0, 2, 256)
+    y, _ = oracle.qgemv(packed, d["scales"], d["biases"], x)
+    xs = [_bf16_fraction(int(b)) for b in x]
+    for r in range(6):
+        exp = sum(_bf16_fraction(int(d["biases"][r, g])) * sum(xs[64 * g:64 * g + 64]) for g in range(4))
+        assert y[r] == pytest.approx(float(exp), rel=1e-14, abs=1e-14)
+
+
+@pytest.mark.parametrize("j", [0, 1, 7, 8, 63, 64, 65, 127, 128, 200, 255])
+def test_one_hot_x_selects_dequantised_column(j):
+    d = _weight()
+    x = np.zeros(256, dtype=np.uint16)
+    x[j] = 0x3F80  # 1.0
+    y, a = oracle.qgemv(d["packed"], d["scales"], d["biases"], x)
+    for r in range(6):
+        s = _bf16_fraction(int(d["scales"][r, j // 64]))
+        b = _bf16_fraction(int(d["biases"][r, j // 64]))
+        w = s * int(d["codes"][r, j]) + b
+        assert y[r] == float(w)
+        assert a[r] == abs(float(w))
+
+
+def test_transposed_operand_would_be_caught():
+    """Non-square shape with distinct rows: y must depend on the row's own codes only."""
+    d = _weight(out=3, in_dim=128)
+    x = I.bf16_normal(0, 2, 128)
+    y, _ = oracle.qgemv(d["packed"], d["scales"], d["biases"], x)
+    y_rows = [oracle.qgemv(d["packed"][r:r + 1], d["scales"][r:r + 1], d["biases"][r:r + 1], x)[0][0] for r in range(3)]
+    assert y.tolist() == y_rows
+
+
+def test_power_of_two_scaling_is_exact():
+    d = _weight()
+    x = I.bf16_normal(0, 2, 256)
+    y, _ = oracle.qgemv(d["packed"], d["scales"], d["biases"], x)
+    # multiply every scale and bias by 4: exponent field + 2 (no overflow for these values)
+    s4 = (d["scales"].astype(np.uint32) + (2 << 7)).astype(np.uint16)
+    b4 = np.where(d["biases"] & 0x7F80, d["biases"].astype(np.uint32) + (2 << 7), d["biases"]).astype(np.uint16)
+    y4, _ = oracle.qgemv(d["packed"], s4, b4, x)
+    np.testing.assert_array_equal(y4, 4.0 * y)
+
+
+def test_linearity_in_x():
+    d = _weight()
+    # x1, x2 bf16 with few significant bits so x1 + x2 is exactly representable in bf16
+    g = np.random.default_rng(1)
+    a1 = g.integers(-8, 9, 256) / 8.0
+    a2 = g.integers(-8, 9, 256) / 4.0
+    x1, x2, x12 = I.f64_to_bf16_bits(a1), I.f64_to_bf16_bits(a2), I.f64_to_bf16_bits(a1 + a2)
+    y1, _ = oracle.qgemv(d["packed"], d["scales"], d["biases"], x1)
+    y2, _ = oracle.qgemv(d["packed"], d["scales"], d["biases"], x2)
+    y12, _ = oracle.qgemv(d["packed"], d["scales"], d["biases"], x12)
+    np.testing.assert_allclose(y12, y1 + y2, rtol=1e-12, atol=1e-12)
+
+
+def test_f32_input_matches_bf16_input_on_bf16_values():
+    d = _weight()
+    xb = I.bf16_normal(0, 2, 256)
+    y1, a1 = oracle.qgemv(d["packed"], d["scales"], d["biases"], xb)
+    y2, a2 = oracle.qgemv(d["packed"], d["scales"], d["biases"], I.bf16_bits_to_f32(xb))
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(a1, a2)
+
+
+# ---------------------------------------------------------------- exact rational brute force
+@pytest.mark.parametrize("out,in_dim", [(1, 64), (3, 64), (2, 128), (3, 128)])
+def test_bruteforce_exact_rational(out, in_dim):
+    g = np.random.default_rng(out * 1000 + in_dim)
+    codes = np.tile(np.arange(16, dtype=np.uint8), out * in_dim // 16).reshape(out, in_dim)
+    codes = np.ascontiguousarray(codes[:, g.permutation(in_dim)])  # every code value on every row
+    packed = I.pack_codes(codes)
+    ng = in_dim // 64
+    scales = I.f64_to_bf16_bits(g.uniform(0.005, 0.02, (out, ng)))
+    biases = I.f64_to_bf16_bits(g.normal(-0.1, 0.05, (out, ng)))
+    x = I.f64_to_bf16_bits(g.standard_normal(in_dim))
+    y, a = oracle.qgemv(packed, scales, biases, x)
+    for r in range(out):
+        acc = Fraction(0)
+        aacc = Fraction(0)
+        for j in range(in_dim):
+            w = _bf16_fraction(int(scales[r, j // 64])) * int(codes[r, j]) + _bf16_fraction(int(biases[r, j // 64]))
+            t = w * _bf16_fraction(int(x[j]))
+            acc += t
+            aacc += abs(t)
+        assert abs(Fraction(y[r]) - acc) <= Fraction(1, 10 ** 15) * aacc
+        assert abs(Fraction(a[r]) - aacc) <= Fraction(1, 10 ** 15) * aacc
+
+
+def test_row_range_matches_full():
+    d = _weight(out=9)
+    x = I.bf16_normal(0, 2, 256)
+    y, a = oracle.qgemv(d["packed"], d["scales"], d["biases"], x)
+    y2, a2 = oracle.qgemv(d["packed"], d["scales"], d["biases"], x, rows=(3, 7))
+    np.testing.assert_array_equal(y[3:7], y2)
+    y3, _ = oracle.qgemv(d["packed"], d["scales"], d["biases"], x, threads=3)
+    np.testing.assert_array_equal(y, y3)
+
+
+# ---------------------------------------------------------------- SwiGLU
+def test_silu_closed_forms():
+    assert oracle.silu(0.0) == 0.0
+    assert oracle.silu(40.0) == pytest.approx(40.0, rel=1e-15)
+    assert abs(oracle.silu(-40.0)) < 1e-15
+    assert oracle.silu(math.log(3.0)) == pytest.approx(math.log(3.0) * 0.75, rel=1e-15)  # sigma(ln 3) = 3/4
+    assert oracle.silu(-math.log(3.0)) == pytest.approx(-math.log(3.0) * 0.25, rel=1e-15)
+    h = oracle.swiglu(np.array([math.log(3.0), 0.0, -math.log(3.0)]), np.array([2.0, 5.0, -4.0]))
+    np.testing.assert_allclose(h, [1.5 * math.log(3.0), 0.0, math.log(3.0)], rtol=1e-15)
+
+
+# ---------------------------------------------------------------- router
+def test_router_pages_example():
+    g = _read_golden("router_topk_pages_example.txt")
+    logits = np.array([float(v) for v in g["logits"]], dtype=np.float32)
+    idx, p = oracle.router_topk(logits, int(g["k"][0]))
+    assert idx.tolist() == [int(v) for v in g["idx"]]
+    np.testing.assert_allclose(p, [float(v) for v in g["p"]], rtol=1e-15)
+    assert p.sum() == pytest.approx(1.0, rel=1e-15)
+    assert p[0] > p[1]
+
+
+def test_router_tie_takes_lower_index():
+    logits = np.array([0.5, 2.0, -1.0, 2.0, 2.0, 0.0], dtype=np.float32)
+    idx, p = oracle.router_topk(logits, 3)
+    assert idx.tolist() == [1, 3, 4]
+    np.testing.assert_allclose(p, [1 / 3] * 3, rtol=1e-15)
+    idx, _ = oracle.router_topk(logits, 4)
+    assert idx.tolist() == [1, 3, 4, 0]
+
+
+def test_router_full_softmax_variant():
+    logits = np.array([1, 5, 3, 4], dtype=np.float32)
+    idx, p = oracle.router_topk(logits, 2, renorm=False)
+    z = sum(math.exp(v) for v in [1, 5, 3, 4])
+    assert idx.tolist() == [1, 3]
+    np.testing.assert_allclose(p, [math.exp(5) / z, math.exp(4) / z], rtol=1e-15)
+
+
+def test_router_k8_of_128_matches_sort():
+    logits = I.f32_normal(0, I.TID_LOGITS, 128)
+    idx, p = oracle.router_topk(logits, 8)
+    order = sorted(range(128), key=lambda e: (-float(logits[e]), e))[:8]
+    assert idx.tolist() == order
+    assert p.sum() == pytest.approx(1.0, rel=1e-14)
+    assert np.all(np.diff(p) <= 0)
+
+
+# ---------------------------------------------------------------- chain8 + residual
+def test_chain_equal_values_and_weights_summing_to_one():
+    v1 = I.f32_normal(0, 1, 64)
+    v = np.tile(v1, (8, 1))
+    p = np.array([0.5, 0.25, 0.125, 0.0625, 0.03125, 0.015625, 0.0078125, 0.0078125])
+    r = I.bf16_normal(0, 2, 64)
+    y, _ = oracle.chain_residual(p, v, r)
+    np.testing.assert_array_equal(y, I.bf16_bits_to_f32(r).astype(np.float64) + v1.astype(np.float64))
+
+
+@pytest.mark.parametrize("k", range(8))
+def test_chain_one_hot_weight_selects_slot(k):
+    v = I.f32_normal(0, 1, (8, 64))
+    p = np.zeros(8)
+    p[k] = 1.0
+    r = I.bf16_normal(0, 2, 64)
+    y, a = oracle.chain_residual(p, v, r)
+    rr = I.bf16_bits_to_f32(r).astype(np.float64)
+    np.testing.assert_array_equal(y, rr + v[k].astype(np.float64))
+    np.testing.assert_array_equal(a, np.abs(rr) + np.abs(v[k].astype(np.float64)))
+
+
+# ---------------------------------------------------------------- MoE
+def _moe_weights(E=6, hidden=128, inter=64):
+    gate = I.int4_weight(0, I.TID_GATE, inter, hidden, n_mat=E)
+    up = I.int4_weight(0, I.TID_UP, inter, hidden, n_mat=E)
+    down = I.int4_weight(0, I.TID_DOWN, hidden, inter, n_mat=E)
+    t = lambda d: (d["packed"], d["scales"], d["biases"])
+    return t(gate), t(up), t(down)
+
+
+def _expert_by_slab(gate, up, down, e, x):
+    """The expert computed from slices of the stacked tensors (numpy indexing, not the oracle's
+    pointer arithmetic)."""
+    g, _ = oracle.qgemv(gate[0][e], gate[1][e], gate[2][e], x)
+    u, _ = oracle.qgemv(up[0][e], up[1][e], up[2][e], x)
+    h = np.array([gi / (1 + math.exp(-gi)) * ui for gi, ui in zip(g, u)])
+    d, _ = oracle.qgemv_f64x(down[0][e], down[1][e], down[2][e], h)
+    return d
+
+
+@pytest.mark.parametrize("e", [0, 3, 5])
+def test_moe_one_hot_router_reduces_to_single_expert(e):
+    gate, up, down = _moe_weights()
+    x = I.bf16_normal(0, 2, 128)
+    r = I.bf16_normal(0, 6, 128)
+    idx = np.array([e, 1, 2, 3, 4, 0, 1, 2], dtype=np.uint32)
+    p = np.array([1.0, 0, 0, 0, 0, 0, 0, 0])
+    y, _, flags = oracle.moe(gate, up, down, idx, p, x, r)
+    assert flags == 0
+    exp = I.bf16_bits_to_f32(r).astype(np.float64) + _expert_by_slab(gate, up, down, e, x)
+    np.testing.assert_allclose(y, exp, rtol=1e-13, atol=1e-13)
+
+
+def test_moe_weighted_sum_of_experts():
+    gate, up, down = _moe_weights()
+    x = I.bf16_normal(0, 2, 128)
+    r = I.bf16_normal(0, 6, 128)
+    idx = np.array([5, 2, 0, 1, 3, 4, 2, 5], dtype=np.uint32)
+    p = np.array([0.3, 0.2, 0.1, 0.1, 0.1, 0.1, 0.05, 0.05])
+    y, a, flags = oracle.moe(gate, up, down, idx, p, x, r)
+    exp = I.bf16_bits_to_f32(r).astype(np.float64)
+    for k in range(8):
+        exp = exp + p[k] * _expert_by_slab(gate, up, down, int(idx[k]), x)
+    np.testing.assert_allclose(y, exp, rtol=1e-12, atol=1e-12)
+    assert np.all(a >= np.abs(y) - 1e-12)
+
+
+def test_moe_out_of_range_index_is_skipped_and_flagged():
+    gate, up, down = _moe_weights()
+    x = I.bf16_normal(0, 2, 128)
+    r = I.bf16_normal(0, 6, 128)
+    idx = np.array([1, 99, 2, 3, 4, 0, 1, 2], dtype=np.uint32)
+    p = np.full(8, 0.125)
+    y, _, flags = oracle.moe(gate, up, down, idx, p, x, r)
+    assert flags == 1 << 1
+    idx2 = idx.copy()
+    idx2[1] = 0
+    p2 = p.copy()
+    p2[1] = 0.0
+    y2, _, _ = oracle.moe(gate, up, down, idx2, p2, x, r)
+    np.testing.assert_array_equal(y, y2)
+
+
+# ---------------------------------------------------------------- GEMM
+def test_qgemm_rows_equal_qgemv_rows():
+    d = _weight(out=5)
+    X = I.bf16_normal(0, 2, (3, 256))
+    Y, A = oracle.qgemm(d["packed"], d["scales"], d["biases"], X)
+    for t in range(3):
+        y, a = oracle.qgemv(d["packed"], d["scales"], d["biases"], X[t])
+        np.testing.assert_array_equal(Y[t], y)
+        np.testing.assert_array_equal(A[t], a)
+    Y2, _ = oracle.qgemm(d["packed"], d["scales"], d["biases"], X, rows=(1, 4))
+    np.testing.assert_array_equal(Y2, Y[:, 1:4])
+
+
+def test_qgemm_zero_padding_rows_do_not_change_real_rows():
+    d = _weight(out=4)
+    X = I.bf16_normal(0, 2, (3, 256))
+    Xp = np.zeros((32, 256), dtype=np.uint16)
+    Xp[:3] = X
+    Y, _ = oracle.qgemm(d["packed"], d["scales"], d["biases"], X)
+    Yp, _ = oracle.qgemm(d["packed"], d["scales"], d["biases"], Xp)
+    np.testing.assert_array_equal(Yp[:3], Y)
+    # padded rows see x = 0, so every term is w*0 and the sum is exactly 0
+    np.testing.assert_array_equal(Yp[3:], 0.0)
+
+
+# ---------------------------------------------------------------- generator sanity (data recipe)
+def test_generator_distribution_recipe():
+    d = I.int4_weight(0, 1, 256, 1024, keep_codes=True)
+    s = I.bf16_bits_to_f32(d["scales"]).astype(np.float64)
+    b = I.bf16_bits_to_f32(d["biases"]).astype(np.float64)
+    assert s.min() >= 0.005 * (1 - 2 ** -8) and s.max() <= 0.02 * (1 + 2 ** -8)
+    assert abs(np.mean(b + 8 * s)) < 2e-4 and 0.5e-3 < np.std(b + 8 * s) < 1.5e-3
+    counts = np.bincount(d["codes"].ravel(), minlength=16)
+    assert counts.min() > 0.9 * counts.mean()
+    x = I.bf16_bits_to_f32(I.bf16_normal(0, 2, 100000)).astype(np.float64)
+    assert abs(x.mean()) < 0.02 and abs(x.std() - 1) < 0.02
+    # reproducible
+    d2 = I.int4_weight(0, 1, 256, 1024)
+    assert np.array_equal(d["packed"], d2["packed"]) and np.array_equal(d["biases"], d2["biases"])
