@@ -1,0 +1,181 @@
+/*
+ * qg.h -- C ABI of libqg: int4 affine group-quantised dequant-GEMV / MoE-gather decode path for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Sources for what each call computes (web pages without section numbers; each citation names
+ * the page and the commit or paragraph):
+ *   [FFAI#14]  thewafflehaus/FFAI pull request #14, "feat(everything-bagel): clean migration of
+ *              PR #9 + #10 onto updated dev"
+ *   [FFAI#9]   thewafflehaus/FFAI pull request #9, "Everything Bagel"
+ *   [ds4#844]  antirez/ds4 pull request #844, "Ornith 1.5 + Qwen 3.8 27B hybrid runtime + DFlash
+ *              speculative decoding on Metal"
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers, owned by the caller, 16-byte aligned.  The library
+ *     never allocates, frees or retains them.  Scratch space, where a call needs it, is a
+ *     caller-owned device workspace whose size qg_workspace_bytes() reports ([FFAI#14] two-pass
+ *     decode commit: scratch buffers "are caller-owned so a decode loop can amortise them").
+ *   - bf16 values are passed as their raw 16-bit patterns (uint16_t).
+ *   - `stream` is a cudaStream_t cast to void* (NULL = the legacy default stream).  Every call is
+ *     asynchronous on that stream; none synchronises the host except qg_device_status().
+ *   - Return value: QG_OK (0) or a negative qg_error.  Argument errors are detected on the host
+ *     before anything is launched.  Conditions only the device can see (an expert index out of
+ *     range, a wait that timed out) set bits in a device status word read by qg_device_status().
+ *   - Outputs of calls in flight must not alias inputs or outputs of other calls in flight.
+ *
+ * Weight format ([FFAI#14] commit "moeRouterTopK / dequantGemvInt4ExpertIndexed": stacked
+ * "[nExperts, outDim, inDim/8] u32"; [FFAI#14] "(weight, scales, biases, input, output)";
+ * [FFAI#14] fast-path preconditions "group_size = 64"; [ds4#844] Q4_64A "BF16 scale/bias"):
+ *   packed  uint32 [n_mat][out][in/8]; element j of a row is the nibble at bits 4*(j%8) of word
+ *           j/8 (low nibble first), an unsigned code q in 0..15.
+ *   scales  bf16   [n_mat][out][in/64]
+ *   biases  bf16   [n_mat][out][in/64]
+ *   w[r][j] = scales[r][j/64] * q[r][j] + biases[r][j/64]       (no zero-point subtraction)
+ *
+ * Accuracy: every fp32 output y satisfies |y - y_exact| <= 1e-3 * sum|w*x| + 1e-6, where y_exact
+ * and sum|w*x| are computed from the same stored inputs in exact arithmetic (checked against an
+ * fp64 oracle); router indices and nibble decoding are exact.
+ */
+#ifndef QG_H
+#define QG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QG_OK = 0,
+  QG_EINVAL = -1,      /* null pointer, bad shape, group_size != 64, bad n/k/T, mismatched widths */
+  QG_EALIGN = -2,      /* a pointer is not 16-byte aligned                                        */
+  QG_EWORKSPACE = -3,  /* workspace missing or smaller than qg_workspace_bytes()                  */
+  QG_ELAUNCH = -4,     /* the CUDA launch failed (cudaGetLastError after the launch)              */
+  QG_ENOTSUP = -5,     /* shape outside the limits stated for the call                            */
+  QG_EDEVICE = -6      /* a CUDA runtime call made by qg_device_status() failed                   */
+} qg_error;
+
+/* Bits of the device status word (qg_device_status). */
+enum qg_status_bits {
+  QG_STATUS_BAD_EXPERT = 1u, /* an expert index >= n_experts was skipped (its slot added nothing) */
+  QG_STATUS_TIMEOUT = 2u     /* a device-side wait gave up after its time limit (result invalid)  */
+};
+
+typedef enum { QG_X_BF16 = 0, QG_X_F32 = 1 } qg_xtype;
+typedef enum { QG_EPI_NONE = 0, QG_EPI_SWIGLU = 1 } qg_epilogue;
+
+typedef struct {
+  const uint32_t *packed; /* [n_mat][out][in/8] */
+  const uint16_t *scales; /* bf16 [n_mat][out][in/group_size] */
+  const uint16_t *biases; /* bf16 [n_mat][out][in/group_size] */
+  int32_t out;            /* rows per matrix, >= 1 */
+  int32_t in;             /* columns, a multiple of 64 */
+  int32_t group_size;     /* must be 64 */
+  int32_t n_mat;          /* 1, or the number of stacked experts */
+} qg_int4_weight;
+
+/*
+ * qgemv_int4 -- dequant-GEMV, M = 1 ([FFAI#14] "dequant_gemv_int4_*"):
+ *   y[r] = sum_j w[r][j] * x[j],  0 <= r < w->out  (fp32 accumulate).
+ * x: [w->in], bf16 bits (xt = QG_X_BF16) or fp32 (QG_X_F32).  y: fp32 [w->out].
+ * w->n_mat must be 1.  Limits: 64 <= in <= 32768, in % 64 == 0, out >= 1.
+ */
+int qgemv_int4(const qg_int4_weight *w, const void *x, int xt, float *y, void *stream);
+
+/*
+ * qgemv_int4_multi -- n in {2,3,4} projections sharing one input vector, one launch ([FFAI#14]
+ * "dequantGemvInt4Two/Three/Four", "ffai_batched_qkv_qgemv_fast", "ffai_batched_4_qgemv_fast":
+ * x is read once for all projections; "explicit precondition that all packed widths match").
+ *   epi = QG_EPI_NONE:   ys[i][r] = sum_j w_i[r][j] x[j]   for each i < n.
+ *   epi = QG_EPI_SWIGLU: n must be 2 with ws[0].out == ws[1].out; ws[0] = gate, ws[1] = up and
+ *                        ys[0][r] = silu(g[r]) * u[r], silu(g) = g / (1 + exp(-g)) (unclamped,
+ *                        [ds4#844] "unclamped SwiGLU"); ys[1] is unused (may be NULL).
+ * ws: host array of n weights, all with the same `in`, n_mat == 1.  ys: host array of n device
+ * pointers.  Limits as qgemv_int4.
+ */
+int qgemv_int4_multi(int n, const qg_int4_weight *ws, const void *x, int xt, float *const *ys, int epi,
+                     void *stream);
+
+/*
+ * moe_router_topk -- GPU router ([FFAI#14] commit "moeRouterTopK": logits [nExperts] -> [k] u32
+ * indices + [k] weights, no host readback; [FFAI#9] top-K order "(value desc, index asc)").
+ * Selects the k largest logits, ties to the lower index; slot s holds the s-th selected expert.
+ *   renorm = 1: p = softmax over the k selected logits (sums to 1).
+ *   renorm = 0: p = softmax over all n_experts logits, read at the selected experts.
+ * logits: fp32 [n_experts] (device, finite); idx: uint32 [k] (device); p: fp32 [k] (device).
+ * Limits: 1 <= k <= 32, k <= n_experts <= 1024.
+ */
+int moe_router_topk(const float *logits, int n_experts, int k, int renorm, uint32_t *idx, float *p, void *stream);
+
+/*
+ * moe_gather_qgemv_int4 -- MoE top-K gather decode step ([FFAI#14] commits "moeRouterTopK /
+ * dequantGemvInt4ExpertIndexed" and "ffai_moe_down_swiglu_accum_int4_chain8"):
+ *   for slot k: e = idx[k]; g = Wg[e] x; u = Wu[e] x; h_k = silu(g) * u; d_k = Wd[e] h_k
+ *   y[i] = residual[i] + sum_k p[k] * d_k[i]
+ * gate, up: n_mat = n_experts stacked [inter][hidden] weights; down: n_experts stacked
+ * [hidden][inter].  idx (uint32 [k]) and p (fp32 [k]) are device arrays, normally the outputs
+ * of moe_router_topk.  An index >= n_experts is skipped (that slot adds nothing) and sets
+ * QG_STATUS_BAD_EXPERT.  x, residual: bf16 [hidden]; y: fp32 [hidden].
+ * workspace: device scratch of at least qg_workspace_bytes(QG_OP_MOE, down, k) bytes (holds the
+ * fp32 SwiGLU activations h[k][inter]).
+ * Limits: 1 <= k <= 8; inter and hidden multiples of 64, at most 32768.
+ */
+int moe_gather_qgemv_int4(const qg_int4_weight *gate, const qg_int4_weight *up, const qg_int4_weight *down,
+                          const uint32_t *idx, const float *p, int k, const uint16_t *x, const uint16_t *residual,
+                          float *y, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * scalar_fma_chain8_residual -- eight (scalar, vector) pairs accumulated in one pass with the
+ * residual folded in ([FFAI#14] scalar-FMA commit: "scalarFMAChain8 ... exact 8-way fused
+ * dispatch", "out[i] = base[i] + scalar[0] * value[i]"; "post-MoE residual add folded in"):
+ *   out[i] = residual[i] + sum_{k<8} p[k] * v[k][i]
+ * p: fp32 [8]; v: fp32 [8][n]; residual: bf16 [n]; out: fp32 [n] (all device).  n >= 1.
+ */
+int scalar_fma_chain8_residual(const float *p, const float *v, const uint16_t *residual, float *out, int n,
+                               void *stream);
+
+/*
+ * qgemm_int4 -- dequant-GEMM for T >= 1 token rows ([FFAI#9] "Ops.dequantGemmDynamicM":
+ * "Pads T -> ceil(T/32)*32 with zero rows, dispatches, slices the first T rows back"):
+ *   Y[t][r] = sum_j w[r][j] * X[t][j],  0 <= t < T.
+ * X: bf16 [T][in]; Y: fp32 [T][out].  The caller passes exactly T rows; padding is internal and
+ * only the T real rows are written.
+ * workspace: at least qg_workspace_bytes(QG_OP_QGEMM, w, T) bytes (0 means none is needed).
+ * Limits: 1 <= T <= 4096.
+ */
+int qgemm_int4(const qg_int4_weight *w, const uint16_t *X, int T, float *Y, void *workspace, size_t ws_bytes,
+               void *stream);
+
+typedef enum { QG_OP_QGEMV = 0, QG_OP_MULTI = 1, QG_OP_MOE = 2, QG_OP_QGEMM = 3 } qg_op;
+
+/* Workspace bytes the call `op` needs for weight `w` and T (QG_OP_QGEMM) or k (QG_OP_MOE; pass
+ * the down weight).  Returns 0 when the call needs none. */
+size_t qg_workspace_bytes(int op, const qg_int4_weight *w, int T_or_k);
+
+/*
+ * qg_set_pdl -- enable (1) or disable (0, the default) programmatic dependent launch for the
+ * kernels launched by this library in this process.  When enabled, a kernel may begin before
+ * the preceding kernel in the stream has finished and streams its weights, scales and biases
+ * into shared memory before waiting for it; activations, indices and outputs are only touched
+ * after the wait.  Enable it only when no kernel immediately preceding a qg call writes that
+ * call's weights (the normal case: weights are loaded once and reused every decode step).
+ * Returns the previous setting.
+ */
+int qg_set_pdl(int enable);
+
+/* Reads the device status word (qg_status_bits) of the current device into *status and clears
+ * it.  Synchronises `stream`.  Returns QG_OK or QG_EDEVICE. */
+int qg_device_status(void *stream, uint32_t *status);
+
+/* Static description of an error code. */
+const char *qg_strerror(int code);
+
+/* Library version, (major << 16) | minor. */
+int qg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QG_H */

@@ -1,0 +1,171 @@
+// api.cu -- the C ABI (include/qg.h): argument validation, workspace sizing, status word, and
+// dispatch to the kernel launchers.  No call allocates device memory.
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "qg_common.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+
+__device__ uint32_t g_status = 0;
+
+namespace {
+std::atomic<int> g_pdl{0};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_weight(const qg_int4_weight* w, bool stacked_ok) {
+  if (!w || !w->packed || !w->scales || !w->biases) return QG_EINVAL;
+  if (w->group_size != 64 || w->in < 64 || w->in % 64 != 0 || w->out < 1 || w->n_mat < 1) return QG_EINVAL;
+  if (!stacked_ok && w->n_mat != 1) return QG_EINVAL;
+  if (w->in > 32768) return QG_ENOTSUP;
+  if (!aligned16(w->packed) || !aligned16(w->scales) || !aligned16(w->biases)) return QG_EALIGN;
+  return QG_OK;
+}
+}  // namespace
+
+const DeviceInfo& device_info() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
+  std::call_once(g_dev_once[dev], [dev]() {
+    DeviceInfo d{};
+    cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (d.num_sms <= 0) d.num_sms = 1;
+    g_dev[dev] = d;
+  });
+  return g_dev[dev];
+}
+
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" {
+
+int qgemv_int4(const qg_int4_weight* w, const void* x, int xt, float* y, void* stream) {
+  int rc = check_weight(w, false);
+  if (rc) return rc;
+  if (!x || !y || (xt != QG_X_BF16 && xt != QG_X_F32)) return QG_EINVAL;
+  if (!aligned16(x) || !aligned16(y)) return QG_EALIGN;
+  GemvMatArg m{w->packed, w->scales, w->biases, y, w->out};
+  return gemv_launch(&m, 1, 0, x, xt, w->in, static_cast<cudaStream_t>(stream));
+}
+
+int qgemv_int4_multi(int n, const qg_int4_weight* ws, const void* x, int xt, float* const* ys, int epi, void* stream) {
+  if (n < 2 || n > 4 || !ws || !ys || !x) return QG_EINVAL;
+  if (xt != QG_X_BF16 && xt != QG_X_F32) return QG_EINVAL;
+  if (epi != QG_EPI_NONE && epi != QG_EPI_SWIGLU) return QG_EINVAL;
+  if (epi == QG_EPI_SWIGLU && (n != 2 || ws[0].out != ws[1].out)) return QG_EINVAL;
+  GemvMatArg m[4];
+  for (int i = 0; i < n; ++i) {
+    int rc = check_weight(&ws[i], false);
+    if (rc) return rc;
+    if (ws[i].in != ws[0].in) return QG_EINVAL;  // all packed widths must match
+    const bool need_y = !(epi == QG_EPI_SWIGLU && i == 1);
+    if (need_y && !ys[i]) return QG_EINVAL;
+    if (need_y && !aligned16(ys[i])) return QG_EALIGN;
+    m[i] = GemvMatArg{ws[i].packed, ws[i].scales, ws[i].biases, need_y ? ys[i] : nullptr, ws[i].out};
+  }
+  if (!aligned16(x)) return QG_EALIGN;
+  return gemv_launch(m, n, epi == QG_EPI_SWIGLU, x, xt, ws[0].in, static_cast<cudaStream_t>(stream));
+}
+
+int moe_router_topk(const float* logits, int n_experts, int k, int renorm, uint32_t* idx, float* p, void* stream) {
+  if (!logits || !idx || !p) return QG_EINVAL;
+  if (k < 1 || k > 32 || n_experts < k || (renorm != 0 && renorm != 1)) return QG_EINVAL;
+  if (n_experts > 1024) return QG_ENOTSUP;
+  if (!aligned16(logits) || !aligned16(idx) || !aligned16(p)) return QG_EALIGN;
+  return router_launch(logits, n_experts, k, renorm, idx, p, static_cast<cudaStream_t>(stream));
+}
+
+int moe_gather_qgemv_int4(const qg_int4_weight* gate, const qg_int4_weight* up, const qg_int4_weight* down,
+                          const uint32_t* idx, const float* p, int k, const uint16_t* x, const uint16_t* residual,
+                          float* y, void* workspace, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_weight(gate, true)) || (rc = check_weight(up, true)) || (rc = check_weight(down, true))) return rc;
+  if (!idx || !p || !x || !residual || !y) return QG_EINVAL;
+  if (k < 1 || k > 8) return QG_EINVAL;
+  if (gate->out != up->out || gate->in != up->in || gate->n_mat != up->n_mat || down->n_mat != gate->n_mat ||
+      down->in != gate->out || down->out != gate->in)
+    return QG_EINVAL;
+  if (!aligned16(idx) || !aligned16(p) || !aligned16(x) || !aligned16(residual) || !aligned16(y)) return QG_EALIGN;
+  const size_t need = qg_workspace_bytes(QG_OP_MOE, down, k);
+  if (!workspace || ws_bytes < need) return QG_EWORKSPACE;
+  if (!aligned16(workspace)) return QG_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* h = static_cast<float*>(workspace);
+  rc = moe_gate_up_launch(gate, up, idx, k, x, h, s);
+  if (rc) return rc;
+  return moe_down_launch(down, idx, p, k, h, residual, y, s);
+}
+
+int scalar_fma_chain8_residual(const float* p, const float* v, const uint16_t* residual, float* out, int n,
+                               void* stream) {
+  if (!p || !v || !residual || !out || n < 1) return QG_EINVAL;
+  if (!aligned16(p) || !aligned16(v) || !aligned16(residual) || !aligned16(out)) return QG_EALIGN;
+  return chain8_launch(p, v, residual, out, n, static_cast<cudaStream_t>(stream));
+}
+
+int qgemm_int4(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void* workspace, size_t ws_bytes,
+               void* stream) {
+  int rc = check_weight(w, false);
+  if (rc) return rc;
+  if (!X || !Y || T < 1 || T > 4096) return QG_EINVAL;
+  if (!aligned16(X) || !aligned16(Y)) return QG_EALIGN;
+  const size_t need = qgemm_workspace_bytes(w, T);
+  if (need && (!workspace || ws_bytes < need)) return QG_EWORKSPACE;
+  if (need && !aligned16(workspace)) return QG_EALIGN;
+  return qgemm_launch(w, X, T, Y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t qg_workspace_bytes(int op, const qg_int4_weight* w, int T_or_k) {
+  if (!w) return 0;
+  switch (op) {
+    case QG_OP_MOE:  // h[k][inter] fp32; inter = down->in
+      return (size_t)(T_or_k > 0 ? T_or_k : 0) * (size_t)w->in * sizeof(float);
+    case QG_OP_QGEMM:
+      return qgemm_workspace_bytes(w, T_or_k);
+    default:
+      return 0;
+  }
+}
+
+int qg_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
+
+int qg_device_status(void* stream, uint32_t* status) {
+  if (!status) return QG_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  static const uint32_t zero = 0;
+  if (cudaMemcpyFromSymbolAsync(status, g_status, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return QG_EDEVICE;
+  if (cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return QG_EDEVICE;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return QG_EDEVICE;
+  return QG_OK;
+}
+
+const char* qg_strerror(int code) {
+  switch (code) {
+    case QG_OK: return "ok";
+    case QG_EINVAL: return "invalid argument";
+    case QG_EALIGN: return "pointer not 16-byte aligned";
+    case QG_EWORKSPACE: return "workspace missing or too small";
+    case QG_ELAUNCH: return "CUDA launch failed";
+    case QG_ENOTSUP: return "shape outside the supported limits";
+    case QG_EDEVICE: return "CUDA runtime call failed";
+    default: return "unknown error";
+  }
+}
+
+int qg_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

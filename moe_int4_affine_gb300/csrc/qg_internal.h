@@ -1,0 +1,71 @@
+// qg_internal.h -- host-side interface between the C ABI layer (api.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "../../include/qg.h"
+
+namespace qg {
+
+// Device properties the planners need (queried once per device).
+struct DeviceInfo {
+  int num_sms;
+  int max_smem_optin;
+};
+const DeviceInfo& device_info();
+
+bool pdl_enabled();
+
+// Launch a kernel with the library's launch attributes (programmatic dependent launch when
+// enabled).  Returns QG_OK or QG_ELAUNCH.
+template <typename... KArgs, typename... Args>
+int launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  int na = 0;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return QG_ELAUNCH;
+  e = cudaGetLastError();
+  return e == cudaSuccess ? QG_OK : QG_ELAUNCH;
+}
+
+// ---------------------------------------------------------------- GEMV family (qgemv.cu)
+struct GemvMatArg {
+  const uint32_t* packed;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  float* y;
+  int out;
+};
+// n matrices sharing x.  pair_swiglu: n == 2, y = silu(W0 x) * (W1 x) written to mats[0].y.
+int gemv_launch(const GemvMatArg* mats, int n, int pair_swiglu, const void* x, int xt, int in, cudaStream_t stream);
+int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, const uint32_t* idx, int k,
+                       const uint16_t* x, float* h, cudaStream_t stream);
+int moe_down_launch(const qg_int4_weight* down, const uint32_t* idx, const float* p, int k, const float* h,
+                    const uint16_t* residual, float* y, cudaStream_t stream);
+
+// ---------------------------------------------------------------- MoE (moe.cu)
+int router_launch(const float* logits, int n_experts, int k, int renorm, uint32_t* idx, float* p,
+                  cudaStream_t stream);
+int chain8_launch(const float* p, const float* v, const uint16_t* residual, float* out, int n, cudaStream_t stream);
+
+// ---------------------------------------------------------------- GEMM (qgemm.cu)
+size_t qgemm_workspace_bytes(const qg_int4_weight* w, int T);
+int qgemm_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void* ws, size_t ws_bytes,
+                 cudaStream_t stream);
+
+}  // namespace qg
