@@ -1,0 +1,232 @@
+"""ctypes binding of libqg (include/qg.h): the same entry points, argument marshalling only.
+
+Tensors are torch CUDA tensors (torch supplies device memory and streams); the binding passes
+their data pointers and the current CUDA stream to the C ABI and raises QGError on a non-zero
+return code.  Importing this module raises ImportError when the compiled library is missing: no
+call can fall back to anything else.  Build it with ``python -m moe_int4_affine_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libqg.so")
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libqg.so not built ({LIB_PATH}); run `python -m moe_int4_affine_gb300.build`")
+lib = ctypes.CDLL(LIB_PATH)
+
+# ---------------------------------------------------------------- constants (include/qg.h)
+QG_OK, QG_EINVAL, QG_EALIGN, QG_EWORKSPACE, QG_ELAUNCH, QG_ENOTSUP, QG_EDEVICE = 0, -1, -2, -3, -4, -5, -6
+QG_STATUS_BAD_EXPERT, QG_STATUS_TIMEOUT = 1, 2
+QG_X_BF16, QG_X_F32 = 0, 1
+QG_EPI_NONE, QG_EPI_SWIGLU = 0, 1
+QG_OP_QGEMV, QG_OP_MULTI, QG_OP_MOE, QG_OP_QGEMM = 0, 1, 2, 3
+
+
+class qg_int4_weight(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
+                ("out", ctypes.c_int32), ("in_", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("n_mat", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_W = ctypes.POINTER(qg_int4_weight)
+lib.qgemv_int4.argtypes = [_W, _P, _I, _P, _P]
+lib.qgemv_int4_multi.argtypes = [_I, _W, _P, _I, ctypes.POINTER(_P), _I, _P]
+lib.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
+lib.moe_gather_qgemv_int4.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]
+lib.scalar_fma_chain8_residual.argtypes = [_P, _P, _P, _P, _I, _P]
+lib.qgemm_int4.argtypes = [_W, _P, _I, _P, _P, ctypes.c_size_t, _P]
+lib.qg_workspace_bytes.argtypes = [_I, _W, _I]
+lib.qg_workspace_bytes.restype = ctypes.c_size_t
+lib.qg_set_pdl.argtypes = [_I]
+lib.qg_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
+lib.qg_strerror.argtypes = [_I]
+lib.qg_strerror.restype = ctypes.c_char_p
+lib.qg_version.argtypes = []
+for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
+           "scalar_fma_chain8_residual", "qgemm_int4", "qg_set_pdl", "qg_device_status", "qg_version"):
+    getattr(lib, _f).restype = ctypes.c_int
+
+
+class QGError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {qg_strerror(code)} ({code})")
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != QG_OK:
+        raise QGError(rc, where)
+
+
+def qg_strerror(code: int) -> str:
+    return lib.qg_strerror(int(code)).decode()
+
+
+# ---------------------------------------------------------------- torch marshalling
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return int(_torch().cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def to_device(a: np.ndarray, device="cuda"):
+    """numpy -> torch CUDA tensor with the same bytes (uint32 -> int32, uint16 bf16 bits -> bfloat16)."""
+    torch = _torch()
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint32:
+        return torch.from_numpy(a.view(np.int32)).to(device)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def to_numpy(t) -> np.ndarray:
+    torch = _torch()
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.int32:
+        return t.numpy().view(np.uint32)
+    return t.numpy()
+
+
+class Int4Weight:
+    """Device tensors of one int4 affine weight (or a stack of n_mat expert weights)."""
+
+    def __init__(self, packed, scales, biases, out: int, in_dim: int, n_mat: int = 1, group_size: int = 64):
+        self.packed, self.scales, self.biases = packed, scales, biases
+        self.out, self.in_dim, self.n_mat, self.group_size = int(out), int(in_dim), int(n_mat), int(group_size)
+        self._s = qg_int4_weight(_ptr(packed), _ptr(scales), _ptr(biases), self.out, self.in_dim,
+                                 self.group_size, self.n_mat)
+
+    @classmethod
+    def from_numpy(cls, d: dict, device="cuda") -> "Int4Weight":
+        packed = d["packed"]
+        if packed.ndim == 3:
+            n_mat, out, w = packed.shape
+        else:
+            (out, w), n_mat = packed.shape, 1
+        return cls(to_device(packed, device), to_device(d["scales"], device), to_device(d["biases"], device),
+                   out, w * 8, n_mat)
+
+    @property
+    def struct(self) -> qg_int4_weight:
+        return self._s
+
+
+def _xtype(x) -> int:
+    torch = _torch()
+    if x.dtype == torch.bfloat16:
+        return QG_X_BF16
+    if x.dtype == torch.float32:
+        return QG_X_F32
+    raise TypeError(f"x must be bfloat16 or float32, got {x.dtype}")
+
+
+# ---------------------------------------------------------------- entry points
+def qgemv_int4(w: Int4Weight, x, y=None, stream=None):
+    torch = _torch()
+    if y is None:
+        y = torch.empty(w.out, dtype=torch.float32, device=x.device)
+    _check(lib.qgemv_int4(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(y), _stream(stream)), "qgemv_int4")
+    return y
+
+
+def qgemv_int4_multi(ws, x, ys=None, epilogue: str = "none", stream=None):
+    torch = _torch()
+    n = len(ws)
+    epi = {"none": QG_EPI_NONE, "swiglu": QG_EPI_SWIGLU}[epilogue]
+    if ys is None:
+        ys = [torch.empty(w.out, dtype=torch.float32, device=x.device) for w in ws]
+        if epi == QG_EPI_SWIGLU:
+            ys[1] = None
+    arr = (qg_int4_weight * n)(*[w.struct for w in ws])
+    yp = (_P * n)(*[_ptr(y) for y in ys])
+    _check(lib.qgemv_int4_multi(n, arr, _ptr(x), _xtype(x), yp, epi, _stream(stream)), "qgemv_int4_multi")
+    return ys[0] if epi == QG_EPI_SWIGLU else ys
+
+
+def moe_router_topk(logits, k: int = 8, renorm: bool = True, idx=None, p=None, stream=None):
+    torch = _torch()
+    if idx is None:
+        idx = torch.empty(k, dtype=torch.int32, device=logits.device)
+    if p is None:
+        p = torch.empty(k, dtype=torch.float32, device=logits.device)
+    _check(lib.moe_router_topk(_ptr(logits), logits.numel(), k, 1 if renorm else 0, _ptr(idx), _ptr(p),
+                               _stream(stream)), "moe_router_topk")
+    return idx, p
+
+
+def qg_workspace_bytes(op: int, w: Int4Weight, t_or_k: int) -> int:
+    return int(lib.qg_workspace_bytes(op, ctypes.byref(w.struct), t_or_k))
+
+
+def moe_gather_qgemv_int4(gate: Int4Weight, up: Int4Weight, down: Int4Weight, idx, p, x, residual, y=None,
+                          workspace=None, stream=None):
+    torch = _torch()
+    k = idx.numel()
+    if y is None:
+        y = torch.empty(down.out, dtype=torch.float32, device=x.device)
+    need = qg_workspace_bytes(QG_OP_MOE, down, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check(lib.moe_gather_qgemv_int4(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
+                                     _ptr(idx), _ptr(p), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_gather_qgemv_int4")
+    return y
+
+
+def scalar_fma_chain8_residual(p, v, residual, out=None, stream=None):
+    torch = _torch()
+    n = residual.numel()
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=v.device)
+    _check(lib.scalar_fma_chain8_residual(_ptr(p), _ptr(v), _ptr(residual), _ptr(out), n, _stream(stream)),
+           "scalar_fma_chain8_residual")
+    return out
+
+
+def qgemm_int4(w: Int4Weight, X, Y=None, workspace=None, stream=None):
+    torch = _torch()
+    T = X.shape[0]
+    if Y is None:
+        Y = torch.empty((T, w.out), dtype=torch.float32, device=X.device)
+    need = qg_workspace_bytes(QG_OP_QGEMM, w, T)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.qgemm_int4(ctypes.byref(w.struct), _ptr(X), T, _ptr(Y), _ptr(workspace), nbytes, _stream(stream)),
+           "qgemm_int4")
+    return Y
+
+
+def qg_set_pdl(enable: bool) -> bool:
+    return bool(lib.qg_set_pdl(1 if enable else 0))
+
+
+def qg_device_status(stream=None) -> int:
+    s = ctypes.c_uint32(0)
+    _check(lib.qg_device_status(_stream(stream), ctypes.byref(s)), "qg_device_status")
+    return int(s.value)
+
+
+def qg_version() -> int:
+    return int(lib.qg_version())

@@ -33,3 +33,18 @@ def assert_within_bound(y, y_ref, absref, rel=REL, abs_=ABS, what="y"):
         raise AssertionError(f"{what}: {bad[0].size} elements out of bound; first at {i}: got {y[i]!r} "
                              f"ref {y_ref[i]!r} err {err[i]:.3e} lim {lim[i]:.3e}; worst err/lim {ratio:.3f}")
     return float(np.max(err / lim)) if err.size else 0.0
+
+
+@pytest.fixture(scope="session")
+def qg():
+    """The CUDA library binding, built in-tree first.  GPU tests only."""
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_int4_affine_gb300 import build
+
+    build.build()
+    from moe_int4_affine_gb300 import qg as _qg
+
+    return _qg

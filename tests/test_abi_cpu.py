@@ -1,0 +1,110 @@
+"""The C ABI library builds for sm_103a, loads, exports every entry point include/qg.h declares,
+and rejects bad arguments on the host before touching a GPU.  CPU only: every call below fails
+validation, so no CUDA runtime call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qg.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|void)\s*\**\s*(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from moe_int4_affine_gb300 import build
+
+    return ctypes.CDLL(build.build())
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ["qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
+              "scalar_fma_chain8_residual", "qgemm_int4", "qg_workspace_bytes", "qg_device_status",
+              "qg_strerror", "qg_set_pdl", "qg_version"]:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), f"libqg.so does not export {n}"
+
+
+class W(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
+                ("out", ctypes.c_int32), ("in_", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("n_mat", ctypes.c_int32)]
+
+
+FAKE = 0x10000  # an aligned non-null address; never dereferenced (validation fails first)
+
+
+def _w(**kw):
+    d = dict(packed=FAKE, scales=FAKE, biases=FAKE, out=8, in_=128, group_size=64, n_mat=1)
+    d.update(kw)
+    return W(**d)
+
+
+def test_host_validation_error_codes(lib):
+    P = ctypes.c_void_p
+    lib.qgemv_int4.argtypes = [ctypes.POINTER(W), P, ctypes.c_int, P, P]
+    call = lambda w, x=FAKE, xt=0, y=FAKE: lib.qgemv_int4(ctypes.byref(w), x, xt, y, None)
+    assert call(_w(group_size=32)) == -1
+    assert call(_w(in_=96)) == -1
+    assert call(_w(in_=0)) == -1
+    assert call(_w(out=0)) == -1
+    assert call(_w(n_mat=2)) == -1
+    assert call(_w(packed=None)) == -1
+    assert call(_w(), x=None) == -1
+    assert call(_w(), xt=7) == -1
+    assert call(_w(in_=65536)) == -5
+    assert call(_w(scales=FAKE + 2)) == -2
+    assert call(_w(), x=FAKE + 8) == -2
+    assert call(_w(), y=FAKE + 4) == -2
+    lib.qgemv_int4_multi.argtypes = [ctypes.c_int, ctypes.POINTER(W), P, ctypes.c_int, ctypes.POINTER(P),
+                                     ctypes.c_int, P]
+    ws = (W * 2)(_w(), _w(in_=256))
+    ys = (P * 2)(FAKE, FAKE)
+    assert lib.qgemv_int4_multi(2, ws, FAKE, 0, ys, 0, None) == -1  # mismatched widths
+    ws = (W * 2)(_w(), _w(out=9))
+    assert lib.qgemv_int4_multi(2, ws, FAKE, 0, ys, 1, None) == -1  # swiglu needs equal outs
+    assert lib.qgemv_int4_multi(5, ws, FAKE, 0, ys, 0, None) == -1
+    lib.moe_router_topk.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P]
+    assert lib.moe_router_topk(FAKE, 4, 5, 1, FAKE, FAKE, None) == -1
+    assert lib.moe_router_topk(FAKE, 2048, 8, 1, FAKE, FAKE, None) == -5
+    assert lib.moe_router_topk(FAKE, 128, 8, 2, FAKE, FAKE, None) == -1
+    lib.moe_gather_qgemv_int4.argtypes = [ctypes.POINTER(W)] * 3 + [P, P, ctypes.c_int, P, P, P, P,
+                                                                     ctypes.c_size_t, P]
+    g, u, dn = _w(out=64, in_=128, n_mat=4), _w(out=64, in_=128, n_mat=4), _w(out=128, in_=64, n_mat=4)
+    args = lambda k=8, ws=FAKE, nb=1 << 20, d=dn: (ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), FAKE, FAKE, k,
+                                                   FAKE, FAKE, FAKE, ws, nb, None)
+    assert lib.moe_gather_qgemv_int4(*args(k=9)) == -1
+    assert lib.moe_gather_qgemv_int4(*args(ws=None)) == -3
+    assert lib.moe_gather_qgemv_int4(*args(nb=100)) == -3
+    assert lib.moe_gather_qgemv_int4(*args(d=_w(out=128, in_=128, n_mat=4))) == -1
+    lib.scalar_fma_chain8_residual.argtypes = [P, P, P, P, ctypes.c_int, P]
+    assert lib.scalar_fma_chain8_residual(FAKE, FAKE, FAKE, FAKE, 0, None) == -1
+    assert lib.scalar_fma_chain8_residual(FAKE, FAKE + 4, FAKE, FAKE, 8, None) == -2
+    lib.qgemm_int4.argtypes = [ctypes.POINTER(W), P, ctypes.c_int, P, P, ctypes.c_size_t, P]
+    assert lib.qgemm_int4(ctypes.byref(_w()), FAKE, 0, FAKE, None, 0, None) == -1
+    assert lib.qgemm_int4(ctypes.byref(_w()), FAKE, 5000, FAKE, None, 0, None) == -1
+
+
+def test_workspace_and_strings(lib):
+    lib.qg_workspace_bytes.argtypes = [ctypes.c_int, ctypes.POINTER(W), ctypes.c_int]
+    lib.qg_workspace_bytes.restype = ctypes.c_size_t
+    down = _w(out=2048, in_=768, n_mat=128)
+    assert lib.qg_workspace_bytes(2, ctypes.byref(down), 8) == 8 * 768 * 4
+    assert lib.qg_workspace_bytes(0, ctypes.byref(down), 8) == 0
+    lib.qg_strerror.restype = ctypes.c_char_p
+    assert lib.qg_strerror(-3) == b"workspace missing or too small"
+    assert lib.qg_set_pdl(1) == 0 and lib.qg_set_pdl(0) == 1
+    assert lib.qg_version() >> 16 == 1
