@@ -164,6 +164,15 @@ size_t qg_workspace_bytes(int op, const qg_int4_weight *w, int T_or_k);
  */
 int qg_set_pdl(int enable);
 
+/*
+ * qg_tune_gemv -- override the streaming GEMV planner for sweeps (process-wide, not thread-safe):
+ * x units per lane (1, 2 or 4), row groups (1..8), rows per stage (>= 1) and ring depth (2..8).
+ * 0 keeps the planner's choice for that field; qg_tune_gemv(0, 0, 0, 0) restores the planner.
+ * Returns QG_EINVAL for values outside those ranges; a launch whose plan exceeds the thread or
+ * shared-memory limits returns QG_ENOTSUP.
+ */
+int qg_tune_gemv(int upl, int ngr, int rt, int nstage);
+
 /* Reads the device status word (qg_status_bits) of the current device into *status and clears
  * it.  Synchronises `stream`.  Returns QG_OK or QG_EDEVICE. */
 int qg_device_status(void *stream, uint32_t *status);

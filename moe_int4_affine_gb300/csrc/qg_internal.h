@@ -52,6 +52,7 @@ struct GemvMatArg {
   int out;
 };
 // n matrices sharing x.  pair_swiglu: n == 2, y = silu(W0 x) * (W1 x) written to mats[0].y.
+int gemv_tune(int upl, int ngr, int rt, int nstage);
 int gemv_launch(const GemvMatArg* mats, int n, int pair_swiglu, const void* x, int xt, int in, cudaStream_t stream);
 int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, const uint32_t* idx, int k,
                        const uint16_t* x, float* h, cudaStream_t stream);

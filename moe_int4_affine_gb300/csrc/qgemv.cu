@@ -42,7 +42,6 @@ namespace qg {
 
 constexpr int kRB = 4;  // rows per register batch
 constexpr int kMaxMats = 8;
-constexpr int kMaxThreads = 384;
 
 // A weight operand: base pointers of a (possibly stacked) weight, and the expert slot whose
 // slab to use (-1: the base itself).
@@ -227,8 +226,15 @@ __device__ __forceinline__ float dot_unit(const uint4& wv, const XUnit<XF32>& X)
 // UPL: x units per lane.  XF32: fp32 x.  SBTMA: scales/biases staged by bulk copies (else read
 // from global by the compute lanes).  PAIR: gate/up pairs with SwiGLU.  SEG: segmented rows
 // (MoE down).
+// Thread cap per variant: one x unit per lane leaves room for 19 compute warps (registers capped at
+// 102 per thread); more units per lane need more registers.
+template <int UPL>
+constexpr int max_threads() {
+  return UPL == 1 ? 640 : 384;
+}
+
 template <int UPL, bool XF32, bool SBTMA, bool PAIR, bool SEG>
-__global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
+__global__ void __launch_bounds__(max_threads<UPL>(), 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NC = PAIR ? 2 : 1;  // weight components per row
   const int S = a.nstage;
@@ -471,17 +477,27 @@ struct GemvPlan {
 
 int gcd_int(int x, int y) { return y ? gcd_int(y, x % y) : x; }
 
+struct Tune {
+  int upl, ngr, rt, nstage;
+};
+Tune g_tune = {0, 0, 0, 0};
+
 GemvPlan plan_gemv(int in, int nseg, int total_rows, bool pair, const int* outs, int nmat) {
   const DeviceInfo& dev = device_info();
+  const Tune tn = g_tune;
   GemvPlan p{};
   const int NC = pair ? 2 : 1;
   const int NP = nseg > 1 ? nseg : NC;
   const int units = nseg * in / 32;
-  p.upl = units <= 352 ? 1 : (units <= 704 ? 2 : 4);
+  // x units per lane: one while the row's units fit 19 warps, else two or four
+  p.upl = tn.upl ? tn.upl : (units <= 19 * 32 ? 1 : (units <= 11 * 32 * 2 ? 2 : 4));
   const int lanes = (units + p.upl - 1) / p.upl;
   p.wpg = (lanes + 31) / 32;
-  const int max_w = kMaxThreads / 32 - 1;
-  p.ngr = std::max(1, std::min(8, max_w / p.wpg));
+  const int max_w = (p.upl == 1 ? 640 : 384) / 32 - 1;
+  if (p.wpg > max_w) {
+    p.upl = 4;
+    p.wpg = (units + 127) / 128;
+  }
   // Bulk copies of scales/biases need 16-byte multiples: stage starts and sizes are multiples of
   // q rows, which every matrix's row count must allow.
   const int sb_row = in / 32;
@@ -491,17 +507,29 @@ GemvPlan plan_gemv(int in, int nseg, int total_rows, bool pair, const int* outs,
   if (!p.sbtma) p.q = 1;
   const size_t row_bytes = (size_t)in / 2;
   const size_t vrow_bytes = NP * (row_bytes + 2 * (size_t)sb_row);
-  int rt = (int)std::max<size_t>(1, 20480 / vrow_bytes);
-  const int fill = (total_rows + dev.num_sms - 1) / dev.num_sms;
-  rt = std::min(rt, std::max(1, fill));
-  rt = std::max(p.q, rt / p.q * p.q);
-  p.ngr = std::max(1, std::min(p.ngr, NC * rt));
+  const int rows_per_cta = std::max(1, (total_rows + dev.num_sms - 1) / dev.num_sms);
+  // Row groups: as many as the warp budget allows, but no more than a stage of <= 48 KB can feed
+  // with kRB rows each, and no more than the CTA has rows for.
+  int ngr = std::max(1, std::min(8, (p.upl == 1 ? 640 : 384) / 32 / p.wpg - (p.wpg == 1 ? 1 : 0)));
+  ngr = std::min(ngr, std::max(1, std::min(max_w / p.wpg, 8)));
+  while (ngr > 1 && ((size_t)(ngr * kRB + NC - 1) / NC * vrow_bytes > 49152 ||
+                     (ngr * kRB + NC - 1) / NC > 2 * rows_per_cta))
+    --ngr;
+  if (tn.ngr) ngr = tn.ngr;
+  p.ngr = ngr;
+  int rt = (ngr * kRB + NC - 1) / NC;  // every row group gets kRB work rows per stage
+  rt = std::min(rt, rows_per_cta);
+  if (tn.rt) rt = tn.rt;
+  rt = std::max(p.q, (rt + p.q - 1) / p.q * p.q);
   p.rt = rt;
+  p.ngr = std::max(1, std::min(p.ngr, NC * rt));
   p.slot_bytes = (uint32_t)(rt * NP * row_bytes);
   p.sb_bytes = p.sbtma ? (uint32_t)(rt * NP * sb_row) : 0u;
   const size_t red_bytes = (size_t)rt * NC * p.wpg * 4;
   const size_t slot_all = p.slot_bytes + 2 * (size_t)p.sb_bytes + red_bytes;
-  p.nstage = (int)std::max<size_t>(2, std::min<size_t>(8, 98304 / slot_all));
+  const size_t budget = (size_t)std::min(dev.max_smem_optin, 200 * 1024) - 64;
+  p.nstage = (int)std::max<size_t>(2, std::min<size_t>(8, budget / slot_all));
+  if (tn.nstage) p.nstage = tn.nstage;
   p.smem = p.nstage * slot_all + 16 + 2 * p.nstage * 8;
   const int nq = total_rows / p.q;
   p.grid = std::max(1, std::min(dev.num_sms, (nq * p.q + rt - 1) / rt));
@@ -541,6 +569,7 @@ int finish_and_launch(GemvArgs& a, bool xf32, bool pair, bool seg, cudaStream_t 
   int outs[kMaxMats];
   for (int i = 0; i < a.nmat; ++i) outs[i] = a.mat[i].out;
   const GemvPlan p = plan_gemv(a.in, a.nseg, a.total_rows, pair, outs, a.nmat);
+  if (p.threads > (p.upl == 1 ? 640 : 384) || p.smem > (size_t)device_info().max_smem_optin) return QG_ENOTSUP;
   a.units = a.nseg * a.in / 32;
   a.rt = p.rt;
   a.nstage = p.nstage;
@@ -555,6 +584,13 @@ int finish_and_launch(GemvArgs& a, bool xf32, bool pair, bool seg, cudaStream_t 
 }
 
 }  // namespace
+
+int gemv_tune(int upl, int ngr, int rt, int nstage) {
+  if (upl != 0 && upl != 1 && upl != 2 && upl != 4) return QG_EINVAL;
+  if (ngr < 0 || ngr > 8 || rt < 0 || nstage < 0 || nstage > 8 || nstage == 1) return QG_EINVAL;
+  g_tune = Tune{upl, ngr, rt, nstage};
+  return QG_OK;
+}
 
 int gemv_launch(const GemvMatArg* mats, int n, int pair_swiglu, const void* x, int xt, int in, cudaStream_t stream) {
   if (n < 1 || n > 4 || (pair_swiglu && n != 2)) return QG_EINVAL;

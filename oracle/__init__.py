@@ -115,7 +115,7 @@ def qgemv(packed, scales, biases, x, group_size: int = 64, rows=None, threads: i
     x = np.ascontiguousarray(x)
     in_dim = x.shape[-1]
     out = packed.size // (in_dim // 8)
-    r0, r1 = (0, out) if rows is None else rows
+    r0, r1 = (0, out) if rows is None else (int(rows[0]), int(rows[1]))
     y = np.empty(r1 - r0, dtype=np.float64)
     a = np.empty(r1 - r0, dtype=np.float64)
     xt = _xtype(x)
@@ -177,7 +177,7 @@ def chain_residual(p: np.ndarray, v: np.ndarray, residual: np.ndarray, rows=None
     v = np.ascontiguousarray(v, dtype=np.float32)
     residual = np.ascontiguousarray(residual, dtype=np.uint16)
     K, n = v.shape
-    i0, i1 = (0, n) if rows is None else rows
+    i0, i1 = (0, n) if rows is None else (int(rows[0]), int(rows[1]))
     y = np.empty(i1 - i0, dtype=np.float64)
     a = np.empty(i1 - i0, dtype=np.float64)
     _L().orc_chain_residual(_p(p), K, _p(v), _p(residual), n, i0, i1, _p(y), _p(a))
@@ -212,7 +212,7 @@ def qgemm(packed, scales, biases, X, group_size: int = 64, rows=None, threads: i
     X = np.ascontiguousarray(X, dtype=np.uint16)
     T, in_dim = X.shape
     out = packed.size // (in_dim // 8)
-    r0, r1 = (0, out) if rows is None else rows
+    r0, r1 = (0, out) if rows is None else (int(rows[0]), int(rows[1]))
     if threads <= 1:
         Y = np.empty((T, r1 - r0), dtype=np.float64)
         A = np.empty((T, r1 - r0), dtype=np.float64)
