@@ -57,7 +57,7 @@ int qgemv_int4(const qg_int4_weight* w, const void* x, int xt, float* y, void* s
   if (!x || !y || (xt != QG_X_BF16 && xt != QG_X_F32)) return QG_EINVAL;
   if (!aligned16(x) || !aligned16(y)) return QG_EALIGN;
   GemvMatArg m{w->packed, w->scales, w->biases, y, w->out};
-  return gemv_launch(&m, 1, 0, x, xt, w->in, static_cast<cudaStream_t>(stream));
+  return gemv_dense_launch(&m, 1, x, xt, w->in, static_cast<cudaStream_t>(stream));
 }
 
 int qgemv_int4_multi(int n, const qg_int4_weight* ws, const void* x, int xt, float* const* ys, int epi, void* stream) {
@@ -76,7 +76,9 @@ int qgemv_int4_multi(int n, const qg_int4_weight* ws, const void* x, int xt, flo
     m[i] = GemvMatArg{ws[i].packed, ws[i].scales, ws[i].biases, need_y ? ys[i] : nullptr, ws[i].out};
   }
   if (!aligned16(x)) return QG_EALIGN;
-  return gemv_launch(m, n, epi == QG_EPI_SWIGLU, x, xt, ws[0].in, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (epi == QG_EPI_SWIGLU) return gemv_pair_launch(m[0], m[1], x, xt, ws[0].in, ys[0], s);
+  return gemv_dense_launch(m, n, x, xt, ws[0].in, s);
 }
 
 int moe_router_topk(const float* logits, int n_experts, int k, int renorm, uint32_t* idx, float* p, void* stream) {

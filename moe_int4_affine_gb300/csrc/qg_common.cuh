@@ -88,6 +88,20 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // Allow the next kernel in the stream (if launched with the attribute) to start launching.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ---------------------------------------------------------------- shared-memory loads (32-bit addresses)
+// volatile: these read buffers filled by the async proxy after an mbarrier wait and must not be
+// hoisted above it.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
 // ---------------------------------------------------------------- small numeric helpers
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
@@ -125,16 +139,19 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc)
 }
 
 // ---------------------------------------------------------------- int4 nibble -> f16 codes
-// One u32 word holds codes q0..q7 (q_i in bits 4i..4i+3).  Each nibble is moved to bits 4..7 of
-// a 16-bit half and OR-ed into the exponent pattern 0x6400 (1024.0 in f16), so the half reads
-// 1024 + 16*q exactly (IEEE binary16: the significand's unit in the last place is 1 at 1024).
-// Returned pairs: h[0] = (q0, q4), h[1] = (q1, q5), h[2] = (q2, q6), h[3] = (q3, q7), low half
-// first.
-__device__ __forceinline__ void nibbles_to_f16_magic(uint32_t w, uint32_t h[4]) {
-  h[0] = ((w << 4) & 0x00F000F0u) | 0x64006400u;
-  h[1] = (w & 0x00F000F0u) | 0x64006400u;
-  h[2] = ((w >> 4) & 0x00F000F0u) | 0x64006400u;
-  h[3] = ((w >> 8) & 0x00F000F0u) | 0x64006400u;
+// One u32 word holds codes q0..q7 (q_i in bits 4i..4i+3).  A 16-bit half whose exponent field
+// (bits 10..14) and sign are zero is an IEEE binary16 subnormal worth (bits) * 2^-24, so masking
+// a nibble into bits 0..3 of a half gives exactly q * 2^-24, and into bits 4..7 gives exactly
+// 16 q * 2^-24 -- no implicit leading one, nothing to subtract.  Returned pairs (low half first):
+//   h[0] = (q0, q4) * 2^-24        h[1] = (q1, q5) * 16 * 2^-24
+//   h[2] = (q2, q6) * 2^-24        h[3] = (q3, q7) * 16 * 2^-24
+// The x operand paired with h[1] and h[3] is pre-divided by 16.
+__device__ __forceinline__ void nibbles_to_f16_subnormal(uint32_t w, uint32_t h[4]) {
+  const uint32_t w8 = w >> 8;
+  h[0] = w & 0x000F000Fu;
+  h[1] = w & 0x00F000F0u;
+  h[2] = w8 & 0x000F000Fu;
+  h[3] = w8 & 0x00F000F0u;
 }
 
 }  // namespace qg

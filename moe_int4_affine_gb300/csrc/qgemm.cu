@@ -18,7 +18,7 @@ int qgemm_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, vo
   (void)ws_bytes;
   for (int t = 0; t < T; ++t) {
     GemvMatArg m{w->packed, w->scales, w->biases, Y + (size_t)t * w->out, w->out};
-    const int rc = gemv_launch(&m, 1, 0, X + (size_t)t * w->in, QG_X_BF16, w->in, stream);
+    const int rc = gemv_dense_launch(&m, 1, X + (size_t)t * w->in, QG_X_BF16, w->in, stream);
     if (rc != QG_OK) return rc;
   }
   return QG_OK;
