@@ -19,16 +19,17 @@
 //     split into contiguous ranges, one per CTA; a CTA's rows of one matrix are one contiguous byte
 //     range of packed codes, scales and biases.
 //   * Warp 0 is the producer: lane 0 streams row blocks ("stages") through a shared-memory ring
-//     with 1-D bulk copies (TMA engine, L2 evict-first), several stages ahead.  The same warp
-//     finishes each stage: it sums the compute warps' partial sums in a fixed order
-//     (deterministic), applies the epilogue (SwiGLU / residual) and writes the outputs.
-//   * Compute lanes own fixed 32-column units of x for the whole kernel.  Each unit of x is held
-//     as 16-bit fixed point: X_j = round(x_j * 2^k) with 2^k chosen so the unit's largest |x| is in
+//     with 1-D bulk copies (TMA engine, L2 evict-first), several stages ahead.  Compute warps
+//     hand a ring slot back as soon as its data is in registers.  Warp 1 is the finisher: it sums
+//     each stage's per-warp partial sums in a fixed order (deterministic), applies the epilogue
+//     (SwiGLU / residual) and writes the outputs, off the refill path.
+//   * Compute lanes own fixed 64-column units of x (one quantization group each) for the whole
+//     kernel.  Each unit of x is held as 16-bit fixed point: X_j = round(x_j * 2^k) with 2^k chosen so the unit's largest |x| is in
 //     [2^14, 2^15) (bf16 x: exact for every element within 2^7 of the unit's largest; otherwise
 //     |X_j - x_j 2^k| <= 1/2).
 //   * Unpack + dot: one shift and two ANDs turn a u32 word into eight unsigned byte codes; integer
 //     dp2a instructions accumulate q_j * X_j exactly in int32, two products per instruction.  Per
-//     unit and row the group's scale and bias are applied once in fp32:
+//     group and row the scale and bias are applied once in fp32:
 //        y += s * (acc * 2^-k) + b * sum_j x_j.
 //   * Programmatic dependent launch: weights are streamed before griddepcontrol.wait; x, the router
 //     outputs and all outputs are touched only after it.
@@ -74,10 +75,11 @@ struct GemvArgs {
   int n_experts;
   long long slab_words, slab_groups;  // per-expert strides of stacked weights
   int in;                             // columns of one segment
-  int units;                          // nseg * in / 32
+  int units;                          // nseg * in / 64
   int total_rows;
   int rt;  // rows per stage
   int nstage;
+  int pf;  // stages of L2 prefetch ahead of the ring
   int ngr, wpg;
   int q;                // row alignment quantum of stage starts and sizes
   uint32_t slot_bytes;  // packed bytes per ring slot
@@ -160,81 +162,92 @@ __device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
-// One lane's 32-column unit of x in 16-bit fixed point, paired for dot_words: per 8-column word,
-// p[0] = (X0, X2), p[1] = (X4, X6), p[2] = (X1, X3), p[3] = (X5, X7) (low half first).
+// One lane's 64-column unit of x (one quantization group) in 16-bit fixed point, paired for
+// dot_rows: per 8-column word w, p[w][0] = (X0, X2), p[w][1] = (X4, X6), p[w][2] = (X1, X3),
+// p[w][3] = (X5, X7) (low half first).  Words are stored in the lane's load order: lanes with
+// bit 2 set read the unit's second 16-byte chunk first (that keeps a warp's 16-byte shared-memory
+// loads free of bank conflicts), so for them p[0..3] hold words 4..7 and p[4..7] words 0..3.
 struct XUnit {
-  uint32_t p[4][4];
+  uint32_t p[8][4];
   float sc;  // 2^-k, times the slot weight in seg mode
   float sx;  // sum of the unscaled x values, times the slot weight in seg mode
 };
 
-__device__ __forceinline__ int to_fixed16(float v) { return max(-32767, min(32767, __float2int_rn(v))); }
+// 16-bit fixed point by the magic-number rule: for |t| < 2^22, t + 1.5 * 2^23 rounded to float
+// has the nearest integer to t in its low mantissa bits.
+__device__ __forceinline__ int round_to_int(float v, float scale) {
+  return __float_as_int(fmaf(v, scale, 12582912.0f)) - 0x4B400000;
+}
 
-__device__ __forceinline__ void load_x_unit(const void* xp, bool xf32, int u, float wgt, XUnit& X) {
-  float v[32];
+// The 8 x values of word wd (columns 8 wd .. 8 wd + 7 of the unit), as floats.
+__device__ __forceinline__ void load_x_word(const void* xp, bool xf32, int u, int wd, float (&c)[8]) {
   if (!xf32) {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(xp) + (size_t)u * 32);
+    const uint4 t = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(xp) + (size_t)u * 64) + wd);
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 t = __ldg(p + q);
-      const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[q * 8 + 2 * i] = __uint_as_float(w[i] << 16);
-        v[q * 8 + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-      }
+    for (int i = 0; i < 4; ++i) {
+      c[2 * i] = __uint_as_float(w[i] << 16);
+      c[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
   } else {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(xp) + (size_t)u * 32);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 t = __ldg(p + q);
-      v[4 * q] = t.x;
-      v[4 * q + 1] = t.y;
-      v[4 * q + 2] = t.z;
-      v[4 * q + 3] = t.w;
-    }
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(xp) + (size_t)u * 64) + 2 * wd;
+    const float4 t0 = __ldg(p), t1 = __ldg(p + 1);
+    c[0] = t0.x, c[1] = t0.y, c[2] = t0.z, c[3] = t0.w, c[4] = t1.x, c[5] = t1.y, c[6] = t1.z, c[7] = t1.w;
   }
+}
+
+// Two passes over the unit's 64 values (the second re-reads them from L1): the largest magnitude
+// and the sum, then the 16-bit fixed-point words in the lane's load order.
+__device__ __forceinline__ void load_x_unit(const void* xp, bool xf32, int u, bool swap, float wgt, XUnit& X) {
   float m = 0.f, sx = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    m = fmaxf(m, fabsf(v[i]));
-    sx += v[i];
+  for (int wd = 0; wd < 8; ++wd) {
+    float c[8];
+    load_x_word(xp, xf32, u, wd, c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      m = fmaxf(m, fabsf(c[i]));
+      sx += c[i];
+    }
   }
-  // E = floor(log2 max|x|), k = 14 - E.  Units whose largest |x| is below 2^-60 contribute less
-  // than 1e-17 per weight through the code term and are dropped from it (the bias term keeps the
-  // exact sum).
+  // E = floor(log2 max|x|), k = 14 - E: |x| * 2^k < 2^15.  Units whose largest |x| is below 2^-60
+  // contribute less than 1e-17 per weight through the code term and are dropped from it (the bias
+  // term keeps the exact sum).
   const bool live = m >= 8.673617e-19f;  // 2^-60
   const int E = max((int)((__float_as_uint(m) >> 23) & 0xFF) - 127, -60);
-  const int k = 14 - E;  // in [-113, 74]
-  const float f1 = exp2i(k / 2), f2 = exp2i(k - k / 2);
-  int Xi[32];
+  const float scale = live ? exp2i(14 - E) : 0.f;  // 14 - E in [-113, 74]
 #pragma unroll
-  for (int i = 0; i < 32; ++i) Xi[i] = live ? to_fixed16((v[i] * f1) * f2) : 0;
+  for (int wd = 0; wd < 8; ++wd) {
+    float c[8];
+    load_x_word(xp, xf32, u, swap ? (wd ^ 4) : wd, c);
+    int q[8];
 #pragma unroll
-  for (int wd = 0; wd < 4; ++wd) {
-    const int* c = Xi + wd * 8;
-    X.p[wd][0] = (uint32_t)(c[0] & 0xFFFF) | ((uint32_t)c[2] << 16);
-    X.p[wd][1] = (uint32_t)(c[4] & 0xFFFF) | ((uint32_t)c[6] << 16);
-    X.p[wd][2] = (uint32_t)(c[1] & 0xFFFF) | ((uint32_t)c[3] << 16);
-    X.p[wd][3] = (uint32_t)(c[5] & 0xFFFF) | ((uint32_t)c[7] << 16);
+    for (int i = 0; i < 8; ++i) q[i] = max(-32767, min(32767, round_to_int(c[i], scale)));
+    X.p[wd][0] = (uint32_t)(q[0] & 0xFFFF) | ((uint32_t)q[2] << 16);
+    X.p[wd][1] = (uint32_t)(q[4] & 0xFFFF) | ((uint32_t)q[6] << 16);
+    X.p[wd][2] = (uint32_t)(q[1] & 0xFFFF) | ((uint32_t)q[3] << 16);
+    X.p[wd][3] = (uint32_t)(q[5] & 0xFFFF) | ((uint32_t)q[7] << 16);
   }
   X.sc = live ? exp2i(E - 14) * wgt : 0.f;  // E - 14 in [-74, 113]
   X.sx = sx * wgt;
 }
 
-// For RB rows at once: acc[r] = sum over the 32 codes of row r's 16-byte chunk of q_j * X_j
-// (exact in int32: |acc| <= 32 * 15 * 32767 < 2^24, so the conversion to float is exact too).
+// For RB rows at once: acc[r] = sum over the 64 codes of row r's 32-byte chunk pair of q_j * X_j
+// (exact in int32: |acc| <= 64 * 15 * 32767 < 2^25, and the two partial sums each < 2^24 convert
+// to float exactly).
 template <int RB>
-__device__ __forceinline__ void dot_rows(const uint4 (&wv)[RB], const XUnit& X, float (&acc)[RB]) {
+__device__ __forceinline__ void dot_rows(const uint4 (&wa)[RB], const uint4 (&wb)[RB], const XUnit& X,
+                                         float (&acc)[RB]) {
   int s0[RB], s1[RB];
 #pragma unroll
   for (int r = 0; r < RB; ++r) s0[r] = s1[r] = 0;
 #pragma unroll
-  for (int wd = 0; wd < 4; ++wd) {
+  for (int wd = 0; wd < 8; ++wd) {
 #pragma unroll
     for (int r = 0; r < RB; ++r) {
-      const uint32_t w = wd == 0 ? wv[r].x : wd == 1 ? wv[r].y : wd == 2 ? wv[r].z : wv[r].w;
+      const uint4& c = wd < 4 ? wa[r] : wb[r];
+      const int e = wd & 3;
+      const uint32_t w = e == 0 ? c.x : e == 1 ? c.y : e == 2 ? c.z : c.w;
       const uint32_t c0 = w & 0x0F0F0F0Fu;         // codes q0, q2, q4, q6 as bytes
       const uint32_t c1 = (w >> 4) & 0x0F0F0F0Fu;  // codes q1, q3, q5, q7
       s0[r] = dp2a_lo(X.p[wd][0], c0, s0[r]);
@@ -244,14 +257,14 @@ __device__ __forceinline__ void dot_rows(const uint4 (&wv)[RB], const XUnit& X, 
     }
   }
 #pragma unroll
-  for (int r = 0; r < RB; ++r) acc[r] = __int2float_rn(s0[r] + s1[r]);
+  for (int r = 0; r < RB; ++r) acc[r] = __int2float_rn(s0[r]) + __int2float_rn(s1[r]);
 }
 
 // Threads and minimum CTAs per SM of each variant: every variant leaves room on the SM for one CTA
 // of the next launch, except the 4-units-per-lane variant for very wide rows.
 template <int UPL>
 constexpr int max_threads() {
-  return UPL == 1 ? 384 : 320;
+  return 352;
 }
 template <int UPL>
 constexpr int min_blocks() {
@@ -270,14 +283,17 @@ __global__ void __launch_bounds__(max_threads<UPL>(), min_blocks<UPL>()) gemv_ke
   const uint32_t row_bytes = (uint32_t)a.in / 2;
   const uint32_t sb_row = (uint32_t)a.in / 32;
   const int ngroups = a.in / 64;
-  const int useg = a.in / 32;  // units per segment
+  const int useg = a.in / 64;  // units (64-column groups) per segment
   uint8_t* ring = smem;
   uint8_t* sring = ring + (size_t)S * a.slot_bytes;
   uint8_t* bring = sring + (size_t)S * a.sb_bytes;
   float* red = reinterpret_cast<float*>(bring + (size_t)S * a.sb_bytes);
-  const int red_slot = a.rt * NC * a.wpg;
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + (((size_t)S * red_slot + 3) & ~(size_t)3));
-  uint64_t* empty = full + S;
+  const int red_slot = a.rt * NC * a.wpg;  // partial sums of one stage; R = 2S buffers, round robin
+  const int R = 2 * S;
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + (((size_t)R * red_slot + 3) & ~(size_t)3));
+  uint64_t* empty = full + S;  // ring slot free again (its data has been read into registers)
+  uint64_t* done = empty + S;  // stage's partial sums written (R barriers, one per buffer)
+  uint64_t* freed = done + R;  // stage finished: its partial-sum buffer may be reused (R barriers)
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -287,10 +303,16 @@ __global__ void __launch_bounds__(max_threads<UPL>(), min_blocks<UPL>()) gemv_ke
       mbar_init(full + s, 1);
       mbar_init(empty + s, nw);
     }
+    for (int s = 0; s < R; ++s) {
+      mbar_init(done + s, nw);
+      mbar_init(freed + s, 1);
+    }
     mbar_fence_init();
     s_abort = 0;
-    pdl_trigger();
   }
+  // every thread signals: the next kernel in the stream may launch now (its CTAs take the room each
+  // SM has left beside this one and start streaming their own weights)
+  pdl_trigger();
   __syncthreads();
 
   // CTA row range, aligned to the quantum q (every matrix's row count is a multiple of q when
@@ -301,21 +323,105 @@ __global__ void __launch_bounds__(max_threads<UPL>(), min_blocks<UPL>()) gemv_ke
       blockIdx.x + 1 == gridDim.x ? a.total_rows : (int)((long long)(blockIdx.x + 1) * nq / gridDim.x) * a.q;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer + finisher
+    // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
-    int v = vb, vf = vb, t = 0, tf = 0;
-    bool waited = false;
-    if (a.idx) {  // expert indices come from the preceding kernel: wait before resolving them
-      pdl_wait();
-      waited = true;
+    if (a.idx) pdl_wait();  // expert indices come from the preceding kernel
+    // Byte ranges of stage st, component/segment c (false for a skipped expert).
+    auto ranges = [&](const Stage& st, int c, const uint32_t*& pk, const uint16_t*& sc, const uint16_t*& bi) {
+      bool ok;
+      const WPtr w = resolve(a, SEG ? WRef{a.seg.packed, a.seg.scales, a.seg.biases, c} : a.mat[st.m].w[c], ok);
+      pk = w.packed + (size_t)st.lr * (a.in / 8);
+      sc = w.scales + (size_t)st.lr * ngroups;
+      bi = w.biases + (size_t)st.lr * ngroups;
+      return ok;
+    };
+    // L2 prefetch runs a.pf stages ahead of the shared-memory ring: the ring only has to cover the
+    // L2 -> SM latency while many more bytes are in flight from HBM.
+    int vp = vb, tp = 0;
+    Stage sp;
+    auto prefetch_to = [&](int upto) {
+      while (tp < upto && next_stage(a, vp, ve, sp)) {
+        if (lane < NP) {
+          const uint32_t *pk;
+          const uint16_t *sc, *bi;
+          if (ranges(sp, lane, pk, sc, bi)) {
+            bulk_prefetch_l2(pk, (uint32_t)sp.n * row_bytes);
+            if (SBTMA) {
+              bulk_prefetch_l2(sc, (uint32_t)sp.n * sb_row);
+              bulk_prefetch_l2(bi, (uint32_t)sp.n * sb_row);
+            }
+          }
+        }
+        ++tp;
+      }
+    };
+    prefetch_to(a.pf);
+    int v = vb, t = 0;
+    Stage st;
+    bool ok_run = true;
+    while (next_stage(a, v, ve, st)) {
+      const int slot = t % S;
+      if (t >= S && (!mbar_wait(empty + slot, ((t / S) - 1) & 1) || s_abort)) {
+        ok_run = false;
+        break;
+      }
+      if (t >= R && (!mbar_wait(freed + t % R, ((t / R) - 1) & 1) || s_abort)) {
+        ok_run = false;
+        break;
+      }
+      if (lane == 0) {
+        const uint32_t pbytes = (uint32_t)st.n * row_bytes;
+        const uint32_t sbytes = SBTMA ? (uint32_t)st.n * sb_row : 0u;
+        uint32_t tx = 0;
+        for (int c = 0; c < NP; ++c) {
+          const uint32_t *pk;
+          const uint16_t *sc, *bi;
+          if (ranges(st, c, pk, sc, bi)) tx += pbytes + 2 * sbytes;
+        }
+        if (tx)
+          mbar_arrive_expect_tx(full + slot, tx);
+        else
+          mbar_arrive(full + slot);
+        for (int c = 0; c < NP; ++c) {
+          const uint32_t *pk;
+          const uint16_t *sc, *bi;
+          if (!ranges(st, c, pk, sc, bi)) continue;
+          bulk_g2s_hint(ring + (size_t)slot * a.slot_bytes + (size_t)c * a.rt * row_bytes, pk, pbytes, full + slot, pol);
+          if (SBTMA) {
+            bulk_g2s_hint(sring + (size_t)slot * a.sb_bytes + (size_t)c * a.rt * sb_row, sc, sbytes, full + slot, pol);
+            bulk_g2s_hint(bring + (size_t)slot * a.sb_bytes + (size_t)c * a.rt * sb_row, bi, sbytes, full + slot, pol);
+          }
+        }
+      }
+      __syncwarp();
+      ++t;
+      prefetch_to(t + a.pf);
     }
-    Stage st, sf;
-    auto finish = [&](int slot, const Stage& s) {
-      const float* rs = red + (size_t)slot * red_slot;
-      const GemvMat& mt = a.mat[s.m];
+    if (!ok_run) {
+      s_abort = 1;
+      // a wait gave up: let this CTA's bulk copies land before it exits (bounded waits)
+      for (int j = max(0, t - S); j < t; ++j) mbar_wait(full + j % S, (j / S) & 1);
+    }
+    return;
+  }
+  if (warp == 1) {
+    // ------------------------------------------------------------ finisher
+    // Stage by stage, in order: wait for its partial sums, add them in a fixed order
+    // (deterministic), apply the epilogue, write the outputs, and free the buffer.
+    pdl_wait();  // outputs may be read by the preceding kernel
+    int v = vb, tf = 0;
+    Stage sf;
+    while (next_stage(a, v, ve, sf)) {
+      const int rb = tf % R;
+      if (!mbar_wait(done + rb, (tf / R) & 1) || s_abort) {
+        s_abort = 1;
+        return;
+      }
+      const float* rs = red + (size_t)rb * red_slot;
+      const GemvMat& mt = a.mat[sf.m];
       bool ok = true;
       if (PAIR && mt.w[0].slot >= 0) resolve(a, mt.w[0], ok);
-      for (int i = lane; i < s.n; i += 32) {
+      for (int i = lane; i < sf.n; i += 32) {
         float acc = 0.f;
         for (int w = 0; w < a.wpg; ++w) acc += rs[i * a.wpg + w];
         if (PAIR) {
@@ -323,72 +429,18 @@ __global__ void __launch_bounds__(max_threads<UPL>(), min_blocks<UPL>()) gemv_ke
           for (int w = 0; w < a.wpg; ++w) u += rs[(a.rt + i) * a.wpg + w];
           acc = ok ? acc / (1.f + expf(-acc)) * u : 0.f;
         }
-        if (SEG && a.resid) acc += bf16_bits_to_f32(a.resid[s.lr + i]);
-        mt.y[s.lr + i] = acc;
-      }
-    };
-    while (next_stage(a, v, ve, st)) {
-      const int slot = t % S;
-      if (t >= S) {
-        if (!mbar_wait(empty + slot, ((t / S) - 1) & 1) || s_abort) {
-          s_abort = 1;
-          break;
-        }
-        if (!waited) {
-          pdl_wait();
-          waited = true;
-        }
-        next_stage(a, vf, ve, sf);
-        finish(slot, sf);
-        ++tf;
-        __syncwarp();
-      }
-      if (lane == 0) {
-        const uint32_t pbytes = (uint32_t)st.n * row_bytes;
-        const uint32_t sbytes = SBTMA ? (uint32_t)st.n * sb_row : 0u;
-        WPtr src[kMaxMats];
-        bool ok[kMaxMats];
-        uint32_t tx = 0;
-        for (int c = 0; c < NP; ++c) {
-          src[c] = resolve(a, SEG ? WRef{a.seg.packed, a.seg.scales, a.seg.biases, c} : a.mat[st.m].w[c], ok[c]);
-          if (ok[c]) tx += pbytes + 2 * sbytes;
-        }
-        if (tx)
-          mbar_arrive_expect_tx(full + slot, tx);
-        else
-          mbar_arrive(full + slot);
-        for (int c = 0; c < NP; ++c) {
-          if (!ok[c]) continue;
-          bulk_g2s_hint(ring + (size_t)slot * a.slot_bytes + (size_t)c * a.rt * row_bytes,
-                        src[c].packed + (size_t)st.lr * (a.in / 8), pbytes, full + slot, pol);
-          if (SBTMA) {
-            bulk_g2s_hint(sring + (size_t)slot * a.sb_bytes + (size_t)c * a.rt * sb_row,
-                          src[c].scales + (size_t)st.lr * ngroups, sbytes, full + slot, pol);
-            bulk_g2s_hint(bring + (size_t)slot * a.sb_bytes + (size_t)c * a.rt * sb_row,
-                          src[c].biases + (size_t)st.lr * ngroups, sbytes, full + slot, pol);
-          }
-        }
+        if (SEG && a.resid) acc += bf16_bits_to_f32(a.resid[sf.lr + i]);
+        mt.y[sf.lr + i] = acc;
       }
       __syncwarp();
-      ++t;
-    }
-    if (!s_abort) {
-      if (!waited) pdl_wait();
-      for (; tf < t; ++tf) {
-        const int slot = tf % S;
-        if (!mbar_wait(empty + slot, (tf / S) & 1)) {
-          s_abort = 1;
-          break;
-        }
-        next_stage(a, vf, ve, sf);
-        finish(slot, sf);
-      }
+      if (lane == 0) mbar_arrive(freed + rb);
+      ++tf;
     }
     return;
   }
 
   // -------------------------------------------------------------- compute warps
-  const int w = warp - 1;
+  const int w = warp - 2;
   const int g = w / a.wpg, wig = w % a.wpg;
   int u[UPL];
   bool uv[UPL];
@@ -414,26 +466,32 @@ __global__ void __launch_bounds__(max_threads<UPL>(), min_blocks<UPL>()) gemv_ke
       }
       wgt = __ldg(a.p + s);
     }
-    load_x_unit(a.x, a.xf32 != 0, u[k], wgt, X[k]);
+    load_x_unit(a.x, a.xf32 != 0, u[k], (lane >> 2) & 1, wgt, X[k]);
   }
   if (PAIR && a.idx && blockIdx.x == 0 && w == 0 && lane < a.nmat) {
     if (__ldg(a.idx + lane) >= (uint32_t)a.n_experts) set_status(QG_STATUS_BAD_EXPERT);
   }
-  // per-unit offsets inside a ring slot (seg mode: the segment's block of rows)
+  // per-unit offsets inside a ring slot (seg mode: the segment's block of rows); the lane's two
+  // 16-byte chunks of a row are read in swizzled order (see XUnit)
+  const bool swap = (lane >> 2) & 1;
   uint32_t woff[UPL], soff[UPL];
 #pragma unroll
   for (int k = 0; k < UPL; ++k) {
-    const int sg = SEG ? u[k] / useg : 0;
-    const int lu = SEG ? u[k] - sg * useg : u[k];
-    woff[k] = (uint32_t)sg * a.rt * row_bytes + (uint32_t)lu * 16u;
-    soff[k] = 2u * ((uint32_t)sg * a.rt * ngroups + (uint32_t)(lu >> 1));
+    // lanes past the last unit read (and ignore) the last unit's bytes, so every shared-memory
+    // load stays inside the ring slot
+    const int uc = min(u[k], a.units - 1);
+    const int sg = SEG ? uc / useg : 0;
+    const int lu = SEG ? uc - sg * useg : uc;
+    woff[k] = (uint32_t)sg * a.rt * row_bytes + (uint32_t)lu * 32u;
+    soff[k] = 2u * ((uint32_t)sg * a.rt * ngroups + (uint32_t)lu);
   }
+  const uint32_t off_a = swap ? 16u : 0u, off_b = swap ? 0u : 16u;
   const uint32_t ring_s = smem_u32(ring), sring_s = smem_u32(sring);
   const uint32_t bdelta = (uint32_t)(bring - sring);  // biases sit at a fixed offset from scales
   constexpr int JB = RB / NC;                          // rows per batch (each with NC components)
   const uint32_t srow_bytes = 2u * ngroups;
 
-  int v = vb, slot = 0;
+  int v = vb, slot = 0, t = 0;
   uint32_t phase = 0;
   Stage st;
   while (next_stage(a, v, ve, st)) {
@@ -443,7 +501,8 @@ __global__ void __launch_bounds__(max_threads<UPL>(), min_blocks<UPL>()) gemv_ke
     }
     const uint32_t wbase = ring_s + (uint32_t)slot * a.slot_bytes;
     const uint32_t sbase = sring_s + (uint32_t)slot * a.sb_bytes;
-    float* rs = red + (size_t)slot * red_slot;
+    float* rs = red + (size_t)(t % R) * red_slot;
+    bool released = false;
     for (int j0 = 0; g + a.ngr * j0 < st.n; j0 += JB) {
       // batch entry r: row i = g + ngr * (j0 + r / NC), component r % NC, at slot row
       // (r % NC) * rt + i.  Rows past the stage are clamped to its last row and not stored.
@@ -453,17 +512,19 @@ __global__ void __launch_bounds__(max_threads<UPL>(), min_blocks<UPL>()) gemv_ke
         const int i = min(g + a.ngr * (j0 + r / NC), st.n - 1);
         srow[r] = (uint32_t)((r % NC) * a.rt + i);
       }
+      const bool last_batch = g + a.ngr * (j0 + JB) >= st.n;
       float yp[RB];
 #pragma unroll
       for (int r = 0; r < RB; ++r) yp[r] = 0.f;
 #pragma unroll
       for (int k = 0; k < UPL; ++k) {
-        if (!uv[k]) continue;
-        uint4 wv[RB];
+        uint4 wa[RB], wb[RB];
         float sv[RB], bv[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
-          wv[r] = lds128(wbase + srow[r] * row_bytes + woff[k]);
+          const uint32_t wad = wbase + srow[r] * row_bytes + woff[k];
+          wa[r] = lds128(wad + off_a);  // the lane's first 16-byte chunk in load order
+          wb[r] = lds128(wad + off_b);  // and the other one
           uint32_t sbits, bbits;
           if (SBTMA) {
             const uint32_t sa = sbase + srow[r] * srow_bytes + soff[k];
@@ -474,15 +535,22 @@ __global__ void __launch_bounds__(max_threads<UPL>(), min_blocks<UPL>()) gemv_ke
             const int sg = SEG ? u[k] / useg : 0;
             bool ok;
             const WPtr pw = resolve(a, SEG ? WRef{a.seg.packed, a.seg.scales, a.seg.biases, sg} : a.mat[st.m].w[c], ok);
-            const size_t gi = (size_t)(st.lr + (int)srow[r] - c * a.rt) * ngroups + ((u[k] - sg * useg) >> 1);
-            sbits = ok ? __ldg(pw.scales + gi) : 0u;
-            bbits = ok ? __ldg(pw.biases + gi) : 0u;
+            const size_t gi = (size_t)(st.lr + (int)srow[r] - c * a.rt) * ngroups + (u[k] - sg * useg);
+            sbits = ok && uv[k] ? __ldg(pw.scales + gi) : 0u;
+            bbits = ok && uv[k] ? __ldg(pw.biases + gi) : 0u;
           }
           sv[r] = bf16_bits_to_f32(sbits);
           bv[r] = bf16_bits_to_f32(bbits);
         }
+        if (k == UPL - 1 && last_batch) {
+          // the stage's last data is in registers: hand the ring slot back to the producer
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty + slot);
+          released = true;
+        }
+        if (!uv[k]) continue;
         float acc[RB];
-        dot_rows<RB>(wv, X[k], acc);
+        dot_rows<RB>(wa, wb, X[k], acc);
 #pragma unroll
         for (int r = 0; r < RB; ++r) yp[r] = fmaf(sv[r], acc[r] * X[k].sc, fmaf(bv[r], X[k].sx, yp[r]));
       }
@@ -494,30 +562,34 @@ __global__ void __launch_bounds__(max_threads<UPL>(), min_blocks<UPL>()) gemv_ke
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty + slot);
+    if (lane == 0) {
+      if (!released) mbar_arrive(empty + slot);
+      mbar_arrive(done + t % R);
+    }
     if (++slot == S) {
       slot = 0;
       phase ^= 1u;
     }
+    ++t;
   }
 }
 
 // ------------------------------------------------------------------ host side: planning
 struct GemvPlan {
-  int upl, rb, ngr, wpg, rt, nstage, grid, threads, q;
+  int upl, rb, ngr, wpg, rt, nstage, pf, grid, threads, q;
   bool sbtma;
   size_t smem;
   uint32_t slot_bytes, sb_bytes;
 };
 
 struct GemvTune {
-  int upl, ngr, rt, nstage;
+  int upl, ngr, rt, nstage, cps, pf;
 };
 extern GemvTune g_gemv_tune;
 
 inline int gcd_int(int x, int y) { return y ? gcd_int(y, x % y) : x; }
 
-inline int plan_max_threads(int upl) { return upl == 1 ? 384 : 320; }
+inline int plan_max_threads(int upl) { return 352; }
 
 // Shared memory per CTA is kept under half an SM so one CTA of the next launch fits beside it.
 constexpr size_t kSmemBudget = 104 * 1024;
@@ -528,11 +600,11 @@ inline GemvPlan plan_gemv(int in, int nseg, int total_rows, bool pair, const int
   GemvPlan p{};
   const int NC = pair ? 2 : 1;
   const int NP = nseg > 1 ? nseg : NC;
-  const int units = nseg * in / 32;
+  const int units = nseg * in / 64;
   p.upl = tn.upl ? tn.upl : (units <= 11 * 32 ? 1 : (units <= 9 * 32 * 2 ? 2 : 4));
   const int lanes = (units + p.upl - 1) / p.upl;
   p.wpg = (lanes + 31) / 32;
-  const int max_w = plan_max_threads(p.upl) / 32 - 1;
+  const int max_w = plan_max_threads(p.upl) / 32 - 2;  // minus the producer and finisher warps
   // Bulk copies of scales/biases need 16-byte multiples: stage starts and sizes are multiples of
   // q rows, which every matrix's row count must allow.
   const int sb_row = in / 32;
@@ -542,10 +614,13 @@ inline GemvPlan plan_gemv(int in, int nseg, int total_rows, bool pair, const int
   if (!p.sbtma) p.q = 1;
   const size_t row_bytes = (size_t)in / 2;
   const size_t vrow_bytes = NP * (row_bytes + 2 * (size_t)sb_row);
-  const int rows_per_cta = std::max(1, (total_rows + dev.num_sms - 1) / dev.num_sms);
+  // CTAs per SM: two when the rows allow, so each SM runs twice the warps (each CTA keeps under
+  // half an SM, which also lets the next launch's CTAs start as these finish).
+  int cps = tn.cps ? tn.cps : 1;
+  const int ctas = cps * dev.num_sms;
+  const int rows_per_cta = std::max(1, (total_rows + ctas - 1) / ctas);
   // Rows per register batch: 4, or 2 when four rows of this width make a stage above 24 KB.
-  p.rb = (4 / NC * vrow_bytes > 24576) ? 2 : 4;
-  if (pair) p.rb = 4;
+  p.rb = 2;
   // Row groups: as many as the warp budget allows, no more than a stage of <= 24 KB feeds with one
   // batch each, and no more than the CTA has rows for.
   int ngr = std::max(1, std::min(8, max_w / std::max(1, p.wpg)));
@@ -559,15 +634,19 @@ inline GemvPlan plan_gemv(int in, int nseg, int total_rows, bool pair, const int
   p.rt = rt;
   p.slot_bytes = (uint32_t)(rt * NP * row_bytes);
   p.sb_bytes = p.sbtma ? (uint32_t)(rt * NP * sb_row) : 0u;
-  const size_t red_bytes = (size_t)rt * NC * p.wpg * 4;
+  const size_t red_bytes = 2 * (size_t)rt * NC * p.wpg * 4;  // two partial-sum buffers per ring slot
   const size_t slot_all = p.slot_bytes + 2 * (size_t)p.sb_bytes + red_bytes;
   p.nstage = (int)std::max<size_t>(2, std::min<size_t>(8, kSmemBudget / slot_all));
   if (tn.nstage) p.nstage = tn.nstage;
-  p.smem = p.nstage * slot_all + 16 + 2 * p.nstage * 8;
+  // L2 prefetch depth: about 384 KB of each CTA's stream beyond the ring (all of it for smaller
+  // problems), so HBM sees several MB of outstanding reads per launch.
+  p.pf = p.nstage + (int)std::max<size_t>(1, (384 * 1024) / (p.slot_bytes + 2 * (size_t)p.sb_bytes));
+  if (tn.pf) p.pf = p.nstage + tn.pf;
+  p.smem = p.nstage * slot_all + 16 + 6 * p.nstage * 8;
   const int nq = total_rows / p.q;
-  p.grid = std::max(1, std::min(dev.num_sms, (nq * p.q + rt - 1) / rt));
+  p.grid = std::max(1, std::min(ctas, (nq * p.q + rt - 1) / rt));
   p.grid = std::min(p.grid, std::max(1, nq));
-  p.threads = 32 * (1 + p.ngr * p.wpg);
+  p.threads = 32 * (2 + p.ngr * p.wpg);
   return p;
 }
 
@@ -585,20 +664,14 @@ int launch_gemv_variant(const GemvArgs& a, const GemvPlan& p, cudaStream_t strea
 
 template <int MODE>
 int dispatch_gemv(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
-  const int key = (p.upl == 1 ? 0 : p.upl == 2 ? 1 : 2) * 4 + (p.rb == 4 ? 2 : 0) + (p.sbtma ? 1 : 0);
+  const int key = (p.upl == 1 ? 0 : p.upl == 2 ? 1 : 2) * 2 + (p.sbtma ? 1 : 0);
   switch (key) {
     case 0: return launch_gemv_variant<1, 2, false, MODE>(a, p, s);
     case 1: return launch_gemv_variant<1, 2, true, MODE>(a, p, s);
-    case 2: return launch_gemv_variant<1, 4, false, MODE>(a, p, s);
-    case 3: return launch_gemv_variant<1, 4, true, MODE>(a, p, s);
-    case 4: return launch_gemv_variant<2, 2, false, MODE>(a, p, s);
-    case 5: return launch_gemv_variant<2, 2, true, MODE>(a, p, s);
-    case 6: return launch_gemv_variant<2, 4, false, MODE>(a, p, s);
-    case 7: return launch_gemv_variant<2, 4, true, MODE>(a, p, s);
-    case 8: return launch_gemv_variant<4, 2, false, MODE>(a, p, s);
-    case 9: return launch_gemv_variant<4, 2, true, MODE>(a, p, s);
-    case 10: return launch_gemv_variant<4, 4, false, MODE>(a, p, s);
-    default: return launch_gemv_variant<4, 4, true, MODE>(a, p, s);
+    case 2: return launch_gemv_variant<2, 2, false, MODE>(a, p, s);
+    case 3: return launch_gemv_variant<2, 2, true, MODE>(a, p, s);
+    case 4: return launch_gemv_variant<4, 2, false, MODE>(a, p, s);
+    default: return launch_gemv_variant<4, 2, true, MODE>(a, p, s);
   }
 }
 
@@ -609,9 +682,10 @@ int plan_and_launch(GemvArgs& a, cudaStream_t stream) {
   for (int i = 0; i < a.nmat; ++i) outs[i] = a.mat[i].out;
   const GemvPlan p = plan_gemv(a.in, a.nseg, a.total_rows, MODE == kPair, outs, a.nmat);
   if (p.threads > plan_max_threads(p.upl) || p.smem > (size_t)device_info().max_smem_optin) return QG_ENOTSUP;
-  a.units = a.nseg * a.in / 32;
+  a.units = a.nseg * a.in / 64;
   a.rt = p.rt;
   a.nstage = p.nstage;
+  a.pf = p.pf;
   a.ngr = p.ngr;
   a.wpg = p.wpg;
   a.q = p.q;
