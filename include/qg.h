@@ -165,14 +165,10 @@ size_t qg_workspace_bytes(int op, const qg_int4_weight *w, int T_or_k);
 int qg_set_pdl(int enable);
 
 /*
- * qg_tune_gemv -- override the streaming GEMV planner for sweeps (process-wide, not thread-safe):
- * x units per lane (1, 2 or 4), row groups (1..8), rows per stage (>= 1), ring depth (2..8), CTAs
- * per SM (1 or 2) and L2-prefetch stages beyond the ring (>= 1).  0 keeps the planner's choice for
- * that field; qg_tune_gemv(0, 0, 0, 0, 0, 0) restores the planner.
- * Returns QG_EINVAL for values outside those ranges; a launch whose plan exceeds the thread or
- * shared-memory limits returns QG_ENOTSUP.
+ * qg_tune_gemv -- CTAs per SM of the streaming GEMV kernels (1..4; 0 restores the default, 1), for
+ * sweeps.  Process-wide, not thread-safe.  Returns QG_EINVAL outside that range.
  */
-int qg_tune_gemv(int upl, int ngr, int rt, int nstage, int cps, int pf);
+int qg_tune_gemv(int ctas_per_sm);
 
 /* Reads the device status word (qg_status_bits) of the current device into *status and clears
  * it.  Synchronises `stream`.  Returns QG_OK or QG_EDEVICE. */

@@ -143,7 +143,7 @@ size_t qg_workspace_bytes(int op, const qg_int4_weight* w, int T_or_k) {
 
 int qg_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
-int qg_tune_gemv(int upl, int ngr, int rt, int nstage, int cps, int pf) { return gemv_tune(upl, ngr, rt, nstage, cps, pf); }
+int qg_tune_gemv(int ctas_per_sm) { return gemv_tune(ctas_per_sm); }
 
 int qg_device_status(void* stream, uint32_t* status) {
   if (!status) return QG_EINVAL;

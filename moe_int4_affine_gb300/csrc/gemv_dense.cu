@@ -4,12 +4,11 @@
 
 namespace qg {
 
-GemvTune g_gemv_tune = {0, 0, 0, 0, 0, 0};
+GemvTune g_gemv_tune = {0};
 
-int gemv_tune(int upl, int ngr, int rt, int nstage, int cps, int pf) {
-  if (upl != 0 && upl != 1 && upl != 2 && upl != 4) return QG_EINVAL;
-  if (ngr < 0 || ngr > 8 || rt < 0 || nstage < 0 || nstage > 8 || nstage == 1 || cps < 0 || cps > 2 || pf < 0) return QG_EINVAL;
-  g_gemv_tune = GemvTune{upl, ngr, rt, nstage, cps, pf};
+int gemv_tune(int ctas_per_sm) {
+  if (ctas_per_sm < 0 || ctas_per_sm > 4) return QG_EINVAL;
+  g_gemv_tune = GemvTune{ctas_per_sm};
   return QG_OK;
 }
 

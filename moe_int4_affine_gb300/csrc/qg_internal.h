@@ -56,7 +56,7 @@ int gemv_dense_launch(const GemvMatArg* mats, int n, const void* x, int xt, int 
 // h = silu(gate x) * (up x)
 int gemv_pair_launch(const GemvMatArg& gate, const GemvMatArg& up, const void* x, int xt, int in, float* h,
                      cudaStream_t stream);
-int gemv_tune(int upl, int ngr, int rt, int nstage, int cps, int pf);
+int gemv_tune(int ctas_per_sm);
 int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, const uint32_t* idx, int k,
                        const uint16_t* x, float* h, cudaStream_t stream);
 int moe_down_launch(const qg_int4_weight* down, const uint32_t* idx, const float* p, int k, const float* h,

@@ -44,7 +44,7 @@ lib.qgemm_int4.argtypes = [_W, _P, _I, _P, _P, ctypes.c_size_t, _P]
 lib.qg_workspace_bytes.argtypes = [_I, _W, _I]
 lib.qg_workspace_bytes.restype = ctypes.c_size_t
 lib.qg_set_pdl.argtypes = [_I]
-lib.qg_tune_gemv.argtypes = [_I, _I, _I, _I, _I, _I]
+lib.qg_tune_gemv.argtypes = [_I]
 lib.qg_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
 lib.qg_strerror.argtypes = [_I]
 lib.qg_strerror.restype = ctypes.c_char_p
@@ -223,8 +223,8 @@ def qg_set_pdl(enable: bool) -> bool:
     return bool(lib.qg_set_pdl(1 if enable else 0))
 
 
-def qg_tune_gemv(upl: int = 0, ngr: int = 0, rt: int = 0, nstage: int = 0, cps: int = 0, pf: int = 0) -> None:
-    _check(lib.qg_tune_gemv(upl, ngr, rt, nstage, cps, pf), "qg_tune_gemv")
+def qg_tune_gemv(ctas_per_sm: int = 0) -> None:
+    _check(lib.qg_tune_gemv(ctas_per_sm), "qg_tune_gemv")
 
 
 def qg_device_status(stream=None) -> int:
