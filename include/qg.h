@@ -126,6 +126,28 @@ int moe_gather_qgemv_int4(const qg_int4_weight *gate, const qg_int4_weight *up, 
                           float *y, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * moe_gather_qgemv_int4_noalloc -- the same computation, arguments and limits as
+ * moe_gather_qgemv_int4, without a workspace argument.  The pages have no counterpart: this entry
+ * point exists for callers that cannot hand over device scratch, such as a host runtime that owns
+ * all device memory and allows no new allocation once it serves requests, or a decode loop that
+ * cannot afford the device-wide synchronisation that allocating and freeing memory implies.
+ *
+ * The activations h[k][inter] go to a fixed array compiled into the library (one per device,
+ * QG_NOALLOC_MOE_MAX_FLOATS fp32 values = 128 KB, kept until the process exits).  No call allocates
+ * or frees device memory.  The first call on a device looks up that array's device address (with
+ * the device current) and caches it: make it before any stream capture on that device.
+ * Every element of h the call reads is written earlier in the same call, so nothing needs clearing.
+ * Returns QG_ENOTSUP when k * down->in exceeds QG_NOALLOC_MOE_MAX_FLOATS (inter up to 4096 at
+ * k = 8), QG_EDEVICE if the address lookup fails, otherwise what moe_gather_qgemv_int4 returns.
+ * All calls on a device share the one array: two calls that may overlap in time (on different
+ * streams, or from different host threads without ordering) race on it and give wrong results.
+ */
+#define QG_NOALLOC_MOE_MAX_FLOATS 32768
+int moe_gather_qgemv_int4_noalloc(const qg_int4_weight *gate, const qg_int4_weight *up,
+                                  const qg_int4_weight *down, const uint32_t *idx, const float *p, int k,
+                                  const uint16_t *x, const uint16_t *residual, float *y, void *stream);
+
+/*
  * scalar_fma_chain8_residual -- eight (scalar, vector) pairs accumulated in one pass with the
  * residual folded in ([FFAI#14] scalar-FMA commit: "scalarFMAChain8 ... exact 8-way fused
  * dispatch", "out[i] = base[i] + scalar[0] * value[i]"; "post-MoE residual add folded in"):

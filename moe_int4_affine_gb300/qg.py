@@ -24,6 +24,7 @@ QG_STATUS_BAD_EXPERT, QG_STATUS_TIMEOUT = 1, 2
 QG_X_BF16, QG_X_F32 = 0, 1
 QG_EPI_NONE, QG_EPI_SWIGLU = 0, 1
 QG_OP_QGEMV, QG_OP_MULTI, QG_OP_MOE, QG_OP_QGEMM = 0, 1, 2, 3
+QG_NOALLOC_MOE_MAX_FLOATS = 32768
 
 
 class qg_int4_weight(ctypes.Structure):
@@ -39,6 +40,7 @@ lib.qgemv_int4.argtypes = [_W, _P, _I, _P, _P]
 lib.qgemv_int4_multi.argtypes = [_I, _W, _P, _I, ctypes.POINTER(_P), _I, _P]
 lib.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
 lib.moe_gather_qgemv_int4.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]
+lib.moe_gather_qgemv_int4_noalloc.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P]
 lib.scalar_fma_chain8_residual.argtypes = [_P, _P, _P, _P, _I, _P]
 lib.qgemm_int4.argtypes = [_W, _P, _I, _P, _P, ctypes.c_size_t, _P]
 lib.qg_workspace_bytes.argtypes = [_I, _W, _I]
@@ -50,6 +52,7 @@ lib.qg_strerror.argtypes = [_I]
 lib.qg_strerror.restype = ctypes.c_char_p
 lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
+           "moe_gather_qgemv_int4_noalloc",
            "scalar_fma_chain8_residual", "qgemm_int4", "qg_set_pdl", "qg_tune_gemv", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
 
@@ -192,6 +195,17 @@ def moe_gather_qgemv_int4(gate: Int4Weight, up: Int4Weight, down: Int4Weight, id
                                      _ptr(idx), _ptr(p), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_gather_qgemv_int4")
+    return y
+
+
+def moe_gather_qgemv_int4_noalloc(gate: Int4Weight, up: Int4Weight, down: Int4Weight, idx, p, x, residual, y,
+                                  stream=None):
+    """moe_gather_qgemv_int4 with the library's fixed scratch; `y` must be supplied (nothing is
+    allocated on this path)."""
+    _check(lib.moe_gather_qgemv_int4_noalloc(ctypes.byref(gate.struct), ctypes.byref(up.struct),
+                                             ctypes.byref(down.struct), _ptr(idx), _ptr(p), idx.numel(), _ptr(x),
+                                             _ptr(residual), _ptr(y), _stream(stream)),
+           "moe_gather_qgemv_int4_noalloc")
     return y
 
 
