@@ -14,8 +14,8 @@
 //
 // Design (GB300, sm_103a)
 //   * Persistent grid, one CTA of 16 warps per SM.  A CTA owns a contiguous range of rows (one contiguous
-//     byte range of codes per matrix) and first asks L2 to prefetch its codes (bulk prefetch, no
-//     shared memory involved), so HBM sees the whole stream at once.
+//     byte range of codes per matrix).  (An L2 bulk prefetch of the CTA's whole range at kernel start
+//     was measured slower: the flood of prefetch requests queued the x and code loads behind it.)
 //   * x is read once per CTA and stored in shared memory as 16-bit fixed point per 64-column group
 //     g: X_j = round(x_j * 2^k_g) with 2^k_g putting the group's largest |x| in [2^14, 2^15) (bf16
 //     x: exact for every element within 2^7 of the group's largest; else |X_j - x_j 2^k_g| <= 1/2).
@@ -29,8 +29,8 @@
 //     and row the scale and bias are applied once in fp32:  y += s * (acc * 2^-k_g) + b * sum_g x.
 //   * Each unit's row sums go to shared memory; after a CTA barrier they are added in a fixed
 //     order (deterministic), the epilogue (SwiGLU / residual) applied and the outputs written.
-//   * Programmatic dependent launch: codes are prefetched and the first unit's codes loaded before
-//     griddepcontrol.wait; x, router outputs and all outputs are touched only after it.
+//   * Programmatic dependent launch: the first unit's codes are loaded before griddepcontrol.wait;
+//     x, router outputs and all outputs are touched only after it.
 #pragma once
 #include <algorithm>
 #include <atomic>
@@ -198,18 +198,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const int nkc = (G + kGroupsPerUnit - 1) / kGroupsPerUnit;  // K chunks per row
 
   pdl_trigger();
-
-  // --- L2 prefetch of the CTA's codes (dense and pair: the pointers are known before the wait) ---
-  if (warp == 0 && !a.idx) {
-    for (int m = 0; m < a.nmat; ++m) {
-      const int lo = max(vb, a.mat[m].row0), hi = min(ve, a.mat[m].row0 + a.mat[m].out);
-      if (lo >= hi || lane >= NC) continue;
-      const uint8_t* pk = reinterpret_cast<const uint8_t*>(a.mat[m].w[lane].packed) +
-                          (size_t)(lo - a.mat[m].row0) * row_bytes;
-      const size_t pb = (size_t)(hi - lo) * row_bytes;
-      for (size_t o = 0; o < pb; o += 65536) bulk_prefetch_l2(pk + o, (uint32_t)min((size_t)65536, pb - o));
-    }
-  }
 
   int nblocks = 0;
   for (int mi = 0; mi < a.nmat; ++mi) {
