@@ -192,6 +192,13 @@ int qg_set_pdl(int enable);
  */
 int qg_tune_gemv(int ctas_per_sm);
 
+/*
+ * qg_tune_qgemm -- smallest T that qgemm_int4 runs on the tensor cores (1..4096; 0 restores the
+ * default, 32); smaller T runs the CUDA-core GEMV once per token row.  Process-wide, not thread-safe;
+ * query qg_workspace_bytes(QG_OP_QGEMM, ...) after changing it.  Returns QG_EINVAL outside that range.
+ */
+int qg_tune_qgemm(int tc_min_T);
+
 /* Reads the device status word (qg_status_bits) of the current device into *status and clears
  * it.  Synchronises `stream`.  Returns QG_OK or QG_EDEVICE. */
 int qg_device_status(void *stream, uint32_t *status);

@@ -145,6 +145,8 @@ int qg_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
 int qg_tune_gemv(int ctas_per_sm) { return gemv_tune(ctas_per_sm); }
 
+int qg_tune_qgemm(int tc_min_T) { return qgemm_tune(tc_min_T); }
+
 int qg_device_status(void* stream, uint32_t* status) {
   if (!status) return QG_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -188,7 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   constexpr int NW = kThreads / 32;
   const int G = a.groups;
   const int ngs = a.in / 64;  // groups per segment
-  const uint32_t row_bytes = (uint32_t)a.in / 2;
   uint32_t* xq = reinterpret_cast<uint32_t*>(smem);               // [G][32]
   float2* gsx = reinterpret_cast<float2*>(smem + (size_t)G * 128);  // [G]
   float* part = reinterpret_cast<float*>(smem + (size_t)G * 136);   // [rows][NC][nkc]

@@ -36,16 +36,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// The suspend-time hint lets the hardware park the waiting thread (no instruction issue) until the
-// phase completes or about a microsecond passes.
+// Non-blocking test of the phase with the given parity (no suspend-time hint: with one, the wait was
+// measured to sleep far past the phase's completion).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -114,51 +114,5 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __ui
 
 // 2^e as a float for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
-
-// Pack two floats into f16x2 (round to nearest even), lo in bits 0..15.
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
-  float f;
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.f32.f16 %0, a;\n\t}" : "=f"(f) : "r"(h2));
-  return f;
-}
-__device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) {
-  float f;
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.f32.f16 %0, b;\n\t}" : "=f"(f) : "r"(h2));
-  return f;
-}
-
-// acc += a.lo * b.lo + a.hi * b.hi with f16 operands and an fp32 accumulator (sm_100+ mixed
-// precision FMA: the f16 x f16 product is exact in fp32, one rounding per add).
-__device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc) {
-  asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
-      "mov.b32 {a0, a1}, %1;\n\t"
-      "mov.b32 {b0, b1}, %2;\n\t"
-      "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
-      "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(a), "r"(b));
-  return acc;
-}
-
-// ---------------------------------------------------------------- int4 nibble -> f16 codes
-// One u32 word holds codes q0..q7 (q_i in bits 4i..4i+3).  A 16-bit half whose exponent field
-// (bits 10..14) and sign are zero is an IEEE binary16 subnormal worth (bits) * 2^-24, so masking
-// a nibble into bits 0..3 of a half gives exactly q * 2^-24, and into bits 4..7 gives exactly
-// 16 q * 2^-24 -- no implicit leading one, nothing to subtract.  Returned pairs (low half first):
-//   h[0] = (q0, q4) * 2^-24        h[1] = (q1, q5) * 16 * 2^-24
-//   h[2] = (q2, q6) * 2^-24        h[3] = (q3, q7) * 16 * 2^-24
-// The x operand paired with h[1] and h[3] is pre-divided by 16.
-__device__ __forceinline__ void nibbles_to_f16_subnormal(uint32_t w, uint32_t h[4]) {
-  const uint32_t w8 = w >> 8;
-  h[0] = w & 0x000F000Fu;
-  h[1] = w & 0x00F000F0u;
-  h[2] = w8 & 0x000F000Fu;
-  h[3] = w8 & 0x00F000F0u;
-}
 
 }  // namespace qg

@@ -71,5 +71,10 @@ int chain8_launch(const float* p, const float* v, const uint16_t* residual, floa
 size_t qgemm_workspace_bytes(const qg_int4_weight* w, int T);
 int qgemm_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void* ws, size_t ws_bytes,
                  cudaStream_t stream);
+int qgemm_tune(int tc_min_T);
+// tensor-core path (qgemm_tc.cu)
+size_t qgemm_tc_workspace_bytes(const qg_int4_weight* w, int T);
+int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void* ws, size_t ws_bytes,
+                    cudaStream_t stream);
 
 }  // namespace qg

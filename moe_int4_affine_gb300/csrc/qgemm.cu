@@ -1,21 +1,28 @@
-// qgemm.cu -- dequant-GEMM for T token rows ([FFAI#9] "Ops.dequantGemmDynamicM").
+// qgemm.cu -- dequant-GEMM for T token rows ([FFAI#9] "Ops.dequantGemmDynamicM"):
 //   Y[t][r] = sum_j w[r][j] * X[t][j]
-// CUDA-core path: one streaming GEMV pass per token row (the weights are re-read per row).
+// Dispatch: T >= the tensor-core threshold (32 unless tuned) runs the tcgen05 kernel of qgemm_tc.cu
+// (the tokens padded to a multiple of 16 inside the kernel's tiles); smaller T runs the streaming
+// CUDA-core GEMV once per token row.
 #include "qg_common.cuh"
 #include "qg_internal.h"
 
 namespace qg {
 
+static int g_tc_min_T = 32;
+
+int qgemm_tune(int tc_min_T) {
+  if (tc_min_T < 0 || tc_min_T > 4096) return QG_EINVAL;
+  g_tc_min_T = tc_min_T ? tc_min_T : 32;
+  return QG_OK;
+}
+
 size_t qgemm_workspace_bytes(const qg_int4_weight* w, int T) {
-  (void)w;
-  (void)T;
-  return 0;
+  return T >= g_tc_min_T ? qgemm_tc_workspace_bytes(w, T) : 0;
 }
 
 int qgemm_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void* ws, size_t ws_bytes,
                  cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
+  if (T >= g_tc_min_T) return qgemm_tc_launch(w, X, T, Y, ws, ws_bytes, stream);
   for (int t = 0; t < T; ++t) {
     GemvMatArg m{w->packed, w->scales, w->biases, Y + (size_t)t * w->out, w->out};
     const int rc = gemv_dense_launch(&m, 1, X + (size_t)t * w->in, QG_X_BF16, w->in, stream);

@@ -1,0 +1,443 @@
+// qgemm_tc.cu -- tensor-core dequant-GEMM for T token rows ([FFAI#9] "Ops.dequantGemmDynamicM"):
+//   Y[t][r] = sum_j w[r][j] * X[t][j],   w[r][j] = scale[r][j/64] * q[r][j] + bias[r][j/64]
+// on the 5th-generation tensor cores (tcgen05.mma, accumulator in tensor memory), sm_103a.
+//
+// Work split: one CTA per (128 weight rows, n_tile tokens) tile; the MMA is D[128 x n_tile] +=
+// A[128 x 16] * B[n_tile x 16]^T with A = the dequantized weights and B = the tokens, both fp16 and
+// K-major in shared memory with the 128-byte swizzle, D fp32 in tensor memory.
+//   * A pipeline stage covers two 64-column quantization groups.  Producer warps (8; thread = one
+//     weight row and one of the stage's two groups) stream the packed codes, scales and biases
+//     through a per-thread cp.async ring (WRING stages ahead), dequantize their 64 weights with
+//     packed half-precision arithmetic (w = s * q + b, one rounding to fp16) and store them into the
+//     stage's A tile (one 16 KB swizzle atom per group).
+//   * The token tile of a stage is one contiguous block of the workspace (written there, already
+//     swizzled, by the prep kernel) and arrives by a single bulk copy (TMA engine) on the stage's
+//     mbarrier.
+//   * One thread of the MMA warp issues eight K=16 MMAs per stage and commits them to the stage's
+//     "empty" mbarrier; a final commit releases the epilogue, which reads the accumulator from tensor
+//     memory (tcgen05.ld), applies each token's power-of-two input scale and writes Y.
+//   * Every mbarrier wait is bounded (2 s): on a timeout the CTA records QG_STATUS_TIMEOUT, stops
+//     issuing, drains what it has in flight and frees its tensor memory before returning.
+//
+// Numerics: each token row of X is scaled by a power of two 2^(14 - e_t) (e_t = floor(log2 max|x_t|))
+// so that it sits in fp16's range, then rounded to fp16 (exact for bf16 inputs within 2^10 of the
+// row's largest magnitude); the weights are rounded to fp16 once (relative error <= 2^-11); products
+// accumulate in fp32.  |y - y_exact| <= (2^-11 + 2^-11 + K 2^-23) * sum |w x| roughly, below the
+// 1e-3 * sum |w x| acceptance bound.  Scales and biases must lie within fp16's range (|w| < 65504).
+#include <algorithm>
+
+#include "qg_common.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+namespace {
+
+constexpr int kBM = 128;                     // weight rows per CTA (MMA M)
+constexpr int kGK = 64;                      // columns of one quantization group (one swizzle atom)
+constexpr int kGroupsPerStage = 2;           // K per pipeline stage: two groups
+constexpr int kMaxN = 256;                   // tokens per CTA (MMA N, tensor-memory columns)
+constexpr int kProducerWarps = 8;            // two threads per weight row
+constexpr int kProducers = kProducerWarps * 32;
+constexpr int kThreads = kProducers + 32;    // + the MMA / tensor-memory warp
+constexpr int kAtom = kBM * kGK * 2;         // 16 KB of fp16: 128 rows x one group
+constexpr int kATile = kAtom * kGroupsPerStage;
+// weight ring, per stage: codes [2 chunks][256 threads][16 B], then scale and bias words [256][8 B]
+constexpr int kWStageBytes = kProducers * 32 + kProducers * 8;
+constexpr int kSmemBudget = 220 * 1024;
+
+struct TcArgs {
+  const uint32_t* packed;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const uint8_t* xt;  // token tiles: [n_tiles][k groups][n_tile][128 B], swizzled, fp16
+  const float* xs;    // [n_tiles * n_tile] per-token output scale
+  float* y;           // [T][out]
+  int out, in, T;
+  int n_tile;
+  int stages;
+  int tmem_cols;
+  uint32_t idesc;
+};
+
+// ---------------------------------------------------------------- tcgen05 / async helpers
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand with the 128-byte swizzle, 8-row groups 1024 bytes
+// apart (stride byte offset), descriptor version 1, swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading byte offset (not used by swizzled K-major layouts)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+  d |= (uint64_t)1 << 46;              // version
+  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp4(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+// fp16x2 arithmetic on raw bits
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// bf16 bits (low 16 of v) -> fp16, in both halves
+__device__ __forceinline__ uint32_t bf16_to_f16x2(uint32_t v) {
+  const float f = __uint_as_float(v << 16);
+  uint32_t h;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.f16.f32 t, %1;\n\tmov.b32 %0, {t, t};\n\t}" : "=r"(h) : "f"(f));
+  return h;
+}
+
+// Eight codes of one u32 word (low nibble first) -> four fp16x2 words of w = s * q + b in the order
+// (q0, q4), (q1, q5), (q2, q6), (q3, q7).  1024 + q is exact as the fp16 with exponent 10 and the
+// nibble as its low mantissa bits; subtracting 1024 is exact, the fma rounds once.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2, uint32_t b2) {
+  const uint32_t k1024 = 0x64006400u;
+  uint4 r;
+  r.x = hfma2(hsub2((w & 0x000F000Fu) | k1024, k1024), s2, b2);
+  r.y = hfma2(hsub2(((w >> 4) & 0x000F000Fu) | k1024, k1024), s2, b2);
+  r.z = hfma2(hsub2(((w >> 8) & 0x000F000Fu) | k1024, k1024), s2, b2);
+  r.w = hfma2(hsub2(((w >> 12) & 0x000F000Fu) | k1024, k1024), s2, b2);
+  return r;
+}
+
+template <int WRING>
+__global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_constant__ TcArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* basep = smem_raw + (base - raw);
+  const int S = a.stages;
+  const uint32_t btile = (uint32_t)a.n_tile * 128u;  // token tile of one group
+  const uint32_t stage_bytes = kATile + kGroupsPerStage * btile;
+  const uint32_t wring = base + (uint32_t)S * stage_bytes;  // weight staging ring
+  // full[s]: the producers' A tile; bfull[s]: the token tile's bytes; empty[s]: the stage's MMAs done
+  uint64_t* full = reinterpret_cast<uint64_t*>(basep + (size_t)S * stage_bytes + (size_t)WRING * kWStageBytes);
+  uint64_t* bfull = full + S;
+  uint64_t* empty = bfull + S;
+  uint64_t* done = empty + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m0 = blockIdx.x * kBM;
+  const int tile = blockIdx.y, n0 = tile * a.n_tile;
+  const int nk = a.in / kGK;                                     // groups
+  const int nst = (nk + kGroupsPerStage - 1) / kGroupsPerStage;  // stages
+
+  if (warp == kProducerWarps) {
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) {
+        mbar_init(full + s, kProducerWarps);
+        mbar_init(bfull + s, 1);
+        mbar_init(empty + s, 1);
+      }
+      mbar_init(done, 1);
+      *abort_flag = 0;
+      mbar_fence_init();
+    }
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_trigger();
+  pdl_wait();
+
+  if (warp < kProducerWarps) {
+    // ---------------- producers: thread (row r, group h of each stage), 64 weights per stage
+    const int r = tid & (kBM - 1), h = tid >> 7;
+    const int row = m0 + r;
+    const bool rv = row < a.out;
+    const int rowc = rv ? row : a.out - 1;
+    const int ngs = a.in / 64;
+    // this thread's group of stage j is 2 j + h: codes advance by 16 words, scale / bias index by 2
+    const uint32_t* wp = a.packed + (size_t)rowc * (a.in / 8) + (size_t)h * 8;
+    const size_t e0 = (size_t)rowc * ngs + h;
+    const size_t n_sb = (size_t)a.out * ngs;
+    const int odd = (int)(e0 & 1);  // which half of the copied 32-bit words holds s and b
+    const uint32_t wcode = wring + (uint32_t)tid * 16;  // chunk c at + c * kProducers * 16
+    const uint32_t wsb = wring + kProducers * 32 + (uint32_t)tid * 8;
+    const uint32_t a_atom = (uint32_t)h * kAtom + (uint32_t)r * 128u;
+    auto wissue = [&](int j) {  // this thread's copies for stage j (an empty group past the end)
+      if (j < nst) {
+        const uint32_t g = (uint32_t)(j % WRING) * kWStageBytes;
+        const bool live = rv && 2 * j + h < nk;
+        const uint32_t* src = live ? wp + (size_t)j * 16 : wp;
+        cp16(wcode + g, src, live ? 16u : 0u);
+        cp16(wcode + g + kProducers * 16, src + 4, live ? 16u : 0u);
+        const size_t e = live ? e0 + 2 * (size_t)j : e0, eo = e & ~(size_t)1;
+        const uint32_t nb = live ? (eo + 1 < n_sb ? 4u : 2u) : 0u;
+        cp4(wsb + g, a.scales + eo, nb);
+        cp4(wsb + g + 4, a.biases + eo, nb);
+      }
+      cp_commit();
+    };
+#pragma unroll 1
+    for (int j = 0; j < WRING - 1; ++j) wissue(j);
+    int b_issued = 0;  // token-tile copies issued (thread 0)
+
+    for (int j = 0; j < nst; ++j) {
+      const int s = j % S;
+      const uint32_t use = (uint32_t)(j / S);
+      if (j >= S && !mbar_wait(empty + s, (use - 1) & 1u)) *abort_flag = 1;
+      if (*abort_flag) break;
+      const uint32_t A = base + (uint32_t)s * stage_bytes;
+      const int ng = min(kGroupsPerStage, nk - kGroupsPerStage * j);  // groups in this stage
+      if (tid == 0) {  // the stage's token tile(s): one bulk copy
+        const uint32_t bytes = (uint32_t)ng * btile;
+        mbar_arrive_expect_tx(bfull + s, bytes);
+        bulk_g2s(A + kATile, a.xt + ((size_t)tile * nk + (size_t)kGroupsPerStage * j) * btile, bytes, bfull + s);
+        ++b_issued;
+      }
+      wissue(j + WRING - 1);
+      cp_wait<WRING - 1>();  // stage j of this thread has landed
+      if (h < ng) {
+        const uint32_t g = (uint32_t)(j % WRING) * kWStageBytes;
+        const uint4 c0 = lds128(wcode + g), c1 = lds128(wcode + g + kProducers * 16);
+        const uint32_t sw = lds32(wsb + g), bw = lds32(wsb + g + 4);
+        const uint32_t s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
+        const uint32_t b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
+        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunk ch = columns 8 ch .. 8 ch + 7 of the group
+          const uint4 v = dequant8(cw[ch], s2, b2);
+          sts128(A + a_atom + (uint32_t)((ch ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
+        }
+        fence_proxy_async();  // the generic-proxy stores above, before the tensor core reads them
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full + s);
+    }
+    cp_wait<0>();
+    if (tid == 0) {
+      // every bulk copy issued here has landed before the CTA can exit (normally long since: the MMA
+      // thread waited for it); the latest use of each stage is the one that may be outstanding
+      for (int j = max(0, b_issued - S); j < b_issued; ++j) mbar_wait(bfull + j % S, (uint32_t)(j / S) & 1u);
+    }
+  } else if (lane == 0) {
+    // ---------------- MMA issuer
+    for (int j = 0; j < nst; ++j) {
+      const int s = j % S;
+      if (!mbar_wait(full + s, (uint32_t)(j / S) & 1u) || !mbar_wait(bfull + s, (uint32_t)(j / S) & 1u))
+        *abort_flag = 1;
+      if (*abort_flag) break;
+      tc_fence_after();
+      const uint32_t A = base + (uint32_t)s * stage_bytes, B = A + kATile;
+      const int ng = min(kGroupsPerStage, nk - kGroupsPerStage * j);
+      for (int gi = 0; gi < ng; ++gi) {
+#pragma unroll
+        for (int k = 0; k < kGK / 16; ++k)
+          mma_f16(tmem, smem_desc(A + gi * kAtom + k * 32), smem_desc(B + gi * btile + k * 32), a.idesc,
+                  (j | gi | k) != 0 ? 1u : 0u);
+      }
+      mma_commit(empty + s);
+    }
+    mma_commit(done);  // arrives once every MMA issued above has completed
+  }
+
+  // ---------------- epilogue: warps w and w + 4 read lanes 32 (w % 4) .. + 31, half of the columns each
+  if (warp < kProducerWarps) {
+    const bool ok = mbar_wait(done, 0);
+    tc_fence_after();
+    if (ok && !*abort_flag) {
+      const int q = warp & 3;
+      const int row = m0 + q * 32 + lane;
+      const int half = a.n_tile / 2;  // multiple of 8
+      const int c0 = (warp >> 2) * half;
+      for (int cc = 0; cc < half; cc += 8) {
+        uint32_t v[8];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+            : "r"(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c0 + cc)));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int t = n0 + c0 + cc + j;
+          if (row < a.out && t < a.T) a.y[(size_t)t * a.out + row] = __uint_as_float(v[j]) * __ldg(a.xs + t);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kProducerWarps) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- prep: X -> scaled fp16 token tiles
+// One CTA per token row n < n_tiles * n_tile.  Row n of tile n / n_tile, group kc: 128 bytes at
+// ((tile * nk + kc) * n_tile + n % n_tile) * 128, the 16-byte chunk j (columns 8j .. 8j + 7 of the
+// group) at position j ^ (n % 8), its eight values in the column order 0, 4, 1, 5, 2, 6, 3, 7 (the
+// order the dequantized weights use).  Rows n >= T are zero.
+__global__ void __launch_bounds__(256) qgemm_prep_kernel(const uint16_t* __restrict__ X, int T, int in, int n_tile,
+                                                         uint8_t* __restrict__ xt, float* __restrict__ xs) {
+  __shared__ float red[8];
+  const int n = blockIdx.x;
+  const int nk = in / 64;
+  const bool live = n < T;
+  const uint16_t* xr = X + (size_t)(live ? n : 0) * in;
+  pdl_trigger();
+  pdl_wait();
+  float m = 0.f;
+  if (live)
+    for (int i = threadIdx.x; i < in; i += blockDim.x) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)xr[i] << 16)));
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  m = red[0];
+  // 2^(14 - e) with e = floor(log2 m): the row's largest magnitude lands in [2^14, 2^15)
+  const int e = m > 0.f ? (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
+  const float sc = live && m > 0.f ? exp2i(min(max(14 - e, -126), 127)) : 0.f;
+  if (threadIdx.x == 0) xs[n] = live && m > 0.f ? exp2i(min(max(e - 14, -126), 127)) : 0.f;
+  const int tile = n / n_tile, nl = n % n_tile;
+  constexpr int kOrder[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+  for (int ch = threadIdx.x; ch < in / 8; ch += blockDim.x) {
+    const int kc = ch >> 3, j = ch & 7;
+    uint32_t hv[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const float f = live ? __uint_as_float((uint32_t)xr[ch * 8 + kOrder[p]] << 16) * sc : 0.f;
+      uint16_t b;
+      asm("cvt.rn.f16.f32 %0, %1;" : "=h"(b) : "f"(f));
+      hv[p] = b;
+    }
+    uint4 o;
+    o.x = hv[0] | (hv[1] << 16);
+    o.y = hv[2] | (hv[3] << 16);
+    o.z = hv[4] | (hv[5] << 16);
+    o.w = hv[6] | (hv[7] << 16);
+    uint8_t* dst = xt + (((size_t)tile * nk + kc) * n_tile + nl) * 128 + (size_t)((j ^ (nl & 7)) << 4);
+    *reinterpret_cast<uint4*>(dst) = o;
+  }
+}
+
+struct TcPlan {
+  int n_tile, n_tiles, stages, wring, tmem_cols;
+  size_t smem;
+};
+
+TcPlan tc_plan(int out, int in, int T) {
+  (void)out;
+  (void)in;
+  TcPlan p{};
+  const int t16 = (T + 15) / 16 * 16;
+  p.n_tile = std::min(kMaxN, t16);
+  p.n_tiles = (T + p.n_tile - 1) / p.n_tile;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < p.n_tile) p.tmem_cols *= 2;
+  const size_t stage = kATile + (size_t)kGroupsPerStage * p.n_tile * 128;
+  const size_t fixed = 1024 + 64 + 8 * 32;  // alignment slack, barriers, slot, flag
+  // the weight ring covers memory latency (deeper for small token tiles, which are memory-bound)
+  p.wring = p.n_tile >= 128 ? 2 : 8;
+  p.stages = (int)std::min<size_t>(4, (kSmemBudget - fixed - (size_t)p.wring * kWStageBytes) / stage);
+  p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
+  return p;
+}
+
+}  // namespace
+
+size_t qgemm_tc_workspace_bytes(const qg_int4_weight* w, int T) {
+  if (T < 1) return 0;
+  const TcPlan p = tc_plan(w->out, w->in, T);
+  const size_t rows = (size_t)p.n_tiles * p.n_tile;
+  return rows * (size_t)w->in * 2 + rows * sizeof(float) + 256;
+}
+
+int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void* ws, size_t ws_bytes,
+                    cudaStream_t stream) {
+  const TcPlan p = tc_plan(w->out, w->in, T);
+  const size_t rows = (size_t)p.n_tiles * p.n_tile;
+  const size_t xt_bytes = rows * (size_t)w->in * 2;
+  if (ws_bytes < qgemm_tc_workspace_bytes(w, T)) return QG_EWORKSPACE;
+  uint8_t* xt = static_cast<uint8_t*>(ws);
+  float* xs = reinterpret_cast<float*>(xt + xt_bytes);
+  int rc = launch(qgemm_prep_kernel, dim3((unsigned)rows), dim3(256), 0, stream, X, T, w->in, p.n_tile, xt, xs);
+  if (rc != QG_OK) return rc;
+  TcArgs a{};
+  a.packed = w->packed;
+  a.scales = w->scales;
+  a.biases = w->biases;
+  a.xt = xt;
+  a.xs = xs;
+  a.y = Y;
+  a.out = w->out;
+  a.in = w->in;
+  a.T = T;
+  a.n_tile = p.n_tile;
+  a.stages = p.stages;
+  a.tmem_cols = p.tmem_cols;
+  // instruction descriptor (kind::f16): D fp32 (bits 4-5 = 1), A and B fp16 (bits 7-12 = 0), both
+  // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
+  a.idesc = (1u << 4) | ((uint32_t)(p.n_tile >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+  const dim3 grid((unsigned)((w->out + kBM - 1) / kBM), (unsigned)p.n_tiles);
+  if (p.wring == 8) {
+    auto k = qgemm_tc_kernel<8>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
+      return QG_ELAUNCH;
+    return launch(k, grid, dim3(kThreads), p.smem, stream, a);
+  }
+  auto k = qgemm_tc_kernel<2>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
+    return QG_ELAUNCH;
+  return launch(k, grid, dim3(kThreads), p.smem, stream, a);
+}
+
+}  // namespace qg

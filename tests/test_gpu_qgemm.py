@@ -34,3 +34,51 @@ def test_config4_full_size_sampled_rows(qg, T):
     for r in sorted(set([0, 17407, 8704] + list(g.integers(0, 17408, 45)))):
         Yr, Ar = oracle.qgemm(d["packed"], d["scales"], d["biases"], X, rows=(r, r + 1))
         assert_within_bound(Y[:, r:r + 1], Yr, Ar, what=f"row {r}")
+
+
+@pytest.mark.parametrize("T,out,in_dim", [(16, 128, 64), (32, 128, 128), (48, 130, 1088), (256, 384, 2048),
+                                          (300, 200, 512), (257, 129, 192)])
+def test_qgemm_tensor_core_shapes(qg, T, out, in_dim):
+    """T >= 32 (and a forced 16) on the tensor-core path: one and several token tiles, ragged rows."""
+    qg.qg_tune_qgemm(16)
+    try:
+        d = I.int4_weight(T + 7, I.TID_W, out, in_dim)
+        X = I.bf16_normal(T + 7, I.TID_X, (T, in_dim))
+        Y = _run(qg, d, X)
+    finally:
+        qg.qg_tune_qgemm(0)
+    Y_ref, A = oracle.qgemm(d["packed"], d["scales"], d["biases"], X)
+    assert_within_bound(Y, Y_ref, A)
+    assert qg.qg_device_status() == 0
+
+
+def test_qgemm_t8_tensor_core_matches_gemv_path(qg):
+    """T = 8 padded onto the tensor cores equals the CUDA-core GEMV path within the bound."""
+    d = I.int4_weight(8, I.TID_W, 640, 1024)
+    X = I.bf16_normal(8, I.TID_X, (8, 1024))
+    y_gemv = _run(qg, d, X)
+    qg.qg_tune_qgemm(1)
+    try:
+        y_tc = _run(qg, d, X)
+    finally:
+        qg.qg_tune_qgemm(0)
+    Y_ref, A = oracle.qgemm(d["packed"], d["scales"], d["biases"], X)
+    assert_within_bound(y_gemv, Y_ref, A, what="gemv path")
+    assert_within_bound(y_tc, Y_ref, A, what="tensor-core path")
+    assert_within_bound(y_tc, y_gemv, 2 * A, what="tensor core vs gemv")
+
+
+def test_qgemm_token_scales_extreme_rows(qg):
+    """Token rows of very different magnitudes (one all zero) keep the per-row bound on the tensor cores."""
+    T, out, in_dim = 32, 256, 512
+    d = I.int4_weight(5, I.TID_W, out, in_dim)
+    x = I.bf16_normal(5, I.TID_X, (T, in_dim)).astype(np.uint32)
+    f = (x << 16).view(np.float32).astype(np.float64)
+    f[1] *= 2.0 ** 40
+    f[2] *= 2.0 ** -40
+    f[3] = 0.0
+    X = I.f64_to_bf16_bits(f).reshape(T, in_dim)
+    Y = _run(qg, d, X)
+    Y_ref, A = oracle.qgemm(d["packed"], d["scales"], d["biases"], X)
+    assert_within_bound(Y, Y_ref, A)
+    assert np.all(Y[3] == 0.0)
