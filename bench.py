@@ -227,6 +227,9 @@ def run_qg(args, rank, world, local_rank):
     us_down_nopdl = time_loop(down_bf16, n_loop)
     qg.qg_set_pdl(not args.no_pdl)
 
+    configs = measure_configs(qg, I, dev, stream) if rank == 0 and not args.no_configs else None
+    qg.qg_set_pdl(not args.no_pdl)
+
     # end to end: x in from pinned host memory, y back to pinned host memory, every step
     x_host = torch.from_numpy(x_np.view(np.int16)).pin_memory()
     y_host = torch.empty(HIDDEN, dtype=torch.float32).pin_memory()
@@ -258,7 +261,7 @@ def run_qg(args, rank, world, local_rank):
     try:
         with open(tf) as f:
             t = json.load(f)
-        src = open(os.path.join(ROOT, "moe_int4_affine_gb300", "csrc", "qgemv.cu"), "rb").read()
+        src = open(os.path.join(ROOT, "moe_int4_affine_gb300", "csrc", "gemv_kernel.cuh"), "rb").read()
         if t.get("source_sha256") == hashlib.sha256(src).hexdigest():
             traffic = t.get("gateup_bytes_per_launch")
     except Exception:
@@ -295,8 +298,124 @@ def run_qg(args, rank, world, local_rank):
                 "us_per_layer": round(e2e_ms * 1e3, 3)},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
+        "configs": configs,
     }
     return line
+
+
+def measure_configs(qg, I, dev, stream):
+    """Every configuration of the workload set, timed back to back with CUDA events on `stream`
+    (median of 3 runs).  Weights rotate over enough copies to exceed L2 unless noted."""
+    import ctypes
+
+    import torch
+
+    P, byref = ctypes.c_void_p, ctypes.byref
+    s = int(stream.cuda_stream)
+    lib = qg.lib
+    peak_hbm, _ = peaks()
+    peak_tf = _peak_tflops()
+    res = {}
+
+    def tl(fn, n):
+        for i in range(6):
+            assert fn(i) == 0
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(3):
+            e0.record(stream)
+            for i in range(n):
+                fn(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / n)
+        return statistics.median(ts)
+
+    def copies(w, n):
+        return [w] + [qg.Int4Weight(w.packed.clone(), w.scales.clone(), w.biases.clone(), w.out, w.in_dim,
+                                    w.n_mat) for _ in range(n - 1)]
+
+    def gb(nbytes, us):
+        return {"us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
+                "frac_of_8000": round(nbytes / us / 1e3 / NOMINAL_HBM_GBS, 4),
+                "frac_of_measured": round(nbytes / us / 1e3 / peak_hbm, 4), "algorithmic_bytes": nbytes}
+
+    # config 0: 256 x 1024 (150 KB: L2-resident, launch-bound)
+    w = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_W, 256, 1024), dev)
+    x = qg.to_device(I.bf16_normal(0, I.TID_X, 1024), dev)
+    y = torch.empty(256, dtype=torch.float32, device=dev)
+    us = tl(lambda i: lib.qgemv_int4(byref(w.struct), P(x.data_ptr()), qg.QG_X_BF16, P(y.data_ptr()), s), 200)
+    res["c0_gemv_256x1024"] = dict(gb(weight_bytes(256, 1024) + 2048 + 1024, us), l2="hot (one 150 KB weight)")
+
+    # config 2: shared-input multi-projection GEMVs, in = 2048
+    for name, outs, ncp in (("c2_quartet_8192_4096_32_32", (8192, 4096, 32, 32), 12),
+                            ("c2_triple_4096_512_512", (4096, 512, 512), 28)):
+        mats = [qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_MULTI + j, o, 2048), dev) for j, o in enumerate(outs)]
+        sets = [mats] + [[copies(m, 2)[1] for m in mats] for _ in range(ncp - 1)]
+        x = qg.to_device(I.bf16_normal(0, I.TID_X, 2048), dev)
+        ys = [torch.empty(o, dtype=torch.float32, device=dev) for o in outs]
+        args = [((qg.qg_int4_weight * len(outs))(*[m.struct for m in st]), (P * len(outs))(*[t.data_ptr() for t in ys]))
+                for st in sets]
+        n = len(outs)
+        us = tl(lambda i: lib.qgemv_int4_multi(n, args[i % ncp][0], P(x.data_ptr()), qg.QG_X_BF16, args[i % ncp][1],
+                                               qg.QG_EPI_NONE, s), 100)
+        nbytes = sum(weight_bytes(o, 2048) for o in outs) + 2048 * 2 + 4 * sum(outs)
+        res[name] = dict(gb(nbytes, us), l2=f"weights rotate over {ncp} copies")
+
+    # config 3: MoE decode T=1 -- router top-8 of 128, gate/up (SwiGLU) and down + residual, one layer
+    E, HID, INTER, K = 128, 2048, 768, 8
+    g = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_GATE, INTER, HID, n_mat=E), dev)
+    u = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_UP, INTER, HID, n_mat=E), dev)
+    d = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_DOWN, HID, INTER, n_mat=E), dev)
+    logits = [qg.to_device(I.f32_normal(i, I.TID_LOGITS, E), dev) for i in range(16)]
+    x = qg.to_device(I.bf16_normal(0, I.TID_X, HID), dev)
+    r = qg.to_device(I.bf16_normal(0, I.TID_RESID, HID), dev)
+    idx = torch.empty(K, dtype=torch.int32, device=dev)
+    pk = torch.empty(K, dtype=torch.float32, device=dev)
+    y = torch.empty(HID, dtype=torch.float32, device=dev)
+    wsb = torch.empty(qg.qg_workspace_bytes(qg.QG_OP_MOE, d, K), dtype=torch.uint8, device=dev)
+
+    def moe(i):
+        rc = lib.moe_router_topk(P(logits[i % 16].data_ptr()), E, K, 1, P(idx.data_ptr()), P(pk.data_ptr()), s)
+        return rc | lib.moe_gather_qgemv_int4(byref(g.struct), byref(u.struct), byref(d.struct), P(idx.data_ptr()),
+                                              P(pk.data_ptr()), K, P(x.data_ptr()), P(r.data_ptr()), P(y.data_ptr()),
+                                              P(wsb.data_ptr()), wsb.numel(), s)
+    us = tl(moe, 100)
+    nbytes = K * 3 * weight_bytes(INTER, HID) + 2 * HID * 2 + E * 4 + HID * 4
+    res["c3_moe_layer_T1"] = dict(gb(nbytes, us), kernels=3,
+                                  l2=f"128-expert pool ({3 * E * weight_bytes(INTER, HID) / 1e6:.0f} MB), router "
+                                     "logits rotate over 16 vectors")
+    del g, u, d
+
+    # config 4: dequant-GEMM, W 17408 x 5120, X T x 5120
+    w = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_W, FFN, HIDDEN), dev)
+    ws_ = copies(w, 12)
+    for T, tc_min, label in ((8, 0, "gemv_path"), (8, 1, "tensor_core_path"), (32, 0, "tensor_core_path"),
+                             (256, 0, "tensor_core_path")):
+        qg.qg_tune_qgemm(tc_min)
+        X = qg.to_device(I.bf16_normal(0, I.TID_X, (T, HIDDEN)), dev)
+        Y = torch.empty((T, FFN), dtype=torch.float32, device=dev)
+        need = qg.qg_workspace_bytes(qg.QG_OP_QGEMM, w, T)
+        wsb = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        args = [(byref(c.struct), P(X.data_ptr()), T, P(Y.data_ptr()), P(wsb.data_ptr()), wsb.numel(), s) for c in ws_]
+        us = tl(lambda i: lib.qgemm_int4(*args[i % 12]), 30 if T == 8 and tc_min == 0 else 60)
+        nbytes = weight_bytes(FFN, HIDDEN) + T * HIDDEN * 2 + T * FFN * 4
+        tf = 2.0 * T * FFN * HIDDEN / us / 1e6
+        e = dict(gb(nbytes, us), path=label, TFLOPs=round(tf, 1), frac_of_tensor_peak=round(tf / peak_tf, 4),
+                 launches=(T if tc_min == 0 and T < 32 else 2))
+        res[f"c4_qgemm_T{T}_{label}"] = e
+    qg.qg_tune_qgemm(0)
+    assert qg.qg_device_status() == 0
+    return res
+
+
+def _peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
 
 
 # ---------------------------------------------------------------------------------------------- oracle
@@ -323,13 +442,22 @@ def oracle_layer_sample(frac: float, threads: int):
 
 
 def cpu_baseline(target_s: float = 12.0):
+    """The oracle on whole-layer row samples, repeated until about target_s seconds of CPU work."""
     threads = os.cpu_count() or 1
     dt, nb = oracle_layer_sample(0.002, threads)  # calibration
     frac = min(1.0, 0.002 * target_s / max(dt, 1e-3))
-    dt, nb = oracle_layer_sample(frac, threads)
-    return {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {frac:.4f} of the rows of gate, up and down ({nb / 1e6:.1f} MB), fp64 C oracle, "
-                      f"{threads} host threads, {dt:.1f} s"}
+    reps = 1
+    if frac >= 1.0:
+        dt1, _ = oracle_layer_sample(1.0, threads)
+        reps = max(1, int(target_s / max(dt1, 1e-3)))
+    tot_t, tot_b = 0.0, 0
+    for _ in range(reps):
+        dt, nb = oracle_layer_sample(frac, threads)
+        tot_t += dt
+        tot_b += nb
+    return {"value": round(tot_b / tot_t / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{reps} x the first {frac:.4f} of the rows of gate, up and down ({tot_b / 1e6:.1f} MB), "
+                      f"fp64 C oracle, {threads} host threads, {tot_t:.1f} s"}
 
 
 def run_reference(args):
@@ -365,6 +493,7 @@ def main(argv=None):
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed steps under the clock sampler")
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration section")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     rank, world, local_rank = dist_env()

@@ -162,9 +162,15 @@ int scalar_fma_chain8_residual(const float *p, const float *v, const uint16_t *r
  * "Pads T -> ceil(T/32)*32 with zero rows, dispatches, slices the first T rows back"):
  *   Y[t][r] = sum_j w[r][j] * X[t][j],  0 <= t < T.
  * X: bf16 [T][in]; Y: fp32 [T][out].  The caller passes exactly T rows; padding is internal and
- * only the T real rows are written.
- * workspace: at least qg_workspace_bytes(QG_OP_QGEMM, w, T) bytes (0 means none is needed).
- * Limits: 1 <= T <= 4096.
+ * only the T real rows are written.  w->n_mat must be 1.
+ * T >= 32 (see qg_tune_qgemm) runs on the tensor cores (tcgen05): the weights are dequantized to
+ * fp16 in shared memory, each token row is scaled by a power of two into fp16's range, products
+ * accumulate in fp32.  That path needs every dequantized weight s*q + b within fp16's range
+ * (|w| < 65504; scales and biases of typical models are far inside it).  Smaller T runs the
+ * CUDA-core GEMV once per token row.
+ * workspace: at least qg_workspace_bytes(QG_OP_QGEMM, w, T) bytes (0 means none is needed): the
+ * tensor-core path stages the converted tokens there.
+ * Limits: 1 <= T <= 4096; in % 64 == 0, 64 <= in <= 32768.
  */
 int qgemm_int4(const qg_int4_weight *w, const uint16_t *X, int T, float *Y, void *workspace, size_t ws_bytes,
                void *stream);
