@@ -1,6 +1,6 @@
 // moe.cu -- MoE decode pieces besides the expert GEMVs: the device router (top-K + softmax) and
 // the standalone scalar-weighted chain with residual.  The expert gather itself runs on the
-// streaming GEMV kernel (qgemv.cu) in its MoE gate/up and MoE down modes.
+// streaming GEMV kernel (gemv_kernel.cuh) in its MoE gate/up and MoE down modes.
 #include <algorithm>
 #include <utility>
 
@@ -11,83 +11,79 @@ namespace qg {
 
 constexpr int kRouterMaxPerLane = 32;  // 32 lanes x 32 = 1024 experts
 
+// Order-preserving key of a finite float: larger floats give larger unsigned keys; -0 and +0 get
+// the same key (they compare equal, so the index decides between them).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Router top-K ([FFAI#14] commit "moeRouterTopK"; order (value desc, index asc) as in [FFAI#9]'s
-// partial-sort commit).  One warp.  Each of k rounds takes, across the warp, the not-yet-taken
-// expert with the largest logit, the lower index on equal logits.  Then the weights: softmax of
-// the selected logits (renorm) or of all logits read at the selected ones.
+// partial-sort commit).  One warp; lane l holds experts l, l + 32, ... (PER of them).  A candidate is
+// the 64-bit key (float_key(logit) << 32) | ~index, so the largest key is the largest logit with
+// the lowest index on ties, and every lane agrees on it.  Round s takes the warp's largest key not
+// yet taken; lane s keeps round s's selection.  Then the weights: softmax of the selected logits
+// (renorm) or of all logits read at the selected ones.
+template <int PER>
 __global__ void __launch_bounds__(32) router_kernel(const float* __restrict__ logits, int n, int k, int renorm,
                                                     uint32_t* __restrict__ idx_out, float* __restrict__ p_out) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x;
-  float v[kRouterMaxPerLane];
-  uint32_t taken = 0;  // bit j: expert lane + 32 j is selected or does not exist
-  const int per = (n + 31) / 32;
+  float v[PER];
+  unsigned long long key[PER];
 #pragma unroll
-  for (int j = 0; j < kRouterMaxPerLane; ++j) {
+  for (int j = 0; j < PER; ++j) {
     const int e = lane + 32 * j;
-    const bool live = j < per && e < n;
-    v[j] = live ? logits[e] : 0.f;
-    if (!live) taken |= 1u << j;
+    v[j] = e < n ? __ldg(logits + e) : 0.f;
+    key[j] = e < n ? ((unsigned long long)float_key(v[j]) << 32) | (uint32_t)~(uint32_t)e : 0ull;
   }
-  float sel_v[32];
-  uint32_t sel_i[32];
+  unsigned long long mine = 0;  // this lane's round's selection (lane s keeps round s)
   for (int s = 0; s < k; ++s) {
-    // lane-local best: largest value, then the smallest index (= smallest j for a fixed lane)
-    float bv = 0.f;
-    int bj = -1;
+    unsigned long long best = key[0];
 #pragma unroll
-    for (int j = 0; j < kRouterMaxPerLane; ++j) {
-      if (taken & (1u << j)) continue;
-      if (bj < 0 || v[j] > bv) {
-        bv = v[j];
-        bj = j;
-      }
-    }
-    int bi = bj < 0 ? 0x7fffffff : lane + 32 * bj;
-    bool has = bj >= 0;
-    // warp arg-best over (has, value desc, index asc): a strict total order, so every lane ends
-    // with the same winner
+    for (int j = 1; j < PER; ++j) best = key[j] > best ? key[j] : best;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      const bool oh = __shfl_xor_sync(0xffffffffu, has, off);
-      const bool better = oh && (!has || ov > bv || (ov == bv && oi < bi));
-      if (better) {
-        bv = ov;
-        bi = oi;
-        has = oh;
-      }
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+      best = o > best ? o : best;
     }
-    sel_v[s] = bv;
-    sel_i[s] = (uint32_t)bi;
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == s) mine = best;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) key[j] = key[j] == best ? 0ull : key[j];  // (keys are unique)
   }
-  const float m = sel_v[0];
-  float z = 0.f;
+  const uint32_t my_idx = ~(uint32_t)mine;
+  const uint32_t kv = (uint32_t)(mine >> 32);
+  const float my_v = __uint_as_float((kv & 0x80000000u) ? (kv & 0x7FFFFFFFu) : ~kv);
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);  // round 0 took the largest logit
+  float z;
   if (renorm) {
-    for (int s = 0; s < k; ++s) z += expf(sel_v[s] - m);
+    z = lane < k ? expf(my_v - m) : 0.f;
   } else {
-    float zl = 0.f;
+    z = 0.f;
 #pragma unroll
-    for (int j = 0; j < kRouterMaxPerLane; ++j) {
-      const int e = lane + 32 * j;
-      if (j < per && e < n) zl += expf(v[j] - m);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) zl += __shfl_xor_sync(0xffffffffu, zl, off);
-    z = zl;
+    for (int j = 0; j < PER; ++j)
+      if (lane + 32 * j < n) z += expf(v[j] - m);
   }
-  for (int s = lane; s < k; s += 32) {
-    idx_out[s] = sel_i[s];
-    p_out[s] = expf(sel_v[s] - m) / z;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+  if (lane < k) {
+    idx_out[lane] = my_idx;
+    p_out[lane] = expf(my_v - m) / z;
   }
 }
 
 int router_launch(const float* logits, int n_experts, int k, int renorm, uint32_t* idx, float* p,
                   cudaStream_t stream) {
-  return launch(router_kernel, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  const int per = (n_experts + 31) / 32;
+  if (per <= 1) return launch(router_kernel<1>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  if (per <= 2) return launch(router_kernel<2>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  if (per <= 4) return launch(router_kernel<4>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  if (per <= 8) return launch(router_kernel<8>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  if (per <= 16)
+    return launch(router_kernel<16>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  return launch(router_kernel<kRouterMaxPerLane>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
 }
 
 // out[i] = residual[i] + sum_{k<8} p[k] * v[k][i], accumulated in slot order ([FFAI#14] scalar-FMA

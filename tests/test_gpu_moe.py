@@ -138,3 +138,17 @@ def test_chain8_one_hot_is_exact(qg):
         p[k] = 1.0
         out = qg.to_numpy(qg.scalar_fma_chain8_residual(qg.to_device(p), qg.to_device(v), qg.to_device(r)))
         np.testing.assert_array_equal(out, (I.bf16_bits_to_f32(r) + v[k]).astype(np.float32))
+
+
+def test_router_signed_zero_and_negative_logits(qg):
+    """-0.0 and +0.0 tie (the lower index wins); all-negative logits order by value."""
+    logits = np.array([-0.0, 0.0, -1.0, -3.0, -0.5, 0.0, -2.0, -0.0], dtype=np.float32)
+    idx, p = qg.moe_router_topk(qg.to_device(logits), k=4)
+    i_ref, p_ref = oracle.router_topk(logits, 4)
+    assert qg.to_numpy(idx).astype(np.uint32).tolist() == i_ref.tolist() == [0, 1, 5, 7]
+    np.testing.assert_allclose(qg.to_numpy(p), p_ref, rtol=2e-6)
+    neg = -np.abs(I.f32_normal(3, I.TID_LOGITS, 300)) - 1.0
+    idx, p = qg.moe_router_topk(qg.to_device(neg.astype(np.float32)), k=8, renorm=False)
+    i_ref, p_ref = oracle.router_topk(neg.astype(np.float32), 8, False)
+    assert qg.to_numpy(idx).astype(np.uint32).tolist() == i_ref.tolist()
+    np.testing.assert_allclose(qg.to_numpy(p), p_ref, rtol=2e-6, atol=1e-9)
