@@ -240,73 +240,87 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   pdl_wait();
   if (u < nunits && a.idx) issue(u, cur);
   {
-    // 8 lanes per group, 8 values (one 8-column word) per lane.  Each thread's loads for up to four
-    // groups are issued together, then processed: one memory latency per four groups.  The loops
-    // are uniform per warp (shuffles below).
+    // 8 lanes per group, 8 values (one 8-column word) per lane.  All of a thread's loads (up to 8
+    // groups of bf16 or 5 of fp32: one round for every in <= 32768 bf16 / 20480 fp32) are issued
+    // together and then processed: one memory latency for the whole prologue.  The loops are
+    // uniform per warp (shuffles below).
     const int sub = lane & 7;
-    constexpr int XB = 4;
-    for (int gb = warp * 4; gb < G; gb += NW * 4 * XB) {
-      float v[XB][8];
+    auto quant = [&](int g, const float (&v)[8]) {
+      float m = 0.f, sx = 0.f;
 #pragma unroll
-      for (int i = 0; i < XB; ++i) {
-        const int g = gb + i * NW * 4 + (lane >> 3);
-        if (g >= G) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[i][j] = 0.f;
-        } else if (!a.xf32) {
-          const uint4 t = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)g * 64) + sub);
-          const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            v[i][2 * j] = __uint_as_float(w[j] << 16);
-            v[i][2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-          }
-        } else {
-          const float4* p4 = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)g * 64) + 2 * sub;
-          const float4 t0 = __ldg(p4), t1 = __ldg(p4 + 1);
-          v[i][0] = t0.x, v[i][1] = t0.y, v[i][2] = t0.z, v[i][3] = t0.w;
-          v[i][4] = t1.x, v[i][5] = t1.y, v[i][6] = t1.z, v[i][7] = t1.w;
-        }
+      for (int j = 0; j < 8; ++j) {
+        m = fmaxf(m, fabsf(v[j]));
+        sx += v[j];
       }
 #pragma unroll
-      for (int i = 0; i < XB; ++i) {
-        const int g = gb + i * NW * 4 + (lane >> 3);
-        float m = 0.f, sx = 0.f;
+      for (int o = 4; o > 0; o >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        sx += __shfl_xor_sync(0xffffffffu, sx, o);
+      }
+      if (g < G) {
+        // E = floor(log2 max|x|), k = 14 - E: |x| 2^k < 2^15.  Groups whose largest |x| is below
+        // 2^-60 contribute less than 1e-17 per weight through the code term and are dropped from
+        // it (the bias term keeps the exact sum).
+        const bool live = m >= 8.673617e-19f;  // 2^-60
+        const int E = max((int)((__float_as_uint(m) >> 23) & 0xFF) - 127, -60);
+        const float scale = live ? exp2i(14 - E) : 0.f;  // 14 - E in [-113, 74]
+        int q[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          m = fmaxf(m, fabsf(v[i][j]));
-          sx += v[i][j];
-        }
-#pragma unroll
-        for (int o = 4; o > 0; o >>= 1) {
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          sx += __shfl_xor_sync(0xffffffffu, sx, o);
-        }
-        if (g < G) {
-          // E = floor(log2 max|x|), k = 14 - E: |x| 2^k < 2^15.  Groups whose largest |x| is below
-          // 2^-60 contribute less than 1e-17 per weight through the code term and are dropped from
-          // it (the bias term keeps the exact sum).
-          const bool live = m >= 8.673617e-19f;  // 2^-60
-          const int E = max((int)((__float_as_uint(m) >> 23) & 0xFF) - 127, -60);
-          const float scale = live ? exp2i(14 - E) : 0.f;  // 14 - E in [-113, 74]
-          int q[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) q[j] = max(-32767, min(32767, round_to_int(v[i][j], scale)));
-          uint4 pk;
-          pk.x = (uint32_t)(q[0] & 0xFFFF) | ((uint32_t)q[2] << 16);
-          pk.y = (uint32_t)(q[4] & 0xFFFF) | ((uint32_t)q[6] << 16);
-          pk.z = (uint32_t)(q[1] & 0xFFFF) | ((uint32_t)q[3] << 16);
-          pk.w = (uint32_t)(q[5] & 0xFFFF) | ((uint32_t)q[7] << 16);
-          reinterpret_cast<uint4*>(xq + (size_t)g * 32)[(sub + g) & 7] = pk;
-          if (sub == 0) {
-            float wgt = 1.f;
-            if (SEG) {
-              bool ok;
-              resolve(a, WRef{a.seg.packed, a.seg.scales, a.seg.biases, g / ngs}, ok);
-              wgt = ok ? __ldg(a.p + g / ngs) : 0.f;
-            }
-            gsx[g] = make_float2(live ? exp2i(E - 14) * wgt : 0.f, sx * wgt);
+        for (int j = 0; j < 8; ++j) q[j] = max(-32767, min(32767, round_to_int(v[j], scale)));
+        uint4 pk;
+        pk.x = (uint32_t)(q[0] & 0xFFFF) | ((uint32_t)q[2] << 16);
+        pk.y = (uint32_t)(q[4] & 0xFFFF) | ((uint32_t)q[6] << 16);
+        pk.z = (uint32_t)(q[1] & 0xFFFF) | ((uint32_t)q[3] << 16);
+        pk.w = (uint32_t)(q[5] & 0xFFFF) | ((uint32_t)q[7] << 16);
+        reinterpret_cast<uint4*>(xq + (size_t)g * 32)[(sub + g) & 7] = pk;
+        if (sub == 0) {
+          float wgt = 1.f;
+          if (SEG) {
+            bool ok;
+            resolve(a, WRef{a.seg.packed, a.seg.scales, a.seg.biases, g / ngs}, ok);
+            wgt = ok ? __ldg(a.p + g / ngs) : 0.f;
           }
+          gsx[g] = make_float2(live ? exp2i(E - 14) * wgt : 0.f, sx * wgt);
+        }
+      }
+    };
+    if (!a.xf32) {
+      constexpr int XB = 8;
+      for (int gb = warp * 4; gb < G; gb += NW * 4 * XB) {
+        uint4 raw[XB];
+#pragma unroll
+        for (int i = 0; i < XB; ++i) {
+          const int g = gb + i * NW * 4 + (lane >> 3);
+          raw[i] = g < G ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)g * 64) + sub)
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < XB; ++i) {
+          const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            v[2 * j] = __uint_as_float(w[j] << 16);
+            v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+          }
+          quant(gb + i * NW * 4 + (lane >> 3), v);
+        }
+      }
+    } else {
+      constexpr int XB = 5;
+      for (int gb = warp * 4; gb < G; gb += NW * 4 * XB) {
+        float4 r0[XB], r1[XB];
+#pragma unroll
+        for (int i = 0; i < XB; ++i) {
+          const int g = gb + i * NW * 4 + (lane >> 3);
+          const float4* p4 = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)g * 64) + 2 * sub;
+          r0[i] = g < G ? __ldg(p4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          r1[i] = g < G ? __ldg(p4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < XB; ++i) {
+          const float v[8] = {r0[i].x, r0[i].y, r0[i].z, r0[i].w, r1[i].x, r1[i].y, r1[i].z, r1[i].w};
+          quant(gb + i * NW * 4 + (lane >> 3), v);
         }
       }
     }
