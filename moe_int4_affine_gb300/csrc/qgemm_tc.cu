@@ -5,15 +5,16 @@
 // Work split: one CTA per (128 weight rows, n_tile tokens) tile; the MMA is D[128 x n_tile] +=
 // A[128 x 16] * B[n_tile x 16]^T with A = the dequantized weights and B = the tokens, both fp16 and
 // K-major in shared memory with the 128-byte swizzle, D fp32 in tensor memory.
-//   * A pipeline stage covers two 64-column quantization groups.  Producer warps (8; thread = one
-//     weight row and one of the stage's two groups) stream the packed codes, scales and biases
-//     through a per-thread cp.async ring (WRING stages ahead), dequantize their 64 weights with
-//     packed half-precision arithmetic (w = s * q + b, one rounding to fp16) and store them into the
-//     stage's A tile (one 16 KB swizzle atom per group).
+//   * A pipeline stage covers one 64-column quantization group (K = 64).  Two producer warp groups
+//     (4 warps each, one thread per weight row) take alternate stages: group h produces stages
+//     j = h, h + 2, ...  A thread streams its row's packed codes, scale and bias through a
+//     per-thread cp.async ring (WRING of its groups ahead), dequantizes the 64 weights with packed
+//     half-precision arithmetic (w = s * q + b, one rounding to fp16) and stores them into the
+//     stage's A tile (one 16 KB swizzle atom).
 //   * The token tile of a stage is one contiguous block of the workspace (written there, already
 //     swizzled, by the prep kernel) and arrives by a single bulk copy (TMA engine) on the stage's
 //     mbarrier.
-//   * One thread of the MMA warp issues eight K=16 MMAs per stage and commits them to the stage's
+//   * One thread of the MMA warp issues four K=16 MMAs per stage and commits them to the stage's
 //     "empty" mbarrier; a final commit releases the epilogue, which reads the accumulator from tensor
 //     memory (tcgen05.ld), applies each token's power-of-two input scale and writes Y.
 //   * Every mbarrier wait is bounded (2 s): on a timeout the CTA records QG_STATUS_TIMEOUT, stops
@@ -33,15 +34,13 @@ namespace qg {
 namespace {
 
 constexpr int kBM = 128;                     // weight rows per CTA (MMA M)
-constexpr int kGK = 64;                      // columns of one quantization group (one swizzle atom)
-constexpr int kGroupsPerStage = 2;           // K per pipeline stage: two groups
+constexpr int kGK = 64;                      // columns of one quantization group = K of one stage
 constexpr int kMaxN = 256;                   // tokens per CTA (MMA N, tensor-memory columns)
-constexpr int kProducerWarps = 8;            // two threads per weight row
+constexpr int kProducerWarps = 8;            // two warp groups of 4: one thread per weight row each
 constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreads = kProducers + 32;    // + the MMA / tensor-memory warp
-constexpr int kAtom = kBM * kGK * 2;         // 16 KB of fp16: 128 rows x one group
-constexpr int kATile = kAtom * kGroupsPerStage;
-// weight ring, per stage: codes [2 chunks][256 threads][16 B], then scale and bias words [256][8 B]
+constexpr int kATile = kBM * kGK * 2;        // 16 KB of fp16: 128 rows x one group (one swizzle atom)
+// weight ring, per pair of groups: codes [2 chunks][256 threads][16 B], then scale and bias words
 constexpr int kWStageBytes = kProducers * 32 + kProducers * 8;
 constexpr int kSmemBudget = 220 * 1024;
 
@@ -151,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   uint8_t* basep = smem_raw + (base - raw);
   const int S = a.stages;
   const uint32_t btile = (uint32_t)a.n_tile * 128u;  // token tile of one group
-  const uint32_t stage_bytes = kATile + kGroupsPerStage * btile;
+  const uint32_t stage_bytes = kATile + btile;
   const uint32_t wring = base + (uint32_t)S * stage_bytes;  // weight staging ring
   // full[s]: the producers' A tile; bfull[s]: the token tile's bytes; empty[s]: the stage's MMAs done
   uint64_t* full = reinterpret_cast<uint64_t*>(basep + (size_t)S * stage_bytes + (size_t)WRING * kWStageBytes);
@@ -164,13 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = blockIdx.x * kBM;
   const int tile = blockIdx.y, n0 = tile * a.n_tile;
-  const int nk = a.in / kGK;                                     // groups
-  const int nst = (nk + kGroupsPerStage - 1) / kGroupsPerStage;  // stages
+  const int nk = a.in / kGK;  // groups = pipeline stages
 
   if (warp == kProducerWarps) {
     if (lane == 0) {
       for (int s = 0; s < S; ++s) {
-        mbar_init(full + s, kProducerWarps);
+        mbar_init(full + s, kProducerWarps / 2);
         mbar_init(bfull + s, 1);
         mbar_init(empty + s, 1);
       }
@@ -193,93 +191,94 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   pdl_wait();
 
   if (warp < kProducerWarps) {
-    // ---------------- producers: thread (row r, group h of each stage), 64 weights per stage
+    // ---------------- producers: thread (row r, warp group h) makes stages j = 2 jj + h
     const int r = tid & (kBM - 1), h = tid >> 7;
     const int row = m0 + r;
     const bool rv = row < a.out;
     const int rowc = rv ? row : a.out - 1;
     const int ngs = a.in / 64;
-    // this thread's group of stage j is 2 j + h: codes advance by 16 words, scale / bias index by 2
+    const int my_n = (nk - h + 1) / 2;  // groups of this thread
+    // group 2 jj + h: codes advance by 16 words per jj, the scale / bias index by 2
     const uint32_t* wp = a.packed + (size_t)rowc * (a.in / 8) + (size_t)h * 8;
     const size_t e0 = (size_t)rowc * ngs + h;
     const size_t n_sb = (size_t)a.out * ngs;
     const int odd = (int)(e0 & 1);  // which half of the copied 32-bit words holds s and b
     const uint32_t wcode = wring + (uint32_t)tid * 16;  // chunk c at + c * kProducers * 16
     const uint32_t wsb = wring + kProducers * 32 + (uint32_t)tid * 8;
-    const uint32_t a_atom = (uint32_t)h * kAtom + (uint32_t)r * 128u;
-    auto wissue = [&](int j) {  // this thread's copies for stage j (an empty group past the end)
-      if (j < nst) {
-        const uint32_t g = (uint32_t)(j % WRING) * kWStageBytes;
-        const bool live = rv && 2 * j + h < nk;
-        const uint32_t* src = live ? wp + (size_t)j * 16 : wp;
-        cp16(wcode + g, src, live ? 16u : 0u);
-        cp16(wcode + g + kProducers * 16, src + 4, live ? 16u : 0u);
-        const size_t e = live ? e0 + 2 * (size_t)j : e0, eo = e & ~(size_t)1;
-        const uint32_t nb = live ? (eo + 1 < n_sb ? 4u : 2u) : 0u;
+    const uint32_t a_row = (uint32_t)r * 128u;
+    auto wissue = [&](int jj) {  // this thread's copies for its group jj (an empty group past the end)
+      if (jj < my_n) {
+        const uint32_t g = (uint32_t)(jj % WRING) * kWStageBytes;
+        const uint32_t* src = wp + (size_t)jj * 16;
+        cp16(wcode + g, src, rv ? 16u : 0u);
+        cp16(wcode + g + kProducers * 16, src + 4, rv ? 16u : 0u);
+        const size_t e = e0 + 2 * (size_t)jj, eo = e & ~(size_t)1;
+        const uint32_t nb = rv ? (eo + 1 < n_sb ? 4u : 2u) : 0u;
         cp4(wsb + g, a.scales + eo, nb);
         cp4(wsb + g + 4, a.biases + eo, nb);
       }
       cp_commit();
     };
 #pragma unroll 1
-    for (int j = 0; j < WRING - 1; ++j) wissue(j);
-    int b_issued = 0;  // token-tile copies issued (thread 0)
+    for (int jj = 0; jj < WRING - 1; ++jj) wissue(jj);
+    int b_issued = 0;  // token-tile copies issued (thread r == 0 of each warp group)
 
-    for (int j = 0; j < nst; ++j) {
+    for (int jj = 0; jj < my_n; ++jj) {
+      const int j = 2 * jj + h;  // the stage
       const int s = j % S;
-      const uint32_t use = (uint32_t)(j / S);
-      if (j >= S && !mbar_wait(empty + s, (use - 1) & 1u)) *abort_flag = 1;
+      if (j >= S && !mbar_wait(empty + s, (uint32_t)(j / S - 1) & 1u)) *abort_flag = 1;
       if (*abort_flag) break;
       const uint32_t A = base + (uint32_t)s * stage_bytes;
-      const int ng = min(kGroupsPerStage, nk - kGroupsPerStage * j);  // groups in this stage
-      if (tid == 0) {  // the stage's token tile(s): one bulk copy
-        const uint32_t bytes = (uint32_t)ng * btile;
-        mbar_arrive_expect_tx(bfull + s, bytes);
-        bulk_g2s(A + kATile, a.xt + ((size_t)tile * nk + (size_t)kGroupsPerStage * j) * btile, bytes, bfull + s);
+      if (r == 0) {  // the stage's token tile: one bulk copy
+        mbar_arrive_expect_tx(bfull + s, btile);
+        bulk_g2s(A + kATile, a.xt + ((size_t)tile * nk + j) * btile, btile, bfull + s);
         ++b_issued;
       }
-      wissue(j + WRING - 1);
-      cp_wait<WRING - 1>();  // stage j of this thread has landed
-      if (h < ng) {
-        const uint32_t g = (uint32_t)(j % WRING) * kWStageBytes;
-        const uint4 c0 = lds128(wcode + g), c1 = lds128(wcode + g + kProducers * 16);
-        const uint32_t sw = lds32(wsb + g), bw = lds32(wsb + g + 4);
-        const uint32_t s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
-        const uint32_t b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
-        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      wissue(jj + WRING - 1);
+      cp_wait<WRING - 1>();  // group jj of this thread has landed
+      const uint32_t g = (uint32_t)(jj % WRING) * kWStageBytes;
+      const uint4 c0 = lds128(wcode + g), c1 = lds128(wcode + g + kProducers * 16);
+      const uint32_t sw = lds32(wsb + g), bw = lds32(wsb + g + 4);
+      const uint32_t s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
+      const uint32_t b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
+      const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunk ch = columns 8 ch .. 8 ch + 7 of the group
-          const uint4 v = dequant8(cw[ch], s2, b2);
-          sts128(A + a_atom + (uint32_t)((ch ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
-        }
-        fence_proxy_async();  // the generic-proxy stores above, before the tensor core reads them
+      for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunk ch = columns 8 ch .. 8 ch + 7 of the group
+        const uint4 v = dequant8(cw[ch], s2, b2);
+        sts128(A + a_row + (uint32_t)((ch ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
       }
+      fence_proxy_async();  // the generic-proxy stores above, before the tensor core reads them
       __syncwarp();
       if (lane == 0) mbar_arrive(full + s);
     }
     cp_wait<0>();
-    if (tid == 0) {
+    if (r == 0) {
       // every bulk copy issued here has landed before the CTA can exit (normally long since: the MMA
-      // thread waited for it); the latest use of each stage is the one that may be outstanding
-      for (int j = max(0, b_issued - S); j < b_issued; ++j) mbar_wait(bfull + j % S, (uint32_t)(j / S) & 1u);
+      // thread waited for it); this thread's latest use of each of its stages may be outstanding
+      for (int jj = max(0, b_issued - S / 2); jj < b_issued; ++jj) {
+        const int j = 2 * jj + h;
+        mbar_wait(bfull + j % S, (uint32_t)(j / S) & 1u);
+      }
     }
   } else if (lane == 0) {
     // ---------------- MMA issuer
-    for (int j = 0; j < nst; ++j) {
-      const int s = j % S;
-      if (!mbar_wait(full + s, (uint32_t)(j / S) & 1u) || !mbar_wait(bfull + s, (uint32_t)(j / S) & 1u))
-        *abort_flag = 1;
+    // Descriptors of stage 0; stage s and K step k add (s * stage_bytes + 32 k) / 16 to the start
+    // address field (bits 0-13: shared addresses stay below 2^18, so the field never carries).
+    const uint64_t da0 = smem_desc(base), db0 = smem_desc(base + kATile);
+    const uint32_t dstage = stage_bytes >> 4;
+    int s = 0;
+    uint32_t ph = 0;  // parity of stage s's current use
+    for (int j = 0; j < nk; ++j) {
+      if (!mbar_wait(full + s, ph) || !mbar_wait(bfull + s, ph)) *abort_flag = 1;
       if (*abort_flag) break;
-      tc_fence_after();
-      const uint32_t A = base + (uint32_t)s * stage_bytes, B = A + kATile;
-      const int ng = min(kGroupsPerStage, nk - kGroupsPerStage * j);
-      for (int gi = 0; gi < ng; ++gi) {
+      const uint64_t da = da0 + (uint64_t)(s * dstage), db = db0 + (uint64_t)(s * dstage);
 #pragma unroll
-        for (int k = 0; k < kGK / 16; ++k)
-          mma_f16(tmem, smem_desc(A + gi * kAtom + k * 32), smem_desc(B + gi * btile + k * 32), a.idesc,
-                  (j | gi | k) != 0 ? 1u : 0u);
-      }
+      for (int k = 0; k < kGK / 16; ++k) mma_f16(tmem, da + 2 * k, db + 2 * k, a.idesc, (j | k) != 0 ? 1u : 0u);
       mma_commit(empty + s);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     mma_commit(done);  // arrives once every MMA issued above has completed
   }
@@ -383,11 +382,12 @@ TcPlan tc_plan(int out, int in, int T) {
   p.n_tiles = (T + p.n_tile - 1) / p.n_tile;
   p.tmem_cols = 32;
   while (p.tmem_cols < p.n_tile) p.tmem_cols *= 2;
-  const size_t stage = kATile + (size_t)kGroupsPerStage * p.n_tile * 128;
+  const size_t stage = kATile + (size_t)p.n_tile * 128;
   const size_t fixed = 1024 + 64 + 8 * 32;  // alignment slack, barriers, slot, flag
   // the weight ring covers memory latency (deeper for small token tiles, which are memory-bound)
-  p.wring = p.n_tile >= 128 ? 2 : 8;
-  p.stages = (int)std::min<size_t>(4, (kSmemBudget - fixed - (size_t)p.wring * kWStageBytes) / stage);
+  // (the two producer warp groups take alternate stages: an even number of stages)
+  p.wring = p.n_tile >= 128 ? 2 : 4;
+  p.stages = (int)std::min<size_t>(8, (kSmemBudget - fixed - (size_t)p.wring * kWStageBytes) / stage) & ~1;
   p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
   return p;
 }
@@ -428,8 +428,8 @@ int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y,
   // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
   a.idesc = (1u << 4) | ((uint32_t)(p.n_tile >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
   const dim3 grid((unsigned)((w->out + kBM - 1) / kBM), (unsigned)p.n_tiles);
-  if (p.wring == 8) {
-    auto k = qgemm_tc_kernel<8>;
+  if (p.wring == 4) {
+    auto k = qgemm_tc_kernel<4>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
       return QG_ELAUNCH;
     return launch(k, grid, dim3(kThreads), p.smem, stream, a);
