@@ -209,6 +209,16 @@ int qg_tune_qgemm(int tc_min_T);
  * it.  Synchronises `stream`.  Returns QG_OK or QG_EDEVICE. */
 int qg_device_status(void *stream, uint32_t *status);
 
+/*
+ * qg_selftest_wait_timeout -- exercises the device-side failure path: launches one kernel whose
+ * single wait (on an mbarrier that nothing completes) gives up after limit_us microseconds
+ * (1 .. 1000000), sets QG_STATUS_TIMEOUT in the device status word and returns normally.  The
+ * context stays usable; qg_device_status() then reports (and clears) the bit.  Every wait in the
+ * library's kernels ends the same way.  Returns QG_EINVAL outside the range, QG_ELAUNCH on a
+ * launch error.  (No counterpart in the pages: a test hook for the status mechanism.)
+ */
+int qg_selftest_wait_timeout(int limit_us, void *stream);
+
 /* Static description of an error code. */
 const char *qg_strerror(int code);
 

@@ -23,10 +23,12 @@
 //     (2048 columns): lane l handles group 32 c + l of each row, keeps that group of x in registers
 //     for the unit, and reads its 32 bytes of codes per row straight from global memory with two
 //     128-bit loads (a warp reads 1 KB contiguous per row) plus the group's scale and bias.  The
-//     next unit's loads are issued before the current unit is computed.
-//   * Unpack + dot: one shift and two ANDs turn a u32 word into eight byte codes; integer dp2a
-//     instructions accumulate q_j * X_j exactly in int32, two products per instruction.  Per group
-//     and row the scale and bias are applied once in fp32:  y += s * (acc * 2^-k_g) + b * sum_g x.
+//     next unit's loads are issued before the current unit is computed (two register buffers in
+//     turn); a warp walks its units u = warp, warp + 16, ... without divisions.
+//   * Unpack + dot: two ANDs split a u32 word into the byte codes of its even and sixteen times its
+//     odd nibbles; integer dp2a instructions accumulate q_j * X_j exactly in int32, two products per
+//     instruction.  Per group and row the scale and bias are applied once in fp32:
+//     y += s * (acc * 2^-k_g) + b * sum_g x.
 //   * Each unit's row sums go to shared memory; after a CTA barrier they are added in a fixed
 //     order (deterministic), the epilogue (SwiGLU / residual) applied and the outputs written.
 //   * Programmatic dependent launch: the first unit's codes are loaded before griddepcontrol.wait;
@@ -152,6 +154,12 @@ struct UnitLoads {
   uint32_t s[RN], t[RN];
 };
 
+// A warp's position in its sequence of work units u = warp, warp + NW, ...: row block u / nkc and
+// K chunk u % nkc, advanced without a division.
+struct UnitCursor {
+  int blk, kc;
+};
+
 // Row block b of a CTA's rows [vb, ve): blocks of RB rows formed per matrix.  Returns false past
 // the last block.
 template <int RB>
@@ -205,11 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   }
   const int nunits = nblocks * nkc;
 
-  // The loads of unit u for this lane (work unit u: row block u / nkc, K chunk u % nkc).
-  auto issue = [&](int u, UnitLoads<RN>& L) {
+  // The loads of a unit for this lane.
+  auto issue = [&](const UnitCursor& uc, UnitLoads<RN>& L) {
     int m = 0, rf = 0, nr = 0, l0 = 0;
-    block_rows<RB>(a, vb, ve, u / nkc, m, rf, nr, l0);
-    const int g = (u % nkc) * kGroupsPerUnit + lane;  // this lane's group (across segments)
+    block_rows<RB>(a, vb, ve, uc.blk, m, rf, nr, l0);
+    const int g = uc.kc * kGroupsPerUnit + lane;  // this lane's group (across segments)
     const bool gv = g < G;
     const int sg = SEG ? (gv ? g / ngs : 0) : 0;
     const int lg = SEG ? g - sg * ngs : g;
@@ -231,14 +239,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       }
     }
   };
+  // u -> u + NW: NW = bstep * nkc + kstep
+  const int bstep = NW / nkc, kstep = NW % nkc;
+  auto advance = [&](UnitCursor uc) {
+    uc.blk += bstep;
+    uc.kc += kstep;
+    if (uc.kc >= nkc) {
+      uc.kc -= nkc;
+      ++uc.blk;
+    }
+    return uc;
+  };
 
-  UnitLoads<RN> cur, nxt;
+  UnitLoads<RN> b0, b1;
   int u = warp;
-  if (u < nunits && !a.idx) issue(u, cur);  // before the dependency wait: weights only
+  UnitCursor uc{warp / nkc, warp % nkc};
+  if (u < nunits && !a.idx) issue(uc, b0);  // before the dependency wait: weights only
 
   // --- x: 16-bit fixed point per group, into shared memory ---
   pdl_wait();
-  if (u < nunits && a.idx) issue(u, cur);
+  if (u < nunits && a.idx) issue(uc, b0);
   {
     // 8 lanes per group, 8 values (one 8-column word) per lane.  All of a thread's loads (up to 8
     // groups of bf16 or 5 of fp32: one round for every in <= 32768 bf16 / 20480 fp32) are issued
@@ -280,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             resolve(a, WRef{a.seg.packed, a.seg.scales, a.seg.biases, g / ngs}, ok);
             wgt = ok ? __ldg(a.p + g / ngs) : 0.f;
           }
-          gsx[g] = make_float2(live ? exp2i(E - 14) * wgt : 0.f, sx * wgt);
+          // (2^-k / 16: the odd codes are accumulated sixteen times over, see the main loop)
+          gsx[g] = make_float2(live ? exp2i(E - 18) * wgt : 0.f, sx * wgt);
         }
       }
     };
@@ -330,12 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   }
   __syncthreads();
 
-  // --- main loop: this warp's units u = warp, warp + NW, ... ---
+  // --- main loop: this warp's units u = warp, warp + NW, ...; two buffers in turn, the next unit's
+  // codes in flight while one is computed ---
   const uint32_t xq_s = smem_u32(xq);
-  for (; u < nunits; u += NW) {
-    if (u + NW < nunits) issue(u + NW, nxt);  // next unit's codes in flight during this one
-    const int kc = u % nkc;
-    const int g = kc * kGroupsPerUnit + lane;
+  auto compute = [&](const UnitLoads<RN>& L, const UnitCursor& c) {
+    const int g = c.kc * kGroupsPerUnit + lane;
     const int gc = min(g, G - 1);
     // this lane's group of x, in registers for all RN entries of the unit
     uint4 X[8];
@@ -348,29 +368,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       int s0 = 0, s1 = 0;
 #pragma unroll
       for (int wd = 0; wd < 8; ++wd) {
-        const uint4& c4 = wd < 4 ? cur.a[e] : cur.b[e];
+        const uint4& c4 = wd < 4 ? L.a[e] : L.b[e];
         const int k = wd & 3;
         const uint32_t w = k == 0 ? c4.x : k == 1 ? c4.y : k == 2 ? c4.z : c4.w;
-        const uint32_t c0 = w & 0x0F0F0F0Fu;         // codes q0, q2, q4, q6 as bytes
-        const uint32_t c1 = (w >> 4) & 0x0F0F0F0Fu;  // codes q1, q3, q5, q7
+        const uint32_t c0 = w & 0x0F0F0F0Fu;  // codes q0, q2, q4, q6 as bytes
+        const uint32_t c1 = w & 0xF0F0F0F0u;  // 16 q1, 16 q3, 16 q5, 16 q7
         s0 = dp2a_lo(X[wd].x, c0, s0);
-        s1 = dp2a_hi(X[wd].y, c0, s1);
-        s0 = dp2a_lo(X[wd].z, c1, s0);
+        s0 = dp2a_hi(X[wd].y, c0, s0);
+        s1 = dp2a_lo(X[wd].z, c1, s1);
         s1 = dp2a_hi(X[wd].w, c1, s1);
       }
-      // |s0|, |s1| <= 32 * 15 * 32767 < 2^24: exact in float
-      const float acc = __int2float_rn(s0) + __int2float_rn(s1);
-      yp[e] = g < G ? fmaf(bf16_bits_to_f32(cur.s[e]), acc * gs.x, bf16_bits_to_f32(cur.t[e]) * gs.y) : 0.f;
+      // |s0| <= 32 * 15 * 32767 and |s1| <= 16 times that: 16 s0 + s1 < 2^29, exact in int32
+      // (rounded once to float, relative error 2^-24); gs.x carries the matching 1/16
+      const float acc = (float)(s0 * 16 + s1);
+      yp[e] = g < G ? fmaf(bf16_bits_to_f32(L.s[e]), acc * gs.x, bf16_bits_to_f32(L.t[e]) * gs.y) : 0.f;
     }
     const float tot = warp_sum_rows<RN>(yp, lane);
     if ((lane & (32 / RN - 1)) == 0) {
       const int e = (lane * RN) >> 5;
       int m = 0, rf = 0, nr = 0, l0 = 0;
-      block_rows<RB>(a, vb, ve, u / nkc, m, rf, nr, l0);
-      const int r = e / NC, c = e % NC;
-      if (r < nr) part[((l0 + r) * NC + c) * nkc + kc] = tot;
+      block_rows<RB>(a, vb, ve, c.blk, m, rf, nr, l0);
+      if (e / NC < nr) part[((l0 + e / NC) * NC + e % NC) * nkc + c.kc] = tot;
     }
-    cur = nxt;
+  };
+  for (; u < nunits; u += NW) {
+    const UnitCursor un = advance(uc);
+    if (u + NW < nunits) issue(un, b1);
+    compute(b0, uc);
+    b0 = b1;
+    uc = un;
   }
   __syncthreads();
 

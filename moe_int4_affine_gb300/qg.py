@@ -48,13 +48,14 @@ lib.qg_workspace_bytes.restype = ctypes.c_size_t
 lib.qg_set_pdl.argtypes = [_I]
 lib.qg_tune_gemv.argtypes = [_I]
 lib.qg_tune_qgemm.argtypes = [_I]
+lib.qg_selftest_wait_timeout.argtypes = [_I, _P]
 lib.qg_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
 lib.qg_strerror.argtypes = [_I]
 lib.qg_strerror.restype = ctypes.c_char_p
 lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
            "moe_gather_qgemv_int4_noalloc",
-           "scalar_fma_chain8_residual", "qgemm_int4", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_device_status", "qg_version"):
+           "scalar_fma_chain8_residual", "qgemm_int4", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
 
 
@@ -240,6 +241,10 @@ def qg_set_pdl(enable: bool) -> bool:
 
 def qg_tune_gemv(ctas_per_sm: int = 0) -> None:
     _check(lib.qg_tune_gemv(ctas_per_sm), "qg_tune_gemv")
+
+
+def qg_selftest_wait_timeout(limit_us: int = 1000, stream=None) -> None:
+    _check(lib.qg_selftest_wait_timeout(limit_us, _stream(stream)), "qg_selftest_wait_timeout")
 
 
 def qg_tune_qgemm(tc_min_T: int = 0) -> None:

@@ -172,3 +172,23 @@ def test_pdl_and_determinism(qg):
     for y in ys:
         np.testing.assert_array_equal(y.astype(np.float64), y0)
     assert qg.qg_device_status() == 0
+
+
+def test_device_wait_timeout_sets_status_and_context_survives(qg):
+    """A device wait that nothing completes gives up after its limit, sets QG_STATUS_TIMEOUT and the
+    context stays usable for the next call."""
+    import torch
+
+    qg.qg_device_status()  # clear
+    qg.qg_selftest_wait_timeout(2000)
+    torch.cuda.synchronize()
+    assert qg.qg_device_status() & qg.QG_STATUS_TIMEOUT
+    assert qg.qg_device_status() == 0  # read-and-clear
+    d = I.int4_weight(1, I.TID_W, 64, 128)
+    x = I.bf16_normal(1, I.TID_X, 128)
+    y = qg.to_numpy(qg.qgemv_int4(qg.Int4Weight.from_numpy(d), qg.to_device(x))).astype(np.float64)
+    y_ref, a = oracle.qgemv(d["packed"], d["scales"], d["biases"], x)
+    assert_within_bound(y, y_ref, a)
+    assert qg.qg_device_status() == 0
+    with pytest.raises(qg.QGError):
+        qg.qg_selftest_wait_timeout(0)
