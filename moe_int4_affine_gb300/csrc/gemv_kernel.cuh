@@ -219,24 +219,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     block_rows<RB>(a, vb, ve, uc.blk, m, rf, nr, l0);
     const int g = uc.kc * kGroupsPerUnit + lane;  // this lane's group (across segments)
     const bool gv = g < G;
-    const int sg = SEG ? (gv ? g / ngs : 0) : 0;
-    const int lg = SEG ? g - sg * ngs : g;
+    const int gl = gv ? g : G - 1;  // (a valid group to load from; its terms are zeroed below)
+    const int sg = SEG ? gl / ngs : 0;
+    const int lg = SEG ? gl - sg * ngs : gl;
 #pragma unroll
     for (int e = 0; e < RN; ++e) {
       const int r = e / NC, c = e % NC;
       bool ok;
       const WPtr w = resolve(a, SEG ? WRef{a.seg.packed, a.seg.scales, a.seg.biases, sg} : a.mat[m].w[c], ok);
       const size_t row = (size_t)(rf + min(r, nr - 1));
-      if (ok && gv && r < nr) {
-        const uint4* src = reinterpret_cast<const uint4*>(w.packed + row * (size_t)(a.in / 8)) + lg * 2;
-        L.a[e] = __ldg(src);
-        L.b[e] = __ldg(src + 1);
-        L.s[e] = __ldg(w.scales + row * (size_t)ngs + lg);
-        L.t[e] = __ldg(w.biases + row * (size_t)ngs + lg);
-      } else {
-        L.a[e] = L.b[e] = make_uint4(0u, 0u, 0u, 0u);
-        L.s[e] = L.t[e] = 0u;
-      }
+      // Every load is in bounds (clamped row and group, the base slab for a bad expert); entries
+      // past the block, past the last group or of a bad expert get scale and bias 0, so add 0.
+      const uint4* src = reinterpret_cast<const uint4*>(w.packed + row * (size_t)(a.in / 8)) + lg * 2;
+      L.a[e] = __ldg(src);
+      L.b[e] = __ldg(src + 1);
+      const bool live = ok && gv && r < nr;
+      L.s[e] = live ? (uint32_t)__ldg(w.scales + row * (size_t)ngs + lg) : 0u;
+      L.t[e] = live ? (uint32_t)__ldg(w.biases + row * (size_t)ngs + lg) : 0u;
     }
   };
   // u -> u + NW: NW = bstep * nkc + kstep
@@ -381,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       // |s0| <= 32 * 15 * 32767 and |s1| <= 16 times that: 16 s0 + s1 < 2^29, exact in int32
       // (rounded once to float, relative error 2^-24); gs.x carries the matching 1/16
       const float acc = (float)(s0 * 16 + s1);
-      yp[e] = g < G ? fmaf(bf16_bits_to_f32(L.s[e]), acc * gs.x, bf16_bits_to_f32(L.t[e]) * gs.y) : 0.f;
+      yp[e] = fmaf(bf16_bits_to_f32(L.s[e]), acc * gs.x, bf16_bits_to_f32(L.t[e]) * gs.y);
     }
     const float tot = warp_sum_rows<RN>(yp, lane);
     if ((lane & (32 / RN - 1)) == 0) {
