@@ -316,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
 #pragma unroll
         for (int i = 0; i < XB; ++i) {
+          if (gb + i * NW * 4 >= G) break;  // (uniform per warp: nothing left in this batch)
           const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
           float v[8];
 #pragma unroll
@@ -339,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
 #pragma unroll
         for (int i = 0; i < XB; ++i) {
+          if (gb + i * NW * 4 >= G) break;  // (uniform per warp: nothing left in this batch)
           const float v[8] = {r0[i].x, r0[i].y, r0[i].z, r0[i].w, r1[i].x, r1[i].y, r1[i].z, r1[i].w};
           quant(gb + i * NW * 4 + (lane >> 3), v);
         }
