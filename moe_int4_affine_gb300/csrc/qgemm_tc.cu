@@ -3,14 +3,15 @@
 // on the 5th-generation tensor cores (tcgen05.mma, accumulator in tensor memory), sm_103a.
 //
 // Work split: one CTA per (128 weight rows, n_tile tokens) tile; the MMA is D[128 x n_tile] +=
-// A[128 x 16] * B[n_tile x 16]^T with A = the dequantized weights and B = the tokens, both fp16 and
-// K-major in shared memory with the 128-byte swizzle, D fp32 in tensor memory.
+// A[128 x 16] * B[n_tile x 16]^T with A = the dequantized weights (fp16, in tensor memory, one
+// weight row per lane) and B = the tokens (fp16, K-major in shared memory with the 128-byte
+// swizzle), D fp32 in tensor memory.
 //   * A pipeline stage covers one 64-column quantization group (K = 64).  Two producer warp groups
 //     (4 warps each, one thread per weight row) take alternate stages: group h produces stages
 //     j = h, h + 2, ...  A thread streams its row's packed codes, scale and bias through a
 //     per-thread cp.async ring (WRING of its groups ahead), dequantizes the 64 weights with packed
-//     half-precision arithmetic (w = s * q + b, one rounding to fp16) and stores them into the
-//     stage's A tile (one 16 KB swizzle atom).
+//     half-precision arithmetic (w = s * q + b, one rounding to fp16) and writes them with one
+//     tensor-memory store (tcgen05.st, 32 columns of its row's lane) into the stage's A columns.
 //   * The token tile of a stage is one contiguous block of the workspace (written there, already
 //     swizzled, by the prep kernel) and arrives by a single bulk copy (TMA engine) on the stage's
 //     mbarrier.
@@ -39,7 +40,10 @@ constexpr int kMaxN = 256;                   // tokens per CTA (MMA N, tensor-me
 constexpr int kProducerWarps = 8;            // two warp groups of 4: one thread per weight row each
 constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreads = kProducers + 32;    // + the MMA / tensor-memory warp
-constexpr int kATile = kBM * kGK * 2;        // 16 KB of fp16: 128 rows x one group (one swizzle atom)
+constexpr int kMaxStages = 8;
+constexpr int kAccCols = 256;                // tensor memory: columns 0..255 accumulator,
+constexpr int kACols = kGK / 2;              //   then 32 columns (64 fp16 per lane) of A per stage
+constexpr int kTmemCols = 512;
 // weight ring, per pair of groups: codes [2 chunks][256 threads][16 B], then scale and bias words
 constexpr int kWStageBytes = kProducers * 32 + kProducers * 8;
 constexpr int kSmemBudget = 220 * 1024;
@@ -54,7 +58,6 @@ struct TcArgs {
   int out, in, T;
   int n_tile;
   int stages;
-  int tmem_cols;
   uint32_t idesc;
 };
 
@@ -79,6 +82,26 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// The same with A in tensor memory (lane m = row m, K packed two fp16 per 32-bit column).
+__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// 32 consecutive 32-bit columns of this thread's lane (warp w % 4 owns lanes 32 (w % 4) .. + 31).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -149,10 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* basep = smem_raw + (base - raw);
   const int S = a.stages;
-  const uint32_t btile = (uint32_t)a.n_tile * 128u;  // token tile of one group
-  const uint32_t stage_bytes = kATile + btile;
+  const uint32_t btile = (uint32_t)a.n_tile * 128u;  // token tile of one group (the stage)
+  const uint32_t stage_bytes = btile;
   const uint32_t wring = base + (uint32_t)S * stage_bytes;  // weight staging ring
-  // full[s]: the producers' A tile; bfull[s]: the token tile's bytes; empty[s]: the stage's MMAs done
+  // full[s]: the producers' A columns; bfull[s]: the token tile's bytes; empty[s]: the stage's MMAs done
   uint64_t* full = reinterpret_cast<uint64_t*>(basep + (size_t)S * stage_bytes + (size_t)WRING * kWStageBytes);
   uint64_t* bfull = full + S;
   uint64_t* empty = bfull + S;
@@ -178,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     }
     __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(a.tmem_cols)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -205,7 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     const int odd = (int)(e0 & 1);  // which half of the copied 32-bit words holds s and b
     const uint32_t wcode = wring + (uint32_t)tid * 16;  // chunk c at + c * kProducers * 16
     const uint32_t wsb = wring + kProducers * 32 + (uint32_t)tid * 8;
-    const uint32_t a_row = (uint32_t)r * 128u;
     auto wissue = [&](int jj) {  // this thread's copies for its group jj (an empty group past the end)
       if (jj < my_n) {
         const uint32_t g = (uint32_t)(jj % WRING) * kWStageBytes;
@@ -228,10 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       const int s = j % S;
       if (j >= S && !mbar_wait(empty + s, (uint32_t)(j / S - 1) & 1u)) *abort_flag = 1;
       if (*abort_flag) break;
-      const uint32_t A = base + (uint32_t)s * stage_bytes;
+      tc_fence_after();  // the MMAs that read this stage's A columns have completed
       if (r == 0) {  // the stage's token tile: one bulk copy
         mbar_arrive_expect_tx(bfull + s, btile);
-        bulk_g2s(A + kATile, a.xt + ((size_t)tile * nk + j) * btile, btile, bfull + s);
+        bulk_g2s(base + (uint32_t)s * stage_bytes, a.xt + ((size_t)tile * nk + j) * btile, btile, bfull + s);
         ++b_issued;
       }
       wissue(jj + WRING - 1);
@@ -242,12 +264,18 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       const uint32_t s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
       const uint32_t b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
       const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      uint32_t v[32];  // column 4 ch + i: the fp16 pair i of 8-column chunk ch
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunk ch = columns 8 ch .. 8 ch + 7 of the group
-        const uint4 v = dequant8(cw[ch], s2, b2);
-        sts128(A + a_row + (uint32_t)((ch ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 d = dequant8(cw[ch], s2, b2);
+        v[4 * ch + 0] = d.x;
+        v[4 * ch + 1] = d.y;
+        v[4 * ch + 2] = d.z;
+        v[4 * ch + 3] = d.w;
       }
-      fence_proxy_async();  // the generic-proxy stores above, before the tensor core reads them
+      tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kAccCols + kACols * s), v);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(full + s);
     }
@@ -262,18 +290,20 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     }
   } else if (lane == 0) {
     // ---------------- MMA issuer
-    // Descriptors of stage 0; stage s and K step k add (s * stage_bytes + 32 k) / 16 to the start
-    // address field (bits 0-13: shared addresses stay below 2^18, so the field never carries).
-    const uint64_t da0 = smem_desc(base), db0 = smem_desc(base + kATile);
+    // B descriptors: stage s and K step k add (s * stage_bytes + 32 k) / 16 to the start address
+    // field (bits 0-13: shared addresses stay below 2^18, so the field never carries).
+    const uint64_t db0 = smem_desc(base);
     const uint32_t dstage = stage_bytes >> 4;
     int s = 0;
     uint32_t ph = 0;  // parity of stage s's current use
     for (int j = 0; j < nk; ++j) {
       if (!mbar_wait(full + s, ph) || !mbar_wait(bfull + s, ph)) *abort_flag = 1;
       if (*abort_flag) break;
-      const uint64_t da = da0 + (uint64_t)(s * dstage), db = db0 + (uint64_t)(s * dstage);
+      tc_fence_after();  // the producers' tensor-memory stores are complete
+      const uint64_t db = db0 + (uint64_t)(s * dstage);
+      const uint32_t ta = tmem + (uint32_t)(kAccCols + kACols * s);
 #pragma unroll
-      for (int k = 0; k < kGK / 16; ++k) mma_f16(tmem, da + 2 * k, db + 2 * k, a.idesc, (j | k) != 0 ? 1u : 0u);
+      for (int k = 0; k < kGK / 16; ++k) mma_f16_ta(tmem, ta + 8 * k, db + 2 * k, a.idesc, (j | k) != 0 ? 1u : 0u);
       mma_commit(empty + s);
       if (++s == S) {
         s = 0;
@@ -311,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   __syncthreads();
   if (warp == kProducerWarps) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
@@ -369,7 +399,7 @@ __global__ void __launch_bounds__(256) qgemm_prep_kernel(const uint16_t* __restr
 }
 
 struct TcPlan {
-  int n_tile, n_tiles, stages, wring, tmem_cols;
+  int n_tile, n_tiles, stages, wring;
   size_t smem;
 };
 
@@ -380,14 +410,13 @@ TcPlan tc_plan(int out, int in, int T) {
   const int t16 = (T + 15) / 16 * 16;
   p.n_tile = std::min(kMaxN, t16);
   p.n_tiles = (T + p.n_tile - 1) / p.n_tile;
-  p.tmem_cols = 32;
-  while (p.tmem_cols < p.n_tile) p.tmem_cols *= 2;
-  const size_t stage = kATile + (size_t)p.n_tile * 128;
+  const size_t stage = (size_t)p.n_tile * 128;
   const size_t fixed = 1024 + 64 + 8 * 32;  // alignment slack, barriers, slot, flag
-  // the weight ring covers memory latency (deeper for small token tiles, which are memory-bound)
-  // (the two producer warp groups take alternate stages: an even number of stages)
-  p.wring = p.n_tile >= 128 ? 2 : 4;
-  p.stages = (int)std::min<size_t>(8, (kSmemBudget - fixed - (size_t)p.wring * kWStageBytes) / stage) & ~1;
+  // stages: even (the two producer warp groups alternate), at most kMaxStages (tensor-memory
+  // columns for A); the rest of shared memory goes to the weight ring (memory latency)
+  p.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - fixed - 2 * (size_t)kWStageBytes) / stage) & ~1;
+  const size_t left = kSmemBudget - fixed - (size_t)p.stages * stage;
+  p.wring = left >= 16 * (size_t)kWStageBytes ? 16 : left >= 8 * (size_t)kWStageBytes ? 8 : left >= 4 * (size_t)kWStageBytes ? 4 : 2;
   p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
   return p;
 }
@@ -423,21 +452,25 @@ int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y,
   a.T = T;
   a.n_tile = p.n_tile;
   a.stages = p.stages;
-  a.tmem_cols = p.tmem_cols;
   // instruction descriptor (kind::f16): D fp32 (bits 4-5 = 1), A and B fp16 (bits 7-12 = 0), both
   // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
   a.idesc = (1u << 4) | ((uint32_t)(p.n_tile >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
   const dim3 grid((unsigned)((w->out + kBM - 1) / kBM), (unsigned)p.n_tiles);
-  if (p.wring == 4) {
-    auto k = qgemm_tc_kernel<4>;
+  auto go = [&](auto k) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
-      return QG_ELAUNCH;
+      return (int)QG_ELAUNCH;
     return launch(k, grid, dim3(kThreads), p.smem, stream, a);
+  };
+  switch (p.wring) {
+    case 16:
+      return go(qgemm_tc_kernel<16>);
+    case 8:
+      return go(qgemm_tc_kernel<8>);
+    case 4:
+      return go(qgemm_tc_kernel<4>);
+    default:
+      return go(qgemm_tc_kernel<2>);
   }
-  auto k = qgemm_tc_kernel<2>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
-    return QG_ELAUNCH;
-  return launch(k, grid, dim3(kThreads), p.smem, stream, a);
 }
 
 }  // namespace qg
