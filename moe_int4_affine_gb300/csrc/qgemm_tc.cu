@@ -104,6 +104,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
+// Both barriers' phases complete?  The two tests are issued together (one latency, not two).
+__device__ __forceinline__ bool test_wait2(uint64_t* b0, uint64_t* b1, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %3;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q, [%2], %3;\n\t"
+      "and.pred p, p, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b0)), "r"(smem_u32(b1)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -297,8 +311,11 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     int s = 0;
     uint32_t ph = 0;  // parity of stage s's current use
     for (int j = 0; j < nk; ++j) {
-      if (!mbar_wait(full + s, ph) || !mbar_wait(bfull + s, ph)) *abort_flag = 1;
-      if (*abort_flag) break;
+      // (fast path: both already complete; else the bounded waits, which also watch the flag)
+      if (!test_wait2(full + s, bfull + s, ph)) {
+        if (!mbar_wait(full + s, ph) || !mbar_wait(bfull + s, ph)) *abort_flag = 1;
+        if (*abort_flag) break;
+      }
       tc_fence_after();  // the producers' tensor-memory stores are complete
       const uint64_t db = db0 + (uint64_t)(s * dstage);
       const uint32_t ta = tmem + (uint32_t)(kAccCols + kACols * s);
