@@ -6,16 +6,16 @@
 // A[128 x 16] * B[n_tile x 16]^T with A = the dequantized weights (fp16, in tensor memory, one
 // weight row per lane) and B = the tokens (fp16, K-major in shared memory with the 128-byte
 // swizzle), D fp32 in tensor memory.
-//   * A pipeline stage covers one 64-column quantization group (K = 64).  Two producer warp groups
-//     (4 warps each, one thread per weight row) take alternate stages: group h produces stages
-//     j = h, h + 2, ...  A thread streams its row's packed codes, scale and bias through a
+//   * A pipeline stage covers two 64-column quantization groups (K = 128).  Two producer warp
+//     groups (4 warps each, one thread per weight row) fill them: group h makes group 2 j + h of
+//     stage j.  A thread streams its row's packed codes, scale and bias through a
 //     per-thread cp.async ring (WRING of its groups ahead), dequantizes the 64 weights with packed
 //     half-precision arithmetic (w = s * q + b, one rounding to fp16) and writes them with one
-//     tensor-memory store (tcgen05.st, 32 columns of its row's lane) into the stage's A columns.
+//     tensor-memory store (tcgen05.st, 32 columns of its row's lane) into its group's A columns.
 //   * The token tile of a stage is one contiguous block of the workspace (written there, already
 //     swizzled, by the prep kernel) and arrives by a single bulk copy (TMA engine) on the stage's
 //     mbarrier.
-//   * One thread of the MMA warp issues four K=16 MMAs per stage and commits them to the stage's
+//   * One thread of the MMA warp issues eight K=16 MMAs per stage and commits them to the stage's
 //     "empty" mbarrier; a final commit releases the epilogue, which reads the accumulator from tensor
 //     memory (tcgen05.ld), applies each token's power-of-two input scale and writes Y.
 //   * Every mbarrier wait is bounded (2 s): on a timeout the CTA records QG_STATUS_TIMEOUT, stops
@@ -40,9 +40,10 @@ constexpr int kMaxN = 256;                   // tokens per CTA (MMA N, tensor-me
 constexpr int kProducerWarps = 8;            // two warp groups of 4: one thread per weight row each
 constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreads = kProducers + 32;    // + the MMA / tensor-memory warp
-constexpr int kMaxStages = 8;
-constexpr int kAccCols = 256;                // tensor memory: columns 0..255 accumulator,
-constexpr int kACols = kGK / 2;              //   then 32 columns (64 fp16 per lane) of A per stage
+constexpr int kMaxStages = 4;
+constexpr int kAccCols = 256;                // tensor memory: columns 0..255 accumulator, then per stage
+constexpr int kACols = kGK / 2;              //   32 columns (64 fp16 per lane) of A per group,
+constexpr int kAStage = 2 * kACols;          //   two groups per stage
 constexpr int kTmemCols = 512;
 // weight ring, per pair of groups: codes [2 chunks][256 threads][16 B], then scale and bias words
 constexpr int kWStageBytes = kProducers * 32 + kProducers * 8;
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   uint8_t* basep = smem_raw + (base - raw);
   const int S = a.stages;
   const uint32_t btile = (uint32_t)a.n_tile * 128u;  // token tile of one group (the stage)
-  const uint32_t stage_bytes = btile;
+  const uint32_t stage_bytes = 2 * btile;  // the token tiles of a stage's two groups
   const uint32_t wring = base + (uint32_t)S * stage_bytes;  // weight staging ring
   // full[s]: the producers' A columns; bfull[s]: the token tile's bytes; empty[s]: the stage's MMAs done
   uint64_t* full = reinterpret_cast<uint64_t*>(basep + (size_t)S * stage_bytes + (size_t)WRING * kWStageBytes);
@@ -200,12 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = blockIdx.x * kBM;
   const int tile = blockIdx.y, n0 = tile * a.n_tile;
-  const int nk = a.in / kGK;  // groups = pipeline stages
+  const int nk = a.in / kGK;         // groups
+  const int nst = (nk + 1) / 2;      // pipeline stages (two groups each)
 
   if (warp == kProducerWarps) {
     if (lane == 0) {
       for (int s = 0; s < S; ++s) {
-        mbar_init(full + s, kProducerWarps / 2);
+        mbar_init(full + s, kProducerWarps);
         mbar_init(bfull + s, 1);
         mbar_init(empty + s, 1);
       }
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   pdl_wait();
 
   if (warp < kProducerWarps) {
-    // ---------------- producers: thread (row r, warp group h) makes stages j = 2 jj + h
+    // ---------------- producers: thread (row r, warp group h) makes group 2 j + h of every stage j
     const int r = tid & (kBM - 1), h = tid >> 7;
     const int row = m0 + r;
     const bool rv = row < a.out;
@@ -257,50 +259,51 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     };
 #pragma unroll 1
     for (int jj = 0; jj < WRING - 1; ++jj) wissue(jj);
-    int b_issued = 0;  // token-tile copies issued (thread r == 0 of each warp group)
+    int b_issued = 0;  // token-tile copies issued (thread 0)
 
-    for (int jj = 0; jj < my_n; ++jj) {
-      const int j = 2 * jj + h;  // the stage
+    for (int j = 0; j < nst; ++j) {  // stage j: groups 2 j (warp group 0) and 2 j + 1 (warp group 1)
       const int s = j % S;
       if (j >= S && !mbar_wait(empty + s, (uint32_t)(j / S - 1) & 1u)) *abort_flag = 1;
       if (*abort_flag) break;
       tc_fence_after();  // the MMAs that read this stage's A columns have completed
-      if (r == 0) {  // the stage's token tile: one bulk copy
-        mbar_arrive_expect_tx(bfull + s, btile);
-        bulk_g2s(base + (uint32_t)s * stage_bytes, a.xt + ((size_t)tile * nk + j) * btile, btile, bfull + s);
+      const int ng = min(2, nk - 2 * j);  // groups in this stage
+      if (tid == 0) {  // the stage's token tiles (contiguous in the workspace): one bulk copy
+        const uint32_t bytes = (uint32_t)ng * btile;
+        mbar_arrive_expect_tx(bfull + s, bytes);
+        bulk_g2s(base + (uint32_t)s * stage_bytes, a.xt + ((size_t)tile * nk + 2 * (size_t)j) * btile, bytes,
+                 bfull + s);
         ++b_issued;
       }
-      wissue(jj + WRING - 1);
-      cp_wait<WRING - 1>();  // group jj of this thread has landed
-      const uint32_t g = (uint32_t)(jj % WRING) * kWStageBytes;
-      const uint4 c0 = lds128(wcode + g), c1 = lds128(wcode + g + kProducers * 16);
-      const uint32_t sw = lds32(wsb + g), bw = lds32(wsb + g + 4);
-      const uint32_t s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
-      const uint32_t b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
-      const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      uint32_t v[32];  // column 4 ch + i: the fp16 pair i of 8-column chunk ch
+      wissue(j + WRING - 1);  // (this thread's group 2 j + h is its j-th)
+      cp_wait<WRING - 1>();   // group j of this thread has landed
+      if (h < ng) {           // (uniform per warp)
+        const uint32_t g = (uint32_t)(j % WRING) * kWStageBytes;
+        const uint4 c0 = lds128(wcode + g), c1 = lds128(wcode + g + kProducers * 16);
+        const uint32_t sw = lds32(wsb + g), bw = lds32(wsb + g + 4);
+        const uint32_t s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
+        const uint32_t b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
+        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t v[32];  // column 4 ch + i: the fp16 pair i of 8-column chunk ch
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 d = dequant8(cw[ch], s2, b2);
-        v[4 * ch + 0] = d.x;
-        v[4 * ch + 1] = d.y;
-        v[4 * ch + 2] = d.z;
-        v[4 * ch + 3] = d.w;
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 d = dequant8(cw[ch], s2, b2);
+          v[4 * ch + 0] = d.x;
+          v[4 * ch + 1] = d.y;
+          v[4 * ch + 2] = d.z;
+          v[4 * ch + 3] = d.w;
+        }
+        tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kAccCols + kAStage * s + kACols * h), v);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kAccCols + kACols * s), v);
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(full + s);
     }
     cp_wait<0>();
-    if (r == 0) {
+    if (tid == 0) {
       // every bulk copy issued here has landed before the CTA can exit (normally long since: the MMA
-      // thread waited for it); this thread's latest use of each of its stages may be outstanding
-      for (int jj = max(0, b_issued - S / 2); jj < b_issued; ++jj) {
-        const int j = 2 * jj + h;
-        mbar_wait(bfull + j % S, (uint32_t)(j / S) & 1u);
-      }
+      // thread waited for it); the latest use of each stage may be outstanding
+      for (int j = max(0, b_issued - S); j < b_issued; ++j) mbar_wait(bfull + j % S, (uint32_t)(j / S) & 1u);
     }
   } else if (lane == 0) {
     // ---------------- MMA issuer
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     const uint32_t dstage = stage_bytes >> 4;
     int s = 0;
     uint32_t ph = 0;  // parity of stage s's current use
-    for (int j = 0; j < nk; ++j) {
+    for (int j = 0; j < nst; ++j) {
       // (fast path: both already complete; else the bounded waits, which also watch the flag)
       if (!test_wait2(full + s, bfull + s, ph)) {
         if (!mbar_wait(full + s, ph) || !mbar_wait(bfull + s, ph)) *abort_flag = 1;
@@ -318,9 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       }
       tc_fence_after();  // the producers' tensor-memory stores are complete
       const uint64_t db = db0 + (uint64_t)(s * dstage);
-      const uint32_t ta = tmem + (uint32_t)(kAccCols + kACols * s);
+      const uint32_t ta = tmem + (uint32_t)(kAccCols + kAStage * s);
+      const int ng = min(2, nk - 2 * j);
+      for (int gi = 0; gi < ng; ++gi) {
 #pragma unroll
-      for (int k = 0; k < kGK / 16; ++k) mma_f16_ta(tmem, ta + 8 * k, db + 2 * k, a.idesc, (j | k) != 0 ? 1u : 0u);
+        for (int k = 0; k < kGK / 16; ++k)
+          mma_f16_ta(tmem, ta + kACols * gi + 8 * k, db + (uint64_t)(gi * (btile >> 4)) + 2 * k, a.idesc,
+                     (j | gi | k) != 0 ? 1u : 0u);
+      }
       mma_commit(empty + s);
       if (++s == S) {
         s = 0;
@@ -367,49 +375,62 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 // ((tile * nk + kc) * n_tile + n % n_tile) * 128, the 16-byte chunk j (columns 8j .. 8j + 7 of the
 // group) at position j ^ (n % 8), its eight values in the column order 0, 4, 1, 5, 2, 6, 3, 7 (the
 // order the dequantized weights use).  Rows n >= T are zero.
-__global__ void __launch_bounds__(256) qgemm_prep_kernel(const uint16_t* __restrict__ X, int T, int in, int n_tile,
-                                                         uint8_t* __restrict__ xt, float* __restrict__ xs) {
-  __shared__ float red[8];
+constexpr int kPrepThreads = 256;
+constexpr int kPrepMaxChunks = 16;  // 16-byte chunks per thread: in <= 16 * 256 * 8 = 32768
+
+__global__ void __launch_bounds__(kPrepThreads) qgemm_prep_kernel(const uint16_t* __restrict__ X, int T, int in,
+                                                                   int n_tile, uint8_t* __restrict__ xt,
+                                                                   float* __restrict__ xs) {
+  __shared__ uint32_t red[kPrepThreads / 32];
   const int n = blockIdx.x;
-  const int nk = in / 64;
+  const int nk = in / 64, nch = in / 8;
   const bool live = n < T;
-  const uint16_t* xr = X + (size_t)(live ? n : 0) * in;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? n : 0) * in);
   pdl_trigger();
   pdl_wait();
-  float m = 0.f;
-  if (live)
-    for (int i = threadIdx.x; i < in; i += blockDim.x) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)xr[i] << 16)));
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (threadIdx.x == 0) red[0] = v;
+  // one round of loads; the largest |x| from the bit patterns (|bf16| bits are ordered like values)
+  uint4 raw[kPrepMaxChunks];
+  uint32_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < kPrepMaxChunks; ++i) {
+    const int ch = (int)threadIdx.x + i * kPrepThreads;
+    raw[i] = live && ch < nch ? __ldg(xr + ch) : make_uint4(0u, 0u, 0u, 0u);
+    mx = __vmaxu2(mx, raw[i].x & 0x7FFF7FFFu);
+    mx = __vmaxu2(mx, raw[i].y & 0x7FFF7FFFu);
+    mx = __vmaxu2(mx, raw[i].z & 0x7FFF7FFFu);
+    mx = __vmaxu2(mx, raw[i].w & 0x7FFF7FFFu);
   }
+  mx = max(mx & 0xFFFFu, mx >> 16);
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
   __syncthreads();
-  m = red[0];
+  mx = 0;
+#pragma unroll
+  for (int w = 0; w < kPrepThreads / 32; ++w) mx = max(mx, red[w]);
+  const float m = __uint_as_float(mx << 16);
   // 2^(14 - e) with e = floor(log2 m): the row's largest magnitude lands in [2^14, 2^15)
   const int e = m > 0.f ? (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
   const float sc = live && m > 0.f ? exp2i(min(max(14 - e, -126), 127)) : 0.f;
   if (threadIdx.x == 0) xs[n] = live && m > 0.f ? exp2i(min(max(e - 14, -126), 127)) : 0.f;
   const int tile = n / n_tile, nl = n % n_tile;
-  constexpr int kOrder[8] = {0, 4, 1, 5, 2, 6, 3, 7};
-  for (int ch = threadIdx.x; ch < in / 8; ch += blockDim.x) {
-    const int kc = ch >> 3, j = ch & 7;
-    uint32_t hv[8];
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const float f = live ? __uint_as_float((uint32_t)xr[ch * 8 + kOrder[p]] << 16) * sc : 0.f;
-      uint16_t b;
-      asm("cvt.rn.f16.f32 %0, %1;" : "=h"(b) : "f"(f));
-      hv[p] = b;
+  for (int i = 0; i < kPrepMaxChunks; ++i) {
+    const int ch = (int)threadIdx.x + i * kPrepThreads;
+    if (ch >= nch) break;
+    const int kc = ch >> 3, j = ch & 7;
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    float f[8];  // the chunk's 8 values, scaled
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      f[2 * q] = __uint_as_float(w[q] << 16) * sc;
+      f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
     }
+    // fp16 pairs in the column order 0, 4, 1, 5, 2, 6, 3, 7 (low half first)
     uint4 o;
-    o.x = hv[0] | (hv[1] << 16);
-    o.y = hv[2] | (hv[3] << 16);
-    o.z = hv[4] | (hv[5] << 16);
-    o.w = hv[6] | (hv[7] << 16);
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.x) : "f"(f[4]), "f"(f[0]));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.y) : "f"(f[5]), "f"(f[1]));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.z) : "f"(f[6]), "f"(f[2]));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.w) : "f"(f[7]), "f"(f[3]));
     uint8_t* dst = xt + (((size_t)tile * nk + kc) * n_tile + nl) * 128 + (size_t)((j ^ (nl & 7)) << 4);
     *reinterpret_cast<uint4*>(dst) = o;
   }
@@ -427,11 +448,11 @@ TcPlan tc_plan(int out, int in, int T) {
   const int t16 = (T + 15) / 16 * 16;
   p.n_tile = std::min(kMaxN, t16);
   p.n_tiles = (T + p.n_tile - 1) / p.n_tile;
-  const size_t stage = (size_t)p.n_tile * 128;
-  const size_t fixed = 1024 + 64 + 8 * 32;  // alignment slack, barriers, slot, flag
-  // stages: even (the two producer warp groups alternate), at most kMaxStages (tensor-memory
-  // columns for A); the rest of shared memory goes to the weight ring (memory latency)
-  p.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - fixed - 2 * (size_t)kWStageBytes) / stage) & ~1;
+  const size_t stage = 2 * (size_t)p.n_tile * 128;  // token tiles of two groups
+  const size_t fixed = 1024 + 64 + 8 * 32;          // alignment slack, barriers, slot, flag
+  // stages: at most kMaxStages (tensor-memory columns for A); the rest of shared memory goes to the
+  // weight ring (memory latency)
+  p.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - fixed - 2 * (size_t)kWStageBytes) / stage);
   const size_t left = kSmemBudget - fixed - (size_t)p.stages * stage;
   p.wring = left >= 16 * (size_t)kWStageBytes ? 16 : left >= 8 * (size_t)kWStageBytes ? 8 : left >= 4 * (size_t)kWStageBytes ? 4 : 2;
   p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
@@ -455,7 +476,8 @@ int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y,
   if (ws_bytes < qgemm_tc_workspace_bytes(w, T)) return QG_EWORKSPACE;
   uint8_t* xt = static_cast<uint8_t*>(ws);
   float* xs = reinterpret_cast<float*>(xt + xt_bytes);
-  int rc = launch(qgemm_prep_kernel, dim3((unsigned)rows), dim3(256), 0, stream, X, T, w->in, p.n_tile, xt, xs);
+  int rc = launch(qgemm_prep_kernel, dim3((unsigned)rows), dim3(kPrepThreads), 0, stream, X, T, w->in, p.n_tile, xt,
+                  xs);
   if (rc != QG_OK) return rc;
   TcArgs a{};
   a.packed = w->packed;
