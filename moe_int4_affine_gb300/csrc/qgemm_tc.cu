@@ -8,7 +8,8 @@
 // swizzle), D fp32 in tensor memory.
 //   * A pipeline stage covers two 64-column quantization groups (K = 128).  Two producer warp
 //     groups (4 warps each, one thread per weight row) fill them: group h makes group 2 j + h of
-//     stage j.  A thread streams its row's packed codes, scale and bias through a
+//     stage j.  (A tenth warp issues the stages' token-tile copies.)  A thread streams its row's
+//     packed codes, scale and bias through a
 //     per-thread cp.async ring (WRING of its groups ahead), dequantizes the 64 weights with packed
 //     half-precision arithmetic (w = s * q + b, one rounding to fp16) and writes them with one
 //     tensor-memory store (tcgen05.st, 32 columns of its row's lane) into its group's A columns.
@@ -39,7 +40,9 @@ constexpr int kGK = 64;                      // columns of one quantization grou
 constexpr int kMaxN = 256;                   // tokens per CTA (MMA N, tensor-memory columns)
 constexpr int kProducerWarps = 8;            // two warp groups of 4: one thread per weight row each
 constexpr int kProducers = kProducerWarps * 32;
-constexpr int kThreads = kProducers + 32;    // + the MMA / tensor-memory warp
+constexpr int kMmaWarp = kProducerWarps;      // the MMA / tensor-memory warp
+constexpr int kLoadWarp = kProducerWarps + 1; // the token-tile loader
+constexpr int kThreads = kProducers + 64;
 constexpr int kMaxStages = 4;
 constexpr int kAccCols = 256;                // tensor memory: columns 0..255 accumulator, then per stage
 constexpr int kACols = kGK / 2;              //   32 columns (64 fp16 per lane) of A per group,
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   const int nk = a.in / kGK;         // groups
   const int nst = (nk + 1) / 2;      // pipeline stages (two groups each)
 
-  if (warp == kProducerWarps) {
+  if (warp == kMmaWarp) {
     if (lane == 0) {
       for (int s = 0; s < S; ++s) {
         mbar_init(full + s, kProducerWarps);
@@ -259,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     };
 #pragma unroll 1
     for (int jj = 0; jj < WRING - 1; ++jj) wissue(jj);
-    int b_issued = 0;  // token-tile copies issued (thread 0)
 
     for (int j = 0; j < nst; ++j) {  // stage j: groups 2 j (warp group 0) and 2 j + 1 (warp group 1)
       const int s = j % S;
@@ -267,13 +269,6 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       if (*abort_flag) break;
       tc_fence_after();  // the MMAs that read this stage's A columns have completed
       const int ng = min(2, nk - 2 * j);  // groups in this stage
-      if (tid == 0) {  // the stage's token tiles (contiguous in the workspace): one bulk copy
-        const uint32_t bytes = (uint32_t)ng * btile;
-        mbar_arrive_expect_tx(bfull + s, bytes);
-        bulk_g2s(base + (uint32_t)s * stage_bytes, a.xt + ((size_t)tile * nk + 2 * (size_t)j) * btile, bytes,
-                 bfull + s);
-        ++b_issued;
-      }
       wissue(j + WRING - 1);  // (this thread's group 2 j + h is its j-th)
       cp_wait<WRING - 1>();   // group j of this thread has landed
       if (h < ng) {           // (uniform per warp)
@@ -300,12 +295,26 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(full + s);
     }
     cp_wait<0>();
-    if (tid == 0) {
+  } else if (warp == kLoadWarp) {
+    // ---------------- token-tile loader: stage j's tiles (contiguous in the workspace), one bulk
+    // copy each, issued as soon as the stage is free
+    if (lane == 0) {
+      int issued = 0;
+      for (int j = 0; j < nst; ++j) {
+        const int s = j % S;
+        if (j >= S && !mbar_wait(empty + s, (uint32_t)(j / S - 1) & 1u)) *abort_flag = 1;
+        if (*abort_flag) break;
+        const uint32_t bytes = (uint32_t)min(2, nk - 2 * j) * btile;
+        mbar_arrive_expect_tx(bfull + s, bytes);
+        bulk_g2s(base + (uint32_t)s * stage_bytes, a.xt + ((size_t)tile * nk + 2 * (size_t)j) * btile, bytes,
+                 bfull + s);
+        ++issued;
+      }
       // every bulk copy issued here has landed before the CTA can exit (normally long since: the MMA
       // thread waited for it); the latest use of each stage may be outstanding
-      for (int j = max(0, b_issued - S); j < b_issued; ++j) mbar_wait(bfull + j % S, (uint32_t)(j / S) & 1u);
+      for (int j = max(0, issued - S); j < issued; ++j) mbar_wait(bfull + j % S, (uint32_t)(j / S) & 1u);
     }
-  } else if (lane == 0) {
+  } else if (lane == 0) {  // (warp kMmaWarp)
     // ---------------- MMA issuer
     // B descriptors: stage s and K step k add (s * stage_bytes + 32 k) / 16 to the start address
     // field (bits 0-13: shared addresses stay below 2^18, so the field never carries).
@@ -364,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kProducerWarps) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
