@@ -383,9 +383,15 @@ def measure_configs(qg, I, dev, stream):
                                               P(wsb.data_ptr()), wsb.numel(), s)
     us = tl(moe, 100)
     nbytes = K * 3 * weight_bytes(INTER, HID) + 2 * HID * 2 + E * 4 + HID * 4
-    res["c3_moe_layer_T1"] = dict(gb(nbytes, us), kernels=3,
-                                  l2=f"128-expert pool ({3 * E * weight_bytes(INTER, HID) / 1e6:.0f} MB), router "
-                                     "logits rotate over 16 vectors")
+    l2 = f"128-expert pool ({3 * E * weight_bytes(INTER, HID) / 1e6:.0f} MB), router logits rotate over 16 vectors"
+    res["c3_moe_layer_T1"] = dict(gb(nbytes, us), kernels=3, call="moe_router_topk + moe_gather_qgemv_int4", l2=l2)
+
+    def moe_fused(i):
+        return lib.moe_layer_int4(P(logits[i % 16].data_ptr()), 1, byref(g.struct), byref(u.struct), byref(d.struct),
+                                  K, P(x.data_ptr()), P(r.data_ptr()), P(y.data_ptr()), P(idx.data_ptr()),
+                                  P(pk.data_ptr()), P(wsb.data_ptr()), wsb.numel(), s)
+    us = tl(moe_fused, 100)
+    res["c3_moe_layer_T1_fused_router"] = dict(gb(nbytes, us), kernels=2, call="moe_layer_int4", l2=l2)
     del g, u, d
 
     # config 4: dequant-GEMM, W 17408 x 5120, X T x 5120

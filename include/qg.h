@@ -126,6 +126,22 @@ int moe_gather_qgemv_int4(const qg_int4_weight *gate, const qg_int4_weight *up, 
                           float *y, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * moe_layer_int4 -- the whole MoE decode step in two launches: moe_router_topk followed by
+ * moe_gather_qgemv_int4, with the router computed inside the expert gate/up kernel (every CTA
+ * selects the top k itself, so no separate router launch and no index round trip through global
+ * memory before the expert weights are read).  Same results as the two calls.
+ * logits: fp32 [gate->n_mat] (device, finite); renorm as in moe_router_topk.
+ * idx (uint32 [k]) and p (fp32 [k]): device outputs, the router's selection (also read by the
+ * down projection).  Other arguments, workspace and limits as moe_gather_qgemv_int4 (1 <= k <= 8),
+ * and n_experts = gate->n_mat <= 1024.
+ * (The pages run the router and the expert kernels as separate dispatches; this fusion is this
+ * library's.)
+ */
+int moe_layer_int4(const float *logits, int renorm, const qg_int4_weight *gate, const qg_int4_weight *up,
+                   const qg_int4_weight *down, int k, const uint16_t *x, const uint16_t *residual, float *y,
+                   uint32_t *idx, float *p, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * moe_gather_qgemv_int4_noalloc -- the same computation, arguments and limits as
  * moe_gather_qgemv_int4, without a workspace argument.  The pages have no counterpart: this entry
  * point exists for callers that cannot hand over device scratch, such as a host runtime that owns

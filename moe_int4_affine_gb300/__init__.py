@@ -8,7 +8,7 @@ back to anything else.  ``inputs`` holds the seeded synthetic data generators.
 """
 from importlib import import_module
 
-_API = ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4", "moe_gather_qgemv_int4_noalloc",
+_API = ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4", "moe_gather_qgemv_int4_noalloc", "moe_layer_int4",
         "scalar_fma_chain8_residual", "qgemm_int4", "qg_workspace_bytes", "qg_device_status",
         "qg_strerror", "qg_set_pdl", "qg_version", "Int4Weight", "QGError", "to_device", "to_numpy")
 

@@ -110,6 +110,30 @@ int moe_gather_qgemv_int4(const qg_int4_weight* gate, const qg_int4_weight* up, 
   return moe_down_launch(down, idx, p, k, h, residual, y, s);
 }
 
+int moe_layer_int4(const float* logits, int renorm, const qg_int4_weight* gate, const qg_int4_weight* up,
+                   const qg_int4_weight* down, int k, const uint16_t* x, const uint16_t* residual, float* y,
+                   uint32_t* idx, float* p, void* workspace, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_weight(gate, true)) || (rc = check_weight(up, true)) || (rc = check_weight(down, true))) return rc;
+  if (!logits || !idx || !p || !x || !residual || !y) return QG_EINVAL;
+  if (k < 1 || k > 8 || (renorm != 0 && renorm != 1) || gate->n_mat < k) return QG_EINVAL;
+  if (gate->n_mat > 1024) return QG_ENOTSUP;
+  if (gate->out != up->out || gate->in != up->in || gate->n_mat != up->n_mat || down->n_mat != gate->n_mat ||
+      down->in != gate->out || down->out != gate->in)
+    return QG_EINVAL;
+  if (!aligned16(logits) || !aligned16(idx) || !aligned16(p) || !aligned16(x) || !aligned16(residual) ||
+      !aligned16(y))
+    return QG_EALIGN;
+  const size_t need = qg_workspace_bytes(QG_OP_MOE, down, k);
+  if (!workspace || ws_bytes < need) return QG_EWORKSPACE;
+  if (!aligned16(workspace)) return QG_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* h = static_cast<float*>(workspace);
+  rc = moe_gate_up_routed_launch(logits, gate->n_mat, renorm, gate, up, k, x, h, idx, p, s);
+  if (rc) return rc;
+  return moe_down_launch(down, idx, p, k, h, residual, y, s);
+}
+
 int scalar_fma_chain8_residual(const float* p, const float* v, const uint16_t* residual, float* out, int n,
                                void* stream) {
   if (!p || !v || !residual || !out || n < 1) return QG_EINVAL;

@@ -80,6 +80,13 @@ struct GemvArgs {
   int groups;                         // nseg * in / 64
   int total_rows;
   int rows_per_cta;  // upper bound of a CTA's row count (sizes the partial-sum buffer)
+  // Router in the kernel (pair mode, MoE gate/up): with `logits` set, every CTA selects the top
+  // nmat of n_logits logits itself (instead of reading idx), and CTA 0 writes the selection to
+  // idx_out / p_out for the kernels that follow.
+  const float* logits;
+  int n_logits, renorm;
+  uint32_t* idx_out;
+  float* p_out;
 };
 
 struct WPtr {
@@ -88,11 +95,12 @@ struct WPtr {
   const uint16_t* biases;
 };
 
-// Resolve a weight reference to this call's slab.  `ok` is false for an out-of-range index.
-__device__ __forceinline__ WPtr resolve(const GemvArgs& a, const WRef& r, bool& ok) {
+// Resolve a weight reference to this call's slab, expert indices from `idx` (global or shared
+// memory).  `ok` is false for an out-of-range index.
+__device__ __forceinline__ WPtr resolve(const GemvArgs& a, const uint32_t* idx, const WRef& r, bool& ok) {
   ok = true;
   if (r.slot < 0) return WPtr{r.packed, r.scales, r.biases};
-  const uint32_t e = __ldg(a.idx + r.slot);
+  const uint32_t e = idx[r.slot];
   if (e >= (uint32_t)a.n_experts) {
     ok = false;
     return WPtr{r.packed, r.scales, r.biases};
@@ -182,6 +190,71 @@ __device__ __forceinline__ bool block_rows(const GemvArgs& a, int vb, int ve, in
   return false;
 }
 
+// ------------------------------------------------------------------ router top-k (one warp)
+// Order-preserving key of a finite float: larger floats give larger unsigned keys; -0 and +0 get
+// the same key (they compare equal, so the index decides between them).
+__device__ __forceinline__ uint32_t router_float_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Top-k of n logits by one warp ([FFAI#14] commit "moeRouterTopK"; order (value desc, index asc)
+// as in [FFAI#9]): a candidate is the 64-bit key (float key << 32) | ~index, unique per expert, so
+// round s takes the warp's largest key below round s - 1's.  Weights: softmax over the k selected
+// logits (renorm) or over all n read at the selected ones.  Results for slot s go to idx[s] / p[s]
+// (shared memory) and, when given, to gidx[s] / gp[s] (global).  k <= 32, n <= 1024.
+__device__ __forceinline__ void route_topk_warp(const float* logits, int n, int k, int renorm, uint32_t* idx,
+                                                float* p, uint32_t* gidx, float* gp) {
+  const int lane = threadIdx.x & 31;
+  // up to 128 experts: the lane's keys stay in registers; beyond, they are re-read each round
+  unsigned long long kr[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = lane + 32 * j;
+    kr[j] = e < n ? ((unsigned long long)router_float_key(__ldg(logits + e)) << 32) | (uint32_t)~(uint32_t)e : 0ull;
+  }
+  unsigned long long prev = ~0ull, mine = 0;
+  for (int s = 0; s < k; ++s) {
+    unsigned long long best = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (kr[j] < prev && kr[j] > best) best = kr[j];
+    for (int e = lane + 128; e < n; e += 32) {
+      const unsigned long long key = ((unsigned long long)router_float_key(__ldg(logits + e)) << 32) | (uint32_t)~(uint32_t)e;
+      if (key < prev && key > best) best = key;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+      best = o > best ? o : best;
+    }
+    if (lane == s) mine = best;
+    prev = best;
+  }
+  const uint32_t my_idx = ~(uint32_t)mine;
+  const uint32_t kv = (uint32_t)(mine >> 32);
+  const float my_v = __uint_as_float((kv & 0x80000000u) ? (kv & 0x7FFFFFFFu) : ~kv);
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);  // round 0 took the largest logit
+  float z = 0.f;
+  if (renorm) {
+    z = lane < k ? expf(my_v - m) : 0.f;
+  } else {
+    for (int e = lane; e < n; e += 32) z += expf(__ldg(logits + e) - m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+  if (lane < k) {
+    const float pv = expf(my_v - m) / z;
+    idx[lane] = my_idx;
+    p[lane] = pv;
+    if (gidx) {
+      gidx[lane] = my_idx;
+      gp[lane] = pv;
+    }
+  }
+}
+
 // Shared memory per CTA: x of group g as 32 u32 (64 int16 values paired for dp2a: per 8-column
 // word w, (X0, X2), (X4, X6), (X1, X3), (X5, X7)) stored at 16-byte slot (w + g) % 8 of the group's
 // 128 bytes -- the rotation keeps a warp's loads (one group per lane, 128 bytes apart) free of bank
@@ -205,6 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const int nkc = (G + kGroupsPerUnit - 1) / kGroupsPerUnit;  // K chunks per row
 
   pdl_trigger();
+  __shared__ uint32_t s_idx[kMaxMats];  // the in-kernel router's selection
+  __shared__ float s_p[kMaxMats];
+  const bool indexed = a.idx != nullptr || a.logits != nullptr;  // slots resolved through indices
+  const uint32_t* idxp = a.logits ? s_idx : a.idx;
 
   int nblocks = 0;
   for (int mi = 0; mi < a.nmat; ++mi) {
@@ -226,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     for (int e = 0; e < RN; ++e) {
       const int r = e / NC, c = e % NC;
       bool ok;
-      const WPtr w = resolve(a, SEG ? WRef{a.seg.packed, a.seg.scales, a.seg.biases, sg} : a.mat[m].w[c], ok);
+      const WPtr w = resolve(a, idxp, SEG ? WRef{a.seg.packed, a.seg.scales, a.seg.biases, sg} : a.mat[m].w[c], ok);
       const size_t row = (size_t)(rf + min(r, nr - 1));
       // Every load is in bounds (clamped row and group, the base slab for a bad expert); entries
       // past the block, past the last group or of a bad expert get scale and bias 0, so add 0.
@@ -253,11 +330,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   UnitLoads<RN> b0, b1;
   int u = warp;
   UnitCursor uc{warp / nkc, warp % nkc};
-  if (u < nunits && !a.idx) issue(uc, b0);  // before the dependency wait: weights only
+  if (u < nunits && !indexed) issue(uc, b0);  // before the dependency wait: weights only
 
   // --- x: 16-bit fixed point per group, into shared memory ---
   pdl_wait();
-  if (u < nunits && a.idx) issue(uc, b0);
+  if (a.logits) {  // the router, in every CTA
+    if (warp == 0) route_topk_warp(a.logits, a.n_logits, a.nmat, a.renorm, s_idx, s_p, blockIdx.x == 0 ? a.idx_out : nullptr,
+                                   blockIdx.x == 0 ? a.p_out : nullptr);
+    __syncthreads();
+  }
+  if (u < nunits && indexed) issue(uc, b0);
   {
     // 8 lanes per group, 8 values (one 8-column word) per lane.  All of a thread's loads (up to 8
     // groups of bf16 or 5 of fp32: one round for every in <= 32768 bf16 / 20480 fp32) are issued
@@ -296,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           float wgt = 1.f;
           if (SEG) {
             bool ok;
-            resolve(a, WRef{a.seg.packed, a.seg.scales, a.seg.biases, g / ngs}, ok);
+            resolve(a, idxp, WRef{a.seg.packed, a.seg.scales, a.seg.biases, g / ngs}, ok);
             wgt = ok ? __ldg(a.p + g / ngs) : 0.f;
           }
           // (2^-k / 16: the odd codes are accumulated sixteen times over, see the main loop)
@@ -348,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
   }
   if (a.idx && blockIdx.x == 0 && (int)threadIdx.x < (SEG ? a.nseg : a.nmat)) {
-    if (__ldg(a.idx + threadIdx.x) >= (uint32_t)a.n_experts) set_status(QG_STATUS_BAD_EXPERT);
+    if (idxp[threadIdx.x] >= (uint32_t)a.n_experts) set_status(QG_STATUS_BAD_EXPERT);
   }
   __syncthreads();
 
@@ -414,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       float up = 0.f;
       for (int kc = 0; kc < nkc; ++kc) up += part[(lr * NC + 1) * nkc + kc];
       bool ok = true;
-      if (mt.w[0].slot >= 0) resolve(a, mt.w[0], ok);
+      if (mt.w[0].slot >= 0) resolve(a, idxp, mt.w[0], ok);
       acc = ok ? acc / (1.f + expf(-acc)) * up : 0.f;
     }
     if (SEG && a.resid) acc += bf16_bits_to_f32(a.resid[row]);

@@ -47,4 +47,35 @@ int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, con
   return plan_and_launch<kPair>(a, stream);
 }
 
+// The same with the router in the kernel: every CTA selects the top k of n_logits logits itself;
+// CTA 0 writes the selection to idx_out / p_out for the down kernel.
+int moe_gate_up_routed_launch(const float* logits, int n_logits, int renorm, const qg_int4_weight* gate,
+                              const qg_int4_weight* up, int k, const uint16_t* x, float* h, uint32_t* idx_out,
+                              float* p_out, cudaStream_t stream) {
+  if (k < 1 || k > kMaxMats) return QG_EINVAL;
+  GemvArgs a{};
+  a.nmat = k;
+  for (int m = 0; m < k; ++m) {
+    a.mat[m].w[0] = WRef{gate->packed, gate->scales, gate->biases, m};
+    a.mat[m].w[1] = WRef{up->packed, up->scales, up->biases, m};
+    a.mat[m].y = h + (size_t)m * gate->out;
+    a.mat[m].out = gate->out;
+    a.mat[m].row0 = m * gate->out;
+  }
+  a.nseg = 1;
+  a.x = x;
+  a.xf32 = 0;
+  a.logits = logits;
+  a.n_logits = n_logits;
+  a.renorm = renorm;
+  a.idx_out = idx_out;
+  a.p_out = p_out;
+  a.n_experts = gate->n_mat;
+  a.slab_words = (long long)gate->out * (gate->in / 8);
+  a.slab_groups = (long long)gate->out * (gate->in / 64);
+  a.in = gate->in;
+  a.total_rows = k * gate->out;
+  return plan_and_launch<kPair>(a, stream);
+}
+
 }  // namespace qg

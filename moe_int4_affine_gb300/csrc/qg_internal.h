@@ -59,6 +59,9 @@ int gemv_pair_launch(const GemvMatArg& gate, const GemvMatArg& up, const void* x
 int gemv_tune(int ctas_per_sm);
 int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, const uint32_t* idx, int k,
                        const uint16_t* x, float* h, cudaStream_t stream);
+int moe_gate_up_routed_launch(const float* logits, int n_logits, int renorm, const qg_int4_weight* gate,
+                              const qg_int4_weight* up, int k, const uint16_t* x, float* h, uint32_t* idx_out,
+                              float* p_out, cudaStream_t stream);
 int moe_down_launch(const qg_int4_weight* down, const uint32_t* idx, const float* p, int k, const float* h,
                     const uint16_t* residual, float* y, cudaStream_t stream);
 

@@ -40,6 +40,7 @@ lib.qgemv_int4.argtypes = [_W, _P, _I, _P, _P]
 lib.qgemv_int4_multi.argtypes = [_I, _W, _P, _I, ctypes.POINTER(_P), _I, _P]
 lib.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
 lib.moe_gather_qgemv_int4.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]
+lib.moe_layer_int4.argtypes = [_P, _I, _W, _W, _W, _I, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
 lib.moe_gather_qgemv_int4_noalloc.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P]
 lib.scalar_fma_chain8_residual.argtypes = [_P, _P, _P, _P, _I, _P]
 lib.qgemm_int4.argtypes = [_W, _P, _I, _P, _P, ctypes.c_size_t, _P]
@@ -54,7 +55,7 @@ lib.qg_strerror.argtypes = [_I]
 lib.qg_strerror.restype = ctypes.c_char_p
 lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
-           "moe_gather_qgemv_int4_noalloc",
+           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4",
            "scalar_fma_chain8_residual", "qgemm_int4", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
 
@@ -198,6 +199,27 @@ def moe_gather_qgemv_int4(gate: Int4Weight, up: Int4Weight, down: Int4Weight, id
                                      workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_gather_qgemv_int4")
     return y
+
+
+def moe_layer_int4(logits, gate: Int4Weight, up: Int4Weight, down: Int4Weight, x, residual, k: int = 8,
+                   renorm: bool = True, y=None, idx=None, p=None, workspace=None, stream=None):
+    """Router + expert gather in one call; returns (y, idx, p)."""
+    torch = _torch()
+    dev = x.device
+    if y is None:
+        y = torch.empty(down.out, dtype=torch.float32, device=dev)
+    if idx is None:
+        idx = torch.empty(k, dtype=torch.int32, device=dev)
+    if p is None:
+        p = torch.empty(k, dtype=torch.float32, device=dev)
+    need = qg_workspace_bytes(QG_OP_MOE, down, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(lib.moe_layer_int4(_ptr(logits), 1 if renorm else 0, ctypes.byref(gate.struct), ctypes.byref(up.struct),
+                              ctypes.byref(down.struct), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(idx), _ptr(p),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_layer_int4")
+    return y, idx, p
 
 
 def moe_gather_qgemv_int4_noalloc(gate: Int4Weight, up: Int4Weight, down: Int4Weight, idx, p, x, residual, y,

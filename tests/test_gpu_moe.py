@@ -152,3 +152,41 @@ def test_router_signed_zero_and_negative_logits(qg):
     i_ref, p_ref = oracle.router_topk(neg.astype(np.float32), 8, False)
     assert qg.to_numpy(idx).astype(np.uint32).tolist() == i_ref.tolist()
     np.testing.assert_allclose(qg.to_numpy(p), p_ref, rtol=2e-6, atol=1e-9)
+
+
+@pytest.mark.parametrize("seed,renorm", [(0, True), (1, True), (2, False)])
+def test_moe_layer_fused_router_matches_oracle_and_two_calls(qg, moe_full, seed, renorm):
+    """moe_layer_int4 (router inside the gate/up kernel): indices bit-exact with the oracle's
+    router, y within the bound, and the same result as moe_router_topk + moe_gather_qgemv_int4."""
+    gate, up, down = moe_full
+    logits = I.f32_normal(seed + 10, I.TID_LOGITS, 128)
+    x = I.bf16_normal(seed + 10, I.TID_X, 2048)
+    r = I.bf16_normal(seed + 10, I.TID_RESID, 2048)
+    G, U, D = (qg.Int4Weight.from_numpy(d) for d in (gate, up, down))
+    lg, xd, rd = qg.to_device(logits), qg.to_device(x), qg.to_device(r)
+    y, idx, p = qg.moe_layer_int4(lg, G, U, D, xd, rd, k=8, renorm=renorm)
+    i_ref, p_ref = oracle.router_topk(logits, 8, renorm)
+    assert qg.to_numpy(idx).astype(np.uint32).tolist() == i_ref.tolist()
+    np.testing.assert_allclose(qg.to_numpy(p), p_ref, rtol=2e-6, atol=1e-9)
+    y_ref, a, flags = oracle.moe(_t(gate), _t(up), _t(down), i_ref, p_ref, x, r)
+    assert flags == 0
+    y_np = qg.to_numpy(y).astype(np.float64)
+    assert_within_bound(y_np, y_ref, a)
+    idx2, p2 = qg.moe_router_topk(lg, k=8, renorm=renorm)
+    y2 = qg.to_numpy(qg.moe_gather_qgemv_int4(G, U, D, idx2, p2, xd, rd)).astype(np.float64)
+    assert_within_bound(y_np, y2, 2 * a, what="fused vs two calls")
+    assert qg.qg_device_status() == 0
+
+
+@pytest.mark.parametrize("E,hidden,inter,k", [(4, 128, 64, 2), (9, 576, 128, 8), (37, 256, 192, 5)])
+def test_moe_layer_fused_small_shapes(qg, E, hidden, inter, k):
+    gate, up, down = _moe_weights(E, hidden, inter, seed=E + 100)
+    logits = I.f32_normal(E, I.TID_LOGITS, E)
+    x = I.bf16_normal(E, I.TID_X, hidden)
+    r = I.bf16_normal(E, I.TID_RESID, hidden)
+    G, U, D = (qg.Int4Weight.from_numpy(d) for d in (gate, up, down))
+    y, idx, p = qg.moe_layer_int4(qg.to_device(logits), G, U, D, qg.to_device(x), qg.to_device(r), k=k)
+    i_ref, p_ref = oracle.router_topk(logits, k)
+    assert qg.to_numpy(idx).astype(np.uint32).tolist() == i_ref.tolist()
+    y_ref, a, _ = oracle.moe(_t(gate), _t(up), _t(down), i_ref, p_ref, x, r)
+    assert_within_bound(qg.to_numpy(y).astype(np.float64), y_ref, a)
