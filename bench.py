@@ -2,15 +2,15 @@
 
 Workload (one "step"): one dense decode layer, hidden 5120, FFN 17408, M = 1 -- gate and up
 (17408 x 5120 each, one fused launch with the SwiGLU epilogue, h in fp32) followed by down
-(5120 x 17408, fp32 h).  Weights are seeded synthetic int4 group-64 data with bf16 scales/biases;
+(5120 x 17408, fp32 h): one dense_layer_int4 call.  Weights are seeded synthetic int4 group-64 data with bf16 scales/biases;
 x is bf16 N(0, 1).  Every step reads a different copy of the layer's weights (12 copies, 1.8 GB,
 far larger than the 129 MB L2), so weights always come from HBM.
 
 The JSON line reports
   value      effective GB/s of the layer (algorithmic bytes: packed codes + scales + biases + x +
              h + y) with inputs resident in HBM,
-  e2e        the same metric through the C-ABI calls with host buffers: each step copies x in from
-             pinned host memory and y back out,
+  e2e        the same metric through the host-buffer C-ABI call (dense_layer_int4_host): each step
+             the GPU reads x from pinned host memory and writes y back into pinned host memory,
   roofline   for the dominant kernel (the fused gate/up SwiGLU GEMV), timed back to back,
   target     the M = 1 GEMV at 5120 x 17408 with bf16 x (us/call, GB/s, fractions of HBM peak),
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the same layer.
@@ -146,26 +146,27 @@ def run_qg(args, rank, world, local_rank):
     layers = [(gate, up, down)] + [(copy_w(gate), copy_w(up), copy_w(down)) for _ in range(N_COPIES - 1)]
     x_np = I.bf16_normal(0, I.TID_X, HIDDEN)
     x = qg.to_device(x_np, dev)
-    h = torch.empty(FFN, dtype=torch.float32, device=dev)
     y = torch.empty(HIDDEN, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     s = int(stream.cuda_stream)
     lib, P = qg.lib, qg.ctypes.c_void_p
     import ctypes
 
-    # pre-marshalled C-ABI arguments per copy: the timed loop makes only the two C calls per step
+    # pre-marshalled C-ABI arguments per copy: the timed loop makes one C call per step
+    # (dense_layer_int4: the gate/up SwiGLU launch, then the down launch; h in the workspace)
+    ws_bytes = qg.qg_workspace_bytes(qg.QG_OP_LAYER, down, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    h = ws[:4 * FFN].view(torch.float32)
     pairs = []
     for g_, u_, d_ in layers:
         arr = (qg.qg_int4_weight * 2)(g_.struct, u_.struct)
         ys = (P * 2)(h.data_ptr(), None)
-        pairs.append((arr, ys, ctypes.byref(d_.struct), d_))
-    xp, hp, yp = P(x.data_ptr()), P(h.data_ptr()), P(y.data_ptr())
+        pairs.append((arr, ys, ctypes.byref(d_.struct), ctypes.byref(g_.struct), ctypes.byref(u_.struct)))
+    xp, hp, yp, wsp = P(x.data_ptr()), P(h.data_ptr()), P(y.data_ptr()), P(ws.data_ptr())
 
     def step(i, xptr=xp):
-        arr, ys, dref, _ = pairs[i % N_COPIES]
-        rc = lib.qgemv_int4_multi(2, arr, xptr, qg.QG_X_BF16, ys, qg.QG_EPI_SWIGLU, s)
-        rc |= lib.qgemv_int4(dref, hp, qg.QG_X_F32, yp, s)
-        return rc
+        _, _, dref, gref, uref = pairs[i % N_COPIES]
+        return lib.dense_layer_int4(gref, uref, dref, xptr, qg.QG_X_BF16, yp, wsp, ws_bytes, s)
 
     qg.qg_set_pdl(not args.no_pdl)
     for i in range(args.warmup):
@@ -211,11 +212,11 @@ def run_qg(args, rank, world, local_rank):
         return e0.elapsed_time(e1) * 1e3 / n  # us per launch
 
     def gateup(i):
-        arr, ys, _, _ = pairs[i % N_COPIES]
+        arr, ys = pairs[i % N_COPIES][:2]
         return lib.qgemv_int4_multi(2, arr, xp, qg.QG_X_BF16, ys, qg.QG_EPI_SWIGLU, s)
 
     def down_bf16(i):
-        _, _, dref, _ = pairs[i % N_COPIES]
+        dref = pairs[i % N_COPIES][2]
         return lib.qgemv_int4(dref, xbig, qg.QG_X_BF16, yp, s)
 
     xbig_t = qg.to_device(I.bf16_normal(0, I.TID_X + 100, FFN), dev)
@@ -230,22 +231,28 @@ def run_qg(args, rank, world, local_rank):
     configs = measure_configs(qg, I, dev, stream) if rank == 0 and not args.no_configs else None
     qg.qg_set_pdl(not args.no_pdl)
 
-    # end to end: x in from pinned host memory, y back to pinned host memory, every step
+    # end to end through the host-buffer call: every step the GPU reads x from pinned host memory
+    # (a one-block copy kernel) and the down kernel writes y into pinned host memory
     x_host = torch.from_numpy(x_np.view(np.int16)).pin_memory()
     y_host = torch.empty(HIDDEN, dtype=torch.float32).pin_memory()
-    x_dev16 = x.view(torch.int16)
+    wsh_bytes = qg.qg_workspace_bytes(qg.QG_OP_LAYER_HOST, down, HIDDEN)
+    wsh = torch.empty(wsh_bytes, dtype=torch.uint8, device=dev)
+    xhp, yhp, wshp = P(x_host.data_ptr()), P(y_host.data_ptr()), P(wsh.data_ptr())
+
+    def step_host(i):
+        _, _, dref, gref, uref = pairs[i % N_COPIES]
+        return lib.dense_layer_int4_host(gref, uref, dref, xhp, qg.QG_X_BF16, yhp, wshp, wsh_bytes, s)
+
     for i in range(args.warmup):
-        x_dev16.copy_(x_host, non_blocking=True)
-        step(i)
-        y_host.copy_(y, non_blocking=True)
+        assert step_host(i) == 0
+    assert step(0) == 0
     torch.cuda.synchronize()
+    assert torch.equal(y_host, y.cpu()), "host-buffer layer differs from the device-buffer layer"
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        x_dev16.copy_(x_host, non_blocking=True)
-        step(i)
-        y_host.copy_(y, non_blocking=True)
+        step_host(i)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
@@ -295,7 +302,10 @@ def run_qg(args, rank, world, local_rank):
                    "us_per_call_without_pdl": round(us_down_nopdl, 3), "algorithmic_bytes": B_DOWN_BF16},
         "e2e": {"value": round(world * B_LAYER / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 4,
-                "us_per_layer": round(e2e_ms * 1e3, 3)},
+                "us_per_layer": round(e2e_ms * 1e3, 3), "call": "dense_layer_int4_host",
+                "transfer": "x read by a GPU copy kernel from pinned host memory, y written by the "
+                            "down kernel into pinned host memory (NVLink-C2C), every step",
+                "gpu_launches_per_step": 3},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "configs": configs,

@@ -142,6 +142,34 @@ int moe_layer_int4(const float *logits, int renorm, const qg_int4_weight *gate, 
                    uint32_t *idx, float *p, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * dense_layer_int4 -- a dense decode FFN layer in one call: the SwiGLU gate/up pair, then the down
+ * projection ([FFAI#14] "dequantGemvInt4Two" for gate + up, then the down dequant-GEMV):
+ *   h = silu(W_g x) * (W_u x),   y = W_down h
+ * gate, up: out = inter, in = hidden; down: in = inter (any out); single matrices (n_mat = 1).
+ * x: bf16 or fp32 [hidden] (x_type); y: fp32 [down->out] (device).
+ * workspace: at least qg_workspace_bytes(QG_OP_LAYER, down, 0) bytes; holds h (fp32 [inter]),
+ * readable after the call.  Two launches (the second programmatically dependent when qg_set_pdl is
+ * on); results equal qgemv_int4_multi(SWIGLU) followed by qgemv_int4 on h.  Limits as qgemv_int4.
+ */
+int dense_layer_int4(const qg_int4_weight *gate, const qg_int4_weight *up, const qg_int4_weight *down,
+                     const void *x, int x_type, float *y, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * dense_layer_int4_host -- dense_layer_int4 with x and y in page-locked HOST memory (cudaHostAlloc
+ * or cudaHostRegister; the GPU reaches it through the CPU-GPU link).  A one-block kernel copies x
+ * into the workspace, then the two GEMV launches run, and the down projection writes y straight
+ * into y_host: three launches in one dependent chain (with qg_set_pdl on), no DMA copies.  y_host
+ * holds the result once the stream has passed the call (synchronise before reading it).
+ * x_host: bf16 or fp32 [hidden]; y_host: fp32 [down->out]; both 16-byte aligned.  Returns
+ * QG_EINVAL when either is not page-locked host memory with a device mapping.
+ * workspace (device): at least qg_workspace_bytes(QG_OP_LAYER_HOST, down, hidden) bytes; h comes
+ * first, as in dense_layer_int4.  Results equal dense_layer_int4 on device copies of x.
+ */
+int dense_layer_int4_host(const qg_int4_weight *gate, const qg_int4_weight *up, const qg_int4_weight *down,
+                          const void *x_host, int x_type, float *y_host, void *workspace, size_t ws_bytes,
+                          void *stream);
+
+/*
  * moe_gather_qgemv_int4_noalloc -- the same computation, arguments and limits as
  * moe_gather_qgemv_int4, without a workspace argument.  The pages have no counterpart: this entry
  * point exists for callers that cannot hand over device scratch, such as a host runtime that owns
@@ -191,10 +219,18 @@ int scalar_fma_chain8_residual(const float *p, const float *v, const uint16_t *r
 int qgemm_int4(const qg_int4_weight *w, const uint16_t *X, int T, float *Y, void *workspace, size_t ws_bytes,
                void *stream);
 
-typedef enum { QG_OP_QGEMV = 0, QG_OP_MULTI = 1, QG_OP_MOE = 2, QG_OP_QGEMM = 3 } qg_op;
+typedef enum {
+  QG_OP_QGEMV = 0,
+  QG_OP_MULTI = 1,
+  QG_OP_MOE = 2,
+  QG_OP_QGEMM = 3,
+  QG_OP_LAYER = 4,     /* dense_layer_int4 */
+  QG_OP_LAYER_HOST = 5 /* dense_layer_int4_host (T_or_k = hidden) */
+} qg_op;
 
 /* Workspace bytes the call `op` needs for weight `w` and T (QG_OP_QGEMM) or k (QG_OP_MOE; pass
- * the down weight).  Returns 0 when the call needs none. */
+ * the down weight; QG_OP_LAYER: the down weight, T_or_k ignored).  Returns 0 when the call needs
+ * none. */
 size_t qg_workspace_bytes(int op, const qg_int4_weight *w, int T_or_k);
 
 /*
@@ -207,6 +243,7 @@ size_t qg_workspace_bytes(int op, const qg_int4_weight *w, int T_or_k);
  * Returns the previous setting.
  */
 int qg_set_pdl(int enable);
+
 
 /*
  * qg_tune_gemv -- CTAs per SM of the streaming GEMV kernels (1..4; 0 restores the default, 1), for

@@ -18,6 +18,17 @@ DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_dev_once[kMaxDevices];
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round16(size_t n) { return (n + 15) & ~(size_t)15; }
+
+// The device address of page-locked host memory, or null when `p` is not such memory.
+void* mapped_host_pointer(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
 
 int check_weight(const qg_int4_weight* w, bool stacked_ok) {
   if (!w || !w->packed || !w->scales || !w->biases) return QG_EINVAL;
@@ -134,6 +145,53 @@ int moe_layer_int4(const float* logits, int renorm, const qg_int4_weight* gate, 
   return moe_down_launch(down, idx, p, k, h, residual, y, s);
 }
 
+int dense_layer_int4(const qg_int4_weight* gate, const qg_int4_weight* up, const qg_int4_weight* down, const void* x,
+                     int xt, float* y, void* workspace, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_weight(gate, false)) || (rc = check_weight(up, false)) || (rc = check_weight(down, false)))
+    return rc;
+  if (!x || !y || (xt != QG_X_BF16 && xt != QG_X_F32)) return QG_EINVAL;
+  if (gate->out != up->out || gate->in != up->in || down->in != gate->out) return QG_EINVAL;
+  if (!aligned16(x) || !aligned16(y)) return QG_EALIGN;
+  const size_t need = qg_workspace_bytes(QG_OP_LAYER, down, 0);
+  if (!workspace || ws_bytes < need) return QG_EWORKSPACE;
+  if (!aligned16(workspace)) return QG_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* h = static_cast<float*>(workspace);
+  const GemvMatArg g{gate->packed, gate->scales, gate->biases, h, gate->out};
+  const GemvMatArg u{up->packed, up->scales, up->biases, nullptr, up->out};
+  const GemvMatArg d{down->packed, down->scales, down->biases, y, down->out};
+  rc = gemv_pair_launch(g, u, x, xt, gate->in, h, s);
+  if (rc) return rc;
+  return gemv_dense_launch(&d, 1, h, QG_X_F32, down->in, s);
+}
+
+int dense_layer_int4_host(const qg_int4_weight* gate, const qg_int4_weight* up, const qg_int4_weight* down,
+                          const void* x_host, int xt, float* y_host, void* workspace, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_weight(gate, false)) || (rc = check_weight(up, false)) || (rc = check_weight(down, false)))
+    return rc;
+  if (!x_host || !y_host || (xt != QG_X_BF16 && xt != QG_X_F32)) return QG_EINVAL;
+  if (gate->out != up->out || gate->in != up->in || down->in != gate->out) return QG_EINVAL;
+  void* xd = mapped_host_pointer(x_host);
+  void* yd = mapped_host_pointer(y_host);
+  if (!xd || !yd) return QG_EINVAL;
+  if (!aligned16(x_host) || !aligned16(y_host) || !aligned16(xd) || !aligned16(yd)) return QG_EALIGN;
+  const size_t need = qg_workspace_bytes(QG_OP_LAYER_HOST, down, gate->in);
+  if (!workspace || ws_bytes < need) return QG_EWORKSPACE;
+  if (!aligned16(workspace)) return QG_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* h = static_cast<float*>(workspace);
+  void* x_dev = static_cast<uint8_t*>(workspace) + round16((size_t)down->in * sizeof(float));
+  const size_t xbytes = (size_t)gate->in * (xt == QG_X_F32 ? 4 : 2);
+  if ((rc = ingest_launch(xd, x_dev, xbytes, s))) return rc;
+  const GemvMatArg g{gate->packed, gate->scales, gate->biases, h, gate->out};
+  const GemvMatArg u{up->packed, up->scales, up->biases, nullptr, up->out};
+  const GemvMatArg d{down->packed, down->scales, down->biases, static_cast<float*>(yd), down->out};
+  if ((rc = gemv_pair_launch(g, u, x_dev, xt, gate->in, h, s))) return rc;
+  return gemv_dense_launch(&d, 1, h, QG_X_F32, down->in, s);
+}
+
 int scalar_fma_chain8_residual(const float* p, const float* v, const uint16_t* residual, float* out, int n,
                                void* stream) {
   if (!p || !v || !residual || !out || n < 1) return QG_EINVAL;
@@ -160,6 +218,10 @@ size_t qg_workspace_bytes(int op, const qg_int4_weight* w, int T_or_k) {
       return (size_t)(T_or_k > 0 ? T_or_k : 0) * (size_t)w->in * sizeof(float);
     case QG_OP_QGEMM:
       return qgemm_workspace_bytes(w, T_or_k);
+    case QG_OP_LAYER:  // h[inter] fp32; inter = down->in
+      return (size_t)w->in * sizeof(float);
+    case QG_OP_LAYER_HOST:  // h[inter], then the device copy of x[hidden] (room for fp32)
+      return round16((size_t)w->in * sizeof(float)) + (size_t)(T_or_k > 0 ? T_or_k : 0) * sizeof(float);
     default:
       return 0;
   }

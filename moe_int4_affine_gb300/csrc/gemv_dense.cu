@@ -14,23 +14,24 @@ int gemv_tune(int ctas_per_sm) {
 
 int gemv_dense_launch(const GemvMatArg* mats, int n, const void* x, int xt, int in, cudaStream_t stream) {
   if (n < 1 || n > 4) return QG_EINVAL;
-  GemvArgs a{};
-  int rows = 0;
-  a.nmat = n;
-  for (int i = 0; i < n; ++i) {
-    a.mat[i].w[0] = WRef{mats[i].packed, mats[i].scales, mats[i].biases, -1};
-    a.mat[i].w[1] = a.mat[i].w[0];
-    a.mat[i].y = mats[i].y;
-    a.mat[i].out = mats[i].out;
-    a.mat[i].row0 = rows;
-    rows += mats[i].out;
-  }
-  a.nseg = 1;
-  a.x = x;
-  a.xf32 = xt == QG_X_F32;
-  a.in = in;
-  a.total_rows = rows;
+  GemvArgs a = dense_args(mats, n, x, xt, in);
   return plan_and_launch<kDense>(a, stream);
+}
+
+// Host-resident input in the launch chain: one CTA copies n16 16-byte words from page-locked host
+// memory (read over the CPU-GPU link through its device mapping) into device memory.  It lets the
+// next launch start at once (programmatic dependent launch) and waits for the previous one first:
+// that one, or one before it, may still read dst.
+__global__ void __launch_bounds__(256) ingest_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int n16) {
+  pdl_trigger();
+  pdl_wait();
+  for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
+}
+
+int ingest_launch(const void* src_dev_mapped, void* dst, size_t bytes, cudaStream_t stream) {
+  if (bytes % 16 != 0 || bytes / 16 > (size_t)INT32_MAX) return QG_EINVAL;
+  return launch(ingest_kernel, dim3(1), dim3(256), 0, stream, static_cast<const uint4*>(src_dev_mapped),
+                static_cast<uint4*>(dst), (int)(bytes / 16));
 }
 
 }  // namespace qg

@@ -87,6 +87,10 @@ struct GemvArgs {
   int n_logits, renorm;
   uint32_t* idx_out;
   float* p_out;
+  // x staging: with `stage` set, x arrives in shared memory (at byte offset stage_off) through one
+  // bulk copy, which the TMA engine serves beside the weight loads already in flight; otherwise the
+  // threads load it into registers.
+  int stage, stage_off;
 };
 
 struct WPtr {
@@ -258,10 +262,20 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
 // Shared memory per CTA: x of group g as 32 u32 (64 int16 values paired for dp2a: per 8-column
 // word w, (X0, X2), (X4, X6), (X1, X3), (X5, X7)) stored at 16-byte slot (w + g) % 8 of the group's
 // 128 bytes -- the rotation keeps a warp's loads (one group per lane, 128 bytes apart) free of bank
-// conflicts; then (2^-k_g, sum of the group's x) per group; then the partial sums [row][NC][chunk].
-template <int MODE, int RN>
+// conflicts; then (2^-k_g, sum of the group's x) per group; then the partial sums [row][NC][chunk];
+// then (STG) the staged copy of x.
+// STG: x arrives through one bulk copy (a.stage set by the planner), else the threads load it.
+template <int MODE, int RN, bool STG>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ uint32_t s_idx[kMaxMats];  // the in-kernel router's selection
+  __shared__ float s_p[kMaxMats];
+  __shared__ __align__(8) uint64_t xbar;  // the x copy's completion
+  pdl_trigger();
+  if (STG && threadIdx.x == 0) {
+    mbar_init(&xbar, 1);
+    mbar_fence_init();
+  }
   constexpr bool PAIR = MODE == kPair, SEG = MODE == kSeg;
   constexpr int NC = PAIR ? 2 : 1;  // components per row
   constexpr int RB = RN / NC;       // rows per work unit
@@ -277,9 +291,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const int ve = (int)((long long)(blockIdx.x + 1) * a.total_rows / gridDim.x);
   const int nkc = (G + kGroupsPerUnit - 1) / kGroupsPerUnit;  // K chunks per row
 
-  pdl_trigger();
-  __shared__ uint32_t s_idx[kMaxMats];  // the in-kernel router's selection
-  __shared__ float s_p[kMaxMats];
   const bool indexed = a.idx != nullptr || a.logits != nullptr;  // slots resolved through indices
   const uint32_t* idxp = a.logits ? s_idx : a.idx;
 
@@ -334,6 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
   // --- x: 16-bit fixed point per group, into shared memory ---
   pdl_wait();
+  uint8_t* stage = smem + a.stage_off;
+  if (STG && threadIdx.x == 0) {
+    // (x was written before this kernel and shared memory is untouched so far: no proxy fence,
+    // which would also wait for this thread's weight loads in flight)
+    constexpr uint32_t kChunk = 32768;
+    const uint32_t xbytes = (uint32_t)G * (a.xf32 ? 256u : 128u);
+    mbar_arrive_expect_tx(&xbar, xbytes);
+    for (uint32_t off = 0; off < xbytes; off += kChunk)
+      bulk_g2s_bytes(stage + off, static_cast<const uint8_t*>(a.x) + off, min(kChunk, xbytes - off), &xbar);
+  }
   if (a.logits) {  // the router, in every CTA
     if (warp == 0) route_topk_warp(a.logits, a.n_logits, a.nmat, a.renorm, s_idx, s_p, blockIdx.x == 0 ? a.idx_out : nullptr,
                                    blockIdx.x == 0 ? a.p_out : nullptr);
@@ -386,7 +407,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
       }
     };
-    if (!a.xf32) {
+    if constexpr (STG) {
+      // one group per 8 lanes, four groups per warp and step, read from the staged copy
+      __syncthreads();  // (the barrier's initialisation, by thread 0, before anyone waits on it)
+      if (!__syncthreads_and(mbar_wait(&xbar, 0))) return;
+      const uint32_t st = smem_u32(stage);
+      for (int g0 = warp * 4; g0 < G; g0 += NW * 4) {
+        const int g = g0 + (lane >> 3);
+        const int gs = g < G ? g : G - 1;  // (in range; its results are not stored)
+        float v[8];
+        if (!a.xf32) {
+          const uint4 r = lds128(st + (uint32_t)gs * 128u + (uint32_t)sub * 16u);
+          const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            v[2 * j] = __uint_as_float(w[j] << 16);
+            v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+          }
+        } else {
+          const uint4 r0 = lds128(st + (uint32_t)gs * 256u + (uint32_t)sub * 32u);
+          const uint4 r1 = lds128(st + (uint32_t)gs * 256u + (uint32_t)sub * 32u + 16u);
+          const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(w[j]);
+        }
+        quant(g, v);
+      }
+    } else if (!a.xf32) {
       constexpr int XB = 8;
       for (int gb = warp * 4; gb < G; gb += NW * 4 * XB) {
         uint4 raw[XB];
@@ -504,6 +551,95 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   }
 }
 
+// ------------------------------------------------------------------ host side: arguments
+// n matrices sharing x, rows of each written to its y.
+inline GemvArgs dense_args(const GemvMatArg* mats, int n, const void* x, int xt, int in) {
+  GemvArgs a{};
+  int rows = 0;
+  a.nmat = n;
+  for (int i = 0; i < n; ++i) {
+    a.mat[i].w[0] = WRef{mats[i].packed, mats[i].scales, mats[i].biases, -1};
+    a.mat[i].w[1] = a.mat[i].w[0];
+    a.mat[i].y = mats[i].y;
+    a.mat[i].out = mats[i].out;
+    a.mat[i].row0 = rows;
+    rows += mats[i].out;
+  }
+  a.nseg = 1;
+  a.x = x;
+  a.xf32 = xt == QG_X_F32;
+  a.in = in;
+  a.total_rows = rows;
+  return a;
+}
+
+// A dense gate/up pair: h = silu(W_g x) * (W_u x).
+inline GemvArgs pair_args(const GemvMatArg& gate, const GemvMatArg& up, const void* x, int xt, int in, float* h) {
+  GemvArgs a{};
+  a.nmat = 1;
+  a.mat[0].w[0] = WRef{gate.packed, gate.scales, gate.biases, -1};
+  a.mat[0].w[1] = WRef{up.packed, up.scales, up.biases, -1};
+  a.mat[0].y = h;
+  a.mat[0].out = gate.out;
+  a.mat[0].row0 = 0;
+  a.nseg = 1;
+  a.x = x;
+  a.xf32 = xt == QG_X_F32;
+  a.in = in;
+  a.total_rows = gate.out;
+  return a;
+}
+
+// The k selected experts' gate/up pairs, h[m] for slot m; experts from idx (set idx or the router
+// fields before launching).
+inline GemvArgs moe_gate_up_args(const qg_int4_weight* gate, const qg_int4_weight* up, const uint32_t* idx, int k,
+                                 const uint16_t* x, float* h) {
+  GemvArgs a{};
+  a.nmat = k;
+  for (int m = 0; m < k; ++m) {
+    a.mat[m].w[0] = WRef{gate->packed, gate->scales, gate->biases, m};
+    a.mat[m].w[1] = WRef{up->packed, up->scales, up->biases, m};
+    a.mat[m].y = h + (size_t)m * gate->out;
+    a.mat[m].out = gate->out;
+    a.mat[m].row0 = m * gate->out;
+  }
+  a.nseg = 1;
+  a.x = x;
+  a.xf32 = 0;
+  a.idx = idx;
+  a.n_experts = gate->n_mat;
+  a.slab_words = (long long)gate->out * (gate->in / 8);
+  a.slab_groups = (long long)gate->out * (gate->in / 64);
+  a.in = gate->in;
+  a.total_rows = k * gate->out;
+  return a;
+}
+
+// MoE down with the slot-weighted accumulate and the residual (one row = k segments).
+inline GemvArgs moe_down_args(const qg_int4_weight* down, const uint32_t* idx, const float* p, int k, const float* h,
+                              const uint16_t* residual, float* y) {
+  GemvArgs a{};
+  a.nmat = 1;
+  a.mat[0].w[0] = WRef{down->packed, down->scales, down->biases, -1};
+  a.mat[0].w[1] = a.mat[0].w[0];
+  a.mat[0].y = y;
+  a.mat[0].out = down->out;
+  a.mat[0].row0 = 0;
+  a.seg = WRef{down->packed, down->scales, down->biases, 0};
+  a.nseg = k;
+  a.x = h;
+  a.xf32 = 1;
+  a.idx = idx;
+  a.p = p;
+  a.resid = residual;
+  a.n_experts = down->n_mat;
+  a.slab_words = (long long)down->out * (down->in / 8);
+  a.slab_groups = (long long)down->out * (down->in / 64);
+  a.in = down->in;
+  a.total_rows = down->out;
+  return a;
+}
+
 // ------------------------------------------------------------------ host side: planning
 struct GemvTune {
   int ctas_per_sm;  // 0: automatic
@@ -515,9 +651,23 @@ inline size_t gemv_smem_bytes(int groups, int rows_per_cta, int nc) {
   return (size_t)groups * 136 + (size_t)rows_per_cta * nc * nkc * 4;
 }
 
-template <int MODE, int RN>
+// Shared memory with the x staging area after `base` bytes, or `base` alone (staging off).  Staging
+// is used for short x only: measured on the decode shapes, the bulk copy beat the threads' own loads
+// for x of up to 128 groups (gate/up 5120 bf16: 20.7 -> 20.1 us; MoE 2048 bf16 and 8 x 768 fp32:
+// 16.0 -> 14.9 us per layer) and lost for the 17408-wide down x (12.37 -> 12.54 us).
+constexpr int kStageMaxGroups = 128;
+inline size_t plan_stage(GemvArgs& a, size_t base, size_t limit) {
+  const size_t off = (base + 127) & ~(size_t)127;
+  const size_t total = off + (size_t)a.groups * (a.xf32 ? 256 : 128);
+  a.stage = total <= limit && a.groups <= kStageMaxGroups ? 1 : 0;
+  a.stage_off = a.stage ? (int)off : 0;
+  return a.stage ? total : base;
+}
+constexpr size_t kStaticSmemReserve = 1024;  // the kernels' static shared variables
+
+template <int MODE, int RN, bool STG>
 int launch_gemv_variant(const GemvArgs& a, int grid, size_t smem, cudaStream_t stream) {
-  auto k = gemv_kernel<MODE, RN>;
+  auto k = gemv_kernel<MODE, RN, STG>;
   static std::atomic<int> smem_set{0};
   if ((int)smem > smem_set.load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -542,10 +692,12 @@ int plan_and_launch(GemvArgs& a, cudaStream_t stream) {
     if (gemv_smem_bytes(a.groups, a.rows_per_cta, NC) <= budget || grid >= a.total_rows) break;
     grid = std::min(a.total_rows, grid * 2);
   }
-  const size_t smem = gemv_smem_bytes(a.groups, a.rows_per_cta, NC);
-  if (smem > (size_t)dev.max_smem_optin) return QG_ENOTSUP;
+  const size_t limit = (size_t)dev.max_smem_optin - kStaticSmemReserve;
+  const size_t smem = plan_stage(a, gemv_smem_bytes(a.groups, a.rows_per_cta, NC), limit);
+  if (smem > limit) return QG_ENOTSUP;
   // rows x components per work unit: 4 (dense and seg: four rows; pair: two rows, gate and up)
-  return launch_gemv_variant<MODE, 4>(a, grid, smem, stream);
+  return a.stage ? launch_gemv_variant<MODE, 4, true>(a, grid, smem, stream)
+                 : launch_gemv_variant<MODE, 4, false>(a, grid, smem, stream);
 }
 
 }  // namespace qg

@@ -66,26 +66,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------- bulk copies (TMA engine)
-// 1-D global -> shared copy, completion counted on `bar` in bytes, with an L2 cache hint.
-// dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                              uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-// Bulk prefetch of a global range into L2 (no shared memory, no completion tracking).  `bytes` a
-// multiple of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-// Weights are streamed once per call: mark them evict-first so activations and outputs stay.
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
+// 1-D global -> shared copy, completion counted on `bar` in bytes.  dst, src and bytes must be
+// multiples of 16.  The copy goes through the async proxy: memory that generic accesses touched
+// earlier in the same kernel needs a proxy fence (fence.proxy.async) before it.
+__device__ __forceinline__ void bulk_g2s_bytes(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
 // ---------------------------------------------------------------- programmatic dependent launch

@@ -62,6 +62,9 @@ int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, con
 int moe_gate_up_routed_launch(const float* logits, int n_logits, int renorm, const qg_int4_weight* gate,
                               const qg_int4_weight* up, int k, const uint16_t* x, float* h, uint32_t* idx_out,
                               float* p_out, cudaStream_t stream);
+// Copy `bytes` (a multiple of 16) from device-mapped host memory to device memory, in the launch
+// chain (gemv_dense.cu).
+int ingest_launch(const void* src_dev_mapped, void* dst, size_t bytes, cudaStream_t stream);
 int moe_down_launch(const qg_int4_weight* down, const uint32_t* idx, const float* p, int k, const float* h,
                     const uint16_t* residual, float* y, cudaStream_t stream);
 

@@ -23,7 +23,7 @@ QG_OK, QG_EINVAL, QG_EALIGN, QG_EWORKSPACE, QG_ELAUNCH, QG_ENOTSUP, QG_EDEVICE =
 QG_STATUS_BAD_EXPERT, QG_STATUS_TIMEOUT = 1, 2
 QG_X_BF16, QG_X_F32 = 0, 1
 QG_EPI_NONE, QG_EPI_SWIGLU = 0, 1
-QG_OP_QGEMV, QG_OP_MULTI, QG_OP_MOE, QG_OP_QGEMM = 0, 1, 2, 3
+QG_OP_QGEMV, QG_OP_MULTI, QG_OP_MOE, QG_OP_QGEMM, QG_OP_LAYER, QG_OP_LAYER_HOST = 0, 1, 2, 3, 4, 5
 QG_NOALLOC_MOE_MAX_FLOATS = 32768
 
 
@@ -41,6 +41,8 @@ lib.qgemv_int4_multi.argtypes = [_I, _W, _P, _I, ctypes.POINTER(_P), _I, _P]
 lib.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
 lib.moe_gather_qgemv_int4.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]
 lib.moe_layer_int4.argtypes = [_P, _I, _W, _W, _W, _I, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+lib.dense_layer_int4.argtypes = [_W, _W, _W, _P, _I, _P, _P, ctypes.c_size_t, _P]
+lib.dense_layer_int4_host.argtypes = [_W, _W, _W, _P, _I, _P, _P, ctypes.c_size_t, _P]
 lib.moe_gather_qgemv_int4_noalloc.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P]
 lib.scalar_fma_chain8_residual.argtypes = [_P, _P, _P, _P, _I, _P]
 lib.qgemm_int4.argtypes = [_W, _P, _I, _P, _P, ctypes.c_size_t, _P]
@@ -55,7 +57,7 @@ lib.qg_strerror.argtypes = [_I]
 lib.qg_strerror.restype = ctypes.c_char_p
 lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
-           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4",
+           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "dense_layer_int4", "dense_layer_int4_host",
            "scalar_fma_chain8_residual", "qgemm_int4", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
 
@@ -220,6 +222,37 @@ def moe_layer_int4(logits, gate: Int4Weight, up: Int4Weight, down: Int4Weight, x
                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_layer_int4")
     return y, idx, p
+
+
+def dense_layer_int4(gate: Int4Weight, up: Int4Weight, down: Int4Weight, x, y=None, workspace=None, stream=None):
+    """y = W_down (silu(W_g x) * (W_u x)); x bf16 or fp32.  Returns y; h (fp32 [inter]) is the
+    first inter floats of the workspace after the call."""
+    torch = _torch()
+    dev = x.device
+    if y is None:
+        y = torch.empty(down.out, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(qg_workspace_bytes(QG_OP_LAYER, down, 0), dtype=torch.uint8, device=dev)
+    _check(lib.dense_layer_int4(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
+                                _ptr(x), _xtype(x), _ptr(y), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)),
+           "dense_layer_int4")
+    return y
+
+
+def dense_layer_int4_host(gate: Int4Weight, up: Int4Weight, down: Int4Weight, x_host, y_host, workspace=None,
+                          stream=None, device="cuda"):
+    """dense_layer_int4 with x_host (bf16 or fp32) and y_host (fp32) pinned CPU tensors; y_host is
+    written by the GPU (synchronise the stream before reading it).  Returns y_host."""
+    torch = _torch()
+    if workspace is None:
+        workspace = torch.empty(qg_workspace_bytes(QG_OP_LAYER_HOST, down, gate.in_dim), dtype=torch.uint8,
+                                device=device)
+    _check(lib.dense_layer_int4_host(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
+                                     _ptr(x_host), _xtype(x_host), _ptr(y_host), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)),
+           "dense_layer_int4_host")
+    return y_host
 
 
 def moe_gather_qgemv_int4_noalloc(gate: Int4Weight, up: Int4Weight, down: Int4Weight, idx, p, x, residual, y,
