@@ -127,10 +127,9 @@ __device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
 }
 
 // 16-bit fixed point by the magic-number rule: for |t| < 2^22, t + 1.5 * 2^23 rounded to float
-// has the nearest integer to t in its low mantissa bits.
-__device__ __forceinline__ int round_to_int(float v, float scale) {
-  return __float_as_int(fmaf(v, scale, 12582912.0f)) - 0x4B400000;
-}
+// has the nearest integer to t (ties to even) in its low mantissa bits: the float's bit pattern is
+// 0x4B400000 + round(t), whose low 16 bits are round(t) as a 16-bit two's-complement value when
+// |round(t)| < 2^15.
 
 // Row sums of RN per-lane values; lane l returns the total of value (l * RN) / 32.
 template <int RN>
@@ -384,16 +383,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         // 2^-60 contribute less than 1e-17 per weight through the code term and are dropped from
         // it (the bias term keeps the exact sum).
         const bool live = m >= 8.673617e-19f;  // 2^-60
-        const int E = max((int)((__float_as_uint(m) >> 23) & 0xFF) - 127, -60);
-        const float scale = live ? exp2i(14 - E) : 0.f;  // 14 - E in [-113, 74]
-        int q[8];
+        int E = max((int)((__float_as_uint(m) >> 23) & 0xFF) - 127, -60);
+        // When max|x| 2^k would round up to 2^15 (fp32 x only: a bf16 max is at most
+        // (2 - 2^-7) 2^14 after scaling), one bit less for this group, so every |X_j| <= 32767.
+        if (live && m * exp2i(14 - E) >= 32767.5f) ++E;
+        const float scale = live ? exp2i(14 - E) : 0.f;  // 14 - E in [-114, 74]
+        // X_j = the low 16 bits of the float x_j 2^k + 1.5 2^23 (the magic-number rule above), paired
+        // for dp2a as (X0, X2), (X4, X6), (X1, X3), (X5, X7)
+        uint32_t b[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) q[j] = max(-32767, min(32767, round_to_int(v[j], scale)));
+        for (int j = 0; j < 8; ++j) b[j] = __float_as_uint(fmaf(v[j], scale, 12582912.0f));
         uint4 pk;
-        pk.x = (uint32_t)(q[0] & 0xFFFF) | ((uint32_t)q[2] << 16);
-        pk.y = (uint32_t)(q[4] & 0xFFFF) | ((uint32_t)q[6] << 16);
-        pk.z = (uint32_t)(q[1] & 0xFFFF) | ((uint32_t)q[3] << 16);
-        pk.w = (uint32_t)(q[5] & 0xFFFF) | ((uint32_t)q[7] << 16);
+        pk.x = __byte_perm(b[0], b[2], 0x5410);
+        pk.y = __byte_perm(b[4], b[6], 0x5410);
+        pk.z = __byte_perm(b[1], b[3], 0x5410);
+        pk.w = __byte_perm(b[5], b[7], 0x5410);
         reinterpret_cast<uint4*>(xq + (size_t)g * 32)[(sub + g) & 7] = pk;
         if (sub == 0) {
           float wgt = 1.f;
