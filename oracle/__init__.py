@@ -72,6 +72,12 @@ def _L():
             lib.orc_moe.restype = I
             lib.orc_qgemm_rows.argtypes = [P, P, P, I64, I64, I64, P, I64, I64, I64, P, P]
             lib.orc_qgemm_rows.restype = I
+            lib.orc_rmsnorm.argtypes = [P, I, P, I64, ctypes.c_double, P]
+            lib.orc_rmsnorm.restype = I
+            lib.orc_sigmoid.argtypes = [ctypes.c_double]
+            lib.orc_sigmoid.restype = ctypes.c_double
+            lib.orc_sigmoid_scalar_fma.argtypes = [ctypes.c_double, P, P, P, I64, P, P]
+            lib.orc_sigmoid_scalar_fma.restype = None
             _lib = lib
     return _lib
 
@@ -204,6 +210,42 @@ def moe(gate, up, down, idx, p, x, residual, group_size: int = 64):
     if flags < 0:
         raise ValueError("orc_moe rejected the shapes")
     return y, a, flags
+
+
+def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """out = x * gamma / sqrt(mean(x^2) + eps) in float64 (x bf16 bits or float32, gamma bf16 bits)."""
+    x = np.ascontiguousarray(x)
+    gamma = np.ascontiguousarray(gamma, dtype=np.uint16)
+    if gamma.size != x.size:
+        raise ValueError("gamma and x differ in length")
+    out = np.empty(x.size, dtype=np.float64)
+    rc = _L().orc_rmsnorm(_p(x), _xtype(x), _p(gamma), x.size, float(eps), _p(out))
+    if rc != 0:
+        raise ValueError("orc_rmsnorm rejected the arguments")
+    return out
+
+
+def rmsnorm_qgemv(packed, scales, biases, x, gamma, eps: float, group_size: int = 64):
+    """y, absref of W rmsnorm(x): the norm in float64, then the GEMV of the normalised vector."""
+    return qgemv_f64x(packed, scales, biases, rmsnorm(x, gamma, eps), group_size)
+
+
+def sigmoid(g: float) -> float:
+    return _L().orc_sigmoid(float(g))
+
+
+def sigmoid_scalar_fma(gate: float, value: np.ndarray, base: np.ndarray, residual=None):
+    """out = base + sigmoid(gate) * value (+ residual bf16 bits), and absref."""
+    value = np.ascontiguousarray(value, dtype=np.float32)
+    base = np.ascontiguousarray(base, dtype=np.float32)
+    if residual is not None:
+        residual = np.ascontiguousarray(residual, dtype=np.uint16)
+    n = value.size
+    out = np.empty(n, dtype=np.float64)
+    a = np.empty(n, dtype=np.float64)
+    _L().orc_sigmoid_scalar_fma(float(gate), _p(value), _p(base), None if residual is None else _p(residual), n,
+                                _p(out), _p(a))
+    return out, a
 
 
 def qgemm(packed, scales, biases, X, group_size: int = 64, rows=None, threads: int = 1):

@@ -267,3 +267,47 @@ int orc_qgemm_rows(const uint32_t *packed, const uint16_t *scales, const uint16_
   }
   return ORC_OK;
 }
+
+/* ---------------------------------------------------------------------------------------
+ * RMSNorm ([FFAI#14] commit wrapping "ffai_rms_norm_qgemv_fast": the norm's output is fed
+ * straight into the int4 dequant-GEMV; the page names the norm without writing it out, and
+ * the plain reading is the usual root-mean-square norm with a per-element weight gamma and an
+ * epsilon inside the root):
+ *   out[j] = x[j] * gamma[j] / sqrt( (1/n) sum_i x[i]^2 + eps )
+ * x bf16 or fp32 [n]; gamma bf16 [n]; out double [n].  The sum of squares runs in index order.
+ * ------------------------------------------------------------------------------------- */
+int orc_rmsnorm(const void *x, int xtype, const uint16_t *gamma, int64_t n, double eps, double *out) {
+  if (n <= 0 || eps < 0.0) return ORC_EINVAL;
+  double ss = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    double v = load_x(x, xtype, i);
+    ss += v * v;
+  }
+  double denom = sqrt(ss / (double)n + eps);
+  if (!(denom > 0.0)) return ORC_EINVAL; /* all-zero x with eps = 0 has no norm */
+  for (int64_t j = 0; j < n; ++j) out[j] = load_x(x, xtype, j) * orc_bf16_to_f64(gamma[j]) / denom;
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Sigmoid-gated scalar FMA with the residual folded in ([FFAI#14] scalar-FMA commit:
+ * "sigmoidScalarFMAResidual(gate, value, base, residual, into:) -- sigmoid-gated FMA with the
+ * post-MoE residual add folded in"; "out[i] = base[i] + scalar[0] * value[i]"; the shared-expert
+ * step of a decode layer: y = routed + sigmoid(shared_gate . x) * shared_expert(x) + r):
+ *   out[i] = base[i] + sigmoid(gate) * value[i] + residual[i]      (residual may be NULL)
+ * sigmoid(g) = 1 / (1 + exp(-g)).  gate: one value; value, base fp32 [n]; residual bf16 [n].
+ * absref[i] = |base[i]| + |sigmoid(gate) * value[i]| + |residual[i]|.
+ * ------------------------------------------------------------------------------------- */
+double orc_sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
+
+void orc_sigmoid_scalar_fma(double gate, const float *value, const float *base, const uint16_t *residual, int64_t n,
+                            double *out, double *absref) {
+  double s = orc_sigmoid(gate);
+  for (int64_t i = 0; i < n; ++i) {
+    double b = (double)base[i];
+    double t = s * (double)value[i];
+    double r = residual ? orc_bf16_to_f64(residual[i]) : 0.0;
+    out[i] = b + t + r;
+    if (absref) absref[i] = fabs(b) + fabs(t) + fabs(r);
+  }
+}

@@ -379,3 +379,114 @@ def test_generator_distribution_recipe():
     # reproducible
     d2 = I.int4_weight(0, 1, 256, 1024)
     assert np.array_equal(d["packed"], d2["packed"]) and np.array_equal(d["biases"], d2["biases"])
+
+
+# ---------------------------------------------------------------- RMSNorm (norm-fused GEMV prologue)
+def _bf16_bits(v: float) -> int:
+    """bf16 bits of a value exactly representable in bf16."""
+    b = np.array([v], dtype=np.float32).view(np.uint32)[0]
+    assert b & 0xFFFF == 0, v
+    return int(b >> 16)
+
+
+def test_rmsnorm_worked_example():
+    """x = (3, 4), gamma = (1, 2), eps = 0: mean square 12.5, so out = (3, 8) / sqrt(12.5)."""
+    out = oracle.rmsnorm(np.array([3.0, 4.0], np.float32), np.array([0x3F80, 0x4000], np.uint16), 0.0)
+    assert out[0] == pytest.approx(3 / math.sqrt(12.5), rel=1e-15)
+    assert out[1] == pytest.approx(8 / math.sqrt(12.5), rel=1e-15)
+
+
+@pytest.mark.parametrize("n,j,a", [(64, 0, 2.5), (5120, 4097, -0.75), (17408, 17407, 1e-3)])
+def test_rmsnorm_one_hot_closed_form(n, j, a):
+    """x = a e_j, gamma = 1, eps = 0: mean square a^2 / n, so out = sqrt(n) sign(a) e_j (a sum in
+    place of the mean, or a missing root, fails this)."""
+    x = np.zeros(n, np.float32)
+    x[j] = a
+    out = oracle.rmsnorm(x, np.full(n, 0x3F80, np.uint16), 0.0)
+    want = np.zeros(n)
+    want[j] = math.copysign(math.sqrt(n), a)
+    np.testing.assert_allclose(out, want, rtol=1e-14, atol=0)
+
+
+def test_rmsnorm_constant_vector_and_gamma():
+    """x = c (every element), eps = 0: out = sign(c) gamma, up to the rounding of the fp64 sum of
+    n squares (relative error below n 2^-53)."""
+    n = 1000
+    g = I.bf16_normal(3, I.TID_X, n)
+    out = oracle.rmsnorm(np.full(n, -0.3, np.float32), g, 0.0)
+    np.testing.assert_allclose(out, -oracle_values(g), rtol=n * 2.0 ** -53)
+
+
+def oracle_values(bits):
+    return np.array([oracle.bf16_to_f64(int(b)) for b in bits])
+
+
+def test_rmsnorm_scale_invariance_and_epsilon():
+    """eps = 0: rmsnorm(alpha x) = rmsnorm(x) for alpha > 0.  eps much larger than the mean
+    square: out -> x gamma / sqrt(eps) (eps outside the root, or added to the sum instead of the
+    mean, fails this)."""
+    n = 2048
+    x = I.bf16_normal(4, I.TID_X, n)
+    g = I.bf16_normal(5, I.TID_X, n)
+    xf = oracle_values(x).astype(np.float32)
+    a = oracle.rmsnorm(xf, g, 0.0)
+    b = oracle.rmsnorm((xf * np.float32(8.0)).astype(np.float32), g, 0.0)
+    np.testing.assert_allclose(a, b, rtol=1e-14)
+    small = (xf * np.float32(2.0 ** -20)).astype(np.float32)
+    eps = 1e4
+    c = oracle.rmsnorm(small, g, eps)
+    want = small.astype(np.float64) * oracle_values(g) / math.sqrt(eps)
+    np.testing.assert_allclose(c, want, rtol=1e-12)
+    # the mean of squares, not the sum: with eps = mean square, out = x gamma / sqrt(2 ms)
+    ms = float(np.mean(xf.astype(np.float64) ** 2))
+    d = oracle.rmsnorm(xf, g, ms)
+    np.testing.assert_allclose(d, xf * oracle_values(g) / math.sqrt(2 * ms), rtol=1e-12)
+
+
+def test_rmsnorm_bf16_and_f32_inputs_agree():
+    x = I.bf16_normal(6, I.TID_X, 576)
+    g = I.bf16_normal(7, I.TID_X, 576)
+    np.testing.assert_array_equal(oracle.rmsnorm(x, g, 1e-6), oracle.rmsnorm(oracle_values(x).astype(np.float32), g, 1e-6))
+
+
+def test_rmsnorm_qgemv_one_hot_selects_scaled_column():
+    """x = a e_j, gamma = g, eps = 0: y = sqrt(n) sign(a) g_j W[:, j], with W[:, j] dequantised
+    from the unpacked code and its group's scale and bias."""
+    out, n, j = 96, 1024, 777
+    d = I.int4_weight(8, I.TID_W, out, n)
+    gamma = I.bf16_normal(8, I.TID_X, n)
+    x = np.zeros(n, np.float32)
+    x[j] = -1.5
+    y, _ = oracle.rmsnorm_qgemv(d["packed"], d["scales"], d["biases"], x, gamma, 0.0)
+    q = oracle.unpack(d["packed"], n)[:, j].astype(np.float64)
+    s = oracle_values(d["scales"].reshape(out, n // 64)[:, j // 64])
+    b = oracle_values(d["biases"].reshape(out, n // 64)[:, j // 64])
+    want = -math.sqrt(n) * oracle.bf16_to_f64(int(gamma[j])) * (s * q + b)
+    np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-300)
+
+
+# ---------------------------------------------------------------- sigmoid-gated scalar FMA (shared expert)
+def test_sigmoid_closed_forms():
+    assert oracle.sigmoid(0.0) == 0.5
+    assert oracle.sigmoid(math.log(3.0)) == pytest.approx(0.75, rel=1e-15)
+    assert oracle.sigmoid(-math.log(3.0)) == pytest.approx(0.25, rel=1e-15)
+    assert oracle.sigmoid(40.0) == pytest.approx(1.0, abs=1e-17)
+    assert 0.0 < oracle.sigmoid(-40.0) < 1e-17
+
+
+def test_sigmoid_scalar_fma_closed_forms():
+    """gate = ln 3 -> sigmoid 3/4; gate = 0 -> 1/2; gate = -40 -> base + residual only; and the
+    residual (bf16) is added once, with the variant without it matching base + s v."""
+    n = 300
+    v = I.f32_normal(9, I.TID_X, n)
+    base = I.f32_normal(10, I.TID_X, n)
+    r = I.bf16_normal(11, I.TID_RESID, n)
+    rv = oracle_values(r)
+    out, a = oracle.sigmoid_scalar_fma(math.log(3.0), v, base, r)
+    np.testing.assert_allclose(out, base + 0.75 * v.astype(np.float64) + rv, rtol=1e-14, atol=1e-15)
+    b64, v64 = base.astype(np.float64), v.astype(np.float64)
+    np.testing.assert_allclose(a, np.abs(b64) + 0.75 * np.abs(v64) + np.abs(rv), rtol=1e-14)
+    out0, _ = oracle.sigmoid_scalar_fma(0.0, v, base)
+    np.testing.assert_allclose(out0, base + 0.5 * v.astype(np.float64), rtol=1e-15, atol=1e-16)
+    outm, _ = oracle.sigmoid_scalar_fma(-40.0, v, base, r)
+    np.testing.assert_allclose(outm, base + rv, rtol=1e-12, atol=1e-15)
