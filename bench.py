@@ -404,6 +404,41 @@ def measure_configs(qg, I, dev, stream):
     res["c3_moe_layer_T1_fused_router"] = dict(gb(nbytes, us), kernels=2, call="moe_layer_int4", l2=l2)
     del g, u, d
 
+    # next rows: the RMSNorm-fused gate/up pair (the FFN input after its norm) against the plain
+    # pair, and the shared-expert down projection with the sigmoid gate, routed base and residual
+    gw = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_GATE, FFN, HIDDEN), dev)
+    uw = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_UP, FFN, HIDDEN), dev)
+    pairs_ = [(gw, uw)] + [(copies(gw, 2)[1], copies(uw, 2)[1]) for _ in range(5)]
+    x = qg.to_device(I.bf16_normal(0, I.TID_X, HIDDEN), dev)
+    gam = qg.to_device(I.bf16_normal(1, I.TID_RESID, HIDDEN), dev)
+    h = torch.empty(FFN, dtype=torch.float32, device=dev)
+    pargs = [((qg.qg_int4_weight * 2)(a_.struct, b_.struct), (P * 2)(h.data_ptr(), None)) for a_, b_ in pairs_]
+    nbytes = 2 * weight_bytes(FFN, HIDDEN) + HIDDEN * 2 + HIDDEN * 2 + FFN * 4
+    us = tl(lambda i: lib.rmsnorm_qgemv_int4_multi(2, pargs[i % 6][0], P(x.data_ptr()), qg.QG_X_BF16,
+                                                   P(gam.data_ptr()), ctypes.c_float(1e-6), pargs[i % 6][1],
+                                                   qg.QG_EPI_SWIGLU, s), 60)
+    us0 = tl(lambda i: lib.qgemv_int4_multi(2, pargs[i % 6][0], P(x.data_ptr()), qg.QG_X_BF16, pargs[i % 6][1],
+                                            qg.QG_EPI_SWIGLU, s), 60)
+    res["n1_rmsnorm_gateup_swiglu_17408x5120"] = dict(gb(nbytes, us), call="rmsnorm_qgemv_int4_multi",
+                                                      us_without_norm=round(us0, 3),
+                                                      l2="weights rotate over 6 copies (1.2 GB)")
+    del gw, uw, pairs_
+    SD_OUT, SD_IN = 2048, 768  # shared expert of the MoE config: down 2048 x 768
+    sd = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_DOWN, SD_OUT, SD_IN), dev)
+    sds = copies(sd, 192)
+    hx = qg.to_device(I.f32_normal(0, I.TID_X, SD_IN), dev)
+    gate = qg.to_device(np.array([0.3], np.float32), dev)
+    base = qg.to_device(I.f32_normal(1, I.TID_X, SD_OUT), dev)
+    r = qg.to_device(I.bf16_normal(0, I.TID_RESID, SD_OUT), dev)
+    y = torch.empty(SD_OUT, dtype=torch.float32, device=dev)
+    us = tl(lambda i: lib.qgemv_int4_sigmoid_fma(byref(sds[i % 192].struct), P(hx.data_ptr()), qg.QG_X_F32,
+                                                 P(gate.data_ptr()), P(base.data_ptr()), P(r.data_ptr()),
+                                                 P(y.data_ptr()), s), 200)
+    nbytes = weight_bytes(SD_OUT, SD_IN) + SD_IN * 4 + 4 + SD_OUT * (4 + 2 + 4)
+    res["n1_shared_down_sigmoid_fma_2048x768"] = dict(gb(nbytes, us), call="qgemv_int4_sigmoid_fma",
+                                                      l2="weights rotate over 192 copies (170 MB, larger than L2)")
+    del sd, sds
+
     # config 4: dequant-GEMM, W 17408 x 5120, X T x 5120
     w = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_W, FFN, HIDDEN), dev)
     ws_ = copies(w, 12)

@@ -98,6 +98,47 @@ int qgemv_int4_multi(int n, const qg_int4_weight *ws, const void *x, int xt, flo
                      void *stream);
 
 /*
+ * rmsnorm_qgemv_int4 -- RMSNorm fused into the GEMV prologue ([FFAI#14] commit wrapping
+ * "ffai_rms_norm_qgemv_fast": the normalised activation goes straight into the int4 dequant-GEMV,
+ * no round trip of the normalised vector through memory):
+ *   y[r] = sum_j w[r][j] * x[j] * gamma[j] / sqrt( (1/in) sum_i x[i]^2 + eps )
+ * (the page names the norm without writing it out; this is the usual RMSNorm with an epsilon
+ * inside the root).  x: bf16 or fp32 [in]; gamma: bf16 [in] (device, 16-byte aligned); eps >= 0.
+ * Every CTA reads x anyway: it also sums x^2, quantizes x * gamma, and scales its outputs by the
+ * root.  Other arguments and limits as qgemv_int4.  An all-zero x with eps = 0 gives non-finite y.
+ */
+int rmsnorm_qgemv_int4(const qg_int4_weight *w, const void *x, int x_type, const uint16_t *gamma, float eps, float *y,
+                       void *stream);
+
+/*
+ * rmsnorm_qgemv_int4_multi -- the same prologue for n in {2, 3, 4} projections sharing x, with the
+ * epilogues of qgemv_int4_multi (QG_EPI_SWIGLU: h = silu(W_g xn) * (W_u xn) for the FFN after a
+ * norm).  Arguments and limits as qgemv_int4_multi plus gamma and eps as above.
+ */
+int rmsnorm_qgemv_int4_multi(int n, const qg_int4_weight *ws, const void *x, int x_type, const uint16_t *gamma,
+                             float eps, float *const *ys, int epi, void *stream);
+
+/*
+ * qgemv_int4_sigmoid_fma -- the shared-expert step fused into its GEMV ([FFAI#14] scalar-FMA
+ * commit, "sigmoidScalarFMAResidual(gate, value, base, residual) -- sigmoid-gated FMA with the
+ * post-MoE residual add folded in"; the value is this GEMV's output):
+ *   y[r] = base[r] + sigmoid(gate[0]) * sum_j w[r][j] x[j]  (+ residual[r] when not NULL)
+ * gate: fp32 [1]; base: fp32 [out]; residual: bf16 [out] or NULL; y: fp32 [out] (may equal
+ * base); all device, 16-byte aligned.  Other arguments as qgemv_int4.
+ */
+int qgemv_int4_sigmoid_fma(const qg_int4_weight *w, const void *x, int x_type, const float *gate, const float *base,
+                           const uint16_t *residual, float *y, void *stream);
+
+/*
+ * sigmoid_scalar_fma_residual -- the same step on its own ([FFAI#14] "sigmoidScalarFMAResidual";
+ * with residual NULL, "sigmoidScalarFMA"):
+ *   out[i] = base[i] + sigmoid(gate[0]) * value[i]  (+ residual[i])
+ * gate: fp32 [1]; value, base, out: fp32 [n]; residual: bf16 [n] or NULL (all device). n >= 1.
+ */
+int sigmoid_scalar_fma_residual(const float *gate, const float *value, const float *base, const uint16_t *residual,
+                                float *out, int n, void *stream);
+
+/*
  * moe_router_topk -- GPU router ([FFAI#14] commit "moeRouterTopK": logits [nExperts] -> [k] u32
  * indices + [k] weights, no host readback; [FFAI#9] top-K order "(value desc, index asc)").
  * Selects the k largest logits, ties to the lower index; slot s holds the s-th selected expert.

@@ -92,6 +92,65 @@ int qgemv_int4_multi(int n, const qg_int4_weight* ws, const void* x, int xt, flo
   return gemv_dense_launch(m, n, x, xt, ws[0].in, s);
 }
 
+int rmsnorm_qgemv_int4(const qg_int4_weight* w, const void* x, int xt, const uint16_t* gamma, float eps, float* y,
+                       void* stream) {
+  int rc = check_weight(w, false);
+  if (rc) return rc;
+  if (!x || !gamma || !y || (xt != QG_X_BF16 && xt != QG_X_F32) || !(eps >= 0.f)) return QG_EINVAL;
+  if (!aligned16(x) || !aligned16(gamma) || !aligned16(y)) return QG_EALIGN;
+  GemvMatArg m{w->packed, w->scales, w->biases, y, w->out};
+  GemvExtras ex{};
+  ex.gamma = gamma;
+  ex.eps = eps;
+  return gemv_dense_launch(&m, 1, x, xt, w->in, static_cast<cudaStream_t>(stream), ex);
+}
+
+int rmsnorm_qgemv_int4_multi(int n, const qg_int4_weight* ws, const void* x, int xt, const uint16_t* gamma, float eps,
+                             float* const* ys, int epi, void* stream) {
+  if (n < 2 || n > 4 || !ws || !ys || !x || !gamma || !(eps >= 0.f)) return QG_EINVAL;
+  if (xt != QG_X_BF16 && xt != QG_X_F32) return QG_EINVAL;
+  if (epi != QG_EPI_NONE && epi != QG_EPI_SWIGLU) return QG_EINVAL;
+  if (epi == QG_EPI_SWIGLU && (n != 2 || ws[0].out != ws[1].out)) return QG_EINVAL;
+  GemvMatArg m[4];
+  for (int i = 0; i < n; ++i) {
+    int rc = check_weight(&ws[i], false);
+    if (rc) return rc;
+    if (ws[i].in != ws[0].in) return QG_EINVAL;
+    const bool need_y = !(epi == QG_EPI_SWIGLU && i == 1);
+    if (need_y && !ys[i]) return QG_EINVAL;
+    if (need_y && !aligned16(ys[i])) return QG_EALIGN;
+    m[i] = GemvMatArg{ws[i].packed, ws[i].scales, ws[i].biases, need_y ? ys[i] : nullptr, ws[i].out};
+  }
+  if (!aligned16(x) || !aligned16(gamma)) return QG_EALIGN;
+  GemvExtras ex{};
+  ex.gamma = gamma;
+  ex.eps = eps;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (epi == QG_EPI_SWIGLU) return gemv_pair_launch(m[0], m[1], x, xt, ws[0].in, ys[0], s, ex);
+  return gemv_dense_launch(m, n, x, xt, ws[0].in, s, ex);
+}
+
+int qgemv_int4_sigmoid_fma(const qg_int4_weight* w, const void* x, int xt, const float* gate, const float* base,
+                           const uint16_t* residual, float* y, void* stream) {
+  int rc = check_weight(w, false);
+  if (rc) return rc;
+  if (!x || !gate || !base || !y || (xt != QG_X_BF16 && xt != QG_X_F32)) return QG_EINVAL;
+  if (!aligned16(x) || !aligned16(base) || !aligned16(y) || (residual && !aligned16(residual))) return QG_EALIGN;
+  GemvMatArg m{w->packed, w->scales, w->biases, y, w->out};
+  GemvExtras ex{};
+  ex.sgate = gate;
+  ex.ebase = base;
+  ex.resid = residual;
+  return gemv_dense_launch(&m, 1, x, xt, w->in, static_cast<cudaStream_t>(stream), ex);
+}
+
+int sigmoid_scalar_fma_residual(const float* gate, const float* value, const float* base, const uint16_t* residual,
+                                float* out, int n, void* stream) {
+  if (!gate || !value || !base || !out || n < 1) return QG_EINVAL;
+  if (!aligned16(value) || !aligned16(base) || !aligned16(out) || (residual && !aligned16(residual))) return QG_EALIGN;
+  return sigmoid_fma_launch(gate, value, base, residual, out, n, static_cast<cudaStream_t>(stream));
+}
+
 int moe_router_topk(const float* logits, int n_experts, int k, int renorm, uint32_t* idx, float* p, void* stream) {
   if (!logits || !idx || !p) return QG_EINVAL;
   if (k < 1 || k > 32 || n_experts < k || (renorm != 0 && renorm != 1)) return QG_EINVAL;

@@ -12,9 +12,11 @@ int gemv_tune(int ctas_per_sm) {
   return QG_OK;
 }
 
-int gemv_dense_launch(const GemvMatArg* mats, int n, const void* x, int xt, int in, cudaStream_t stream) {
+int gemv_dense_launch(const GemvMatArg* mats, int n, const void* x, int xt, int in, cudaStream_t stream,
+                      const GemvExtras& ex) {
   if (n < 1 || n > 4) return QG_EINVAL;
   GemvArgs a = dense_args(mats, n, x, xt, in);
+  apply_extras(a, ex);
   return plan_and_launch<kDense>(a, stream);
 }
 

@@ -91,6 +91,13 @@ struct GemvArgs {
   // bulk copy, which the TMA engine serves beside the weight loads already in flight; otherwise the
   // threads load it into registers.
   int stage, stage_off;
+  // RMSNorm prologue (NORM kernels): the product is taken with x * gamma / sqrt(mean(x^2) + eps):
+  // x * gamma is what gets quantized, and the finisher multiplies by the root (y is linear in x).
+  const uint16_t* gamma;  // bf16 [in]
+  float eps;
+  // Gated epilogue (dense): y = ebase + sigmoid(*sgate) * (W x), then + resid when set.
+  const float* sgate;
+  const float* ebase;
 };
 
 struct WPtr {
@@ -264,11 +271,12 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
 // conflicts; then (2^-k_g, sum of the group's x) per group; then the partial sums [row][NC][chunk];
 // then (STG) the staged copy of x.
 // STG: x arrives through one bulk copy (a.stage set by the planner), else the threads load it.
-template <int MODE, int RN, bool STG>
+template <int MODE, int RN, bool STG, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ uint32_t s_idx[kMaxMats];  // the in-kernel router's selection
   __shared__ float s_p[kMaxMats];
+  __shared__ float s_ss[kThreads / 32];  // NORM: per-warp sums of x^2
   __shared__ __align__(8) uint64_t xbar;  // the x copy's completion
   pdl_trigger();
   if (STG && threadIdx.x == 0) {
@@ -350,9 +358,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // which would also wait for this thread's weight loads in flight)
     constexpr uint32_t kChunk = 32768;
     const uint32_t xbytes = (uint32_t)G * (a.xf32 ? 256u : 128u);
-    mbar_arrive_expect_tx(&xbar, xbytes);
+    const uint32_t gbytes = NORM ? (uint32_t)G * 128u : 0u;  // gamma after x
+    mbar_arrive_expect_tx(&xbar, xbytes + gbytes);
     for (uint32_t off = 0; off < xbytes; off += kChunk)
       bulk_g2s_bytes(stage + off, static_cast<const uint8_t*>(a.x) + off, min(kChunk, xbytes - off), &xbar);
+    for (uint32_t off = 0; off < gbytes; off += kChunk)
+      bulk_g2s_bytes(stage + xbytes + off, reinterpret_cast<const uint8_t*>(a.gamma) + off, min(kChunk, gbytes - off),
+                     &xbar);
   }
   if (a.logits) {  // the router, in every CTA
     if (warp == 0) route_topk_warp(a.logits, a.n_logits, a.nmat, a.renorm, s_idx, s_p, blockIdx.x == 0 ? a.idx_out : nullptr,
@@ -366,6 +378,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // together and then processed: one memory latency for the whole prologue.  The loops are
     // uniform per warp (shuffles below).
     const int sub = lane & 7;
+    float ss = 0.f;  // NORM: this thread's sum of x^2
+    // NORM: accumulate x^2 (live groups only), then x *= gamma (eight bf16 in gw)
+    auto apply_norm = [&](int g, float (&v)[8], const uint4& gw) {
+      if (g < G) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
+      }
+      const uint32_t w[4] = {gw.x, gw.y, gw.z, gw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] *= __uint_as_float(w[j] << 16);
+        v[2 * j + 1] *= __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    };
     auto quant = [&](int g, const float (&v)[8]) {
       float m = 0.f, sx = 0.f;
 #pragma unroll
@@ -435,17 +461,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
           for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(w[j]);
         }
+        if constexpr (NORM) {
+          const uint32_t gofs = (uint32_t)G * (a.xf32 ? 256u : 128u);  // gamma after x
+          apply_norm(g, v, lds128(st + gofs + (uint32_t)gs * 128u + (uint32_t)sub * 16u));
+        }
         quant(g, v);
       }
     } else if (!a.xf32) {
-      constexpr int XB = 8;
+      constexpr int XB = NORM ? 4 : 8;  // (NORM: gamma's words take the other half of the registers)
       for (int gb = warp * 4; gb < G; gb += NW * 4 * XB) {
-        uint4 raw[XB];
+        uint4 raw[XB], graw[NORM ? XB : 1];
 #pragma unroll
         for (int i = 0; i < XB; ++i) {
           const int g = gb + i * NW * 4 + (lane >> 3);
           raw[i] = g < G ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)g * 64) + sub)
                          : make_uint4(0u, 0u, 0u, 0u);
+          if constexpr (NORM)
+            graw[i] = g < G ? __ldg(reinterpret_cast<const uint4*>(a.gamma + (size_t)g * 64) + sub) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int i = 0; i < XB; ++i) {
@@ -457,27 +489,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             v[2 * j] = __uint_as_float(w[j] << 16);
             v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
           }
+          if constexpr (NORM) apply_norm(gb + i * NW * 4 + (lane >> 3), v, graw[i]);
           quant(gb + i * NW * 4 + (lane >> 3), v);
         }
       }
     } else {
-      constexpr int XB = 5;
+      constexpr int XB = NORM ? 3 : 5;
       for (int gb = warp * 4; gb < G; gb += NW * 4 * XB) {
         float4 r0[XB], r1[XB];
+        uint4 graw[NORM ? XB : 1];
 #pragma unroll
         for (int i = 0; i < XB; ++i) {
           const int g = gb + i * NW * 4 + (lane >> 3);
           const float4* p4 = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)g * 64) + 2 * sub;
           r0[i] = g < G ? __ldg(p4) : make_float4(0.f, 0.f, 0.f, 0.f);
           r1[i] = g < G ? __ldg(p4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if constexpr (NORM)
+            graw[i] = g < G ? __ldg(reinterpret_cast<const uint4*>(a.gamma + (size_t)g * 64) + sub) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int i = 0; i < XB; ++i) {
           if (gb + i * NW * 4 >= G) break;  // (uniform per warp: nothing left in this batch)
-          const float v[8] = {r0[i].x, r0[i].y, r0[i].z, r0[i].w, r1[i].x, r1[i].y, r1[i].z, r1[i].w};
+          float v[8] = {r0[i].x, r0[i].y, r0[i].z, r0[i].w, r1[i].x, r1[i].y, r1[i].z, r1[i].w};
+          if constexpr (NORM) apply_norm(gb + i * NW * 4 + (lane >> 3), v, graw[i]);
           quant(gb + i * NW * 4 + (lane >> 3), v);
         }
       }
+    }
+    if constexpr (NORM) {  // the CTA's sum of x^2, per warp (added in warp order by the finisher)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) s_ss[warp] = ss;
     }
   }
   if (a.idx && blockIdx.x == 0 && (int)threadIdx.x < (SEG ? a.nseg : a.nmat)) {
@@ -535,6 +577,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   __syncthreads();
 
   // --- finish: sum each row's K chunks in order, epilogue, write ---
+  float rn = 1.f;  // NORM: 1 / sqrt(mean(x^2) + eps)
+  if constexpr (NORM) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) t += s_ss[w];
+    rn = 1.f / sqrtf(t / (float)a.in + a.eps);
+  }
+  const float sig = a.sgate ? 1.f / (1.f + expf(-__ldg(a.sgate))) : 0.f;
   for (int lr = threadIdx.x; lr < ve - vb; lr += kThreads) {
     const int v = vb + lr;
     int m = 0;
@@ -543,14 +593,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int row = v - mt.row0;
     float acc = 0.f;
     for (int kc = 0; kc < nkc; ++kc) acc += part[(lr * NC) * nkc + kc];
+    if (NORM) acc *= rn;
     if (PAIR) {
       float up = 0.f;
       for (int kc = 0; kc < nkc; ++kc) up += part[(lr * NC + 1) * nkc + kc];
+      if (NORM) up *= rn;
       bool ok = true;
       if (mt.w[0].slot >= 0) resolve(a, idxp, mt.w[0], ok);
       acc = ok ? acc / (1.f + expf(-acc)) * up : 0.f;
     }
-    if (SEG && a.resid) acc += bf16_bits_to_f32(a.resid[row]);
+    if (a.sgate) acc = fmaf(sig, acc, __ldg(a.ebase + row));
+    if (a.resid) acc += bf16_bits_to_f32(a.resid[row]);
     mt.y[row] = acc;
   }
 }
@@ -644,6 +697,14 @@ inline GemvArgs moe_down_args(const qg_int4_weight* down, const uint32_t* idx, c
   return a;
 }
 
+inline void apply_extras(GemvArgs& a, const GemvExtras& ex) {
+  a.gamma = ex.gamma;
+  a.eps = ex.eps;
+  a.sgate = ex.sgate;
+  a.ebase = ex.ebase;
+  a.resid = ex.resid;
+}
+
 // ------------------------------------------------------------------ host side: planning
 struct GemvTune {
   int ctas_per_sm;  // 0: automatic
@@ -662,16 +723,16 @@ inline size_t gemv_smem_bytes(int groups, int rows_per_cta, int nc) {
 constexpr int kStageMaxGroups = 128;
 inline size_t plan_stage(GemvArgs& a, size_t base, size_t limit) {
   const size_t off = (base + 127) & ~(size_t)127;
-  const size_t total = off + (size_t)a.groups * (a.xf32 ? 256 : 128);
+  const size_t total = off + (size_t)a.groups * ((a.xf32 ? 256 : 128) + (a.gamma ? 128 : 0));
   a.stage = total <= limit && a.groups <= kStageMaxGroups ? 1 : 0;
   a.stage_off = a.stage ? (int)off : 0;
   return a.stage ? total : base;
 }
 constexpr size_t kStaticSmemReserve = 1024;  // the kernels' static shared variables
 
-template <int MODE, int RN, bool STG>
+template <int MODE, int RN, bool STG, bool NORM>
 int launch_gemv_variant(const GemvArgs& a, int grid, size_t smem, cudaStream_t stream) {
-  auto k = gemv_kernel<MODE, RN, STG>;
+  auto k = gemv_kernel<MODE, RN, STG, NORM>;
   static std::atomic<int> smem_set{0};
   if ((int)smem > smem_set.load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -700,8 +761,13 @@ int plan_and_launch(GemvArgs& a, cudaStream_t stream) {
   const size_t smem = plan_stage(a, gemv_smem_bytes(a.groups, a.rows_per_cta, NC), limit);
   if (smem > limit) return QG_ENOTSUP;
   // rows x components per work unit: 4 (dense and seg: four rows; pair: two rows, gate and up)
-  return a.stage ? launch_gemv_variant<MODE, 4, true>(a, grid, smem, stream)
-                 : launch_gemv_variant<MODE, 4, false>(a, grid, smem, stream);
+  if constexpr (MODE != kSeg) {
+    if (a.gamma)
+      return a.stage ? launch_gemv_variant<MODE, 4, true, true>(a, grid, smem, stream)
+                     : launch_gemv_variant<MODE, 4, false, true>(a, grid, smem, stream);
+  }
+  return a.stage ? launch_gemv_variant<MODE, 4, true, false>(a, grid, smem, stream)
+                 : launch_gemv_variant<MODE, 4, false, false>(a, grid, smem, stream);
 }
 
 }  // namespace qg

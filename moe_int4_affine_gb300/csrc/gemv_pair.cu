@@ -7,8 +7,9 @@
 namespace qg {
 
 int gemv_pair_launch(const GemvMatArg& gate, const GemvMatArg& up, const void* x, int xt, int in, float* h,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, const GemvExtras& ex) {
   GemvArgs a = pair_args(gate, up, x, xt, in, h);
+  apply_extras(a, ex);
   return plan_and_launch<kPair>(a, stream);
 }
 

@@ -132,4 +132,49 @@ int chain8_launch(const float* p, const float* v, const uint16_t* residual, floa
   return launch(chain8_kernel, dim3(blocks), dim3(threads), 0, stream, p, v, residual, out, n);
 }
 
+// The shared-expert step ([FFAI#14] scalar-FMA commit, "sigmoidScalarFMAResidual"):
+//   out[i] = base[i] + sigmoid(gate) * value[i] (+ resid[i])
+// gate read once per thread from device memory; 16-byte vectors when n % 4 == 0.
+__global__ void __launch_bounds__(256) sigmoid_fma_kernel(const float* __restrict__ gate, const float* __restrict__ value,
+                                                          const float* __restrict__ base,
+                                                          const uint16_t* __restrict__ resid, float* __restrict__ out,
+                                                          int n) {
+  pdl_trigger();
+  pdl_wait();
+  const float s = 1.f / (1.f + expf(-__ldg(gate)));
+  const int nthreads = gridDim.x * blockDim.x;
+  const bool vec = (n & 3) == 0;
+  for (int i4 = blockIdx.x * blockDim.x + threadIdx.x; i4 * 4 < n; i4 += nthreads) {
+    const int i = i4 * 4;
+    if (vec) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(value + i));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(base + i));
+      float4 o = make_float4(fmaf(s, v.x, b.x), fmaf(s, v.y, b.y), fmaf(s, v.z, b.z), fmaf(s, v.w, b.w));
+      if (resid) {
+        const uint2 rb = __ldg(reinterpret_cast<const uint2*>(resid + i));
+        o.x += bf16_bits_to_f32(rb.x & 0xFFFFu);
+        o.y += bf16_bits_to_f32(rb.x >> 16);
+        o.z += bf16_bits_to_f32(rb.y & 0xFFFFu);
+        o.w += bf16_bits_to_f32(rb.y >> 16);
+      }
+      *reinterpret_cast<float4*>(out + i) = o;
+    } else {
+      for (int ii = i; ii < min(i + 4, n); ++ii) {
+        float o = fmaf(s, value[ii], base[ii]);
+        if (resid) o += bf16_bits_to_f32(resid[ii]);
+        out[ii] = o;
+      }
+    }
+  }
+}
+
+int sigmoid_fma_launch(const float* gate, const float* value, const float* base, const uint16_t* resid, float* out,
+                       int n, cudaStream_t stream) {
+  const int threads = 256;
+  const int quads = (n + 3) / 4;
+  int blocks = (quads + threads - 1) / threads;
+  blocks = std::max(1, std::min(blocks, 4 * device_info().num_sms));
+  return launch(sigmoid_fma_kernel, dim3(blocks), dim3(threads), 0, stream, gate, value, base, resid, out, n);
+}
+
 }  // namespace qg

@@ -51,11 +51,24 @@ struct GemvMatArg {
   float* y;
   int out;
 };
+// Optional prologue / epilogue of a dense or pair GEMV: RMSNorm of x (gamma set), and the gated
+// epilogue y = base + sigmoid(*sgate) * (W x) (sgate set) followed by + resid (resid set).
+struct GemvExtras {
+  const uint16_t* gamma;
+  float eps;
+  const float* sgate;
+  const float* ebase;
+  const uint16_t* resid;
+};
 // n in 1..4 matrices sharing x (rows of each written to its y).
-int gemv_dense_launch(const GemvMatArg* mats, int n, const void* x, int xt, int in, cudaStream_t stream);
+int gemv_dense_launch(const GemvMatArg* mats, int n, const void* x, int xt, int in, cudaStream_t stream,
+                      const GemvExtras& ex = GemvExtras{});
 // h = silu(gate x) * (up x)
 int gemv_pair_launch(const GemvMatArg& gate, const GemvMatArg& up, const void* x, int xt, int in, float* h,
-                     cudaStream_t stream);
+                     cudaStream_t stream, const GemvExtras& ex = GemvExtras{});
+// out[i] = base[i] + sigmoid(*gate) * value[i] (+ resid[i] when set)  (moe.cu)
+int sigmoid_fma_launch(const float* gate, const float* value, const float* base, const uint16_t* resid, float* out,
+                       int n, cudaStream_t stream);
 int gemv_tune(int ctas_per_sm);
 int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, const uint32_t* idx, int k,
                        const uint16_t* x, float* h, cudaStream_t stream);

@@ -41,6 +41,10 @@ lib.qgemv_int4_multi.argtypes = [_I, _W, _P, _I, ctypes.POINTER(_P), _I, _P]
 lib.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
 lib.moe_gather_qgemv_int4.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]
 lib.moe_layer_int4.argtypes = [_P, _I, _W, _W, _W, _I, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+lib.rmsnorm_qgemv_int4.argtypes = [_W, _P, _I, _P, ctypes.c_float, _P, _P]
+lib.rmsnorm_qgemv_int4_multi.argtypes = [_I, _W, _P, _I, _P, ctypes.c_float, ctypes.POINTER(_P), _I, _P]
+lib.qgemv_int4_sigmoid_fma.argtypes = [_W, _P, _I, _P, _P, _P, _P, _P]
+lib.sigmoid_scalar_fma_residual.argtypes = [_P, _P, _P, _P, _P, _I, _P]
 lib.dense_layer_int4.argtypes = [_W, _W, _W, _P, _I, _P, _P, ctypes.c_size_t, _P]
 lib.dense_layer_int4_host.argtypes = [_W, _W, _W, _P, _I, _P, _P, ctypes.c_size_t, _P]
 lib.moe_gather_qgemv_int4_noalloc.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P]
@@ -57,7 +61,8 @@ lib.qg_strerror.argtypes = [_I]
 lib.qg_strerror.restype = ctypes.c_char_p
 lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
-           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "dense_layer_int4", "dense_layer_int4_host",
+           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "dense_layer_int4", "dense_layer_int4_host", "rmsnorm_qgemv_int4",
+           "rmsnorm_qgemv_int4_multi", "qgemv_int4_sigmoid_fma", "sigmoid_scalar_fma_residual",
            "scalar_fma_chain8_residual", "qgemm_int4", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
 
@@ -170,6 +175,52 @@ def qgemv_int4_multi(ws, x, ys=None, epilogue: str = "none", stream=None):
     yp = (_P * n)(*[_ptr(y) for y in ys])
     _check(lib.qgemv_int4_multi(n, arr, _ptr(x), _xtype(x), yp, epi, _stream(stream)), "qgemv_int4_multi")
     return ys[0] if epi == QG_EPI_SWIGLU else ys
+
+
+def rmsnorm_qgemv_int4(w: Int4Weight, x, gamma, eps: float = 1e-6, y=None, stream=None):
+    """y = W (x * gamma / sqrt(mean(x^2) + eps)); gamma bf16 [in]."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(w.out, dtype=torch.float32, device=x.device)
+    _check(lib.rmsnorm_qgemv_int4(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(gamma), float(eps), _ptr(y),
+                                  _stream(stream)), "rmsnorm_qgemv_int4")
+    return y
+
+
+def rmsnorm_qgemv_int4_multi(ws, x, gamma, eps: float = 1e-6, ys=None, epilogue: str = "none", stream=None):
+    torch = _torch()
+    n = len(ws)
+    epi = {"none": QG_EPI_NONE, "swiglu": QG_EPI_SWIGLU}[epilogue]
+    if ys is None:
+        ys = [torch.empty(w.out, dtype=torch.float32, device=x.device) for w in ws]
+        if epi == QG_EPI_SWIGLU:
+            ys[1] = None
+    arr = (qg_int4_weight * n)(*[w.struct for w in ws])
+    yp = (_P * n)(*[_ptr(y) for y in ys])
+    _check(lib.rmsnorm_qgemv_int4_multi(n, arr, _ptr(x), _xtype(x), _ptr(gamma), float(eps), yp, epi,
+                                        _stream(stream)), "rmsnorm_qgemv_int4_multi")
+    return ys[0] if epi == QG_EPI_SWIGLU else ys
+
+
+def qgemv_int4_sigmoid_fma(w: Int4Weight, x, gate, base, residual=None, y=None, stream=None):
+    """y = base + sigmoid(gate[0]) * (W x) (+ residual bf16)."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(w.out, dtype=torch.float32, device=x.device)
+    _check(lib.qgemv_int4_sigmoid_fma(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(gate), _ptr(base),
+                                      _ptr(residual), _ptr(y), _stream(stream)), "qgemv_int4_sigmoid_fma")
+    return y
+
+
+def sigmoid_scalar_fma_residual(gate, value, base, residual=None, out=None, stream=None):
+    """out = base + sigmoid(gate[0]) * value (+ residual bf16)."""
+    torch = _torch()
+    n = value.numel()
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=value.device)
+    _check(lib.sigmoid_scalar_fma_residual(_ptr(gate), _ptr(value), _ptr(base), _ptr(residual), _ptr(out), n,
+                                           _stream(stream)), "sigmoid_scalar_fma_residual")
+    return out
 
 
 def moe_router_topk(logits, k: int = 8, renorm: bool = True, idx=None, p=None, stream=None):
