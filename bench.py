@@ -457,6 +457,33 @@ def measure_configs(qg, I, dev, stream):
                  launches=(T if tc_min == 0 and T < 32 else 2))
         res[f"c4_qgemm_T{T}_{label}"] = e
     qg.qg_tune_qgemm(0)
+
+    # next row N2: the prefill form of the shared-input quartet (in 2048), one launch for all four
+    # projections against one qgemm_int4 call each
+    outs = (8192, 4096, 32, 32)
+    mats = [qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_MULTI + j, o, 2048), dev) for j, o in enumerate(outs)]
+    sets = [mats] + [[copies(m, 2)[1] for m in mats] for _ in range(11)]
+    for T in (32, 256):
+        X = qg.to_device(I.bf16_normal(0, I.TID_X, (T, 2048)), dev)
+        Ys = [torch.empty((T, o), dtype=torch.float32, device=dev) for o in outs]
+        need = qg.qg_workspace_bytes(qg.QG_OP_QGEMM, mats[0], T)
+        wsb = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        margs = [((qg.qg_int4_weight * 4)(*[m.struct for m in st]), (P * 4)(*[t.data_ptr() for t in Ys])) for st in sets]
+        us = tl(lambda i: lib.qgemm_int4_multi(4, margs[i % 12][0], P(X.data_ptr()), T, margs[i % 12][1],
+                                               P(wsb.data_ptr()), wsb.numel(), s), 60)
+
+        def separate(i):
+            rc = 0
+            for j in range(4):
+                rc |= lib.qgemm_int4(byref(sets[i % 12][j].struct), P(X.data_ptr()), T, P(Ys[j].data_ptr()),
+                                     P(wsb.data_ptr()), wsb.numel(), s)
+            return rc
+        us_sep = tl(separate, 30)
+        nbytes = sum(weight_bytes(o, 2048) for o in outs) + T * 2048 * 2 + T * 4 * sum(outs)
+        tf = 2.0 * T * sum(outs) * 2048 / us / 1e6
+        res[f"n2_qgemm_multi_quartet_T{T}"] = dict(gb(nbytes, us), call="qgemm_int4_multi", TFLOPs=round(tf, 1),
+                                                   us_separate_calls=round(us_sep, 3), launches=2,
+                                                   l2="weights rotate over 12 copies")
     assert qg.qg_device_status() == 0
     return res
 

@@ -260,6 +260,19 @@ int scalar_fma_chain8_residual(const float *p, const float *v, const uint16_t *r
 int qgemm_int4(const qg_int4_weight *w, const uint16_t *X, int T, float *Y, void *workspace, size_t ws_bytes,
                void *stream);
 
+/*
+ * qgemm_int4_multi -- n in {2, 3, 4} projections of the same T tokens ([FFAI#14]
+ * "ffai_batched_qkv_qmm_fast" / "ffai_batched_4_qmm_fast": the M > 1 prefill form of the fused
+ * QKV / GDN-input projections, x read once for all of them):
+ *   Ys[i][t][r] = sum_j w_i[r][j] * X[t][j]
+ * ws[i]: single matrices with the same in; X: bf16 [T][in]; Ys[i]: fp32 [T][ws[i].out] (device).
+ * For T >= 32 one tensor-core launch covers the row tiles of all n matrices (the tokens staged
+ * once); below that, one GEMV launch per token covers all n.  workspace: at least
+ * qg_workspace_bytes(QG_OP_QGEMM, &ws[0], T) bytes.  Limits as qgemm_int4.
+ */
+int qgemm_int4_multi(int n, const qg_int4_weight *ws, const uint16_t *X, int T, float *const *Ys, void *workspace,
+                     size_t ws_bytes, void *stream);
+
 typedef enum {
   QG_OP_QGEMV = 0,
   QG_OP_MULTI = 1,

@@ -270,6 +270,22 @@ int qgemm_int4(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void
   return qgemm_launch(w, X, T, Y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
+int qgemm_int4_multi(int n, const qg_int4_weight* ws, const uint16_t* X, int T, float* const* Ys, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  if (n < 2 || n > 4 || !ws || !Ys || !X || T < 1 || T > 4096) return QG_EINVAL;
+  for (int i = 0; i < n; ++i) {
+    int rc = check_weight(&ws[i], false);
+    if (rc) return rc;
+    if (ws[i].in != ws[0].in || !Ys[i]) return QG_EINVAL;
+    if (!aligned16(Ys[i])) return QG_EALIGN;
+  }
+  if (!aligned16(X)) return QG_EALIGN;
+  const size_t need = qgemm_workspace_bytes(&ws[0], T);
+  if (need && (!workspace || ws_bytes < need)) return QG_EWORKSPACE;
+  if (need && !aligned16(workspace)) return QG_EALIGN;
+  return qgemm_multi_launch(ws, n, X, T, Ys, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
 size_t qg_workspace_bytes(int op, const qg_int4_weight* w, int T_or_k) {
   if (!w) return 0;
   switch (op) {

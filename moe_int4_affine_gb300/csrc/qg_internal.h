@@ -95,5 +95,10 @@ int qgemm_tune(int tc_min_T);
 size_t qgemm_tc_workspace_bytes(const qg_int4_weight* w, int T);
 int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void* ws, size_t ws_bytes,
                     cudaStream_t stream);
+// n in 1..4 weights sharing X (same in): Y[i] = X W_i^T, one launch over all their row tiles.
+int qgemm_tc_launch_multi(const qg_int4_weight* w, int n, const uint16_t* X, int T, float* const* Y, void* ws,
+                          size_t ws_bytes, cudaStream_t stream);
+int qgemm_multi_launch(const qg_int4_weight* w, int n, const uint16_t* X, int T, float* const* Y, void* ws,
+                       size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace qg

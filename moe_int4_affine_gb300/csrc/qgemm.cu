@@ -31,4 +31,19 @@ int qgemm_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, vo
   return QG_OK;
 }
 
+// Projections sharing X: one tensor-core launch over all row tiles, or per token one GEMV launch
+// over all n matrices.
+int qgemm_multi_launch(const qg_int4_weight* w, int n, const uint16_t* X, int T, float* const* Y, void* ws,
+                       size_t ws_bytes, cudaStream_t stream) {
+  if (n < 1 || n > 4) return QG_EINVAL;
+  if (T >= g_tc_min_T) return qgemm_tc_launch_multi(w, n, X, T, Y, ws, ws_bytes, stream);
+  for (int t = 0; t < T; ++t) {
+    GemvMatArg m[4];
+    for (int i = 0; i < n; ++i) m[i] = GemvMatArg{w[i].packed, w[i].scales, w[i].biases, Y[i] + (size_t)t * w[i].out, w[i].out};
+    const int rc = gemv_dense_launch(m, n, X + (size_t)t * w[0].in, QG_X_BF16, w[0].in, stream);
+    if (rc != QG_OK) return rc;
+  }
+  return QG_OK;
+}
+
 }  // namespace qg

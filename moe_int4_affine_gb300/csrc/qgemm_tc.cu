@@ -52,14 +52,23 @@ constexpr int kTmemCols = 512;
 constexpr int kWStageBytes = kProducers * 32 + kProducers * 8;
 constexpr int kSmemBudget = 220 * 1024;
 
-struct TcArgs {
+// One weight of a (multi-projection) call; its 128-row tiles are grid columns tile0, tile0 + 1, ...
+struct TcMat {
   const uint32_t* packed;
   const uint16_t* scales;
   const uint16_t* biases;
+  float* y;  // [T][out]
+  int out;
+  int tile0;
+};
+constexpr int kTcMaxMats = 4;
+
+struct TcArgs {
+  TcMat mat[kTcMaxMats];  // matrices sharing the tokens (same in)
+  int nmat;
   const uint8_t* xt;  // token tiles: [n_tiles][k groups][n_tile][128 B], swizzled, fp16
   const float* xs;    // [n_tiles * n_tile] per-token output scale
-  float* y;           // [T][out]
-  int out, in, T;
+  int in, T;
   int n_tile;
   int stages;
   uint32_t idesc;
@@ -191,7 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.x * kBM;
+  int mi = 0;  // this CTA's matrix: the last one whose first tile is at or before blockIdx.x
+  while (mi + 1 < a.nmat && (int)blockIdx.x >= a.mat[mi + 1].tile0) ++mi;
+  const TcMat& mt = a.mat[mi];
+  const int m0 = ((int)blockIdx.x - mt.tile0) * kBM;
   const int tile = blockIdx.y, n0 = tile * a.n_tile;
   const int nk = a.in / kGK;         // groups
   const int nst = (nk + 1) / 2;      // pipeline stages (two groups each)
@@ -225,14 +237,14 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     // ---------------- producers: thread (row r, warp group h) makes group 2 j + h of every stage j
     const int r = tid & (kBM - 1), h = tid >> 7;
     const int row = m0 + r;
-    const bool rv = row < a.out;
-    const int rowc = rv ? row : a.out - 1;
+    const bool rv = row < mt.out;
+    const int rowc = rv ? row : mt.out - 1;
     const int ngs = a.in / 64;
     const int my_n = (nk - h + 1) / 2;  // groups of this thread
     // group 2 jj + h: codes advance by 16 words per jj, the scale / bias index by 2
-    const uint32_t* wp = a.packed + (size_t)rowc * (a.in / 8) + (size_t)h * 8;
+    const uint32_t* wp = mt.packed + (size_t)rowc * (a.in / 8) + (size_t)h * 8;
     const size_t e0 = (size_t)rowc * ngs + h;
-    const size_t n_sb = (size_t)a.out * ngs;
+    const size_t n_sb = (size_t)mt.out * ngs;
     const int odd = (int)(e0 & 1);  // which half of the copied 32-bit words holds s and b
     const uint32_t wcode = wring + (uint32_t)tid * 16;  // chunk c at + c * kProducers * 16
     const uint32_t wsb = wring + kProducers * 32 + (uint32_t)tid * 8;
@@ -244,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         cp16(wcode + g + kProducers * 16, src + 4, rv ? 16u : 0u);
         const size_t e = e0 + 2 * (size_t)jj, eo = e & ~(size_t)1;
         const uint32_t nb = rv ? (eo + 1 < n_sb ? 4u : 2u) : 0u;
-        cp4(wsb + g, a.scales + eo, nb);
-        cp4(wsb + g + 4, a.biases + eo, nb);
+        cp4(wsb + g, mt.scales + eo, nb);
+        cp4(wsb + g + 4, mt.biases + eo, nb);
       }
       cp_commit();
     };
@@ -355,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int t = n0 + c0 + cc + j;
-          if (row < a.out && t < a.T) a.y[(size_t)t * a.out + row] = __uint_as_float(v[j]) * __ldg(a.xs + t);
+          if (row < mt.out && t < a.T) mt.y[(size_t)t * mt.out + row] = __uint_as_float(v[j]) * __ldg(a.xs + t);
         }
       }
     }
@@ -466,33 +478,35 @@ size_t qgemm_tc_workspace_bytes(const qg_int4_weight* w, int T) {
   return rows * (size_t)w->in * 2 + rows * sizeof(float) + 256;
 }
 
-int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void* ws, size_t ws_bytes,
-                    cudaStream_t stream) {
-  const TcPlan p = tc_plan(w->out, w->in, T);
+int qgemm_tc_launch_multi(const qg_int4_weight* w, int n, const uint16_t* X, int T, float* const* Y, void* ws,
+                          size_t ws_bytes, cudaStream_t stream) {
+  if (n < 1 || n > kTcMaxMats) return QG_EINVAL;
+  const TcPlan p = tc_plan(w[0].out, w[0].in, T);
   const size_t rows = (size_t)p.n_tiles * p.n_tile;
-  const size_t xt_bytes = rows * (size_t)w->in * 2;
-  if (ws_bytes < qgemm_tc_workspace_bytes(w, T)) return QG_EWORKSPACE;
+  const size_t xt_bytes = rows * (size_t)w[0].in * 2;
+  if (ws_bytes < qgemm_tc_workspace_bytes(&w[0], T)) return QG_EWORKSPACE;
   uint8_t* xt = static_cast<uint8_t*>(ws);
   float* xs = reinterpret_cast<float*>(xt + xt_bytes);
-  int rc = launch(qgemm_prep_kernel, dim3((unsigned)rows), dim3(kPrepThreads), 0, stream, X, T, w->in, p.n_tile, xt,
-                  xs);
+  int rc = launch(qgemm_prep_kernel, dim3((unsigned)rows), dim3(kPrepThreads), 0, stream, X, T, w[0].in, p.n_tile,
+                  xt, xs);
   if (rc != QG_OK) return rc;
   TcArgs a{};
-  a.packed = w->packed;
-  a.scales = w->scales;
-  a.biases = w->biases;
+  int tiles = 0;
+  for (int i = 0; i < n; ++i) {
+    a.mat[i] = TcMat{w[i].packed, w[i].scales, w[i].biases, Y[i], w[i].out, tiles};
+    tiles += (w[i].out + kBM - 1) / kBM;
+  }
+  a.nmat = n;
   a.xt = xt;
   a.xs = xs;
-  a.y = Y;
-  a.out = w->out;
-  a.in = w->in;
+  a.in = w[0].in;
   a.T = T;
   a.n_tile = p.n_tile;
   a.stages = p.stages;
   // instruction descriptor (kind::f16): D fp32 (bits 4-5 = 1), A and B fp16 (bits 7-12 = 0), both
   // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
   a.idesc = (1u << 4) | ((uint32_t)(p.n_tile >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-  const dim3 grid((unsigned)((w->out + kBM - 1) / kBM), (unsigned)p.n_tiles);
+  const dim3 grid((unsigned)tiles, (unsigned)p.n_tiles);
   auto go = [&](auto k) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
       return (int)QG_ELAUNCH;
@@ -508,6 +522,11 @@ int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y,
     default:
       return go(qgemm_tc_kernel<2>);
   }
+}
+
+int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void* ws, size_t ws_bytes,
+                    cudaStream_t stream) {
+  return qgemm_tc_launch_multi(w, 1, X, T, &Y, ws, ws_bytes, stream);
 }
 
 }  // namespace qg

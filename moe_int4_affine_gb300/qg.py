@@ -50,6 +50,7 @@ lib.dense_layer_int4_host.argtypes = [_W, _W, _W, _P, _I, _P, _P, ctypes.c_size_
 lib.moe_gather_qgemv_int4_noalloc.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P]
 lib.scalar_fma_chain8_residual.argtypes = [_P, _P, _P, _P, _I, _P]
 lib.qgemm_int4.argtypes = [_W, _P, _I, _P, _P, ctypes.c_size_t, _P]
+lib.qgemm_int4_multi.argtypes = [_I, _W, _P, _I, ctypes.POINTER(_P), _P, ctypes.c_size_t, _P]
 lib.qg_workspace_bytes.argtypes = [_I, _W, _I]
 lib.qg_workspace_bytes.restype = ctypes.c_size_t
 lib.qg_set_pdl.argtypes = [_I]
@@ -63,7 +64,7 @@ lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
            "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "dense_layer_int4", "dense_layer_int4_host", "rmsnorm_qgemv_int4",
            "rmsnorm_qgemv_int4_multi", "qgemv_int4_sigmoid_fma", "sigmoid_scalar_fma_residual",
-           "scalar_fma_chain8_residual", "qgemm_int4", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
+           "scalar_fma_chain8_residual", "qgemm_int4", "qgemm_int4_multi", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
 
 
@@ -325,6 +326,22 @@ def scalar_fma_chain8_residual(p, v, residual, out=None, stream=None):
     _check(lib.scalar_fma_chain8_residual(_ptr(p), _ptr(v), _ptr(residual), _ptr(out), n, _stream(stream)),
            "scalar_fma_chain8_residual")
     return out
+
+
+def qgemm_int4_multi(ws, X, Ys=None, workspace=None, stream=None):
+    """Ys[i] = X W_i^T for n in {2,3,4} weights sharing in; X bf16 [T][in]."""
+    torch = _torch()
+    n, T = len(ws), X.shape[0]
+    if Ys is None:
+        Ys = [torch.empty((T, w.out), dtype=torch.float32, device=X.device) for w in ws]
+    need = qg_workspace_bytes(QG_OP_QGEMM, ws[0], T)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    arr = (qg_int4_weight * n)(*[w.struct for w in ws])
+    yp = (_P * n)(*[_ptr(y) for y in Ys])
+    _check(lib.qgemm_int4_multi(n, arr, _ptr(X), T, yp, _ptr(workspace), nbytes, _stream(stream)), "qgemm_int4_multi")
+    return Ys
 
 
 def qgemm_int4(w: Int4Weight, X, Y=None, workspace=None, stream=None):

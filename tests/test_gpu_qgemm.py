@@ -82,3 +82,40 @@ def test_qgemm_token_scales_extreme_rows(qg):
     Y_ref, A = oracle.qgemm(d["packed"], d["scales"], d["biases"], X)
     assert_within_bound(Y, Y_ref, A)
     assert np.all(Y[3] == 0.0)
+
+
+def _multi(qg, outs, in_dim, T, seed):
+    ds = [I.int4_weight(seed, I.TID_MULTI + i, o, in_dim) for i, o in enumerate(outs)]
+    X = I.bf16_normal(seed, I.TID_X, (T, in_dim))
+    Ys = qg.qgemm_int4_multi([qg.Int4Weight.from_numpy(d) for d in ds], qg.to_device(X))
+    return ds, X, [qg.to_numpy(Y).astype(np.float64) for Y in Ys]
+
+
+@pytest.mark.parametrize("outs,in_dim,T", [((8192, 4096, 32, 32), 2048, 256), ((8192, 4096, 32, 32), 2048, 8),
+                                           ((4096, 512, 512), 2048, 100), ((200, 64), 576, 33),
+                                           ((130, 260, 1), 1088, 300)])
+def test_qgemm_multi_vs_oracle(qg, outs, in_dim, T):
+    """Prefill form of the shared-input projections (quartet / triple of config 2, and ragged
+    sets): every matrix's rows against the oracle (large matrices on sampled rows), every token."""
+    ds, X, Ys = _multi(qg, outs, in_dim, T, seed=T + len(outs))
+    g = np.random.default_rng(T)
+    for d, Y, o in zip(ds, Ys, outs):
+        assert Y.shape == (T, o)
+        rows = range(o) if o <= 300 else sorted(set([0, o - 1, 127, 128] + list(g.integers(0, o, 20))))
+        if o <= 300:
+            Yr, Ar = oracle.qgemm(d["packed"], d["scales"], d["biases"], X)
+            assert_within_bound(Y, Yr, Ar)
+            continue
+        for r in rows:
+            Yr, Ar = oracle.qgemm(d["packed"], d["scales"], d["biases"], X, rows=(r, r + 1))
+            assert_within_bound(Y[:, r:r + 1], Yr, Ar, what=f"row {r}")
+    assert qg.qg_device_status() == 0
+
+
+@pytest.mark.parametrize("T", [8, 64])
+def test_qgemm_multi_equals_separate_calls(qg, T):
+    """One launch over all matrices gives bit for bit what one qgemm_int4 call per matrix gives."""
+    outs = (1000, 300, 64)
+    ds, X, Ys = _multi(qg, outs, 1024, T, seed=77)
+    for d, Y in zip(ds, Ys):
+        np.testing.assert_array_equal(Y, _run(qg, d, X))
