@@ -72,6 +72,10 @@ def _L():
             lib.orc_moe.restype = I
             lib.orc_qgemm_rows.argtypes = [P, P, P, I64, I64, I64, P, I64, I64, I64, P, P]
             lib.orc_qgemm_rows.restype = I
+            lib.orc_bf16_round.argtypes = [ctypes.c_float]
+            lib.orc_bf16_round.restype = ctypes.c_uint16
+            lib.orc_quantize_rows.argtypes = [P, I, I64, I64, I, I64, I64, P, P, P]
+            lib.orc_quantize_rows.restype = I
             lib.orc_rmsnorm.argtypes = [P, I, P, I64, ctypes.c_double, P]
             lib.orc_rmsnorm.restype = I
             lib.orc_sigmoid.argtypes = [ctypes.c_double]
@@ -228,6 +232,26 @@ def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
 def rmsnorm_qgemv(packed, scales, biases, x, gamma, eps: float, group_size: int = 64):
     """y, absref of W rmsnorm(x): the norm in float64, then the GEMV of the normalised vector."""
     return qgemv_f64x(packed, scales, biases, rmsnorm(x, gamma, eps), group_size)
+
+
+def bf16_round(f: float) -> int:
+    """bf16 bits of a binary32 value, round to nearest, ties to even."""
+    return int(_L().orc_bf16_round(float(f)))
+
+
+def quantize(w: np.ndarray, bits: int = 4, rows=None):
+    """Affine group-64 encode of w (bf16 bits or float32, [out][in]): (packed uint32
+    [out][in*bits/32], scales bf16 bits [out][in/64], biases bf16 bits [out][in/64])."""
+    w = np.ascontiguousarray(w)
+    out, in_dim = w.shape
+    r0, r1 = (0, out) if rows is None else (int(rows[0]), int(rows[1]))
+    packed = np.zeros((out, in_dim * bits // 32), dtype=np.uint32)
+    scales = np.zeros((out, in_dim // 64), dtype=np.uint16)
+    biases = np.zeros((out, in_dim // 64), dtype=np.uint16)
+    rc = _L().orc_quantize_rows(_p(w), _xtype(w), out, in_dim, bits, r0, r1, _p(packed), _p(scales), _p(biases))
+    if rc != 0:
+        raise ValueError("orc_quantize_rows rejected the arguments")
+    return packed[r0:r1], scales[r0:r1], biases[r0:r1]
 
 
 def sigmoid(g: float) -> float:

@@ -311,3 +311,75 @@ void orc_sigmoid_scalar_fma(double gate, const float *value, const float *base, 
     if (absref) absref[i] = fabs(b) + fabs(t) + fabs(r);
   }
 }
+
+/* ---------------------------------------------------------------------------------------
+ * Affine group-64 quantizer (encode) for the Q4_64A / Q2_64A formats ([ds4#844]: "Q4_64A and
+ * Q2_64A codes are derived from the serialized BF16 scale/bias"; the page gives no formula for
+ * the scale and bias themselves -- the plain reading is min/max affine):
+ *   lo = min of the group, hi = max;  scale = (hi - lo) / (2^bits - 1);  bias = lo
+ *   s = bf16(scale), b = bf16(bias)            (round to nearest, ties to even)
+ *   q_j = clamp(round_to_nearest_even((w_j - b) / s), 0, 2^bits - 1);   q_j = 0 when s == 0
+ * The codes are an integer decided by floating point, so they are computed here in the precision
+ * the GPU kernel uses, IEEE binary32 with correctly rounded subtract, divide and
+ * round-to-integer (the pages fix no precision).  Packing: bits = 4 -> 8 codes per u32, element
+ * 8w + i at bits 4i; bits = 2 -> 16 codes per u32, element 16w + i at bits 2i (low first).
+ * w bf16 or fp32 [out][in]; packed [out][in * bits / 32]; scales, biases bf16 [out][in / 64].
+ * ------------------------------------------------------------------------------------- */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7F800000u) == 0x7F800000u) return (uint16_t)(u >> 16); /* inf / nan: not expected */
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7FFFu + lsb;
+  return (uint16_t)(u >> 16);
+}
+
+static float bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+uint16_t orc_bf16_round(float f) { return f32_to_bf16_rne(f); }
+
+int orc_quantize_rows(const void *w, int wtype, int64_t out, int64_t in, int bits, int64_t r0, int64_t r1,
+                      uint32_t *packed, uint16_t *scales, uint16_t *biases) {
+  if ((bits != 4 && bits != 2) || in % 64 != 0 || in <= 0 || r0 < 0 || r1 > out || r0 > r1) return ORC_EINVAL;
+  const int per_word = 32 / bits;
+  const unsigned qmax = (1u << bits) - 1u;
+  const int64_t ngs = in / 64, nwords = in / per_word;
+  for (int64_t r = r0; r < r1; ++r) {
+    for (int64_t g = 0; g < ngs; ++g) {
+      float lo = 0.f, hi = 0.f;
+      for (int64_t j = 0; j < 64; ++j) {
+        float v = (float)load_x(w, wtype, r * in + g * 64 + j); /* bf16 / fp32: exact in binary32 */
+        if (j == 0 || v < lo) lo = v;
+        if (j == 0 || v > hi) hi = v;
+      }
+      volatile float range = hi - lo;                 /* binary32 operations, one rounding each */
+      volatile float scale = range / (float)qmax;
+      uint16_t sb = f32_to_bf16_rne(scale), bb = f32_to_bf16_rne(lo);
+      scales[r * ngs + g] = sb;
+      biases[r * ngs + g] = bb;
+      float s = bf16_to_f32(sb), b = bf16_to_f32(bb);
+      for (int64_t j = 0; j < 64; j += per_word) {
+        uint32_t word = 0;
+        for (int i = 0; i < per_word; ++i) {
+          unsigned q = 0;
+          if (s != 0.f) {
+            volatile float d = (float)load_x(w, wtype, r * in + g * 64 + j + i) - b;
+            volatile float t = d / s;
+            float qf = rintf(t); /* round to nearest, ties to even (default rounding mode) */
+            if (qf < 0.f) qf = 0.f;
+            if (qf > (float)qmax) qf = (float)qmax;
+            q = (unsigned)qf;
+          }
+          word |= (uint32_t)q << (bits * i);
+        }
+        packed[r * nwords + (g * 64 + j) / per_word] = word;
+      }
+    }
+  }
+  return ORC_OK;
+}

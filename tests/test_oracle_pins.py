@@ -490,3 +490,89 @@ def test_sigmoid_scalar_fma_closed_forms():
     np.testing.assert_allclose(out0, base + 0.5 * v.astype(np.float64), rtol=1e-15, atol=1e-16)
     outm, _ = oracle.sigmoid_scalar_fma(-40.0, v, base, r)
     np.testing.assert_allclose(outm, base + rv, rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------- affine quantizer (encode), next row N3
+def _grid_group(rng, bits, s_bits=0x3C50, k=-20):
+    """A group on an exact grid: s bf16 (here 0.0126953125), b = k s, w_j = b + q_j s with q_j
+    random in [0, 2^bits - 1] and both ends present; every value exact in binary32."""
+    qmax = (1 << bits) - 1
+    q = rng.integers(0, qmax + 1, 64)
+    q[rng.integers(0, 64)] = 0
+    q[rng.integers(0, 64)] = qmax
+    if q.min() != 0:
+        q[np.argmin(q)] = 0
+    s = oracle.bf16_to_f64(s_bits)
+    w = ((k + q) * s).astype(np.float32)
+    return q, s, k * s, w
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_quantize_exact_grid_round_trip(bits):
+    """Values on an exact grid b + q s (both ends present): scale s, bias b and every code q come
+    back exactly; the packing order is low bits first."""
+    rng = np.random.default_rng(bits)
+    q, s, b, w = _grid_group(rng, bits)
+    packed, sc, bi = oracle.quantize(w.reshape(1, 64), bits)
+    assert oracle.bf16_to_f64(int(sc[0, 0])) == s and oracle.bf16_to_f64(int(bi[0, 0])) == b
+    per = 32 // bits
+    got = [(int(packed[0, j // per]) >> (bits * (j % per))) & ((1 << bits) - 1) for j in range(64)]
+    assert got == q.tolist()
+
+
+def test_quantize_constant_group():
+    w = np.full((2, 128), 0.3, np.float32)
+    packed, sc, bi = oracle.quantize(w)
+    assert np.all(packed == 0) and np.all(sc == 0)
+    assert np.all(bi == oracle.bf16_round(np.float32(0.3)))
+
+
+def test_quantize_codes_come_from_bf16_scale_and_bias():
+    """lo = 0, hi = 1: with the binary32 scale 1/15, w = 0.968 sits at 14.52 (code 15); with the
+    bf16 scale 0.06689453125 at 14.47 (code 14) -- the codes are derived from the rounded scale,
+    as the pages require."""
+    w = np.zeros(64, np.float32)
+    w[1] = 1.0
+    w[2] = 0.968
+    packed, sc, bi = oracle.quantize(w.reshape(1, 64))
+    s = oracle.bf16_to_f64(int(sc[0, 0]))
+    assert s == 0.06689453125 and bi[0, 0] == 0
+    q2 = (int(packed[0, 0]) >> 8) & 0xF
+    assert q2 == 14
+    assert np.rint(np.float32(0.968) / (np.float32(1.0) / np.float32(15))) == 15  # unrounded scale
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_quantize_nearest_grid_point_and_error_bound(bits):
+    """Random groups: every code is the nearest grid point b + q s in exact arithmetic (clamped to
+    [0, 2^bits - 1]), except within 1e-5 of a tie, where binary32 decides; and the dequantised value
+    is within s/2 plus the bf16 rounding of scale and bias of the input."""
+    rng = np.random.default_rng(10 + bits)
+    qmax = (1 << bits) - 1
+    w = rng.normal(0, 0.05, (8, 256)).astype(np.float32)
+    packed, sc, bi = oracle.quantize(w, bits)
+    per = 32 // bits
+    for r in range(8):
+        for g in range(4):
+            s = oracle.bf16_to_f64(int(sc[r, g]))
+            b = oracle.bf16_to_f64(int(bi[r, g]))
+            grp = w[r, 64 * g:64 * g + 64].astype(np.float64)
+            lo, hi = grp.min(), grp.max()
+            assert abs(b - lo) <= abs(lo) * 2.0 ** -8 and s > 0
+            for j in range(64):
+                col = 64 * g + j
+                q = (int(packed[r, col // per]) >> (bits * (col % per))) & qmax
+                t = (grp[j] - b) / s
+                frac = t - math.floor(t)
+                if abs(frac - 0.5) > 1e-5:
+                    assert q == min(max(int(math.floor(t + 0.5)), 0), qmax), (r, g, j, t, q)
+                err = abs(grp[j] - (b + q * s))
+                assert err <= s / 2 + abs(b - lo) + qmax * abs(s - (hi - lo) / qmax) + 1e-12
+
+
+def test_quantize_bf16_and_f32_inputs_agree():
+    x = I.bf16_normal(12, I.TID_X, (4, 192))
+    a = oracle.quantize(x)
+    b = oracle.quantize(np.array([[oracle.bf16_to_f64(int(v)) for v in row] for row in x], np.float32))
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
