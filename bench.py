@@ -439,6 +439,19 @@ def measure_configs(qg, I, dev, stream):
                                                       l2="weights rotate over 192 copies (170 MB, larger than L2)")
     del sd, sds
 
+    # next row N3: the affine encoder over the FFN gate's shape (bf16 weights in, Q4_64A / Q2_64A out)
+    wq = [qg.to_device(I.bf16_normal(i, I.TID_W, (FFN, HIDDEN)), dev) for i in range(2)]
+    for bits in (4, 2):
+        pq = torch.empty((FFN, HIDDEN * bits // 32), dtype=torch.int32, device=dev)
+        sq = torch.empty((FFN, HIDDEN // 64), dtype=torch.bfloat16, device=dev)
+        bq = torch.empty((FFN, HIDDEN // 64), dtype=torch.bfloat16, device=dev)
+        us = tl(lambda i: lib.quantize_affine_q64a(P(wq[i % 2].data_ptr()), qg.QG_X_BF16, FFN, HIDDEN, bits,
+                                                   P(pq.data_ptr()), P(sq.data_ptr()), P(bq.data_ptr()), s), 30)
+        nbytes = FFN * HIDDEN * 2 + FFN * HIDDEN * bits // 8 + FFN * (HIDDEN // 64) * 4
+        res[f"n3_quantize_q{bits}_64a_17408x5120"] = dict(gb(nbytes, us), call="quantize_affine_q64a",
+                                                         l2="two 178 MB inputs alternate")
+    del wq
+
     # config 4: dequant-GEMM, W 17408 x 5120, X T x 5120
     w = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_W, FFN, HIDDEN), dev)
     ws_ = copies(w, 12)

@@ -273,6 +273,23 @@ int qgemm_int4(const qg_int4_weight *w, const uint16_t *X, int T, float *Y, void
 int qgemm_int4_multi(int n, const qg_int4_weight *ws, const uint16_t *X, int T, float *const *Ys, void *workspace,
                      size_t ws_bytes, void *stream);
 
+/*
+ * quantize_affine_q64a -- the affine group-64 encoder that makes this library's weights (Q4_64A,
+ * bits = 4) and the 2-bit variant (Q2_64A, bits = 2) ([ds4#844]: "Q4_64A and Q2_64A codes are
+ * derived from the serialized BF16 scale/bias").  Per row r and group g of 64 columns:
+ *   lo = min, hi = max (-0 taken as +0);  s = bf16((hi - lo) / (2^bits - 1));  b = bf16(lo)
+ *   q_j = clamp(rint((w_j - b) / s), 0, 2^bits - 1), 0 when s = 0
+ * (bf16 rounding: nearest, ties to even; the code arithmetic in binary32 with correctly rounded
+ * subtract and divide).  The pages give only the bf16 rule; the min/max affine form is the plain
+ * reading.  w: bf16 or fp32 [out][in] (w_type QG_X_BF16 / QG_X_F32), finite; packed: u32
+ * [out][in * bits / 32], low bits first (4 bits: element 8k + i at bits 4i of word k; 2 bits:
+ * element 16k + i at bits 2i); scales, biases: bf16 [out][in / 64].  All device, 16-byte
+ * aligned.  in % 64 == 0; out * in / 64 < 2^31 (QG_ENOTSUP beyond).  With bits = 4 the outputs
+ * form a qg_int4_weight for every GEMV call.
+ */
+int quantize_affine_q64a(const void *w, int w_type, int out, int in, int bits, uint32_t *packed, uint16_t *scales,
+                         uint16_t *biases, void *stream);
+
 typedef enum {
   QG_OP_QGEMV = 0,
   QG_OP_MULTI = 1,

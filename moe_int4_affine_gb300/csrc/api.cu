@@ -286,6 +286,14 @@ int qgemm_int4_multi(int n, const qg_int4_weight* ws, const uint16_t* X, int T, 
   return qgemm_multi_launch(ws, n, X, T, Ys, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
+int quantize_affine_q64a(const void* w, int wt, int out, int in, int bits, uint32_t* packed, uint16_t* scales,
+                         uint16_t* biases, void* stream) {
+  if (!w || !packed || !scales || !biases || (wt != QG_X_BF16 && wt != QG_X_F32)) return QG_EINVAL;
+  if ((bits != 4 && bits != 2) || out < 1 || in < 64 || in % 64 != 0) return QG_EINVAL;
+  if (!aligned16(w) || !aligned16(packed) || !aligned16(scales) || !aligned16(biases)) return QG_EALIGN;
+  return quant_launch(w, wt, out, in, bits, packed, scales, biases, static_cast<cudaStream_t>(stream));
+}
+
 size_t qg_workspace_bytes(int op, const qg_int4_weight* w, int T_or_k) {
   if (!w) return 0;
   switch (op) {

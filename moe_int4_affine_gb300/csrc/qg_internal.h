@@ -78,6 +78,9 @@ int moe_gate_up_routed_launch(const float* logits, int n_logits, int renorm, con
 // Copy `bytes` (a multiple of 16) from device-mapped host memory to device memory, in the launch
 // chain (gemv_dense.cu).
 int ingest_launch(const void* src_dev_mapped, void* dst, size_t bytes, cudaStream_t stream);
+// Affine group-64 encode (quant.cu): bits 4 or 2, w bf16 or fp32 [out][in].
+int quant_launch(const void* w, int wt, int out, int in, int bits, uint32_t* packed, uint16_t* scales,
+                 uint16_t* biases, cudaStream_t stream);
 int moe_down_launch(const qg_int4_weight* down, const uint32_t* idx, const float* p, int k, const float* h,
                     const uint16_t* residual, float* y, cudaStream_t stream);
 

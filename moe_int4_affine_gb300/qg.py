@@ -50,6 +50,7 @@ lib.dense_layer_int4_host.argtypes = [_W, _W, _W, _P, _I, _P, _P, ctypes.c_size_
 lib.moe_gather_qgemv_int4_noalloc.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P]
 lib.scalar_fma_chain8_residual.argtypes = [_P, _P, _P, _P, _I, _P]
 lib.qgemm_int4.argtypes = [_W, _P, _I, _P, _P, ctypes.c_size_t, _P]
+lib.quantize_affine_q64a.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P]
 lib.qgemm_int4_multi.argtypes = [_I, _W, _P, _I, ctypes.POINTER(_P), _P, ctypes.c_size_t, _P]
 lib.qg_workspace_bytes.argtypes = [_I, _W, _I]
 lib.qg_workspace_bytes.restype = ctypes.c_size_t
@@ -64,7 +65,7 @@ lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
            "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "dense_layer_int4", "dense_layer_int4_host", "rmsnorm_qgemv_int4",
            "rmsnorm_qgemv_int4_multi", "qgemv_int4_sigmoid_fma", "sigmoid_scalar_fma_residual",
-           "scalar_fma_chain8_residual", "qgemm_int4", "qgemm_int4_multi", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
+           "scalar_fma_chain8_residual", "qgemm_int4", "qgemm_int4_multi", "quantize_affine_q64a", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
 
 
@@ -326,6 +327,19 @@ def scalar_fma_chain8_residual(p, v, residual, out=None, stream=None):
     _check(lib.scalar_fma_chain8_residual(_ptr(p), _ptr(v), _ptr(residual), _ptr(out), n, _stream(stream)),
            "scalar_fma_chain8_residual")
     return out
+
+
+def quantize_affine_q64a(w, bits: int = 4, stream=None):
+    """Encode w (bf16 or fp32 [out][in]) in the affine group-64 format: (packed int32
+    [out][in*bits/32], scales bf16 [out][in/64], biases bf16 [out][in/64])."""
+    torch = _torch()
+    out, in_dim = w.shape
+    packed = torch.empty((out, in_dim * bits // 32), dtype=torch.int32, device=w.device)
+    scales = torch.empty((out, in_dim // 64), dtype=torch.bfloat16, device=w.device)
+    biases = torch.empty((out, in_dim // 64), dtype=torch.bfloat16, device=w.device)
+    _check(lib.quantize_affine_q64a(_ptr(w), _xtype(w), out, in_dim, bits, _ptr(packed), _ptr(scales), _ptr(biases),
+                                    _stream(stream)), "quantize_affine_q64a")
+    return packed, scales, biases
 
 
 def qgemm_int4_multi(ws, X, Ys=None, workspace=None, stream=None):

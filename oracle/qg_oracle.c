@@ -316,7 +316,7 @@ void orc_sigmoid_scalar_fma(double gate, const float *value, const float *base, 
  * Affine group-64 quantizer (encode) for the Q4_64A / Q2_64A formats ([ds4#844]: "Q4_64A and
  * Q2_64A codes are derived from the serialized BF16 scale/bias"; the page gives no formula for
  * the scale and bias themselves -- the plain reading is min/max affine):
- *   lo = min of the group, hi = max;  scale = (hi - lo) / (2^bits - 1);  bias = lo
+ *   lo = min of the group (-0 taken as +0), hi = max;  scale = (hi - lo) / (2^bits - 1);  bias = lo
  *   s = bf16(scale), b = bf16(bias)            (round to nearest, ties to even)
  *   q_j = clamp(round_to_nearest_even((w_j - b) / s), 0, 2^bits - 1);   q_j = 0 when s == 0
  * The codes are an integer decided by floating point, so they are computed here in the precision
@@ -357,6 +357,8 @@ int orc_quantize_rows(const void *w, int wtype, int64_t out, int64_t in, int bit
         if (j == 0 || v < lo) lo = v;
         if (j == 0 || v > hi) hi = v;
       }
+      volatile float lz = lo + 0.0f; /* -0 taken as +0 */
+      lo = lz;
       volatile float range = hi - lo;                 /* binary32 operations, one rounding each */
       volatile float scale = range / (float)qmax;
       uint16_t sb = f32_to_bf16_rne(scale), bb = f32_to_bf16_rne(lo);
