@@ -72,6 +72,10 @@ def _L():
             lib.orc_moe.restype = I
             lib.orc_qgemm_rows.argtypes = [P, P, P, I64, I64, I64, P, I64, I64, I64, P, P]
             lib.orc_qgemm_rows.restype = I
+            lib.orc_code2.argtypes = [P, I64, I64, I64]
+            lib.orc_code2.restype = ctypes.c_uint
+            lib.orc_qgemv2_rows.argtypes = [P, P, P, I64, I64, P, I, I64, I64, P, P]
+            lib.orc_qgemv2_rows.restype = I
             lib.orc_bf16_round.argtypes = [ctypes.c_float]
             lib.orc_bf16_round.restype = ctypes.c_uint16
             lib.orc_quantize_rows.argtypes = [P, I, I64, I64, I, I64, I64, P, P, P]
@@ -232,6 +236,29 @@ def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
 def rmsnorm_qgemv(packed, scales, biases, x, gamma, eps: float, group_size: int = 64):
     """y, absref of W rmsnorm(x): the norm in float64, then the GEMV of the normalised vector."""
     return qgemv_f64x(packed, scales, biases, rmsnorm(x, gamma, eps), group_size)
+
+
+def code2(packed, in_dim: int, row: int, j: int) -> int:
+    """2-bit code of element j of row `row` (16 per u32, low first)."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint32)
+    return int(_L().orc_code2(_p(packed), in_dim, row, j))
+
+
+def qgemv2(packed, scales, biases, x, rows=None):
+    """y, absref of the 2-bit affine GEMV (packed uint32 [out][in/16])."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint32)
+    x = np.ascontiguousarray(x)
+    in_dim = x.shape[-1]
+    out = packed.size // (in_dim // 16)
+    r0, r1 = (0, out) if rows is None else (int(rows[0]), int(rows[1]))
+    y = np.empty(r1 - r0, dtype=np.float64)
+    a = np.empty(r1 - r0, dtype=np.float64)
+    rc = _L().orc_qgemv2_rows(_p(packed), _p(np.ascontiguousarray(scales, dtype=np.uint16)),
+                              _p(np.ascontiguousarray(biases, dtype=np.uint16)), out, in_dim, _p(x), _xtype(x), r0,
+                              r1, _p(y), _p(a))
+    if rc != 0:
+        raise ValueError("orc_qgemv2_rows rejected the shape")
+    return y, a
 
 
 def bf16_round(f: float) -> int:

@@ -385,3 +385,33 @@ int orc_quantize_rows(const void *w, int wtype, int64_t out, int64_t in, int bit
   }
   return ORC_OK;
 }
+
+/* ---------------------------------------------------------------------------------------
+ * 2-bit affine variant (Q2_64A, [ds4#844]): 16 codes per u32, element 16w + i at bits 2i of word
+ * w (low first), codes 0..3; w = s * q + b per group of 64 with bf16 s, b; y = W x in double, as
+ * orc_qgemv_rows.  packed [out][in / 16].
+ * ------------------------------------------------------------------------------------- */
+unsigned orc_code2(const uint32_t *packed, int64_t in, int64_t row, int64_t j) {
+  uint32_t word = packed[row * (in / 16) + j / 16];
+  return (unsigned)((word >> (2 * (j % 16))) & 0x3u);
+}
+
+int orc_qgemv2_rows(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases, int64_t out, int64_t in,
+                    const void *x, int xtype, int64_t r0, int64_t r1, double *y, double *absref) {
+  if (in <= 0 || in % 64 != 0 || r0 < 0 || r1 > out || r0 > r1) return ORC_EINVAL;
+  if (xtype != ORC_X_BF16 && xtype != ORC_X_F32) return ORC_EINVAL;
+  const int64_t ng = in / 64;
+  for (int64_t r = r0; r < r1; ++r) {
+    double acc = 0.0, aacc = 0.0;
+    for (int64_t j = 0; j < in; ++j) {
+      double s = orc_bf16_to_f64(scales[r * ng + j / 64]);
+      double b = orc_bf16_to_f64(biases[r * ng + j / 64]);
+      double t = (s * (double)orc_code2(packed, in, r, j) + b) * load_x(x, xtype, j);
+      acc += t;
+      aacc += fabs(t);
+    }
+    y[r - r0] = acc;
+    if (absref) absref[r - r0] = aacc;
+  }
+  return ORC_OK;
+}

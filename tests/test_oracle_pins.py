@@ -576,3 +576,65 @@ def test_quantize_bf16_and_f32_inputs_agree():
     b = oracle.quantize(np.array([[oracle.bf16_to_f64(int(v)) for v in row] for row in x], np.float32))
     for u, v in zip(a, b):
         np.testing.assert_array_equal(u, v)
+
+
+# ---------------------------------------------------------------- 2-bit GEMV (Q2_64A), next row N4
+def test_code2_known_words():
+    w = np.array([[0xE4E4E4E4, 0x00000003]], np.uint32)  # 0xE4 = codes 0,1,2,3 (low first)
+    assert [oracle.code2(w, 32, 0, j) for j in range(16)] == [0, 1, 2, 3] * 4
+    assert [oracle.code2(w, 32, 0, j) for j in range(16, 32)] == [3] + [0] * 15
+
+
+def _q2_weight(seed, out, in_dim):
+    rng = np.random.default_rng(seed)
+    packed = rng.integers(0, 2 ** 32, (out, in_dim // 16), dtype=np.uint64).astype(np.uint32)
+    s = np.array([oracle.bf16_round(v) for v in rng.uniform(0.005, 0.02, out * in_dim // 64)], np.uint16)
+    b = np.array([oracle.bf16_round(v) for v in rng.normal(-0.02, 0.01, out * in_dim // 64)], np.uint16)
+    return packed, s.reshape(out, -1), b.reshape(out, -1)
+
+
+def test_qgemv2_all_zero_codes_and_one_hot():
+    """Codes all 0: y = sum_g b_g * sum_{j in g} x_j; one-hot x: y = s q + b of that column."""
+    out, n = 9, 192
+    packed, s, b = _q2_weight(1, out, n)
+    x = I.bf16_normal(1, I.TID_X, n)
+    xv = oracle_values(x)
+    y0, _ = oracle.qgemv2(np.zeros_like(packed), s, b, x)
+    want = [sum(oracle.bf16_to_f64(int(b[r, g])) * xv[64 * g:64 * g + 64].sum() for g in range(3)) for r in range(out)]
+    np.testing.assert_allclose(y0, want, rtol=1e-12)
+    for j in (0, 17, 100, 191):
+        e = np.zeros(n, np.float32)
+        e[j] = 1.0
+        y, _ = oracle.qgemv2(packed, s, b, e)
+        col = [oracle.bf16_to_f64(int(s[r, j // 64])) * oracle.code2(packed, n, r, j) + oracle.bf16_to_f64(int(b[r, j // 64]))
+               for r in range(out)]
+        np.testing.assert_array_equal(y, col)
+
+
+def test_qgemv2_bruteforce_exact_rational():
+    out, n = 3, 128
+    packed, s, b = _q2_weight(2, out, n)
+    x = I.bf16_normal(2, I.TID_X, n)
+    y, _ = oracle.qgemv2(packed, s, b, x)
+    for r in range(out):
+        exact = Fraction(0)
+        for j in range(n):
+            word = int(packed[r, j // 16])
+            q = (word >> (2 * (j % 16))) & 3
+            exact += (_bf16_fraction(int(s[r, j // 64])) * q + _bf16_fraction(int(b[r, j // 64]))) * _bf16_fraction(int(x[j]))
+        assert abs(Fraction(y[r]) - exact) <= abs(exact) * Fraction(1, 2 ** 40) + Fraction(1, 2 ** 60)
+
+
+def test_qgemv2_of_the_2bit_encoding():
+    """The encoder's 2-bit output read back by the 2-bit GEMV: with one-hot x every column is its
+    dequantised weight b + q s, within s/2 + bf16 effects of the original weight."""
+    rng = np.random.default_rng(3)
+    w = rng.normal(0, 0.03, (4, 128)).astype(np.float32)
+    packed, s, b = oracle.quantize(w, 2)
+    for j in (0, 63, 64, 127):
+        e = np.zeros(128, np.float32)
+        e[j] = 1.0
+        y, _ = oracle.qgemv2(packed, s, b, e)
+        for r in range(4):
+            sv = oracle.bf16_to_f64(int(s[r, j // 64]))
+            assert abs(y[r] - w[r, j]) <= sv / 2 + abs(w[r, 64 * (j // 64):64 * (j // 64) + 64]).max() * 2.0 ** -7
