@@ -452,6 +452,32 @@ def measure_configs(qg, I, dev, stream):
                                                          l2="two 178 MB inputs alternate")
     del wq
 
+    # next row N4: the 2-bit (Q2_64A) GEMV on the decode layer's shapes
+    def q2w(seed, tid, out, in_dim):
+        d = I.int2_weight(seed, tid, out, in_dim)
+        t = lambda a: qg.to_device(a, dev)
+        return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim)
+
+    def q2bytes(out, in_dim):
+        return out * in_dim // 4 + 4 * out * (in_dim // 64)
+    dq = q2w(0, I.TID_DOWN, HIDDEN, FFN)
+    dqs = copies(dq, 24)
+    xb = qg.to_device(I.bf16_normal(0, I.TID_X, FFN), dev)
+    yq = torch.empty(HIDDEN, dtype=torch.float32, device=dev)
+    us = tl(lambda i: lib.qgemv_q2(byref(dqs[i % 24].struct), P(xb.data_ptr()), qg.QG_X_BF16, P(yq.data_ptr()), s), 100)
+    res["n4_q2_gemv_5120x17408"] = dict(gb(q2bytes(HIDDEN, FFN) + FFN * 2 + HIDDEN * 4, us), call="qgemv_q2",
+                                        l2="weights rotate over 24 copies (0.6 GB)")
+    gq, uq = q2w(0, I.TID_GATE, FFN, HIDDEN), q2w(0, I.TID_UP, FFN, HIDDEN)
+    gqs, uqs = copies(gq, 12), copies(uq, 12)
+    x = qg.to_device(I.bf16_normal(0, I.TID_X, HIDDEN), dev)
+    hq = torch.empty(FFN, dtype=torch.float32, device=dev)
+    qargs = [((qg.qg_int4_weight * 2)(a_.struct, b_.struct), (P * 2)(hq.data_ptr(), None)) for a_, b_ in zip(gqs, uqs)]
+    us = tl(lambda i: lib.qgemv_q2_multi(2, qargs[i % 12][0], P(x.data_ptr()), qg.QG_X_BF16, qargs[i % 12][1],
+                                         qg.QG_EPI_SWIGLU, s), 100)
+    res["n4_q2_gateup_swiglu_17408x5120"] = dict(gb(2 * q2bytes(FFN, HIDDEN) + HIDDEN * 2 + FFN * 4, us),
+                                                call="qgemv_q2_multi (SwiGLU)", l2="weights rotate over 12 copies")
+    del dq, dqs, gq, uq, gqs, uqs
+
     # config 4: dequant-GEMM, W 17408 x 5120, X T x 5120
     w = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_W, FFN, HIDDEN), dev)
     ws_ = copies(w, 12)

@@ -98,6 +98,17 @@ int qgemv_int4_multi(int n, const qg_int4_weight *ws, const void *x, int xt, flo
                      void *stream);
 
 /*
+ * qgemv_q2, qgemv_q2_multi -- the 2-bit affine variant (Q2_64A, [ds4#844]) of qgemv_int4 and
+ * qgemv_int4_multi: w[r][j] = s * q + b with 2-bit codes q in 0..3, sixteen per u32 (element
+ * 16k + i at bits 2i of word k: `packed` is [out][in / 16]); scales and biases bf16 [out][in / 64]
+ * as for 4 bits (the qg_int4_weight struct carries them unchanged).  quantize_affine_q64a with
+ * bits = 2 writes this layout.  Arguments, epilogues and limits otherwise as the 4-bit calls.
+ */
+int qgemv_q2(const qg_int4_weight *w, const void *x, int x_type, float *y, void *stream);
+int qgemv_q2_multi(int n, const qg_int4_weight *ws, const void *x, int x_type, float *const *ys, int epi,
+                   void *stream);
+
+/*
  * rmsnorm_qgemv_int4 -- RMSNorm fused into the GEMV prologue ([FFAI#14] commit wrapping
  * "ffai_rms_norm_qgemv_fast": the normalised activation goes straight into the int4 dequant-GEMV,
  * no round trip of the normalised vector through memory):

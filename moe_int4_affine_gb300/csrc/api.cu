@@ -38,6 +38,27 @@ int check_weight(const qg_int4_weight* w, bool stacked_ok) {
   if (!aligned16(w->packed) || !aligned16(w->scales) || !aligned16(w->biases)) return QG_EALIGN;
   return QG_OK;
 }
+// Validation and dispatch shared by the multi-projection calls (ex: prologue / epilogue / bits).
+int multi_call(int n, const qg_int4_weight* ws, const void* x, int xt, float* const* ys, int epi,
+               const GemvExtras& ex, cudaStream_t s) {
+  if (n < 2 || n > 4 || !ws || !ys || !x) return QG_EINVAL;
+  if (xt != QG_X_BF16 && xt != QG_X_F32) return QG_EINVAL;
+  if (epi != QG_EPI_NONE && epi != QG_EPI_SWIGLU) return QG_EINVAL;
+  if (epi == QG_EPI_SWIGLU && (n != 2 || ws[0].out != ws[1].out)) return QG_EINVAL;
+  GemvMatArg m[4];
+  for (int i = 0; i < n; ++i) {
+    int rc = check_weight(&ws[i], false);
+    if (rc) return rc;
+    if (ws[i].in != ws[0].in) return QG_EINVAL;  // all packed widths must match
+    const bool need_y = !(epi == QG_EPI_SWIGLU && i == 1);
+    if (need_y && !ys[i]) return QG_EINVAL;
+    if (need_y && !aligned16(ys[i])) return QG_EALIGN;
+    m[i] = GemvMatArg{ws[i].packed, ws[i].scales, ws[i].biases, need_y ? ys[i] : nullptr, ws[i].out};
+  }
+  if (!aligned16(x)) return QG_EALIGN;
+  if (epi == QG_EPI_SWIGLU) return gemv_pair_launch(m[0], m[1], x, xt, ws[0].in, ys[0], s, ex);
+  return gemv_dense_launch(m, n, x, xt, ws[0].in, s, ex);
+}
 }  // namespace
 
 const DeviceInfo& device_info() {
@@ -72,24 +93,24 @@ int qgemv_int4(const qg_int4_weight* w, const void* x, int xt, float* y, void* s
 }
 
 int qgemv_int4_multi(int n, const qg_int4_weight* ws, const void* x, int xt, float* const* ys, int epi, void* stream) {
-  if (n < 2 || n > 4 || !ws || !ys || !x) return QG_EINVAL;
-  if (xt != QG_X_BF16 && xt != QG_X_F32) return QG_EINVAL;
-  if (epi != QG_EPI_NONE && epi != QG_EPI_SWIGLU) return QG_EINVAL;
-  if (epi == QG_EPI_SWIGLU && (n != 2 || ws[0].out != ws[1].out)) return QG_EINVAL;
-  GemvMatArg m[4];
-  for (int i = 0; i < n; ++i) {
-    int rc = check_weight(&ws[i], false);
-    if (rc) return rc;
-    if (ws[i].in != ws[0].in) return QG_EINVAL;  // all packed widths must match
-    const bool need_y = !(epi == QG_EPI_SWIGLU && i == 1);
-    if (need_y && !ys[i]) return QG_EINVAL;
-    if (need_y && !aligned16(ys[i])) return QG_EALIGN;
-    m[i] = GemvMatArg{ws[i].packed, ws[i].scales, ws[i].biases, need_y ? ys[i] : nullptr, ws[i].out};
-  }
-  if (!aligned16(x)) return QG_EALIGN;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (epi == QG_EPI_SWIGLU) return gemv_pair_launch(m[0], m[1], x, xt, ws[0].in, ys[0], s);
-  return gemv_dense_launch(m, n, x, xt, ws[0].in, s);
+  return multi_call(n, ws, x, xt, ys, epi, GemvExtras{}, static_cast<cudaStream_t>(stream));
+}
+
+int qgemv_q2(const qg_int4_weight* w, const void* x, int xt, float* y, void* stream) {
+  int rc = check_weight(w, false);
+  if (rc) return rc;
+  if (!x || !y || (xt != QG_X_BF16 && xt != QG_X_F32)) return QG_EINVAL;
+  if (!aligned16(x) || !aligned16(y)) return QG_EALIGN;
+  GemvMatArg m{w->packed, w->scales, w->biases, y, w->out};
+  GemvExtras ex{};
+  ex.bits = 2;
+  return gemv_dense_launch(&m, 1, x, xt, w->in, static_cast<cudaStream_t>(stream), ex);
+}
+
+int qgemv_q2_multi(int n, const qg_int4_weight* ws, const void* x, int xt, float* const* ys, int epi, void* stream) {
+  GemvExtras ex{};
+  ex.bits = 2;
+  return multi_call(n, ws, x, xt, ys, epi, ex, static_cast<cudaStream_t>(stream));
 }
 
 int rmsnorm_qgemv_int4(const qg_int4_weight* w, const void* x, int xt, const uint16_t* gamma, float eps, float* y,
@@ -107,27 +128,12 @@ int rmsnorm_qgemv_int4(const qg_int4_weight* w, const void* x, int xt, const uin
 
 int rmsnorm_qgemv_int4_multi(int n, const qg_int4_weight* ws, const void* x, int xt, const uint16_t* gamma, float eps,
                              float* const* ys, int epi, void* stream) {
-  if (n < 2 || n > 4 || !ws || !ys || !x || !gamma || !(eps >= 0.f)) return QG_EINVAL;
-  if (xt != QG_X_BF16 && xt != QG_X_F32) return QG_EINVAL;
-  if (epi != QG_EPI_NONE && epi != QG_EPI_SWIGLU) return QG_EINVAL;
-  if (epi == QG_EPI_SWIGLU && (n != 2 || ws[0].out != ws[1].out)) return QG_EINVAL;
-  GemvMatArg m[4];
-  for (int i = 0; i < n; ++i) {
-    int rc = check_weight(&ws[i], false);
-    if (rc) return rc;
-    if (ws[i].in != ws[0].in) return QG_EINVAL;
-    const bool need_y = !(epi == QG_EPI_SWIGLU && i == 1);
-    if (need_y && !ys[i]) return QG_EINVAL;
-    if (need_y && !aligned16(ys[i])) return QG_EALIGN;
-    m[i] = GemvMatArg{ws[i].packed, ws[i].scales, ws[i].biases, need_y ? ys[i] : nullptr, ws[i].out};
-  }
-  if (!aligned16(x) || !aligned16(gamma)) return QG_EALIGN;
+  if (!gamma || !(eps >= 0.f)) return QG_EINVAL;
+  if (!aligned16(gamma)) return QG_EALIGN;
   GemvExtras ex{};
   ex.gamma = gamma;
   ex.eps = eps;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (epi == QG_EPI_SWIGLU) return gemv_pair_launch(m[0], m[1], x, xt, ws[0].in, ys[0], s, ex);
-  return gemv_dense_launch(m, n, x, xt, ws[0].in, s, ex);
+  return multi_call(n, ws, x, xt, ys, epi, ex, static_cast<cudaStream_t>(stream));
 }
 
 int qgemv_int4_sigmoid_fma(const qg_int4_weight* w, const void* x, int xt, const float* gate, const float* base,

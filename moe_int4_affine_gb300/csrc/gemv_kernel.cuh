@@ -98,6 +98,7 @@ struct GemvArgs {
   // Gated epilogue (dense): y = ebase + sigmoid(*sgate) * (W x), then + resid when set.
   const float* sgate;
   const float* ebase;
+  int bits;  // code width: 4 (Q4_64A, 8 codes per u32) or 2 (Q2_64A, 16 per u32)
 };
 
 struct WPtr {
@@ -271,7 +272,8 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
 // conflicts; then (2^-k_g, sum of the group's x) per group; then the partial sums [row][NC][chunk];
 // then (STG) the staged copy of x.
 // STG: x arrives through one bulk copy (a.stage set by the planner), else the threads load it.
-template <int MODE, int RN, bool STG, bool NORM>
+// BITS: 4 or 2 (the 2-bit variant is built for the dense and pair modes without NORM).
+template <int MODE, int RN, bool STG, bool NORM, int BITS = 4>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ uint32_t s_idx[kMaxMats];  // the in-kernel router's selection
@@ -325,9 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       const size_t row = (size_t)(rf + min(r, nr - 1));
       // Every load is in bounds (clamped row and group, the base slab for a bad expert); entries
       // past the block, past the last group or of a bad expert get scale and bias 0, so add 0.
-      const uint4* src = reinterpret_cast<const uint4*>(w.packed + row * (size_t)(a.in / 8)) + lg * 2;
-      L.a[e] = __ldg(src);
-      L.b[e] = __ldg(src + 1);
+      if constexpr (BITS == 4) {
+        const uint4* src = reinterpret_cast<const uint4*>(w.packed + row * (size_t)(a.in / 8)) + lg * 2;
+        L.a[e] = __ldg(src);
+        L.b[e] = __ldg(src + 1);
+      } else {  // a group's 64 2-bit codes: one 16-byte word
+        L.a[e] = __ldg(reinterpret_cast<const uint4*>(w.packed + row * (size_t)(a.in / 16)) + lg);
+      }
       const bool live = ok && gv && r < nr;
       L.s[e] = live ? (uint32_t)__ldg(w.scales + row * (size_t)ngs + lg) : 0u;
       L.t[e] = live ? (uint32_t)__ldg(w.biases + row * (size_t)ngs + lg) : 0u;
@@ -420,10 +426,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
         for (int j = 0; j < 8; ++j) b[j] = __float_as_uint(fmaf(v[j], scale, 12582912.0f));
         uint4 pk;
-        pk.x = __byte_perm(b[0], b[2], 0x5410);
-        pk.y = __byte_perm(b[4], b[6], 0x5410);
-        pk.z = __byte_perm(b[1], b[3], 0x5410);
-        pk.w = __byte_perm(b[5], b[7], 0x5410);
+        if constexpr (BITS == 4) {
+          pk.x = __byte_perm(b[0], b[2], 0x5410);
+          pk.y = __byte_perm(b[4], b[6], 0x5410);
+          pk.z = __byte_perm(b[1], b[3], 0x5410);
+          pk.w = __byte_perm(b[5], b[7], 0x5410);
+        } else {  // 2-bit pairs: (X0, X4), (X1, X5), (X2, X6), (X3, X7) (see the main loop)
+          pk.x = __byte_perm(b[0], b[4], 0x5410);
+          pk.y = __byte_perm(b[1], b[5], 0x5410);
+          pk.z = __byte_perm(b[2], b[6], 0x5410);
+          pk.w = __byte_perm(b[3], b[7], 0x5410);
+        }
         reinterpret_cast<uint4*>(xq + (size_t)g * 32)[(sub + g) & 7] = pk;
         if (sub == 0) {
           float wgt = 1.f;
@@ -433,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             wgt = ok ? __ldg(a.p + g / ngs) : 0.f;
           }
           // (2^-k / 16: the odd codes are accumulated sixteen times over, see the main loop)
-          gsx[g] = make_float2(live ? exp2i(E - 18) * wgt : 0.f, sx * wgt);
+          gsx[g] = make_float2(live ? exp2i(E - (BITS == 4 ? 18 : 20)) * wgt : 0.f, sx * wgt);
         }
       }
     };
@@ -541,22 +554,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     float yp[RN];
 #pragma unroll
     for (int e = 0; e < RN; ++e) {
-      int s0 = 0, s1 = 0;
+      float acc;
+      if constexpr (BITS == 4) {
+        int s0 = 0, s1 = 0;
 #pragma unroll
-      for (int wd = 0; wd < 8; ++wd) {
-        const uint4& c4 = wd < 4 ? L.a[e] : L.b[e];
-        const int k = wd & 3;
-        const uint32_t w = k == 0 ? c4.x : k == 1 ? c4.y : k == 2 ? c4.z : c4.w;
-        const uint32_t c0 = w & 0x0F0F0F0Fu;  // codes q0, q2, q4, q6 as bytes
-        const uint32_t c1 = w & 0xF0F0F0F0u;  // 16 q1, 16 q3, 16 q5, 16 q7
-        s0 = dp2a_lo(X[wd].x, c0, s0);
-        s0 = dp2a_hi(X[wd].y, c0, s0);
-        s1 = dp2a_lo(X[wd].z, c1, s1);
-        s1 = dp2a_hi(X[wd].w, c1, s1);
+        for (int wd = 0; wd < 8; ++wd) {
+          const uint4& c4 = wd < 4 ? L.a[e] : L.b[e];
+          const int k = wd & 3;
+          const uint32_t w = k == 0 ? c4.x : k == 1 ? c4.y : k == 2 ? c4.z : c4.w;
+          const uint32_t c0 = w & 0x0F0F0F0Fu;  // codes q0, q2, q4, q6 as bytes
+          const uint32_t c1 = w & 0xF0F0F0F0u;  // 16 q1, 16 q3, 16 q5, 16 q7
+          s0 = dp2a_lo(X[wd].x, c0, s0);
+          s0 = dp2a_hi(X[wd].y, c0, s0);
+          s1 = dp2a_lo(X[wd].z, c1, s1);
+          s1 = dp2a_hi(X[wd].w, c1, s1);
+        }
+        // |s0| <= 32 * 15 * 32767 and |s1| <= 16 times that: 16 s0 + s1 < 2^29, exact in int32
+        // (rounded once to float, relative error 2^-24); gs.x carries the matching 1/16
+        acc = (float)(s0 * 16 + s1);
+      } else {
+        // 2-bit: word k holds columns 16k .. 16k + 15 at bits 2i; masks 3 << 2m pick codes
+        // m, m + 4, m + 8, m + 12 as bytes (times 4^m), paired with (X_m, X_m+4) of x's word 2k
+        // and (X_m+8, X_m+12) of word 2k + 1
+        int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t w = k == 0 ? L.a[e].x : k == 1 ? L.a[e].y : k == 2 ? L.a[e].z : L.a[e].w;
+          const uint4& A = X[2 * k];
+          const uint4& B = X[2 * k + 1];
+          const uint32_t c0 = w & 0x03030303u, c1 = w & 0x0C0C0C0Cu, c2 = w & 0x30303030u, c3 = w & 0xC0C0C0C0u;
+          s0 = dp2a_hi(B.x, c0, dp2a_lo(A.x, c0, s0));
+          s1 = dp2a_hi(B.y, c1, dp2a_lo(A.y, c1, s1));
+          s2 = dp2a_hi(B.z, c2, dp2a_lo(A.z, c2, s2));
+          s3 = dp2a_hi(B.w, c3, dp2a_lo(A.w, c3, s3));
+        }
+        // |s_m| <= 4^m * 16 * 3 * 32767: 64 s0 + 16 s1 + 4 s2 + s3 < 2^29, exact; gs.x carries 1/64
+        acc = (float)(s0 * 64 + s1 * 16 + s2 * 4 + s3);
       }
-      // |s0| <= 32 * 15 * 32767 and |s1| <= 16 times that: 16 s0 + s1 < 2^29, exact in int32
-      // (rounded once to float, relative error 2^-24); gs.x carries the matching 1/16
-      const float acc = (float)(s0 * 16 + s1);
       yp[e] = fmaf(bf16_bits_to_f32(L.s[e]), acc * gs.x, bf16_bits_to_f32(L.t[e]) * gs.y);
     }
     const float tot = warp_sum_rows<RN>(yp, lane);
@@ -698,6 +732,7 @@ inline GemvArgs moe_down_args(const qg_int4_weight* down, const uint32_t* idx, c
 }
 
 inline void apply_extras(GemvArgs& a, const GemvExtras& ex) {
+  a.bits = ex.bits ? ex.bits : 4;
   a.gamma = ex.gamma;
   a.eps = ex.eps;
   a.sgate = ex.sgate;
@@ -730,9 +765,9 @@ inline size_t plan_stage(GemvArgs& a, size_t base, size_t limit) {
 }
 constexpr size_t kStaticSmemReserve = 1024;  // the kernels' static shared variables
 
-template <int MODE, int RN, bool STG, bool NORM>
+template <int MODE, int RN, bool STG, bool NORM, int BITS = 4>
 int launch_gemv_variant(const GemvArgs& a, int grid, size_t smem, cudaStream_t stream) {
-  auto k = gemv_kernel<MODE, RN, STG, NORM>;
+  auto k = gemv_kernel<MODE, RN, STG, NORM, BITS>;
   static std::atomic<int> smem_set{0};
   if ((int)smem > smem_set.load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -762,6 +797,11 @@ int plan_and_launch(GemvArgs& a, cudaStream_t stream) {
   if (smem > limit) return QG_ENOTSUP;
   // rows x components per work unit: 4 (dense and seg: four rows; pair: two rows, gate and up)
   if constexpr (MODE != kSeg) {
+    if (a.bits == 2) {
+      if (a.gamma) return QG_ENOTSUP;
+      return a.stage ? launch_gemv_variant<MODE, 4, true, false, 2>(a, grid, smem, stream)
+                     : launch_gemv_variant<MODE, 4, false, false, 2>(a, grid, smem, stream);
+    }
     if (a.gamma)
       return a.stage ? launch_gemv_variant<MODE, 4, true, true>(a, grid, smem, stream)
                      : launch_gemv_variant<MODE, 4, false, true>(a, grid, smem, stream);

@@ -59,6 +59,7 @@ struct GemvExtras {
   const float* sgate;
   const float* ebase;
   const uint16_t* resid;
+  int bits;  // 0 or 4: Q4_64A codes; 2: Q2_64A
 };
 // n in 1..4 matrices sharing x (rows of each written to its y).
 int gemv_dense_launch(const GemvMatArg* mats, int n, const void* x, int xt, int in, cudaStream_t stream,

@@ -41,6 +41,8 @@ lib.qgemv_int4_multi.argtypes = [_I, _W, _P, _I, ctypes.POINTER(_P), _I, _P]
 lib.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
 lib.moe_gather_qgemv_int4.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]
 lib.moe_layer_int4.argtypes = [_P, _I, _W, _W, _W, _I, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+lib.qgemv_q2.argtypes = [_W, _P, _I, _P, _P]
+lib.qgemv_q2_multi.argtypes = [_I, _W, _P, _I, ctypes.POINTER(_P), _I, _P]
 lib.rmsnorm_qgemv_int4.argtypes = [_W, _P, _I, _P, ctypes.c_float, _P, _P]
 lib.rmsnorm_qgemv_int4_multi.argtypes = [_I, _W, _P, _I, _P, ctypes.c_float, ctypes.POINTER(_P), _I, _P]
 lib.qgemv_int4_sigmoid_fma.argtypes = [_W, _P, _I, _P, _P, _P, _P, _P]
@@ -63,7 +65,7 @@ lib.qg_strerror.argtypes = [_I]
 lib.qg_strerror.restype = ctypes.c_char_p
 lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
-           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "dense_layer_int4", "dense_layer_int4_host", "rmsnorm_qgemv_int4",
+           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "dense_layer_int4", "dense_layer_int4_host", "rmsnorm_qgemv_int4", "qgemv_q2", "qgemv_q2_multi",
            "rmsnorm_qgemv_int4_multi", "qgemv_int4_sigmoid_fma", "sigmoid_scalar_fma_residual",
            "scalar_fma_chain8_residual", "qgemm_int4", "qgemm_int4_multi", "quantize_affine_q64a", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
@@ -176,6 +178,29 @@ def qgemv_int4_multi(ws, x, ys=None, epilogue: str = "none", stream=None):
     arr = (qg_int4_weight * n)(*[w.struct for w in ws])
     yp = (_P * n)(*[_ptr(y) for y in ys])
     _check(lib.qgemv_int4_multi(n, arr, _ptr(x), _xtype(x), yp, epi, _stream(stream)), "qgemv_int4_multi")
+    return ys[0] if epi == QG_EPI_SWIGLU else ys
+
+
+def qgemv_q2(w: Int4Weight, x, y=None, stream=None):
+    """2-bit affine GEMV (w.packed [out][in/16])."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(w.out, dtype=torch.float32, device=x.device)
+    _check(lib.qgemv_q2(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(y), _stream(stream)), "qgemv_q2")
+    return y
+
+
+def qgemv_q2_multi(ws, x, ys=None, epilogue: str = "none", stream=None):
+    torch = _torch()
+    n = len(ws)
+    epi = {"none": QG_EPI_NONE, "swiglu": QG_EPI_SWIGLU}[epilogue]
+    if ys is None:
+        ys = [torch.empty(w.out, dtype=torch.float32, device=x.device) for w in ws]
+        if epi == QG_EPI_SWIGLU:
+            ys[1] = None
+    arr = (qg_int4_weight * n)(*[w.struct for w in ws])
+    yp = (_P * n)(*[_ptr(y) for y in ys])
+    _check(lib.qgemv_q2_multi(n, arr, _ptr(x), _xtype(x), yp, epi, _stream(stream)), "qgemv_q2_multi")
     return ys[0] if epi == QG_EPI_SWIGLU else ys
 
 
