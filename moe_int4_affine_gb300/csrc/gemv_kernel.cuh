@@ -368,9 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     mbar_arrive_expect_tx(&xbar, xbytes + gbytes);
     for (uint32_t off = 0; off < xbytes; off += kChunk)
       bulk_g2s_bytes(stage + off, static_cast<const uint8_t*>(a.x) + off, min(kChunk, xbytes - off), &xbar);
-    for (uint32_t off = 0; off < gbytes; off += kChunk)
-      bulk_g2s_bytes(stage + xbytes + off, reinterpret_cast<const uint8_t*>(a.gamma) + off, min(kChunk, gbytes - off),
-                     &xbar);
+    if constexpr (NORM) {
+      for (uint32_t off = 0; off < gbytes; off += kChunk)
+        bulk_g2s_bytes(stage + xbytes + off, reinterpret_cast<const uint8_t*>(a.gamma) + off, min(kChunk, gbytes - off),
+                       &xbar);
+    }
   }
   if (a.logits) {  // the router, in every CTA
     if (warp == 0) route_topk_warp(a.logits, a.n_logits, a.nmat, a.renorm, s_idx, s_p, blockIdx.x == 0 ? a.idx_out : nullptr,
