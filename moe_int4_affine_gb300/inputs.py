@@ -77,16 +77,18 @@ def int4_weight(seed: int, tensor_id: int, out: int, in_dim: int, n_mat: int | N
     return d
 
 
-def int2_weight(seed: int, tensor_id: int, out: int, in_dim: int) -> dict:
+def int2_weight(seed: int, tensor_id: int, out: int, in_dim: int, n_mat: int | None = None) -> dict:
     """A random 2-bit affine group-64 weight [out][in] (the Q2_64A layout): codes uniform 0..3
     packed sixteen per u32 (low first), scales U[0.005, 0.02], biases -1.5 s + N(0, 1e-3) (the
-    4-bit recipe with the code midpoint 1.5), bf16.  dict(packed=u32 [out, in/16], scales, biases)."""
+    4-bit recipe with the code midpoint 1.5), bf16.  dict(packed=u32 [.., out, in/16], scales,
+    biases); stacked [n_mat][out][in] when n_mat is given."""
     assert in_dim % GROUP == 0
+    lead = () if n_mat is None else (n_mat,)
     g = rng(seed, tensor_id)
-    codes = g.integers(0, 4, size=(out, in_dim), dtype=np.uint32)
-    shifts = (2 * np.arange(16, dtype=np.uint32))[None, None, :]
-    packed = (codes.reshape(out, in_dim // 16, 16) << shifts).sum(axis=2, dtype=np.uint64).astype(np.uint32)
-    s64 = g.uniform(0.005, 0.02, size=(out, in_dim // GROUP))
+    codes = g.integers(0, 4, size=lead + (out, in_dim), dtype=np.uint32)
+    shifts = (2 * np.arange(16, dtype=np.uint32))
+    packed = (codes.reshape(lead + (out, in_dim // 16, 16)) << shifts).sum(axis=-1, dtype=np.uint64).astype(np.uint32)
+    s64 = g.uniform(0.005, 0.02, size=lead + (out, in_dim // GROUP))
     scales = f64_to_bf16_bits(s64)
     s_b = bf16_bits_to_f32(scales).astype(np.float64)
     biases = f64_to_bf16_bits(-1.5 * s_b + g.normal(0.0, 1e-3, size=s_b.shape))

@@ -76,6 +76,10 @@ def _L():
             lib.orc_code2.restype = ctypes.c_uint
             lib.orc_qgemv2_rows.argtypes = [P, P, P, I64, I64, P, I, I64, I64, P, P]
             lib.orc_qgemv2_rows.restype = I
+            lib.orc_qgemv2_rows_f64x.argtypes = [P, P, P, I64, I64, P, I64, I64, P, P]
+            lib.orc_qgemv2_rows_f64x.restype = I
+            lib.orc_moe2.argtypes = [P] * 9 + [I64, I64, I64, P, P, I, P, P, P, P]
+            lib.orc_moe2.restype = I
             lib.orc_bf16_round.argtypes = [ctypes.c_float]
             lib.orc_bf16_round.restype = ctypes.c_uint16
             lib.orc_quantize_rows.argtypes = [P, I, I64, I64, I, I64, I64, P, P, P]
@@ -259,6 +263,27 @@ def qgemv2(packed, scales, biases, x, rows=None):
     if rc != 0:
         raise ValueError("orc_qgemv2_rows rejected the shape")
     return y, a
+
+
+def moe2(gate, up, down, idx, p, x, residual):
+    """The MoE decode step with 2-bit experts (gate/up packed [E][inter][hidden/16], down
+    [E][hidden][inter/16]); returns y, absref and the invalid-slot flag bits, as moe()."""
+    gq, gs, gb = (np.ascontiguousarray(a) for a in gate)
+    uq, us, ub = (np.ascontiguousarray(a) for a in up)
+    dq, ds, db = (np.ascontiguousarray(a) for a in down)
+    E, inter, hw = gq.shape
+    hidden = hw * 16
+    idx = np.ascontiguousarray(idx, dtype=np.uint32)
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    residual = np.ascontiguousarray(residual, dtype=np.uint16)
+    y = np.empty(hidden, dtype=np.float64)
+    a = np.empty(hidden, dtype=np.float64)
+    flags = _L().orc_moe2(_p(gq), _p(gs), _p(gb), _p(uq), _p(us), _p(ub), _p(dq), _p(ds), _p(db), E, hidden, inter,
+                          _p(idx), _p(p), idx.size, _p(x), _p(residual), _p(y), _p(a))
+    if flags < 0:
+        raise ValueError("orc_moe2 rejected the shapes")
+    return y, a, flags
 
 
 def bf16_round(f: float) -> int:

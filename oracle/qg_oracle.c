@@ -415,3 +415,68 @@ int orc_qgemv2_rows(const uint32_t *packed, const uint16_t *scales, const uint16
   }
   return ORC_OK;
 }
+
+/* 2-bit GEMV with a double-precision input vector (the 2-bit MoE down projection's h). */
+int orc_qgemv2_rows_f64x(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases, int64_t out,
+                         int64_t in, const double *x, int64_t r0, int64_t r1, double *y, double *absref) {
+  if (in <= 0 || in % 64 != 0 || r0 < 0 || r1 > out || r0 > r1) return ORC_EINVAL;
+  const int64_t ng = in / 64;
+  for (int64_t r = r0; r < r1; ++r) {
+    double acc = 0.0, aacc = 0.0;
+    for (int64_t j = 0; j < in; ++j) {
+      double s = orc_bf16_to_f64(scales[r * ng + j / 64]);
+      double b = orc_bf16_to_f64(biases[r * ng + j / 64]);
+      double t = (s * (double)orc_code2(packed, in, r, j) + b) * x[j];
+      acc += t;
+      aacc += fabs(t);
+    }
+    y[r - r0] = acc;
+    if (absref) absref[r - r0] = aacc;
+  }
+  return ORC_OK;
+}
+
+/* The MoE decode step of orc_moe with 2-bit experts (Q2_64A): stacked gate/up packed
+ * [E][inter][hidden / 16], down [E][hidden][inter / 16]; the same steps in the same order. */
+int orc_moe2(const uint32_t *gq, const uint16_t *gs_, const uint16_t *gb, const uint32_t *uq, const uint16_t *us,
+             const uint16_t *ub, const uint32_t *dq, const uint16_t *ds, const uint16_t *db, int64_t n_experts,
+             int64_t hidden, int64_t inter, const uint32_t *idx, const double *p, int K, const uint16_t *x,
+             const uint16_t *resid, double *y, double *absref) {
+  if (hidden % 64 || inter % 64) return ORC_EINVAL;
+  double *g = (double *)malloc(sizeof(double) * (size_t)inter);
+  double *u = (double *)malloc(sizeof(double) * (size_t)inter);
+  double *h = (double *)malloc(sizeof(double) * (size_t)inter);
+  double *d = (double *)malloc(sizeof(double) * (size_t)hidden);
+  double *da = (double *)malloc(sizeof(double) * (size_t)hidden);
+  if (!g || !u || !h || !d || !da) return ORC_EINVAL;
+  int flags = 0;
+  for (int64_t i = 0; i < hidden; ++i) {
+    y[i] = orc_bf16_to_f64(resid[i]);
+    if (absref) absref[i] = fabs(y[i]);
+  }
+  const int64_t gu_words = inter * (hidden / 16), gu_groups = inter * (hidden / 64);
+  const int64_t d_words = hidden * (inter / 16), d_groups = hidden * (inter / 64);
+  for (int k = 0; k < K; ++k) {
+    int64_t e = (int64_t)idx[k];
+    if (e < 0 || e >= n_experts) {
+      flags |= 1 << k;
+      continue;
+    }
+    orc_qgemv2_rows(gq + e * gu_words, gs_ + e * gu_groups, gb + e * gu_groups, inter, hidden, x, ORC_X_BF16, 0,
+                    inter, g, NULL);
+    orc_qgemv2_rows(uq + e * gu_words, us + e * gu_groups, ub + e * gu_groups, inter, hidden, x, ORC_X_BF16, 0,
+                    inter, u, NULL);
+    orc_swiglu(g, u, inter, h);
+    orc_qgemv2_rows_f64x(dq + e * d_words, ds + e * d_groups, db + e * d_groups, hidden, inter, h, 0, hidden, d, da);
+    for (int64_t i = 0; i < hidden; ++i) {
+      y[i] += p[k] * d[i];
+      if (absref) absref[i] += fabs(p[k]) * da[i];
+    }
+  }
+  free(g);
+  free(u);
+  free(h);
+  free(d);
+  free(da);
+  return flags;
+}

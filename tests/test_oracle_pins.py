@@ -638,3 +638,42 @@ def test_qgemv2_of_the_2bit_encoding():
         for r in range(4):
             sv = oracle.bf16_to_f64(int(s[r, j // 64]))
             assert abs(y[r] - w[r, j]) <= sv / 2 + abs(w[r, 64 * (j // 64):64 * (j // 64) + 64]).max() * 2.0 ** -7
+
+
+def _repack_2bit_as_4bit(packed2, in_dim):
+    """The 2-bit codes of a weight as 4-bit codes (values 0..3), eight per u32, low first."""
+    lead = packed2.shape[:-1]
+    words = packed2.reshape(-1, in_dim // 16).astype(np.uint64)
+    codes = (words[:, :, None] >> (2 * np.arange(16, dtype=np.uint64))) & 3
+    codes = codes.reshape(words.shape[0], in_dim // 8, 8)
+    out = (codes << (4 * np.arange(8, dtype=np.uint64))).sum(axis=2).astype(np.uint32)
+    return out.reshape(lead + (in_dim // 8,))
+
+
+def test_qgemv2_equals_4bit_path_on_repacked_codes():
+    """2-bit codes are valid 4-bit codes: the 2-bit GEMV equals the (pinned) 4-bit GEMV of the same
+    weights repacked eight per word, bit for bit."""
+    d = I.int2_weight(4, I.TID_W, 50, 576)
+    x = I.bf16_normal(4, I.TID_X, 576)
+    y2, a2 = oracle.qgemv2(d["packed"], d["scales"], d["biases"], x)
+    y4, a4 = oracle.qgemv(_repack_2bit_as_4bit(d["packed"], 576), d["scales"], d["biases"], x)
+    np.testing.assert_array_equal(y2, y4)
+    np.testing.assert_array_equal(a2, a4)
+
+
+def test_moe2_equals_4bit_moe_on_repacked_codes():
+    E, hidden, inter = 6, 256, 192
+    g = I.int2_weight(5, I.TID_GATE, inter, hidden, n_mat=E)
+    u = I.int2_weight(5, I.TID_UP, inter, hidden, n_mat=E)
+    d = I.int2_weight(5, I.TID_DOWN, hidden, inter, n_mat=E)
+    idx = np.array([4, 1, 5], np.uint32)
+    p = np.array([0.5, 0.3, 0.2])
+    x = I.bf16_normal(5, I.TID_X, hidden)
+    r = I.bf16_normal(5, I.TID_RESID, hidden)
+    t = lambda w: (w["packed"], w["scales"], w["biases"])
+    y2, a2, f2 = oracle.moe2(t(g), t(u), t(d), idx, p, x, r)
+    rp = lambda w, n: (_repack_2bit_as_4bit(w["packed"], n), w["scales"], w["biases"])
+    y4, a4, f4 = oracle.moe(rp(g, hidden), rp(u, hidden), rp(d, inter), idx, p, x, r)
+    np.testing.assert_array_equal(y2, y4)
+    np.testing.assert_array_equal(a2, a4)
+    assert f2 == f4 == 0
