@@ -477,6 +477,27 @@ def measure_configs(qg, I, dev, stream):
     res["n4_q2_gateup_swiglu_17408x5120"] = dict(gb(2 * q2bytes(FFN, HIDDEN) + HIDDEN * 2 + FFN * 4, us),
                                                 call="qgemv_q2_multi (SwiGLU)", l2="weights rotate over 12 copies")
     del dq, dqs, gq, uq, gqs, uqs
+    # ... and the 2-bit MoE layer on the MoE config's shapes (router inside the gate/up kernel)
+    E2, H2, I2, K2 = 128, 2048, 768, 8
+    def q2stack(tid, out, in_dim):
+        d = I.int2_weight(0, tid, out, in_dim, n_mat=E2)
+        t = lambda a: qg.to_device(a, dev)
+        return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim, n_mat=E2)
+    g2, u2, d2 = q2stack(I.TID_GATE, I2, H2), q2stack(I.TID_UP, I2, H2), q2stack(I.TID_DOWN, H2, I2)
+    lg2 = [qg.to_device(I.f32_normal(i, I.TID_LOGITS, E2), dev) for i in range(16)]
+    x2 = qg.to_device(I.bf16_normal(0, I.TID_X, H2), dev)
+    r2 = qg.to_device(I.bf16_normal(0, I.TID_RESID, H2), dev)
+    i2 = torch.empty(K2, dtype=torch.int32, device=dev)
+    p2 = torch.empty(K2, dtype=torch.float32, device=dev)
+    y2 = torch.empty(H2, dtype=torch.float32, device=dev)
+    w2 = torch.empty(qg.qg_workspace_bytes(qg.QG_OP_MOE, d2, K2), dtype=torch.uint8, device=dev)
+    us = tl(lambda i: lib.moe_layer_q2(P(lg2[i % 16].data_ptr()), 1, byref(g2.struct), byref(u2.struct),
+                                       byref(d2.struct), K2, P(x2.data_ptr()), P(r2.data_ptr()), P(y2.data_ptr()),
+                                       P(i2.data_ptr()), P(p2.data_ptr()), P(w2.data_ptr()), w2.numel(), s), 100)
+    nb2 = K2 * (2 * q2bytes(I2, H2) + q2bytes(H2, I2)) + 2 * H2 * 2 + E2 * 4 + H2 * 4
+    res["n4_q2_moe_layer_T1"] = dict(gb(nb2, us), call="moe_layer_q2", kernels=2,
+                                     l2="128-expert 2-bit pool, router logits rotate over 16 vectors")
+    del g2, u2, d2
 
     # config 4: dequant-GEMM, W 17408 x 5120, X T x 5120
     w = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_W, FFN, HIDDEN), dev)

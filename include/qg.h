@@ -109,6 +109,19 @@ int qgemv_q2_multi(int n, const qg_int4_weight *ws, const void *x, int x_type, f
                    void *stream);
 
 /*
+ * moe_gather_qgemv_q2, moe_layer_q2 -- moe_gather_qgemv_int4 and moe_layer_int4 for 2-bit experts
+ * (Q2_64A layout as qgemv_q2: stacked gate/up packed [n_mat][inter][hidden / 16], down
+ * [n_mat][hidden][inter / 16]; scales and biases as for 4 bits).  Arguments, workspace
+ * (qg_workspace_bytes(QG_OP_MOE, down, k)), results and limits as the 4-bit calls.
+ */
+int moe_gather_qgemv_q2(const qg_int4_weight *gate, const qg_int4_weight *up, const qg_int4_weight *down,
+                        const uint32_t *idx, const float *p, int k, const uint16_t *x, const uint16_t *residual,
+                        float *y, void *workspace, size_t ws_bytes, void *stream);
+int moe_layer_q2(const float *logits, int renorm, const qg_int4_weight *gate, const qg_int4_weight *up,
+                 const qg_int4_weight *down, int k, const uint16_t *x, const uint16_t *residual, float *y,
+                 uint32_t *idx, float *p, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * rmsnorm_qgemv_int4 -- RMSNorm fused into the GEMV prologue ([FFAI#14] commit wrapping
  * "ffai_rms_norm_qgemv_fast": the normalised activation goes straight into the int4 dequant-GEMV,
  * no round trip of the normalised vector through memory):

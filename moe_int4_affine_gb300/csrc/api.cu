@@ -165,9 +165,13 @@ int moe_router_topk(const float* logits, int n_experts, int k, int renorm, uint3
   return router_launch(logits, n_experts, k, renorm, idx, p, static_cast<cudaStream_t>(stream));
 }
 
-int moe_gather_qgemv_int4(const qg_int4_weight* gate, const qg_int4_weight* up, const qg_int4_weight* down,
-                          const uint32_t* idx, const float* p, int k, const uint16_t* x, const uint16_t* residual,
-                          float* y, void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// The MoE calls for both code widths (bits 4: Q4_64A, 2: Q2_64A).
+int moe_gather_call(const qg_int4_weight* gate, const qg_int4_weight* up, const qg_int4_weight* down,
+                    const uint32_t* idx, const float* p, int k, const uint16_t* x, const uint16_t* residual, float* y,
+                    void* workspace, size_t ws_bytes, void* stream, int bits) {
   int rc;
   if ((rc = check_weight(gate, true)) || (rc = check_weight(up, true)) || (rc = check_weight(down, true))) return rc;
   if (!idx || !p || !x || !residual || !y) return QG_EINVAL;
@@ -181,14 +185,14 @@ int moe_gather_qgemv_int4(const qg_int4_weight* gate, const qg_int4_weight* up, 
   if (!aligned16(workspace)) return QG_EALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* h = static_cast<float*>(workspace);
-  rc = moe_gate_up_launch(gate, up, idx, k, x, h, s);
+  rc = moe_gate_up_launch(gate, up, idx, k, x, h, s, bits);
   if (rc) return rc;
-  return moe_down_launch(down, idx, p, k, h, residual, y, s);
+  return moe_down_launch(down, idx, p, k, h, residual, y, s, bits);
 }
 
-int moe_layer_int4(const float* logits, int renorm, const qg_int4_weight* gate, const qg_int4_weight* up,
+int moe_layer_call(const float* logits, int renorm, const qg_int4_weight* gate, const qg_int4_weight* up,
                    const qg_int4_weight* down, int k, const uint16_t* x, const uint16_t* residual, float* y,
-                   uint32_t* idx, float* p, void* workspace, size_t ws_bytes, void* stream) {
+                   uint32_t* idx, float* p, void* workspace, size_t ws_bytes, void* stream, int bits) {
   int rc;
   if ((rc = check_weight(gate, true)) || (rc = check_weight(up, true)) || (rc = check_weight(down, true))) return rc;
   if (!logits || !idx || !p || !x || !residual || !y) return QG_EINVAL;
@@ -205,9 +209,36 @@ int moe_layer_int4(const float* logits, int renorm, const qg_int4_weight* gate, 
   if (!aligned16(workspace)) return QG_EALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* h = static_cast<float*>(workspace);
-  rc = moe_gate_up_routed_launch(logits, gate->n_mat, renorm, gate, up, k, x, h, idx, p, s);
+  rc = moe_gate_up_routed_launch(logits, gate->n_mat, renorm, gate, up, k, x, h, idx, p, s, bits);
   if (rc) return rc;
-  return moe_down_launch(down, idx, p, k, h, residual, y, s);
+  return moe_down_launch(down, idx, p, k, h, residual, y, s, bits);
+}
+}  // namespace
+
+extern "C" {
+
+int moe_gather_qgemv_int4(const qg_int4_weight* gate, const qg_int4_weight* up, const qg_int4_weight* down,
+                          const uint32_t* idx, const float* p, int k, const uint16_t* x, const uint16_t* residual,
+                          float* y, void* workspace, size_t ws_bytes, void* stream) {
+  return moe_gather_call(gate, up, down, idx, p, k, x, residual, y, workspace, ws_bytes, stream, 4);
+}
+
+int moe_gather_qgemv_q2(const qg_int4_weight* gate, const qg_int4_weight* up, const qg_int4_weight* down,
+                        const uint32_t* idx, const float* p, int k, const uint16_t* x, const uint16_t* residual,
+                        float* y, void* workspace, size_t ws_bytes, void* stream) {
+  return moe_gather_call(gate, up, down, idx, p, k, x, residual, y, workspace, ws_bytes, stream, 2);
+}
+
+int moe_layer_int4(const float* logits, int renorm, const qg_int4_weight* gate, const qg_int4_weight* up,
+                   const qg_int4_weight* down, int k, const uint16_t* x, const uint16_t* residual, float* y,
+                   uint32_t* idx, float* p, void* workspace, size_t ws_bytes, void* stream) {
+  return moe_layer_call(logits, renorm, gate, up, down, k, x, residual, y, idx, p, workspace, ws_bytes, stream, 4);
+}
+
+int moe_layer_q2(const float* logits, int renorm, const qg_int4_weight* gate, const qg_int4_weight* up,
+                 const qg_int4_weight* down, int k, const uint16_t* x, const uint16_t* residual, float* y,
+                 uint32_t* idx, float* p, void* workspace, size_t ws_bytes, void* stream) {
+  return moe_layer_call(logits, renorm, gate, up, down, k, x, residual, y, idx, p, workspace, ws_bytes, stream, 2);
 }
 
 int dense_layer_int4(const qg_int4_weight* gate, const qg_int4_weight* up, const qg_int4_weight* down, const void* x,

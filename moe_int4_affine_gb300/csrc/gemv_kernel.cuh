@@ -272,7 +272,7 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
 // conflicts; then (2^-k_g, sum of the group's x) per group; then the partial sums [row][NC][chunk];
 // then (STG) the staged copy of x.
 // STG: x arrives through one bulk copy (a.stage set by the planner), else the threads load it.
-// BITS: 4 or 2 (the 2-bit variant is built for the dense and pair modes without NORM).
+// BITS: 4 or 2 (the 2-bit variant is built without NORM).
 template <int MODE, int RN, bool STG, bool NORM, int BITS = 4>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -686,7 +686,7 @@ inline GemvArgs pair_args(const GemvMatArg& gate, const GemvMatArg& up, const vo
 // The k selected experts' gate/up pairs, h[m] for slot m; experts from idx (set idx or the router
 // fields before launching).
 inline GemvArgs moe_gate_up_args(const qg_int4_weight* gate, const qg_int4_weight* up, const uint32_t* idx, int k,
-                                 const uint16_t* x, float* h) {
+                                 const uint16_t* x, float* h, int bits = 4) {
   GemvArgs a{};
   a.nmat = k;
   for (int m = 0; m < k; ++m) {
@@ -701,16 +701,17 @@ inline GemvArgs moe_gate_up_args(const qg_int4_weight* gate, const qg_int4_weigh
   a.xf32 = 0;
   a.idx = idx;
   a.n_experts = gate->n_mat;
-  a.slab_words = (long long)gate->out * (gate->in / 8);
+  a.slab_words = (long long)gate->out * (gate->in * bits / 32);
   a.slab_groups = (long long)gate->out * (gate->in / 64);
   a.in = gate->in;
   a.total_rows = k * gate->out;
+  a.bits = bits;
   return a;
 }
 
 // MoE down with the slot-weighted accumulate and the residual (one row = k segments).
 inline GemvArgs moe_down_args(const qg_int4_weight* down, const uint32_t* idx, const float* p, int k, const float* h,
-                              const uint16_t* residual, float* y) {
+                              const uint16_t* residual, float* y, int bits = 4) {
   GemvArgs a{};
   a.nmat = 1;
   a.mat[0].w[0] = WRef{down->packed, down->scales, down->biases, -1};
@@ -726,10 +727,11 @@ inline GemvArgs moe_down_args(const qg_int4_weight* down, const uint32_t* idx, c
   a.p = p;
   a.resid = residual;
   a.n_experts = down->n_mat;
-  a.slab_words = (long long)down->out * (down->in / 8);
+  a.slab_words = (long long)down->out * (down->in * bits / 32);
   a.slab_groups = (long long)down->out * (down->in / 64);
   a.in = down->in;
   a.total_rows = down->out;
+  a.bits = bits;
   return a;
 }
 
@@ -798,12 +800,12 @@ int plan_and_launch(GemvArgs& a, cudaStream_t stream) {
   const size_t smem = plan_stage(a, gemv_smem_bytes(a.groups, a.rows_per_cta, NC), limit);
   if (smem > limit) return QG_ENOTSUP;
   // rows x components per work unit: 4 (dense and seg: four rows; pair: two rows, gate and up)
+  if (a.bits == 2) {
+    if (a.gamma) return QG_ENOTSUP;
+    return a.stage ? launch_gemv_variant<MODE, 4, true, false, 2>(a, grid, smem, stream)
+                   : launch_gemv_variant<MODE, 4, false, false, 2>(a, grid, smem, stream);
+  }
   if constexpr (MODE != kSeg) {
-    if (a.bits == 2) {
-      if (a.gamma) return QG_ENOTSUP;
-      return a.stage ? launch_gemv_variant<MODE, 4, true, false, 2>(a, grid, smem, stream)
-                     : launch_gemv_variant<MODE, 4, false, false, 2>(a, grid, smem, stream);
-    }
     if (a.gamma)
       return a.stage ? launch_gemv_variant<MODE, 4, true, true>(a, grid, smem, stream)
                      : launch_gemv_variant<MODE, 4, false, true>(a, grid, smem, stream);

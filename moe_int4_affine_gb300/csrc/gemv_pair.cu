@@ -14,9 +14,9 @@ int gemv_pair_launch(const GemvMatArg& gate, const GemvMatArg& up, const void* x
 }
 
 int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, const uint32_t* idx, int k,
-                       const uint16_t* x, float* h, cudaStream_t stream) {
+                       const uint16_t* x, float* h, cudaStream_t stream, int bits) {
   if (k < 1 || k > kMaxMats) return QG_EINVAL;
-  GemvArgs a = moe_gate_up_args(gate, up, idx, k, x, h);
+  GemvArgs a = moe_gate_up_args(gate, up, idx, k, x, h, bits);
   return plan_and_launch<kPair>(a, stream);
 }
 
@@ -24,9 +24,9 @@ int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, con
 // CTA 0 writes the selection to idx_out / p_out for the down kernel.
 int moe_gate_up_routed_launch(const float* logits, int n_logits, int renorm, const qg_int4_weight* gate,
                               const qg_int4_weight* up, int k, const uint16_t* x, float* h, uint32_t* idx_out,
-                              float* p_out, cudaStream_t stream) {
+                              float* p_out, cudaStream_t stream, int bits) {
   if (k < 1 || k > kMaxMats) return QG_EINVAL;
-  GemvArgs a = moe_gate_up_args(gate, up, nullptr, k, x, h);
+  GemvArgs a = moe_gate_up_args(gate, up, nullptr, k, x, h, bits);
   a.logits = logits;
   a.n_logits = n_logits;
   a.renorm = renorm;

@@ -7,9 +7,9 @@
 namespace qg {
 
 int moe_down_launch(const qg_int4_weight* down, const uint32_t* idx, const float* p, int k, const float* h,
-                    const uint16_t* residual, float* y, cudaStream_t stream) {
+                    const uint16_t* residual, float* y, cudaStream_t stream, int bits) {
   if (k < 1 || k > kMaxMats) return QG_EINVAL;
-  GemvArgs a = moe_down_args(down, idx, p, k, h, residual, y);
+  GemvArgs a = moe_down_args(down, idx, p, k, h, residual, y, bits);
   return plan_and_launch<kSeg>(a, stream);
 }
 

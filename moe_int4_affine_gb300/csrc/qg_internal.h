@@ -72,10 +72,10 @@ int sigmoid_fma_launch(const float* gate, const float* value, const float* base,
                        int n, cudaStream_t stream);
 int gemv_tune(int ctas_per_sm);
 int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, const uint32_t* idx, int k,
-                       const uint16_t* x, float* h, cudaStream_t stream);
+                       const uint16_t* x, float* h, cudaStream_t stream, int bits = 4);
 int moe_gate_up_routed_launch(const float* logits, int n_logits, int renorm, const qg_int4_weight* gate,
                               const qg_int4_weight* up, int k, const uint16_t* x, float* h, uint32_t* idx_out,
-                              float* p_out, cudaStream_t stream);
+                              float* p_out, cudaStream_t stream, int bits = 4);
 // Copy `bytes` (a multiple of 16) from device-mapped host memory to device memory, in the launch
 // chain (gemv_dense.cu).
 int ingest_launch(const void* src_dev_mapped, void* dst, size_t bytes, cudaStream_t stream);
@@ -83,7 +83,7 @@ int ingest_launch(const void* src_dev_mapped, void* dst, size_t bytes, cudaStrea
 int quant_launch(const void* w, int wt, int out, int in, int bits, uint32_t* packed, uint16_t* scales,
                  uint16_t* biases, cudaStream_t stream);
 int moe_down_launch(const qg_int4_weight* down, const uint32_t* idx, const float* p, int k, const float* h,
-                    const uint16_t* residual, float* y, cudaStream_t stream);
+                    const uint16_t* residual, float* y, cudaStream_t stream, int bits = 4);
 
 // ---------------------------------------------------------------- MoE (moe.cu)
 int router_launch(const float* logits, int n_experts, int k, int renorm, uint32_t* idx, float* p,

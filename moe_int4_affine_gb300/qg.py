@@ -42,6 +42,8 @@ lib.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
 lib.moe_gather_qgemv_int4.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]
 lib.moe_layer_int4.argtypes = [_P, _I, _W, _W, _W, _I, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
 lib.qgemv_q2.argtypes = [_W, _P, _I, _P, _P]
+lib.moe_gather_qgemv_q2.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]
+lib.moe_layer_q2.argtypes = [_P, _I, _W, _W, _W, _I, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
 lib.qgemv_q2_multi.argtypes = [_I, _W, _P, _I, ctypes.POINTER(_P), _I, _P]
 lib.rmsnorm_qgemv_int4.argtypes = [_W, _P, _I, _P, ctypes.c_float, _P, _P]
 lib.rmsnorm_qgemv_int4_multi.argtypes = [_I, _W, _P, _I, _P, ctypes.c_float, ctypes.POINTER(_P), _I, _P]
@@ -65,7 +67,7 @@ lib.qg_strerror.argtypes = [_I]
 lib.qg_strerror.restype = ctypes.c_char_p
 lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
-           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "dense_layer_int4", "dense_layer_int4_host", "rmsnorm_qgemv_int4", "qgemv_q2", "qgemv_q2_multi",
+           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "dense_layer_int4", "dense_layer_int4_host", "rmsnorm_qgemv_int4", "qgemv_q2", "qgemv_q2_multi", "moe_gather_qgemv_q2", "moe_layer_q2",
            "rmsnorm_qgemv_int4_multi", "qgemv_int4_sigmoid_fma", "sigmoid_scalar_fma_residual",
            "scalar_fma_chain8_residual", "qgemm_int4", "qgemm_int4_multi", "quantize_affine_q64a", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
@@ -266,7 +268,7 @@ def qg_workspace_bytes(op: int, w: Int4Weight, t_or_k: int) -> int:
 
 
 def moe_gather_qgemv_int4(gate: Int4Weight, up: Int4Weight, down: Int4Weight, idx, p, x, residual, y=None,
-                          workspace=None, stream=None):
+                          workspace=None, stream=None, bits: int = 4):
     torch = _torch()
     k = idx.numel()
     if y is None:
@@ -274,15 +276,16 @@ def moe_gather_qgemv_int4(gate: Int4Weight, up: Int4Weight, down: Int4Weight, id
     need = qg_workspace_bytes(QG_OP_MOE, down, k)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
-    _check(lib.moe_gather_qgemv_int4(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
-                                     _ptr(idx), _ptr(p), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(workspace),
-                                     workspace.numel() * workspace.element_size(), _stream(stream)),
-           "moe_gather_qgemv_int4")
+    fn = lib.moe_gather_qgemv_int4 if bits == 4 else lib.moe_gather_qgemv_q2
+    _check(fn(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
+              _ptr(idx), _ptr(p), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(workspace),
+              workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_gather_qgemv_int4" if bits == 4 else "moe_gather_qgemv_q2")
     return y
 
 
 def moe_layer_int4(logits, gate: Int4Weight, up: Int4Weight, down: Int4Weight, x, residual, k: int = 8,
-                   renorm: bool = True, y=None, idx=None, p=None, workspace=None, stream=None):
+                   renorm: bool = True, y=None, idx=None, p=None, workspace=None, stream=None, bits: int = 4):
     """Router + expert gather in one call; returns (y, idx, p)."""
     torch = _torch()
     dev = x.device
@@ -295,10 +298,11 @@ def moe_layer_int4(logits, gate: Int4Weight, up: Int4Weight, down: Int4Weight, x
     need = qg_workspace_bytes(QG_OP_MOE, down, k)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-    _check(lib.moe_layer_int4(_ptr(logits), 1 if renorm else 0, ctypes.byref(gate.struct), ctypes.byref(up.struct),
-                              ctypes.byref(down.struct), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(idx), _ptr(p),
-                              _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
-           "moe_layer_int4")
+    fn = lib.moe_layer_int4 if bits == 4 else lib.moe_layer_q2
+    _check(fn(_ptr(logits), 1 if renorm else 0, ctypes.byref(gate.struct), ctypes.byref(up.struct),
+              ctypes.byref(down.struct), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(idx), _ptr(p),
+              _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_layer_int4" if bits == 4 else "moe_layer_q2")
     return y, idx, p
 
 

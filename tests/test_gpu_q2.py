@@ -69,3 +69,33 @@ def test_q2_encoder_feeds_the_q2_gemv(qg):
     pr, sr, br = oracle.quantize(w, 2)
     y_ref, a = oracle.qgemv2(pr, sr, br, x)
     assert_within_bound(y, y_ref, a)
+
+
+def _stack(qg, d, E, out, in_dim):
+    t = qg.to_device
+    return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim, n_mat=E)
+
+
+@pytest.mark.parametrize("E,hidden,inter,k", [(128, 2048, 768, 8), (9, 576, 128, 8), (5, 256, 192, 3)])
+def test_moe_q2_vs_oracle(qg, E, hidden, inter, k):
+    """The 2-bit MoE step: expert gather with the device router's selection, and the layer call
+    with the router inside the gate/up kernel; both against the oracle's 2-bit MoE."""
+    g = I.int2_weight(E, I.TID_GATE, inter, hidden, n_mat=E)
+    u = I.int2_weight(E, I.TID_UP, inter, hidden, n_mat=E)
+    d = I.int2_weight(E, I.TID_DOWN, hidden, inter, n_mat=E)
+    G, U, D = _stack(qg, g, E, inter, hidden), _stack(qg, u, E, inter, hidden), _stack(qg, d, E, hidden, inter)
+    logits = I.f32_normal(E, I.TID_LOGITS, E)
+    x = I.bf16_normal(E, I.TID_X, hidden)
+    r = I.bf16_normal(E, I.TID_RESID, hidden)
+    lg, xd, rd = qg.to_device(logits), qg.to_device(x), qg.to_device(r)
+    i_ref, p_ref = oracle.router_topk(logits, k)
+    t = lambda w: (w["packed"], w["scales"], w["biases"])
+    y_ref, a, flags = oracle.moe2(t(g), t(u), t(d), i_ref, p_ref, x, r)
+    assert flags == 0
+    idx, p = qg.moe_router_topk(lg, k=k)
+    y1 = qg.to_numpy(qg.moe_gather_qgemv_int4(G, U, D, idx, p, xd, rd, bits=2)).astype(np.float64)
+    assert_within_bound(y1, y_ref, a, what="gather")
+    y2, idx2, _ = qg.moe_layer_int4(lg, G, U, D, xd, rd, k=k, bits=2)
+    assert qg.to_numpy(idx2).astype(np.uint32).tolist() == i_ref.tolist()
+    assert_within_bound(qg.to_numpy(y2).astype(np.float64), y_ref, a, what="layer")
+    assert qg.qg_device_status() == 0
