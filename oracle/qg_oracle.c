@@ -357,8 +357,9 @@ int orc_quantize_rows(const void *w, int wtype, int64_t out, int64_t in, int bit
         if (j == 0 || v < lo) lo = v;
         if (j == 0 || v > hi) hi = v;
       }
-      volatile float lz = lo + 0.0f; /* -0 taken as +0 */
+      volatile float lz = lo + 0.0f, hz = hi + 0.0f; /* a zero of either sign taken as +0 */
       lo = lz;
+      hi = hz;
       volatile float range = hi - lo;                 /* binary32 operations, one rounding each */
       volatile float scale = range / (float)qmax;
       uint16_t sb = f32_to_bf16_rne(scale), bb = f32_to_bf16_rne(lo);

@@ -527,6 +527,18 @@ def test_quantize_constant_group():
     assert np.all(bi == oracle.bf16_round(np.float32(0.3)))
 
 
+def test_quantize_zero_groups_store_positive_zero():
+    """Groups of zeros of both signs, whichever sign comes first, store scale +0 and bias +0 and
+    codes 0 (the range of a set of zeros is zero, not -0)."""
+    w = np.zeros((3, 64), np.float32)
+    w[0, 0::2] = -0.0
+    w[1, :] = -0.0
+    w[2, 1::2] = -0.0
+    for bits in (4, 2):
+        packed, sc, bi = oracle.quantize(w, bits)
+        assert np.all(sc == 0) and np.all(bi == 0) and np.all(packed == 0)
+
+
 def test_quantize_codes_come_from_bf16_scale_and_bias():
     """lo = 0, hi = 1: with the binary32 scale 1/15, w = 0.968 sits at 14.52 (code 15); with the
     bf16 scale 0.06689453125 at 14.47 (code 14) -- the codes are derived from the rounded scale,
