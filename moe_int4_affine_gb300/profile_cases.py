@@ -4,6 +4,7 @@
     python -m moe_int4_affine_gb300.profile_cases down_bf16  # the M = 1 GEMV 5120 x 17408, bf16 x
     python -m moe_int4_affine_gb300.profile_cases moe        # router + MoE gather (128 experts, top 8)
     python -m moe_int4_affine_gb300.profile_cases qgemm T    # dequant-GEMM 17408 x 5120, T tokens
+    python -m moe_int4_affine_gb300.profile_cases quant B K  # encode 17408 x 5120 weights (K = bf16 | f32) to B bits
 
 Each case builds its seeded synthetic inputs (a few hundred MB at most on the device), runs the
 calls three times and prints "ok <device status>".  Nothing is timed here.
@@ -56,6 +57,13 @@ def main(argv=None) -> int:
         X = qg.to_device(I.bf16_normal(0, I.TID_X, (T, 5120)))
         for _ in range(reps):
             qg.qgemm_int4(w, X)
+    elif case == "quant":
+        bits = int(argv[1]) if len(argv) > 1 else 4
+        kind = argv[2] if len(argv) > 2 else "bf16"
+        shape = (17408, 5120)
+        w = qg.to_device(I.bf16_normal(0, I.TID_W, shape) if kind == "bf16" else I.f32_normal(0, I.TID_W, shape))
+        for _ in range(reps):
+            qg.quantize_affine_q64a(w, bits)
     else:
         print(f"unknown case {case!r}", file=sys.stderr)
         return 2

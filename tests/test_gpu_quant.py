@@ -1,7 +1,8 @@
 """GPU parity of quantize_affine_q64a (the affine group-64 encoder, Q4_64A and Q2_64A) against the
 oracle's encoder: codes, scales and biases bit-exact (the code decision is made in binary32 on
 both sides), including crafted groups (constant, signed zeros, an exact grid, a code that the bf16
-scale moves), and the encoder's output fed to the GEMV."""
+scale moves, scales too small or too large for the reciprocal, quotients on and next to
+half-integers), and the encoder's output fed to the GEMV."""
 import numpy as np
 import pytest
 
@@ -25,6 +26,19 @@ def _weights(seed, out, in_dim, kind):
         w[2, 2] = 0.968
         k = np.arange(64) % 16              # an exact grid
         w[3, 64:128] = ((k - 20) * np.float32(0.0126953125)).astype(np.float32)
+    if out >= 8 and in_dim >= 128:
+        k = np.arange(64)
+        w[4, :64] = (k % 5) * np.float32(2.0 ** -130)     # subnormal weights: 1/s overflows binary32
+        w[5, 64:128] = (k % 16) * np.float32(2.0 ** 122)  # s = 2^122: beyond the reciprocal's range
+        w[6, :64] = (k % 16) * np.float32(2.0 ** -118)    # s = 2^-118: the smallest scales of the fast path
+        w[7, :64] = 0.0                                   # zeros, -0 first
+        w[7, 0::2] = -0.0
+    if out >= 9 and in_dim >= 128:
+        # quotients on and next to every half-integer: s = 2^-4, b = 0 for 4 bits
+        h = (np.arange(15, dtype=np.float32) + np.float32(0.5)) / np.float32(16)
+        t = np.concatenate([[0.0, 15 / 16], h, np.nextafter(h, np.float32(1)), np.nextafter(h, np.float32(0))])
+        w[8, :64] = np.float32(0.5)
+        w[8, :t.size] = t.astype(np.float32)
     if kind == "bf16":
         bits = (w.view(np.uint32) + 0x7FFF + ((w.view(np.uint32) >> 16) & 1)) >> 16
         return bits.astype(np.uint16)

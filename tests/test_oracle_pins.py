@@ -539,6 +539,24 @@ def test_quantize_zero_groups_store_positive_zero():
         assert np.all(sc == 0) and np.all(bi == 0) and np.all(packed == 0)
 
 
+def test_quantize_ties_round_to_even():
+    """w = (k + 1/2) s exactly (s = 2^-4, b = 0): the code is the even one of k and k + 1; one ulp
+    above the tie rounds up, one ulp below rounds down."""
+    k = np.arange(15)
+    h = ((k + 0.5) / 16).astype(np.float32)
+    w = np.full((3, 64), 0.5, np.float32)
+    for r, vals in enumerate((h, np.nextafter(h, np.float32(1)), np.nextafter(h, np.float32(0)))):
+        w[r, 0], w[r, 1] = 0.0, 15 / 16
+        w[r, 2:17] = vals
+    packed, sc, bi = oracle.quantize(w, 4)
+    assert np.all(sc == 0x3D80) and np.all(bi == 0)  # 2^-4 and 0
+    codes = (packed[:, :, None] >> (4 * np.arange(8))) & 0xF
+    codes = codes.reshape(3, 64)[:, 2:17]
+    assert codes[0].tolist() == [int(c + (c % 2)) for c in k]   # ties: the even neighbour
+    assert codes[1].tolist() == (k + 1).tolist()
+    assert codes[2].tolist() == k.tolist()
+
+
 def test_quantize_codes_come_from_bf16_scale_and_bias():
     """lo = 0, hi = 1: with the binary32 scale 1/15, w = 0.968 sits at 14.52 (code 15); with the
     bf16 scale 0.06689453125 at 14.47 (code 14) -- the codes are derived from the rounded scale,
