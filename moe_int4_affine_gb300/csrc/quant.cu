@@ -126,13 +126,15 @@ __device__ __forceinline__ GroupK group_constants(float l, float h, uint32_t& sb
   bb = f32_to_bf16_rne(l);
   const float s = __uint_as_float(sb << 16), b = __uint_as_float(bb << 16);
   GroupK g;
-  g.ps = s < 0x1p-100f ? 0x1p64f : (s > 0x1p100f ? 0x1p-64f : 1.f);
-  g.nb = -__fmul_rn(b, g.ps);
   if (s == 0.f) {
+    g.ps = 1.f;
+    g.nb = -b;
     g.yk = 0.f;
     g.yek = 0.f;
     safe = true;
   } else {
+    g.ps = s < 0x1p-100f ? 0x1p64f : (s > 0x1p100f ? 0x1p-64f : 1.f);
+    g.nb = -__fmul_rn(b, g.ps);
     const float sp = __fmul_rn(s, g.ps);
     const float y = __frcp_rn(sp);
     const float e0 = __fmaf_rn(-sp, y, 1.f);
@@ -232,7 +234,7 @@ __device__ __forceinline__ void codes_step(const uint4 (&cur)[4], const GroupK& 
   for (int k = 0; k < kSlots; ++k) {
     const int src = (lane & 24) + k;
     GroupK g;
-    g.ps = __shfl_sync(0xffffffffu, go.ps, src);
+    g.ps = CLAMP ? __shfl_sync(0xffffffffu, go.ps, src) : 1.f;  // steps without the clamp have ps = 1
     g.nb = __shfl_sync(0xffffffffu, go.nb, src);
     g.yk = __shfl_sync(0xffffffffu, go.yk, src);
     g.yek = __shfl_sync(0xffffffffu, go.yek, src);
