@@ -207,6 +207,27 @@ int moe_layer_int4(const float *logits, int renorm, const qg_int4_weight *gate, 
                    uint32_t *idx, float *p, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * moe_prefill_int4 -- the MoE layer for T tokens at once (prefill; [FFAI#14] names the MoE prefill
+ * gather GEMM: tokens sorted by expert, grouped tiles, unpermuted back):
+ *   for token t: (idx[t], p[t]) = moe_router_topk(logits[t], renorm);
+ *     for slot s: e = idx[t][s]; h = silu(Wg[e] X[t]) * (Wu[e] X[t]); d_s = Wd[e] h
+ *     Y[t][i] = residual[t][i] + sum_s p[t][s] d_s[i]            (slot order)
+ * i.e. moe_layer_int4 applied to every token.  On the device the (token, slot) pairs are grouped by
+ * expert (counts, tile offsets, a row map), every expert's weights are read once per tile of its
+ * tokens, and the gate/up and down projections run on the tensor cores (fp16 operands, fp32
+ * accumulation, the numerics of qgemm_int4), seven launches in all.
+ * logits: fp32 [T][n_experts]; X: bf16 [T][hidden]; residual: bf16 [T][hidden] or NULL (zero);
+ * Y: fp32 [T][hidden]; idx (uint32) and p (fp32): device outputs [T][k].  gate, up, down: expert
+ * stacks as for moe_gather_qgemv_int4 (n_mat = n_experts).
+ * workspace: at least qg_workspace_bytes(QG_OP_MOE_PREFILL, down, T) bytes.
+ * Limits: 1 <= T <= 65535, 1 <= k <= 8, k <= n_experts <= 1024; hidden and inter multiples of 64,
+ * hidden <= 32768; scales and biases within fp16's range (as qgemm_int4).
+ */
+int moe_prefill_int4(const float *logits, int T, int renorm, const qg_int4_weight *gate, const qg_int4_weight *up,
+                     const qg_int4_weight *down, int k, const uint16_t *X, const uint16_t *residual, float *Y,
+                     uint32_t *idx, float *p, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * dense_layer_int4 -- a dense decode FFN layer in one call: the SwiGLU gate/up pair, then the down
  * projection ([FFAI#14] "dequantGemvInt4Two" for gate + up, then the down dequant-GEMV):
  *   h = silu(W_g x) * (W_u x),   y = W_down h
@@ -320,7 +341,8 @@ typedef enum {
   QG_OP_MOE = 2,
   QG_OP_QGEMM = 3,
   QG_OP_LAYER = 4,     /* dense_layer_int4 */
-  QG_OP_LAYER_HOST = 5 /* dense_layer_int4_host (T_or_k = hidden) */
+  QG_OP_LAYER_HOST = 5, /* dense_layer_int4_host (T_or_k = hidden) */
+  QG_OP_MOE_PREFILL = 6 /* moe_prefill_int4 (the down weight, T_or_k = T; room for any k <= 8) */
 } qg_op;
 
 /* Workspace bytes the call `op` needs for weight `w` and T (QG_OP_QGEMM) or k (QG_OP_MOE; pass

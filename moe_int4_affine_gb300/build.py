@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libqg.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["gemv_dense.cu", "gemv_pair.cu", "gemv_seg.cu", "moe.cu", "qgemm.cu", "qgemm_tc.cu", "quant.cu", "api.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["gemv_dense.cu", "gemv_pair.cu", "gemv_seg.cu", "moe.cu", "moe_prefill.cu", "qgemm.cu", "qgemm_tc.cu", "quant.cu", "api.cu", "noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-rdc=true", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

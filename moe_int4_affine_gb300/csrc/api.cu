@@ -241,6 +241,27 @@ int moe_layer_q2(const float* logits, int renorm, const qg_int4_weight* gate, co
   return moe_layer_call(logits, renorm, gate, up, down, k, x, residual, y, idx, p, workspace, ws_bytes, stream, 2);
 }
 
+int moe_prefill_int4(const float* logits, int T, int renorm, const qg_int4_weight* gate, const qg_int4_weight* up,
+                     const qg_int4_weight* down, int k, const uint16_t* X, const uint16_t* residual, float* Y,
+                     uint32_t* idx, float* p, void* workspace, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_weight(gate, true)) || (rc = check_weight(up, true)) || (rc = check_weight(down, true))) return rc;
+  if (!logits || !idx || !p || !X || !Y) return QG_EINVAL;
+  if (T < 1 || T > 65535 || k < 1 || k > 8 || (renorm != 0 && renorm != 1) || gate->n_mat < k) return QG_EINVAL;
+  if (gate->n_mat > 1024) return QG_ENOTSUP;
+  if (gate->out != up->out || gate->in != up->in || gate->n_mat != up->n_mat || down->n_mat != gate->n_mat ||
+      down->in != gate->out || down->out != gate->in)
+    return QG_EINVAL;
+  if (!aligned16(logits) || !aligned16(idx) || !aligned16(p) || !aligned16(X) || (residual && !aligned16(residual)) ||
+      !aligned16(Y))
+    return QG_EALIGN;
+  const size_t need = qg_workspace_bytes(QG_OP_MOE_PREFILL, down, T);
+  if (!workspace || ws_bytes < need) return QG_EWORKSPACE;
+  if (!aligned16(workspace)) return QG_EALIGN;
+  return moe_prefill_launch(logits, T, renorm, gate, up, down, k, X, residual, Y, idx, p, workspace, ws_bytes,
+                            static_cast<cudaStream_t>(stream));
+}
+
 int dense_layer_int4(const qg_int4_weight* gate, const qg_int4_weight* up, const qg_int4_weight* down, const void* x,
                      int xt, float* y, void* workspace, size_t ws_bytes, void* stream) {
   int rc;
@@ -342,6 +363,8 @@ size_t qg_workspace_bytes(int op, const qg_int4_weight* w, int T_or_k) {
       return (size_t)w->in * sizeof(float);
     case QG_OP_LAYER_HOST:  // h[inter], then the device copy of x[hidden] (room for fp32)
       return round16((size_t)w->in * sizeof(float)) + (size_t)(T_or_k > 0 ? T_or_k : 0) * sizeof(float);
+    case QG_OP_MOE_PREFILL:  // plan tables, grouped token tiles, G, U, h tiles, down outputs
+      return moe_prefill_workspace_bytes(w, T_or_k);
     default:
       return 0;
   }

@@ -24,12 +24,16 @@ __device__ __forceinline__ uint32_t float_key(float f) {
 // the 64-bit key (float_key(logit) << 32) | ~index, so the largest key is the largest logit with
 // the lowest index on ties, and every lane agrees on it.  Round s takes the warp's largest key not
 // yet taken; lane s keeps round s's selection.  Then the weights: softmax of the selected logits
-// (renorm) or of all logits read at the selected ones.
+// (renorm) or of all logits read at the selected ones.  Block b routes token b (logits row b,
+// outputs row b of [T][k]).
 template <int PER>
 __global__ void __launch_bounds__(32) router_kernel(const float* __restrict__ logits, int n, int k, int renorm,
                                                     uint32_t* __restrict__ idx_out, float* __restrict__ p_out) {
   pdl_trigger();
   pdl_wait();
+  logits += (size_t)blockIdx.x * n;
+  idx_out += (size_t)blockIdx.x * k;
+  p_out += (size_t)blockIdx.x * k;
   const int lane = threadIdx.x;
   float v[PER];
   unsigned long long key[PER];
@@ -74,16 +78,21 @@ __global__ void __launch_bounds__(32) router_kernel(const float* __restrict__ lo
   }
 }
 
+int router_batch_launch(const float* logits, int T, int n_experts, int k, int renorm, uint32_t* idx, float* p,
+                        cudaStream_t stream) {
+  const int per = (n_experts + 31) / 32;
+  const dim3 grid((unsigned)T);
+  if (per <= 1) return launch(router_kernel<1>, grid, dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  if (per <= 2) return launch(router_kernel<2>, grid, dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  if (per <= 4) return launch(router_kernel<4>, grid, dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  if (per <= 8) return launch(router_kernel<8>, grid, dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  if (per <= 16) return launch(router_kernel<16>, grid, dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  return launch(router_kernel<kRouterMaxPerLane>, grid, dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+}
+
 int router_launch(const float* logits, int n_experts, int k, int renorm, uint32_t* idx, float* p,
                   cudaStream_t stream) {
-  const int per = (n_experts + 31) / 32;
-  if (per <= 1) return launch(router_kernel<1>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
-  if (per <= 2) return launch(router_kernel<2>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
-  if (per <= 4) return launch(router_kernel<4>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
-  if (per <= 8) return launch(router_kernel<8>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
-  if (per <= 16)
-    return launch(router_kernel<16>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
-  return launch(router_kernel<kRouterMaxPerLane>, dim3(1), dim3(32), 0, stream, logits, n_experts, k, renorm, idx, p);
+  return router_batch_launch(logits, 1, n_experts, k, renorm, idx, p, stream);
 }
 
 // out[i] = residual[i] + sum_{k<8} p[k] * v[k][i], accumulated in slot order ([FFAI#14] scalar-FMA

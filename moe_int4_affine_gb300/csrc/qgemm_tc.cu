@@ -60,12 +60,16 @@ struct TcMat {
   float* y;  // [T][out]
   int out;
   int tile0;
+  long long ew, esb;  // grouped mode: expert e's codes at packed + e * ew, scales, biases at + e * esb
 };
 constexpr int kTcMaxMats = 4;
 
 struct TcArgs {
   TcMat mat[kTcMaxMats];  // matrices sharing the tokens (same in)
   int nmat;
+  // grouped (MoE) mode: token tile y belongs to expert tile_expert[y] (< 0: no tile, the CTA
+  // exits); every matrix is then a stack of experts (TcMat::ew, esb)
+  const int* tile_expert;
   const uint8_t* xt;  // token tiles: [n_tiles][k groups][n_tile][128 B], swizzled, fp16
   const float* xs;    // [n_tiles * n_tile] per-token output scale
   int in, T;
@@ -202,7 +206,15 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int mi = 0;  // this CTA's matrix: the last one whose first tile is at or before blockIdx.x
   while (mi + 1 < a.nmat && (int)blockIdx.x >= a.mat[mi + 1].tile0) ++mi;
-  const TcMat& mt = a.mat[mi];
+  TcMat mt = a.mat[mi];
+  if (a.tile_expert) {  // grouped: the tile table is the previous kernel's output
+    pdl_wait();
+    const int e = a.tile_expert[blockIdx.y];
+    if (e < 0) return;  // (before any barrier, tensor memory or copy: the whole CTA leaves)
+    mt.packed += (size_t)e * (size_t)mt.ew;
+    mt.scales += (size_t)e * (size_t)mt.esb;
+    mt.biases += (size_t)e * (size_t)mt.esb;
+  }
   const int m0 = ((int)blockIdx.x - mt.tile0) * kBM;
   const int tile = blockIdx.y, n0 = tile * a.n_tile;
   const int nk = a.in / kGK;         // groups
@@ -384,20 +396,23 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 // One CTA per token row n < n_tiles * n_tile.  Row n of tile n / n_tile, group kc: 128 bytes at
 // ((tile * nk + kc) * n_tile + n % n_tile) * 128, the 16-byte chunk j (columns 8j .. 8j + 7 of the
 // group) at position j ^ (n % 8), its eight values in the column order 0, 4, 1, 5, 2, 6, 3, 7 (the
-// order the dequantized weights use).  Rows n >= T are zero.
+// order the dequantized weights use).  Rows n >= T are zero.  With a row map, row n of the tiles is
+// row rowmap[n] of X (< 0: a zero row), so that the tiles hold the tokens grouped by expert.
 constexpr int kPrepThreads = 256;
 constexpr int kPrepMaxChunks = 16;  // 16-byte chunks per thread: in <= 16 * 256 * 8 = 32768
 
 __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_kernel(const uint16_t* __restrict__ X, int T, int in,
-                                                                   int n_tile, uint8_t* __restrict__ xt,
+                                                                   int n_tile, const int* __restrict__ rowmap,
+                                                                   uint8_t* __restrict__ xt,
                                                                    float* __restrict__ xs) {
   __shared__ uint32_t red[kPrepThreads / 32];
   const int n = blockIdx.x;
   const int nk = in / 64, nch = in / 8;
-  const bool live = n < T;
-  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? n : 0) * in);
   pdl_trigger();
   pdl_wait();
+  const int src = rowmap ? rowmap[n] : n;
+  const bool live = src >= 0 && src < T;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? src : 0) * in);
   // one round of loads; the largest |x| from the bit patterns (|bf16| bits are ordered like values)
   uint4 raw[kPrepMaxChunks];
   uint32_t mx = 0;
@@ -446,18 +461,80 @@ __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_kernel(const uint16_t
   }
 }
 
+// The down projection's token tiles in grouped (MoE) mode: row n is h = silu(G[n]) * U[n] (fp32
+// [rows][in], the grouped gate/up outputs), scaled by a power of two and stored as above; rows
+// with rowmap[n] < 0 (tile padding) are zero.  Two passes over the row (its largest |h|, then the
+// conversion; the second reads hit L2), so in is not limited by registers.
+__device__ __forceinline__ void swiglu8(const float* __restrict__ G, const float* __restrict__ U, size_t off,
+                                        float (&h)[8]) {
+  const float4* g4 = reinterpret_cast<const float4*>(G + off);
+  const float4* u4 = reinterpret_cast<const float4*>(U + off);
+  const float4 ga = __ldg(g4), gb = __ldg(g4 + 1), ua = __ldg(u4), ub = __ldg(u4 + 1);
+  const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+  const float u[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) h[q] = g[q] / (1.f + expf(-g[q])) * u[q];
+}
+
+__global__ void __launch_bounds__(kPrepThreads) qgemm_prep_swiglu_kernel(const float* __restrict__ G,
+                                                                          const float* __restrict__ U, int in,
+                                                                          int n_tile, const int* __restrict__ rowmap,
+                                                                          uint8_t* __restrict__ xt,
+                                                                          float* __restrict__ xs) {
+  __shared__ float red[kPrepThreads / 32];
+  const int n = blockIdx.x;
+  const int nk = in / 64, nch = in / 8;
+  pdl_trigger();
+  pdl_wait();
+  const bool live = rowmap[n] >= 0;
+  const size_t row0 = (size_t)n * in;
+  float mx = 0.f;
+  if (live) {
+    for (int ch = threadIdx.x; ch < nch; ch += kPrepThreads) {
+      float h[8];
+      swiglu8(G, U, row0 + (size_t)ch * 8, h);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(h[q]));
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = 0.f;
+#pragma unroll
+  for (int w = 0; w < kPrepThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+  const int e = mx > 0.f ? (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127 : 0;
+  const float sc = mx > 0.f ? exp2i(min(max(14 - e, -126), 127)) : 0.f;
+  if (threadIdx.x == 0) xs[n] = mx > 0.f ? exp2i(min(max(e - 14, -126), 127)) : 0.f;
+  const int tile = n / n_tile, nl = n % n_tile;
+  for (int ch = threadIdx.x; ch < nch; ch += kPrepThreads) {
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (live) {
+      swiglu8(G, U, row0 + (size_t)ch * 8, f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) f[q] *= sc;
+    }
+    const int kc = ch >> 3, j = ch & 7;
+    uint4 o;  // fp16 pairs in the column order 0, 4, 1, 5, 2, 6, 3, 7 (low half first)
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.x) : "f"(f[4]), "f"(f[0]));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.y) : "f"(f[5]), "f"(f[1]));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.z) : "f"(f[6]), "f"(f[2]));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.w) : "f"(f[7]), "f"(f[3]));
+    uint8_t* dst = xt + (((size_t)tile * nk + kc) * n_tile + nl) * 128 + (size_t)((j ^ (nl & 7)) << 4);
+    *reinterpret_cast<uint4*>(dst) = o;
+  }
+}
+
 struct TcPlan {
   int n_tile, n_tiles, stages, wring;
   size_t smem;
 };
 
-TcPlan tc_plan(int out, int in, int T) {
-  (void)out;
-  (void)in;
+// Pipeline depth and weight ring for a token tile of n_tile rows (a multiple of 16, <= kMaxN).
+TcPlan tc_plan_ntile(int n_tile) {
   TcPlan p{};
-  const int t16 = (T + 15) / 16 * 16;
-  p.n_tile = std::min(kMaxN, t16);
-  p.n_tiles = (T + p.n_tile - 1) / p.n_tile;
+  p.n_tile = n_tile;
+  p.n_tiles = 1;
   const size_t stage = 2 * (size_t)p.n_tile * 128;  // token tiles of two groups
   const size_t fixed = 1024 + 64 + 8 * 32;          // alignment slack, barriers, slot, flag
   // stages: at most kMaxStages (tensor-memory columns for A); the rest of shared memory goes to the
@@ -468,6 +545,36 @@ TcPlan tc_plan(int out, int in, int T) {
   p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
   return p;
 }
+
+TcPlan tc_plan(int out, int in, int T) {
+  (void)out;
+  (void)in;
+  TcPlan p = tc_plan_ntile(std::min(kMaxN, (T + 15) / 16 * 16));
+  p.n_tiles = (T + p.n_tile - 1) / p.n_tile;
+  return p;
+}
+
+int tc_launch(const TcArgs& a, const TcPlan& p, dim3 grid, cudaStream_t stream) {
+  auto go = [&](auto k) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
+      return (int)QG_ELAUNCH;
+    return launch(k, grid, dim3(kThreads), p.smem, stream, a);
+  };
+  switch (p.wring) {
+    case 16:
+      return go(qgemm_tc_kernel<16>);
+    case 8:
+      return go(qgemm_tc_kernel<8>);
+    case 4:
+      return go(qgemm_tc_kernel<4>);
+    default:
+      return go(qgemm_tc_kernel<2>);
+  }
+}
+
+// instruction descriptor (kind::f16): D fp32 (bits 4-5 = 1), A and B fp16 (bits 7-12 = 0), both
+// K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
+uint32_t tc_idesc(int n_tile) { return (1u << 4) | ((uint32_t)(n_tile >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24); }
 
 }  // namespace
 
@@ -488,12 +595,12 @@ int qgemm_tc_launch_multi(const qg_int4_weight* w, int n, const uint16_t* X, int
   uint8_t* xt = static_cast<uint8_t*>(ws);
   float* xs = reinterpret_cast<float*>(xt + xt_bytes);
   int rc = launch(qgemm_prep_kernel, dim3((unsigned)rows), dim3(kPrepThreads), 0, stream, X, T, w[0].in, p.n_tile,
-                  xt, xs);
+                  static_cast<const int*>(nullptr), xt, xs);
   if (rc != QG_OK) return rc;
   TcArgs a{};
   int tiles = 0;
   for (int i = 0; i < n; ++i) {
-    a.mat[i] = TcMat{w[i].packed, w[i].scales, w[i].biases, Y[i], w[i].out, tiles};
+    a.mat[i] = TcMat{w[i].packed, w[i].scales, w[i].biases, Y[i], w[i].out, tiles, 0, 0};
     tiles += (w[i].out + kBM - 1) / kBM;
   }
   a.nmat = n;
@@ -503,30 +610,48 @@ int qgemm_tc_launch_multi(const qg_int4_weight* w, int n, const uint16_t* X, int
   a.T = T;
   a.n_tile = p.n_tile;
   a.stages = p.stages;
-  // instruction descriptor (kind::f16): D fp32 (bits 4-5 = 1), A and B fp16 (bits 7-12 = 0), both
-  // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
-  a.idesc = (1u << 4) | ((uint32_t)(p.n_tile >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-  const dim3 grid((unsigned)tiles, (unsigned)p.n_tiles);
-  auto go = [&](auto k) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
-      return (int)QG_ELAUNCH;
-    return launch(k, grid, dim3(kThreads), p.smem, stream, a);
-  };
-  switch (p.wring) {
-    case 16:
-      return go(qgemm_tc_kernel<16>);
-    case 8:
-      return go(qgemm_tc_kernel<8>);
-    case 4:
-      return go(qgemm_tc_kernel<4>);
-    default:
-      return go(qgemm_tc_kernel<2>);
-  }
+  a.idesc = tc_idesc(p.n_tile);
+  return tc_launch(a, p, dim3((unsigned)tiles, (unsigned)p.n_tiles), stream);
 }
 
 int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y, void* ws, size_t ws_bytes,
                     cudaStream_t stream) {
   return qgemm_tc_launch_multi(w, 1, X, T, &Y, ws, ws_bytes, stream);
+}
+
+int qgemm_prep_rows_launch(const uint16_t* X, int T, int in, const int* rowmap, int rows, int n_tile, uint8_t* xt,
+                           float* xs, cudaStream_t stream) {
+  return launch(qgemm_prep_kernel, dim3((unsigned)rows), dim3(kPrepThreads), 0, stream, X, T, in, n_tile, rowmap, xt,
+                xs);
+}
+
+int qgemm_prep_swiglu_launch(const float* G, const float* U, int in, const int* rowmap, int rows, int n_tile,
+                             uint8_t* xt, float* xs, cudaStream_t stream) {
+  return launch(qgemm_prep_swiglu_kernel, dim3((unsigned)rows), dim3(kPrepThreads), 0, stream, G, U, in, n_tile,
+                rowmap, xt, xs);
+}
+
+int qgemm_tc_grouped_launch(const qg_int4_weight* w, int n, const uint8_t* xt, const float* xs, int n_tiles,
+                            int n_tile, const int* tile_expert, float* const* Y, cudaStream_t stream) {
+  if (n < 1 || n > kTcMaxMats || n_tile < 16 || n_tile > kMaxN || n_tile % 16 != 0 || n_tiles < 1) return QG_EINVAL;
+  const TcPlan p = tc_plan_ntile(n_tile);
+  TcArgs a{};
+  int tiles = 0;
+  for (int i = 0; i < n; ++i) {
+    a.mat[i] = TcMat{w[i].packed, w[i].scales, w[i].biases, Y[i], w[i].out, tiles,
+                     (long long)w[i].out * (w[i].in / 8), (long long)w[i].out * (w[i].in / 64)};
+    tiles += (w[i].out + kBM - 1) / kBM;
+  }
+  a.nmat = n;
+  a.tile_expert = tile_expert;
+  a.xt = xt;
+  a.xs = xs;
+  a.in = w[0].in;
+  a.T = n_tiles * n_tile;
+  a.n_tile = n_tile;
+  a.stages = p.stages;
+  a.idesc = tc_idesc(n_tile);
+  return tc_launch(a, p, dim3((unsigned)tiles, (unsigned)n_tiles), stream);
 }
 
 }  // namespace qg
