@@ -2,9 +2,11 @@
 // E experts, the tokens grouped by expert so that each expert's weights are read once per tile of
 // up to n_tile of its tokens, on the tensor cores:
 //   1. router     logits [T][E] -> idx, p [T][k]             (one warp per token)
-//   2. plan       idx -> per-expert counts, tile offsets; the expert of every token tile, the token
-//                 of every grouped row, the grouped row of every (token, slot) pair (one CTA)
-//   3. prep       X rows gathered into fp16 token tiles, grouped by expert
+//   2. plan       idx -> per-expert counts, tile offsets; the expert of every token tile and the
+//                 grouped row of every (token, slot) pair (one CTA)
+//   3. prep       X rows gathered into fp16 token tiles, grouped by expert (one block per pair;
+//                 the tiles' padding rows are not written: an MMA output column depends on its own
+//                 token row only, and padding outputs are never read)
 //   4. gate/up    G, U [rows][inter] = grouped rows x W_g[e]^T, W_u[e]^T   (tcgen05, one launch)
 //   5. prep       h = silu(G) * U into fp16 token tiles
 //   6. down       D [rows][hidden] = h x W_d[e]^T                             (tcgen05)
@@ -40,7 +42,7 @@ int prefill_max_tiles(int T, int k, int E, int n_tile) {
 
 struct PrefillLayout {
   int n_tile, max_tiles, rows;
-  size_t o_tile, o_rowmap, o_pos, o_xt1, o_xs1, o_g, o_u, o_xt2, o_xs2, o_d, total;
+  size_t o_tile, o_pos, o_xt1, o_xs1, o_g, o_u, o_xt2, o_xs2, o_d, total;
 };
 
 size_t up256(size_t b) { return (b + 255) / 256 * 256; }
@@ -53,7 +55,6 @@ PrefillLayout prefill_layout(int T, int k, int E, int hidden, int inter) {
   const size_t rows = (size_t)L.rows;
   size_t o = 0;
   L.o_tile = o;   o += up256((size_t)L.max_tiles * 4);
-  L.o_rowmap = o; o += up256(rows * 4);
   L.o_pos = o;    o += up256((size_t)T * k * 4);
   L.o_xt1 = o;    o += up256(rows * hidden * 2);
   L.o_xs1 = o;    o += up256(rows * 4);
@@ -68,23 +69,19 @@ PrefillLayout prefill_layout(int T, int k, int E, int hidden, int inter) {
 
 // Step 2.  npairs = T k pairs (token t = i / k, slot i % k) with expert idx[i].
 //   tile_expert[y]: the expert of token tile y (-1 past the last used tile);
-//   rowmap[r]:      the token of grouped row r (-1: padding of a tile);
 //   pos[i]:         the grouped row of pair i (-1: an expert index >= E, which adds nothing and
 //                   sets QG_STATUS_BAD_EXPERT).
 // Expert e's rows start at tile offset toff[e] (exclusive scan of ceil(count_e / n_tile)).
-__global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const uint32_t* __restrict__ idx, int npairs, int k,
-                                                                int E, int n_tile, int max_tiles,
-                                                                int* __restrict__ tile_expert,
-                                                                int* __restrict__ rowmap, int* __restrict__ pos) {
+__global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const uint32_t* __restrict__ idx, int npairs, int E,
+                                                                int n_tile, int max_tiles,
+                                                                int* __restrict__ tile_expert, int* __restrict__ pos) {
   __shared__ int cnt[kPlanThreads];
-  __shared__ int toff[kPlanThreads + 1];
+  __shared__ int toff[kPlanThreads];
   __shared__ int wsum[kPlanThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
   pdl_wait();
   cnt[tid] = 0;
-  const int rows = max_tiles * n_tile;
-  for (int r = tid; r < rows; r += kPlanThreads) rowmap[r] = -1;
   for (int y = tid; y < max_tiles; y += kPlanThreads) tile_expert[y] = -1;
   __syncthreads();
   for (int i = tid; i < npairs; i += kPlanThreads) {
@@ -125,11 +122,7 @@ __global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const uint32_t* 
   }
   for (int i = tid; i < npairs; i += kPlanThreads) {
     const uint32_t e = idx[i];
-    if (e < (uint32_t)E) {
-      const int r = toff[e] * n_tile + pos[i];
-      pos[i] = r;
-      rowmap[r] = i / k;
-    }
+    if (e < (uint32_t)E) pos[i] = toff[e] * n_tile + pos[i];
   }
 }
 
@@ -181,7 +174,6 @@ int moe_prefill_launch(const float* logits, int T, int renorm, const qg_int4_wei
   if (ws_bytes < L.total) return QG_EWORKSPACE;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~(uintptr_t)255);
   int* tile_expert = reinterpret_cast<int*>(base + L.o_tile);
-  int* rowmap = reinterpret_cast<int*>(base + L.o_rowmap);
   int* pos = reinterpret_cast<int*>(base + L.o_pos);
   uint8_t* xt1 = base + L.o_xt1;
   float* xs1 = reinterpret_cast<float*>(base + L.o_xs1);
@@ -193,16 +185,16 @@ int moe_prefill_launch(const float* logits, int T, int renorm, const qg_int4_wei
 
   int rc = router_batch_launch(logits, T, E, k, renorm, idx, p, stream);
   if (rc != QG_OK) return rc;
-  rc = launch(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, static_cast<const uint32_t*>(idx), T * k, k, E,
-              L.n_tile, L.max_tiles, tile_expert, rowmap, pos);
+  rc = launch(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, static_cast<const uint32_t*>(idx), T * k, E,
+              L.n_tile, L.max_tiles, tile_expert, pos);
   if (rc != QG_OK) return rc;
-  rc = qgemm_prep_rows_launch(X, T, hidden, rowmap, L.rows, L.n_tile, xt1, xs1, stream);
+  rc = qgemm_prep_pairs_launch(X, T, hidden, pos, T * k, k, L.n_tile, xt1, xs1, stream);
   if (rc != QG_OK) return rc;
   const qg_int4_weight gu[2] = {*gate, *up};
   float* const gy[2] = {G, U};
   rc = qgemm_tc_grouped_launch(gu, 2, xt1, xs1, L.max_tiles, L.n_tile, tile_expert, gy, stream);
   if (rc != QG_OK) return rc;
-  rc = qgemm_prep_swiglu_launch(G, U, inter, rowmap, L.rows, L.n_tile, xt2, xs2, stream);
+  rc = qgemm_prep_swiglu_launch(G, U, inter, pos, T * k, L.n_tile, xt2, xs2, stream);
   if (rc != QG_OK) return rc;
   float* const dy[1] = {D};
   rc = qgemm_tc_grouped_launch(down, 1, xt2, xs2, L.max_tiles, L.n_tile, tile_expert, dy, stream);

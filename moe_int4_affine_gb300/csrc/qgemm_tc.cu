@@ -47,7 +47,6 @@ constexpr int kMaxStages = 4;
 constexpr int kAccCols = 256;                // tensor memory: columns 0..255 accumulator, then per stage
 constexpr int kACols = kGK / 2;              //   32 columns (64 fp16 per lane) of A per group,
 constexpr int kAStage = 2 * kACols;          //   two groups per stage
-constexpr int kTmemCols = 512;
 // weight ring, per pair of groups: codes [2 chunks][256 threads][16 B], then scale and bias words
 constexpr int kWStageBytes = kProducers * 32 + kProducers * 8;
 constexpr int kSmemBudget = 220 * 1024;
@@ -185,8 +184,13 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2, uint32_t b2) 
   return r;
 }
 
-template <int WRING>
+// TMEMC: tensor-memory columns the CTA allocates.  512: accumulator in columns 0-255 (N <= 256), A
+// stages from column 256 (up to four).  256: accumulator in columns 0-63 (N <= 64), up to three A
+// stages from column 64 -- two such CTAs share an SM (with at most half its shared memory each), so
+// one CTA's start and epilogue overlap the other's main loop (many short tiles: grouped mode).
+template <int WRING, int TMEMC>
 __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_constant__ TcArgs a) {
+  constexpr uint32_t kABase = TMEMC == 512 ? (uint32_t)kAccCols : 64u;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     }
     __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
+                 "r"(TMEMC)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
           v[4 * ch + 2] = d.z;
           v[4 * ch + 3] = d.w;
         }
-        tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kAccCols + kAStage * s + kACols * h), v);
+        tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (kABase + (uint32_t)(kAStage * s + kACols * h)), v);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       tc_fence_before();
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       }
       tc_fence_after();  // the producers' tensor-memory stores are complete
       const uint64_t db = db0 + (uint64_t)(s * dstage);
-      const uint32_t ta = tmem + (uint32_t)(kAccCols + kAStage * s);
+      const uint32_t ta = tmem + kABase + (uint32_t)(kAStage * s);
       const int ng = min(2, nk - 2 * j);
       for (int gi = 0; gi < ng; ++gi) {
 #pragma unroll
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEMC) : "memory");
   }
 }
 
@@ -396,22 +400,25 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 // One CTA per token row n < n_tiles * n_tile.  Row n of tile n / n_tile, group kc: 128 bytes at
 // ((tile * nk + kc) * n_tile + n % n_tile) * 128, the 16-byte chunk j (columns 8j .. 8j + 7 of the
 // group) at position j ^ (n % 8), its eight values in the column order 0, 4, 1, 5, 2, 6, 3, 7 (the
-// order the dequantized weights use).  Rows n >= T are zero.  With a row map, row n of the tiles is
-// row rowmap[n] of X (< 0: a zero row), so that the tiles hold the tokens grouped by expert.
+// order the dequantized weights use).  Rows n >= T are zero.  Grouped mode (rowpos != null): block
+// i writes row rowpos[i] (< 0: nothing) from X row i / kdiv -- the (token, slot) pairs placed in
+// their experts' tiles; the tiles' padding rows are left unwritten (each MMA output column depends
+// on its own token row only, and padding outputs are never read).
 constexpr int kPrepThreads = 256;
 constexpr int kPrepMaxChunks = 16;  // 16-byte chunks per thread: in <= 16 * 256 * 8 = 32768
 
 __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_kernel(const uint16_t* __restrict__ X, int T, int in,
-                                                                   int n_tile, const int* __restrict__ rowmap,
-                                                                   uint8_t* __restrict__ xt,
+                                                                   int n_tile, const int* __restrict__ rowpos,
+                                                                   int kdiv, uint8_t* __restrict__ xt,
                                                                    float* __restrict__ xs) {
   __shared__ uint32_t red[kPrepThreads / 32];
-  const int n = blockIdx.x;
   const int nk = in / 64, nch = in / 8;
   pdl_trigger();
   pdl_wait();
-  const int src = rowmap ? rowmap[n] : n;
-  const bool live = src >= 0 && src < T;
+  const int n = rowpos ? rowpos[blockIdx.x] : (int)blockIdx.x;
+  if (n < 0) return;  // (uniform per block)
+  const int src = rowpos ? (int)blockIdx.x / kdiv : n;
+  const bool live = src < T;
   const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? src : 0) * in);
   // one round of loads; the largest |x| from the bit patterns (|bf16| bits are ordered like values)
   uint4 raw[kPrepMaxChunks];
@@ -461,10 +468,10 @@ __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_kernel(const uint16_t
   }
 }
 
-// The down projection's token tiles in grouped (MoE) mode: row n is h = silu(G[n]) * U[n] (fp32
-// [rows][in], the grouped gate/up outputs), scaled by a power of two and stored as above; rows
-// with rowmap[n] < 0 (tile padding) are zero.  Two passes over the row (its largest |h|, then the
-// conversion; the second reads hit L2), so in is not limited by registers.
+// The down projection's token tiles in grouped (MoE) mode: block i makes row n = rowpos[i] (< 0:
+// nothing), h = silu(G[n]) * U[n] (fp32 [rows][in], the grouped gate/up outputs), scaled by a power
+// of two and stored as above.  Two passes over the row (its largest |h|, then the conversion; the
+// second reads hit L2), so in is not limited by registers.
 __device__ __forceinline__ void swiglu8(const float* __restrict__ G, const float* __restrict__ U, size_t off,
                                         float (&h)[8]) {
   const float4* g4 = reinterpret_cast<const float4*>(G + off);
@@ -478,15 +485,16 @@ __device__ __forceinline__ void swiglu8(const float* __restrict__ G, const float
 
 __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_swiglu_kernel(const float* __restrict__ G,
                                                                           const float* __restrict__ U, int in,
-                                                                          int n_tile, const int* __restrict__ rowmap,
+                                                                          int n_tile, const int* __restrict__ rowpos,
                                                                           uint8_t* __restrict__ xt,
                                                                           float* __restrict__ xs) {
   __shared__ float red[kPrepThreads / 32];
-  const int n = blockIdx.x;
   const int nk = in / 64, nch = in / 8;
   pdl_trigger();
   pdl_wait();
-  const bool live = rowmap[n] >= 0;
+  const int n = rowpos[blockIdx.x];
+  if (n < 0) return;  // (uniform per block)
+  const bool live = true;
   const size_t row0 = (size_t)n * in;
   float mx = 0.f;
   if (live) {
@@ -528,6 +536,7 @@ __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_swiglu_kernel(const f
 struct TcPlan {
   int n_tile, n_tiles, stages, wring;
   size_t smem;
+  int tmem;  // tensor-memory columns per CTA (512, or 256 for two CTAs per SM)
 };
 
 // Pipeline depth and weight ring for a token tile of n_tile rows (a multiple of 16, <= kMaxN).
@@ -542,6 +551,24 @@ TcPlan tc_plan_ntile(int n_tile) {
   p.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - fixed - 2 * (size_t)kWStageBytes) / stage);
   const size_t left = kSmemBudget - fixed - (size_t)p.stages * stage;
   p.wring = left >= 16 * (size_t)kWStageBytes ? 16 : left >= 8 * (size_t)kWStageBytes ? 8 : left >= 4 * (size_t)kWStageBytes ? 4 : 2;
+  p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
+  p.tmem = 512;
+  return p;
+}
+
+// Two CTAs per SM (grouped mode, n_tile <= 64): 256 tensor-memory columns (three A stages) and at
+// most kSmemHalf bytes of shared memory each.
+constexpr size_t kSmemHalf = 110 * 1024;
+TcPlan tc_plan_ntile_pair(int n_tile) {
+  TcPlan p{};
+  p.n_tile = n_tile;
+  p.n_tiles = 1;
+  p.tmem = 256;
+  const size_t stage = 2 * (size_t)n_tile * 128;
+  const size_t fixed = 1024 + 64 + 8 * 32;
+  p.stages = (int)std::min<size_t>(3, (kSmemHalf - fixed - 2 * (size_t)kWStageBytes) / stage);
+  const size_t left = kSmemHalf - fixed - (size_t)p.stages * stage;
+  p.wring = left >= 8 * (size_t)kWStageBytes ? 8 : left >= 4 * (size_t)kWStageBytes ? 4 : 2;
   p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
   return p;
 }
@@ -558,17 +585,30 @@ int tc_launch(const TcArgs& a, const TcPlan& p, dim3 grid, cudaStream_t stream) 
   auto go = [&](auto k) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
       return (int)QG_ELAUNCH;
+    // the largest shared-memory carve-out, so that two half-size CTAs fit on an SM
+    if (cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+      return (int)QG_ELAUNCH;
     return launch(k, grid, dim3(kThreads), p.smem, stream, a);
   };
+  if (p.tmem == 256) {
+    switch (p.wring) {
+      case 8:
+        return go(qgemm_tc_kernel<8, 256>);
+      case 4:
+        return go(qgemm_tc_kernel<4, 256>);
+      default:
+        return go(qgemm_tc_kernel<2, 256>);
+    }
+  }
   switch (p.wring) {
     case 16:
-      return go(qgemm_tc_kernel<16>);
+      return go(qgemm_tc_kernel<16, 512>);
     case 8:
-      return go(qgemm_tc_kernel<8>);
+      return go(qgemm_tc_kernel<8, 512>);
     case 4:
-      return go(qgemm_tc_kernel<4>);
+      return go(qgemm_tc_kernel<4, 512>);
     default:
-      return go(qgemm_tc_kernel<2>);
+      return go(qgemm_tc_kernel<2, 512>);
   }
 }
 
@@ -595,7 +635,7 @@ int qgemm_tc_launch_multi(const qg_int4_weight* w, int n, const uint16_t* X, int
   uint8_t* xt = static_cast<uint8_t*>(ws);
   float* xs = reinterpret_cast<float*>(xt + xt_bytes);
   int rc = launch(qgemm_prep_kernel, dim3((unsigned)rows), dim3(kPrepThreads), 0, stream, X, T, w[0].in, p.n_tile,
-                  static_cast<const int*>(nullptr), xt, xs);
+                  static_cast<const int*>(nullptr), 1, xt, xs);
   if (rc != QG_OK) return rc;
   TcArgs a{};
   int tiles = 0;
@@ -619,22 +659,24 @@ int qgemm_tc_launch(const qg_int4_weight* w, const uint16_t* X, int T, float* Y,
   return qgemm_tc_launch_multi(w, 1, X, T, &Y, ws, ws_bytes, stream);
 }
 
-int qgemm_prep_rows_launch(const uint16_t* X, int T, int in, const int* rowmap, int rows, int n_tile, uint8_t* xt,
-                           float* xs, cudaStream_t stream) {
-  return launch(qgemm_prep_kernel, dim3((unsigned)rows), dim3(kPrepThreads), 0, stream, X, T, in, n_tile, rowmap, xt,
-                xs);
+constexpr bool g_tc_pair = true;  // grouped mode: two CTAs per SM for token tiles of at most 64 rows
+
+int qgemm_prep_pairs_launch(const uint16_t* X, int T, int in, const int* rowpos, int npairs, int k, int n_tile,
+                            uint8_t* xt, float* xs, cudaStream_t stream) {
+  return launch(qgemm_prep_kernel, dim3((unsigned)npairs), dim3(kPrepThreads), 0, stream, X, T, in, n_tile, rowpos, k,
+                xt, xs);
 }
 
-int qgemm_prep_swiglu_launch(const float* G, const float* U, int in, const int* rowmap, int rows, int n_tile,
+int qgemm_prep_swiglu_launch(const float* G, const float* U, int in, const int* rowpos, int npairs, int n_tile,
                              uint8_t* xt, float* xs, cudaStream_t stream) {
-  return launch(qgemm_prep_swiglu_kernel, dim3((unsigned)rows), dim3(kPrepThreads), 0, stream, G, U, in, n_tile,
-                rowmap, xt, xs);
+  return launch(qgemm_prep_swiglu_kernel, dim3((unsigned)npairs), dim3(kPrepThreads), 0, stream, G, U, in, n_tile,
+                rowpos, xt, xs);
 }
 
 int qgemm_tc_grouped_launch(const qg_int4_weight* w, int n, const uint8_t* xt, const float* xs, int n_tiles,
                             int n_tile, const int* tile_expert, float* const* Y, cudaStream_t stream) {
   if (n < 1 || n > kTcMaxMats || n_tile < 16 || n_tile > kMaxN || n_tile % 16 != 0 || n_tiles < 1) return QG_EINVAL;
-  const TcPlan p = tc_plan_ntile(n_tile);
+  const TcPlan p = n_tile <= 64 && g_tc_pair ? tc_plan_ntile_pair(n_tile) : tc_plan_ntile(n_tile);
   TcArgs a{};
   int tiles = 0;
   for (int i = 0; i < n; ++i) {

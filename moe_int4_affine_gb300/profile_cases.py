@@ -5,6 +5,7 @@
     python -m moe_int4_affine_gb300.profile_cases moe        # router + MoE gather (128 experts, top 8)
     python -m moe_int4_affine_gb300.profile_cases qgemm T    # dequant-GEMM 17408 x 5120, T tokens
     python -m moe_int4_affine_gb300.profile_cases quant B K  # encode 17408 x 5120 weights (K = bf16 | f32) to B bits
+    python -m moe_int4_affine_gb300.profile_cases moe_prefill T  # MoE layer for T tokens (128 experts, top 8)
 
 Each case builds its seeded synthetic inputs (a few hundred MB at most on the device), runs the
 calls three times and prints "ok <device status>".  Nothing is timed here.
@@ -64,6 +65,15 @@ def main(argv=None) -> int:
         w = qg.to_device(I.bf16_normal(0, I.TID_W, shape) if kind == "bf16" else I.f32_normal(0, I.TID_W, shape))
         for _ in range(reps):
             qg.quantize_affine_q64a(w, bits)
+    elif case == "moe_prefill":
+        T = int(argv[1]) if len(argv) > 1 else 256
+        g = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_GATE, 768, 2048, n_mat=128))
+        u = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_UP, 768, 2048, n_mat=128))
+        d = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_DOWN, 2048, 768, n_mat=128))
+        X = qg.to_device(I.bf16_normal(0, I.TID_X, (T, 2048)))
+        r = qg.to_device(I.bf16_normal(0, I.TID_RESID, (T, 2048)))
+        for i in range(reps):
+            qg.moe_prefill_int4(qg.to_device(I.f32_normal(i, I.TID_LOGITS, (T, 128))), g, u, d, X, r, k=8)
     else:
         print(f"unknown case {case!r}", file=sys.stderr)
         return 2
