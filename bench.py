@@ -402,6 +402,26 @@ def measure_configs(qg, I, dev, stream):
                                   P(pk.data_ptr()), P(wsb.data_ptr()), wsb.numel(), s)
     us = tl(moe_fused, 100)
     res["c3_moe_layer_T1_fused_router"] = dict(gb(nbytes, us), kernels=2, call="moe_layer_int4", l2=l2)
+
+    # next row N2: the MoE layer for T tokens (prefill), tokens grouped by expert on the tensor cores
+    for T in (32, 256):
+        lgT = [qg.to_device(I.f32_normal(i, I.TID_LOGITS, (T, E)), dev) for i in range(4)]
+        XT = qg.to_device(I.bf16_normal(0, I.TID_X, (T, HID)), dev)
+        RT = qg.to_device(I.bf16_normal(0, I.TID_RESID, (T, HID)), dev)
+        YT = torch.empty((T, HID), dtype=torch.float32, device=dev)
+        iT = torch.empty((T, K), dtype=torch.int32, device=dev)
+        pT = torch.empty((T, K), dtype=torch.float32, device=dev)
+        wsT = torch.empty(qg.qg_workspace_bytes(qg.QG_OP_MOE_PREFILL, d, T), dtype=torch.uint8, device=dev)
+        us = tl(lambda i: lib.moe_prefill_int4(P(lgT[i % 4].data_ptr()), T, 1, byref(g.struct), byref(u.struct),
+                                               byref(d.struct), K, P(XT.data_ptr()), P(RT.data_ptr()),
+                                               P(YT.data_ptr()), P(iT.data_ptr()), P(pT.data_ptr()),
+                                               P(wsT.data_ptr()), wsT.numel(), s), 20)
+        hit = int(torch.unique(iT).numel())  # experts whose weights the last call read
+        nbytes = hit * 3 * weight_bytes(INTER, HID) + T * HID * (2 + 2 + 4) + T * E * 4
+        tf = 2.0 * T * K * 3 * INTER * HID / us / 1e6
+        res[f"n2_moe_prefill_T{T}"] = dict(gb(nbytes, us), call="moe_prefill_int4", launches=7, experts_hit=hit,
+                                          TFLOPs=round(tf, 1), l2=f"{hit} experts' weights ({hit * 3 * weight_bytes(INTER, HID) / 1e6:.0f} MB) per call")
+        del lgT, XT, RT, YT, iT, pT, wsT
     del g, u, d
 
     # next rows: the RMSNorm-fused gate/up pair (the FFN input after its norm) against the plain

@@ -207,8 +207,8 @@ int moe_layer_int4(const float *logits, int renorm, const qg_int4_weight *gate, 
                    uint32_t *idx, float *p, void *workspace, size_t ws_bytes, void *stream);
 
 /*
- * moe_prefill_int4 -- the MoE layer for T tokens at once (prefill; [FFAI#14] names the MoE prefill
- * gather GEMM: tokens sorted by expert, grouped tiles, unpermuted back):
+ * moe_prefill_int4 -- the MoE layer for T tokens at once (prefill; [FFAI#9] "moeGatherDequantGemmInt4",
+ * "mt_moe_gather_qmm_int4": rows sorted by expert with CSR expert offsets, for prefill):
  *   for token t: (idx[t], p[t]) = moe_router_topk(logits[t], renorm);
  *     for slot s: e = idx[t][s]; h = silu(Wg[e] X[t]) * (Wu[e] X[t]); d_s = Wd[e] h
  *     Y[t][i] = residual[t][i] + sum_s p[t][s] d_s[i]            (slot order)
