@@ -585,8 +585,9 @@ int tc_launch(const TcArgs& a, const TcPlan& p, dim3 grid, cudaStream_t stream) 
   auto go = [&](auto k) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
       return (int)QG_ELAUNCH;
-    // the largest shared-memory carve-out, so that two half-size CTAs fit on an SM
-    if (cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    // two CTAs per SM: the largest shared-memory carve-out, so that both half-size CTAs fit (the
+    // one-CTA kernel keeps the driver's choice, which leaves more L1 for the scale/bias loads)
+    if (p.tmem == 256 && cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
       return (int)QG_ELAUNCH;
     return launch(k, grid, dim3(kThreads), p.smem, stream, a);
   };
