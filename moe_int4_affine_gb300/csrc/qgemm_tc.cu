@@ -47,8 +47,9 @@ constexpr int kMaxStages = 4;
 constexpr int kAccCols = 256;                // tensor memory: columns 0..255 accumulator, then per stage
 constexpr int kACols = kGK / 2;              //   32 columns (64 fp16 per lane) of A per group,
 constexpr int kAStage = 2 * kACols;          //   two groups per stage
-// weight ring, per pair of groups: codes [2 chunks][256 threads][16 B], then scale and bias words
-constexpr int kWStageBytes = kProducers * 32 + kProducers * 8;
+// weight ring entry (one group per producer thread): the codes, plus the scale and bias words when
+// they come through the ring (SBREG = false) rather than 16-byte chunks held in registers
+__host__ __device__ constexpr int wstage_bytes(bool sbreg) { return sbreg ? kProducers * 32 : kProducers * 40; }
 constexpr int kSmemBudget = 220 * 1024;
 
 // One weight of a (multi-projection) call; its 128-row tiles are grid columns tile0, tile0 + 1, ...
@@ -141,15 +142,15 @@ __device__ __forceinline__ void cp16(uint32_t dst, const void* src, uint32_t byt
 __device__ __forceinline__ void cp4(uint32_t dst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // fp16x2 arithmetic on raw bits
@@ -188,9 +189,12 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2, uint32_t b2) 
 // stages from column 256 (up to four).  256: accumulator in columns 0-63 (N <= 64), up to three A
 // stages from column 64 -- two such CTAs share an SM (with at most half its shared memory each), so
 // one CTA's start and epilogue overlap the other's main loop (many short tiles: grouped mode).
-template <int WRING, int TMEMC>
-__global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_constant__ TcArgs a) {
+// SBREG: scales and biases as 16-byte chunks in registers (faster for token tiles of 128 and more:
+// T = 256 54.3 -> 49.6 us) or as 4-byte copies through the weight ring (faster for small tiles).
+template <int WRING, int TMEMC, bool SBREG>
+__global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kernel(const __grid_constant__ TcArgs a) {
   constexpr uint32_t kABase = TMEMC == 512 ? (uint32_t)kAccCols : 64u;
+  constexpr int kWStageBytes = wstage_bytes(SBREG);
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -259,24 +263,58 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     const int my_n = (nk - h + 1) / 2;  // groups of this thread
     // group 2 jj + h: codes advance by 16 words per jj, the scale / bias index by 2
     const uint32_t* wp = mt.packed + (size_t)rowc * (a.in / 8) + (size_t)h * 8;
-    const size_t e0 = (size_t)rowc * ngs + h;
+    const size_t e0 = (size_t)rowc * ngs + h;  // scale / bias element of this thread's group 0
     const size_t n_sb = (size_t)mt.out * ngs;
-    const int odd = (int)(e0 & 1);  // which half of the copied 32-bit words holds s and b
     const uint32_t wcode = wring + (uint32_t)tid * 16;  // chunk c at + c * kProducers * 16
-    const uint32_t wsb = wring + kProducers * 32 + (uint32_t)tid * 8;
+    const uint32_t wsb = wring + kProducers * 32 + (uint32_t)tid * 8;  // (SBREG = false)
+    const int odd = (int)(e0 & 1);  // which half of a copied 32-bit word holds s and b
     auto wissue = [&](int jj) {  // this thread's copies for its group jj (an empty group past the end)
       if (jj < my_n) {
         const uint32_t g = (uint32_t)(jj % WRING) * kWStageBytes;
         const uint32_t* src = wp + (size_t)jj * 16;
         cp16(wcode + g, src, rv ? 16u : 0u);
         cp16(wcode + g + kProducers * 16, src + 4, rv ? 16u : 0u);
-        const size_t e = e0 + 2 * (size_t)jj, eo = e & ~(size_t)1;
-        const uint32_t nb = rv ? (eo + 1 < n_sb ? 4u : 2u) : 0u;
-        cp4(wsb + g, mt.scales + eo, nb);
-        cp4(wsb + g + 4, mt.biases + eo, nb);
+        if constexpr (!SBREG) {
+          const size_t e = e0 + 2 * (size_t)jj, eo = e & ~(size_t)1;
+          const uint32_t nb = rv ? (eo + 1 < n_sb ? 4u : 2u) : 0u;
+          cp4(wsb + g, mt.scales + eo, nb);
+          cp4(wsb + g + 4, mt.biases + eo, nb);
+        }
       }
       cp_commit();
     };
+    // Scales and biases: 16-byte chunks of 8 consecutive elements (4 of this thread's groups) held
+    // in registers, the next chunk loaded while the current one is used.  At the array's end (or
+    // for arrays not 16-byte aligned) element by element, nothing read past the end.
+    const bool sb_vec = ((reinterpret_cast<uintptr_t>(mt.scales) | reinterpret_cast<uintptr_t>(mt.biases)) & 15u) == 0;
+    auto ld_chunk = [&](size_t q, uint4& sc, uint4& bc) {
+      if (sb_vec && 8 * q + 8 <= n_sb) {
+        sc = __ldg(reinterpret_cast<const uint4*>(mt.scales) + q);
+        bc = __ldg(reinterpret_cast<const uint4*>(mt.biases) + q);
+      } else {
+        uint32_t s4[4] = {0u, 0u, 0u, 0u}, b4[4] = {0u, 0u, 0u, 0u};
+        for (int i = 0; i < 8; ++i) {
+          const size_t el = 8 * q + (size_t)i;
+          if (el < n_sb) {
+            s4[i >> 1] |= (uint32_t)__ldg(mt.scales + el) << (16 * (i & 1));
+            b4[i >> 1] |= (uint32_t)__ldg(mt.biases + el) << (16 * (i & 1));
+          }
+        }
+        sc = make_uint4(s4[0], s4[1], s4[2], s4[3]);
+        bc = make_uint4(b4[0], b4[1], b4[2], b4[3]);
+      }
+    };
+    auto pick16 = [](const uint4& v, int o) {  // element o (0..7) of a chunk
+      const int w = o >> 1;
+      const uint32_t x = w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+      return (o & 1) ? x >> 16 : x & 0xFFFFu;
+    };
+    size_t qc = e0 >> 3;  // the chunk in s_cur / b_cur
+    uint4 s_cur{}, b_cur{}, s_nxt{}, b_nxt{};
+    if constexpr (SBREG) {
+      ld_chunk(qc, s_cur, b_cur);
+      ld_chunk(qc + 1, s_nxt, b_nxt);
+    }
 #pragma unroll 1
     for (int jj = 0; jj < WRING - 1; ++jj) wissue(jj);
 
@@ -291,9 +329,22 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       if (h < ng) {           // (uniform per warp)
         const uint32_t g = (uint32_t)(j % WRING) * kWStageBytes;
         const uint4 c0 = lds128(wcode + g), c1 = lds128(wcode + g + kProducers * 16);
-        const uint32_t sw = lds32(wsb + g), bw = lds32(wsb + g + 4);
-        const uint32_t s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
-        const uint32_t b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
+        uint32_t s2, b2;
+        if constexpr (SBREG) {
+          const size_t e = e0 + 2 * (size_t)j;  // (advances 2 per stage: at most one chunk)
+          if ((e >> 3) != qc) {
+            s_cur = s_nxt;
+            b_cur = b_nxt;
+            ++qc;
+            ld_chunk(qc + 1, s_nxt, b_nxt);
+          }
+          s2 = bf16_to_f16x2(pick16(s_cur, (int)(e & 7)));
+          b2 = bf16_to_f16x2(pick16(b_cur, (int)(e & 7)));
+        } else {
+          const uint32_t sw = lds32(wsb + g), bw = lds32(wsb + g + 4);
+          s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
+          b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
+        }
         const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
         uint32_t v[32];  // column 4 ch + i: the fp16 pair i of 8-column chunk ch
 #pragma unroll
@@ -536,7 +587,8 @@ __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_swiglu_kernel(const f
 struct TcPlan {
   int n_tile, n_tiles, stages, wring;
   size_t smem;
-  int tmem;  // tensor-memory columns per CTA (512, or 256 for two CTAs per SM)
+  int tmem;    // tensor-memory columns per CTA (512, or 256 for two CTAs per SM)
+  bool sbreg;  // scales and biases in registers (token tiles of 128 and more, one CTA per SM)
 };
 
 // Pipeline depth and weight ring for a token tile of n_tile rows (a multiple of 16, <= kMaxN).
@@ -544,6 +596,8 @@ TcPlan tc_plan_ntile(int n_tile) {
   TcPlan p{};
   p.n_tile = n_tile;
   p.n_tiles = 1;
+  p.sbreg = n_tile >= 128;
+  const size_t kWStageBytes = (size_t)wstage_bytes(p.sbreg);
   const size_t stage = 2 * (size_t)p.n_tile * 128;  // token tiles of two groups
   const size_t fixed = 1024 + 64 + 8 * 32;          // alignment slack, barriers, slot, flag
   // stages: at most kMaxStages (tensor-memory columns for A); the rest of shared memory goes to the
@@ -563,12 +617,16 @@ TcPlan tc_plan_ntile_pair(int n_tile) {
   TcPlan p{};
   p.n_tile = n_tile;
   p.n_tiles = 1;
+  p.sbreg = false;
+  const size_t kWStageBytes = (size_t)wstage_bytes(false);
   p.tmem = 256;
   const size_t stage = 2 * (size_t)n_tile * 128;
   const size_t fixed = 1024 + 64 + 8 * 32;
   p.stages = (int)std::min<size_t>(3, (kSmemHalf - fixed - 2 * (size_t)kWStageBytes) / stage);
   const size_t left = kSmemHalf - fixed - (size_t)p.stages * stage;
-  p.wring = left >= 8 * (size_t)kWStageBytes ? 8 : left >= 4 * (size_t)kWStageBytes ? 4 : 2;
+  // a four-group weight ring: less shared memory leaves more L1 for the scale/bias loads (faster
+  // than eight groups: MoE prefill T = 256, 232.7 -> 219.0 us)
+  p.wring = left >= 4 * (size_t)kWStageBytes ? 4 : 2;
   p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
   return p;
 }
@@ -585,31 +643,42 @@ int tc_launch(const TcArgs& a, const TcPlan& p, dim3 grid, cudaStream_t stream) 
   auto go = [&](auto k) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
       return (int)QG_ELAUNCH;
-    // two CTAs per SM: the largest shared-memory carve-out, so that both half-size CTAs fit (the
-    // one-CTA kernel keeps the driver's choice, which leaves more L1 for the scale/bias loads)
-    if (p.tmem == 256 && cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    // two CTAs per SM: a shared-memory carve-out that just fits both (the rest stays L1, which the
+    // scale/bias loads use); the one-CTA kernel keeps the driver's choice
+    const int carve = (int)std::min<size_t>(100, (2 * p.smem + 2048) * 100 / (228 * 1024) + 1);
+    if (p.tmem == 256 && cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, carve) != cudaSuccess)
       return (int)QG_ELAUNCH;
     return launch(k, grid, dim3(kThreads), p.smem, stream, a);
   };
   if (p.tmem == 256) {
     switch (p.wring) {
-      case 8:
-        return go(qgemm_tc_kernel<8, 256>);
       case 4:
-        return go(qgemm_tc_kernel<4, 256>);
+        return go(qgemm_tc_kernel<4, 256, false>);
       default:
-        return go(qgemm_tc_kernel<2, 256>);
+        return go(qgemm_tc_kernel<2, 256, false>);
+    }
+  }
+  if (p.sbreg) {
+    switch (p.wring) {
+      case 16:
+        return go(qgemm_tc_kernel<16, 512, true>);
+      case 8:
+        return go(qgemm_tc_kernel<8, 512, true>);
+      case 4:
+        return go(qgemm_tc_kernel<4, 512, true>);
+      default:
+        return go(qgemm_tc_kernel<2, 512, true>);
     }
   }
   switch (p.wring) {
     case 16:
-      return go(qgemm_tc_kernel<16, 512>);
+      return go(qgemm_tc_kernel<16, 512, false>);
     case 8:
-      return go(qgemm_tc_kernel<8, 512>);
+      return go(qgemm_tc_kernel<8, 512, false>);
     case 4:
-      return go(qgemm_tc_kernel<4, 512>);
+      return go(qgemm_tc_kernel<4, 512, false>);
     default:
-      return go(qgemm_tc_kernel<2, 512>);
+      return go(qgemm_tc_kernel<2, 512, false>);
   }
 }
 
