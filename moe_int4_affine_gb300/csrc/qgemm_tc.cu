@@ -605,9 +605,10 @@ TcPlan tc_plan_ntile(int n_tile) {
   p.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - fixed - 2 * (size_t)kWStageBytes) / stage);
   const size_t left = kSmemBudget - fixed - (size_t)p.stages * stage;
   p.wring = left >= 16 * (size_t)kWStageBytes ? 16 : left >= 8 * (size_t)kWStageBytes ? 8 : left >= 4 * (size_t)kWStageBytes ? 4 : 2;
-  // scale/bias copies through L1 (small tiles): an eight-group ring leaves more shared memory to
-  // L1 (17408x5120 T = 32: 39.5 -> 37.3 us against sixteen groups)
-  if (!p.sbreg && p.wring > 8) p.wring = 8;
+  // scale/bias copies through L1 (tiles of 32 to 64 tokens): an eight-group ring leaves more shared
+  // memory to L1 (17408x5120 T = 32: 39.5 -> 37.3 us against sixteen groups; 16-token tiles keep
+  // sixteen: T = 8 39.3 us against 47.1 with eight)
+  if (!p.sbreg && n_tile >= 32 && p.wring > 8) p.wring = 8;
   p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
   p.tmem = 512;
   return p;
