@@ -46,7 +46,6 @@ constexpr int kThreads = kProducers + 64;
 constexpr int kMaxStages = 4;
 constexpr int kAccCols = 256;                // tensor memory: columns 0..255 accumulator, then per stage
 constexpr int kACols = kGK / 2;              //   32 columns (64 fp16 per lane) of A per group,
-constexpr int kAStage = 2 * kACols;          //   two groups per stage
 // weight ring entry (one group per producer thread): the codes, plus the scale and bias words when
 // they come through the ring (SBREG = false) rather than 16-byte chunks held in registers
 __host__ __device__ constexpr int wstage_bytes(bool sbreg) { return sbreg ? kProducers * 32 : kProducers * 40; }
@@ -191,9 +190,14 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2, uint32_t b2) 
 // one CTA's start and epilogue overlap the other's main loop (many short tiles: grouped mode).
 // SBREG: scales and biases as 16-byte chunks in registers (faster for token tiles of 128 and more:
 // T = 256 54.3 -> 49.6 us) or as 4-byte copies through the weight ring (faster for small tiles).
-template <int WRING, int TMEMC, bool SBREG>
+// GPS: quantization groups per pipeline stage (K = 64 GPS).  Four halve the number of stage
+// hand-overs for small token tiles (accumulator N <= 64 in columns 0-63, up to three A stages of 128
+// columns from column 64); two otherwise.
+template <int WRING, int TMEMC, bool SBREG, int GPS>
 __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kernel(const __grid_constant__ TcArgs a) {
-  constexpr uint32_t kABase = TMEMC == 512 ? (uint32_t)kAccCols : 64u;
+  static_assert(GPS == 2 || (GPS == 4 && TMEMC == 512), "four groups per stage: one-CTA kernel only");
+  constexpr uint32_t kABase = (TMEMC == 512 && GPS == 2) ? (uint32_t)kAccCols : 64u;
+  constexpr uint32_t kAStageT = (uint32_t)(GPS * kACols);  // A columns of one stage
   constexpr int kWStageBytes = wstage_bytes(SBREG);
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
   uint8_t* basep = smem_raw + (base - raw);
   const int S = a.stages;
   const uint32_t btile = (uint32_t)a.n_tile * 128u;  // token tile of one group (the stage)
-  const uint32_t stage_bytes = 2 * btile;  // the token tiles of a stage's two groups
+  const uint32_t stage_bytes = GPS * btile;  // the token tiles of a stage's groups
   const uint32_t wring = base + (uint32_t)S * stage_bytes;  // weight staging ring
   // full[s]: the producers' A columns; bfull[s]: the token tile's bytes; empty[s]: the stage's MMAs done
   uint64_t* full = reinterpret_cast<uint64_t*>(basep + (size_t)S * stage_bytes + (size_t)WRING * kWStageBytes);
@@ -226,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
   const int m0 = ((int)blockIdx.x - mt.tile0) * kBM;
   const int tile = blockIdx.y, n0 = tile * a.n_tile;
   const int nk = a.in / kGK;         // groups
-  const int nst = (nk + 1) / 2;      // pipeline stages (two groups each)
+  const int nst = (nk + GPS - 1) / GPS;  // pipeline stages (GPS groups each)
 
   if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -318,46 +322,51 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
 #pragma unroll 1
     for (int jj = 0; jj < WRING - 1; ++jj) wissue(jj);
 
-    for (int j = 0; j < nst; ++j) {  // stage j: groups 2 j (warp group 0) and 2 j + 1 (warp group 1)
+    for (int j = 0; j < nst; ++j) {  // stage j: groups GPS j + 2 q + h, q < GPS / 2 (thread group jj)
       const int s = j % S;
       if (j >= S && !mbar_wait(empty + s, (uint32_t)(j / S - 1) & 1u)) *abort_flag = 1;
       if (*abort_flag) break;
       tc_fence_after();  // the MMAs that read this stage's A columns have completed
-      const int ng = min(2, nk - 2 * j);  // groups in this stage
-      wissue(j + WRING - 1);  // (this thread's group 2 j + h is its j-th)
-      cp_wait<WRING - 1>();   // group j of this thread has landed
-      if (h < ng) {           // (uniform per warp)
-        const uint32_t g = (uint32_t)(j % WRING) * kWStageBytes;
-        const uint4 c0 = lds128(wcode + g), c1 = lds128(wcode + g + kProducers * 16);
-        uint32_t s2, b2;
-        if constexpr (SBREG) {
-          const size_t e = e0 + 2 * (size_t)j;  // (advances 2 per stage: at most one chunk)
-          if ((e >> 3) != qc) {
-            s_cur = s_nxt;
-            b_cur = b_nxt;
-            ++qc;
-            ld_chunk(qc + 1, s_nxt, b_nxt);
-          }
-          s2 = bf16_to_f16x2(pick16(s_cur, (int)(e & 7)));
-          b2 = bf16_to_f16x2(pick16(b_cur, (int)(e & 7)));
-        } else {
-          const uint32_t sw = lds32(wsb + g), bw = lds32(wsb + g + 4);
-          s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
-          b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
-        }
-        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint32_t v[32];  // column 4 ch + i: the fp16 pair i of 8-column chunk ch
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 d = dequant8(cw[ch], s2, b2);
-          v[4 * ch + 0] = d.x;
-          v[4 * ch + 1] = d.y;
-          v[4 * ch + 2] = d.z;
-          v[4 * ch + 3] = d.w;
+      for (int q = 0; q < GPS / 2; ++q) {
+        const int jj = (GPS / 2) * j + q;  // this thread's group 2 jj + h (its jj-th)
+        wissue(jj + WRING - 1);
+        cp_wait<WRING - 1>();  // group jj of this thread has landed
+        if (2 * jj + h < nk) {  // (uniform per warp)
+          const uint32_t g = (uint32_t)(jj % WRING) * kWStageBytes;
+          const uint4 c0 = lds128(wcode + g), c1 = lds128(wcode + g + kProducers * 16);
+          uint32_t s2, b2;
+          if constexpr (SBREG) {
+            const size_t e = e0 + 2 * (size_t)jj;  // (advances 2 per group: at most one chunk)
+            if ((e >> 3) != qc) {
+              s_cur = s_nxt;
+              b_cur = b_nxt;
+              ++qc;
+              ld_chunk(qc + 1, s_nxt, b_nxt);
+            }
+            s2 = bf16_to_f16x2(pick16(s_cur, (int)(e & 7)));
+            b2 = bf16_to_f16x2(pick16(b_cur, (int)(e & 7)));
+          } else {
+            const uint32_t sw = lds32(wsb + g), bw = lds32(wsb + g + 4);
+            s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
+            b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
+          }
+          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint32_t v[32];  // column 4 ch + i: the fp16 pair i of 8-column chunk ch
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 d = dequant8(cw[ch], s2, b2);
+            v[4 * ch + 0] = d.x;
+            v[4 * ch + 1] = d.y;
+            v[4 * ch + 2] = d.z;
+            v[4 * ch + 3] = d.w;
+          }
+          tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) +
+                        (kABase + kAStageT * (uint32_t)s + (uint32_t)(kACols * (2 * q + h))),
+                    v);
         }
-        tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (kABase + (uint32_t)(kAStage * s + kACols * h)), v);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(full + s);
@@ -372,9 +381,9 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
         const int s = j % S;
         if (j >= S && !mbar_wait(empty + s, (uint32_t)(j / S - 1) & 1u)) *abort_flag = 1;
         if (*abort_flag) break;
-        const uint32_t bytes = (uint32_t)min(2, nk - 2 * j) * btile;
+        const uint32_t bytes = (uint32_t)min(GPS, nk - GPS * j) * btile;
         mbar_arrive_expect_tx(bfull + s, bytes);
-        bulk_g2s(base + (uint32_t)s * stage_bytes, a.xt + ((size_t)tile * nk + 2 * (size_t)j) * btile, bytes,
+        bulk_g2s(base + (uint32_t)s * stage_bytes, a.xt + ((size_t)tile * nk + (size_t)GPS * j) * btile, bytes,
                  bfull + s);
         ++issued;
       }
@@ -398,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
       }
       tc_fence_after();  // the producers' tensor-memory stores are complete
       const uint64_t db = db0 + (uint64_t)(s * dstage);
-      const uint32_t ta = tmem + kABase + (uint32_t)(kAStage * s);
-      const int ng = min(2, nk - 2 * j);
+      const uint32_t ta = tmem + kABase + kAStageT * (uint32_t)s;
+      const int ng = min(GPS, nk - GPS * j);
       for (int gi = 0; gi < ng; ++gi) {
 #pragma unroll
         for (int k = 0; k < kGK / 16; ++k)
@@ -589,6 +598,7 @@ struct TcPlan {
   size_t smem;
   int tmem;    // tensor-memory columns per CTA (512, or 256 for two CTAs per SM)
   bool sbreg;  // scales and biases in registers (token tiles of 128 and more, one CTA per SM)
+  int gps;     // quantization groups per pipeline stage (4 for tiles of at most 64 tokens)
 };
 
 // Pipeline depth and weight ring for a token tile of n_tile rows (a multiple of 16, <= kMaxN).
@@ -597,12 +607,14 @@ TcPlan tc_plan_ntile(int n_tile) {
   p.n_tile = n_tile;
   p.n_tiles = 1;
   p.sbreg = n_tile >= 128;
+  p.gps = n_tile <= 64 ? 4 : 2;
   const size_t kWStageBytes = (size_t)wstage_bytes(p.sbreg);
-  const size_t stage = 2 * (size_t)p.n_tile * 128;  // token tiles of two groups
+  const size_t stage = (size_t)p.gps * p.n_tile * 128;  // token tiles of a stage's groups
   const size_t fixed = 1024 + 64 + 8 * 32;          // alignment slack, barriers, slot, flag
   // stages: at most kMaxStages (tensor-memory columns for A); the rest of shared memory goes to the
   // weight ring (memory latency)
-  p.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - fixed - 2 * (size_t)kWStageBytes) / stage);
+  // (four-group stages: three fit the tensor memory after a 64-column accumulator)
+  p.stages = (int)std::min<size_t>(p.gps == 4 ? 3 : kMaxStages, (kSmemBudget - fixed - 2 * (size_t)kWStageBytes) / stage);
   const size_t left = kSmemBudget - fixed - (size_t)p.stages * stage;
   p.wring = left >= 16 * (size_t)kWStageBytes ? 16 : left >= 8 * (size_t)kWStageBytes ? 8 : left >= 4 * (size_t)kWStageBytes ? 4 : 2;
   // scale/bias copies through L1 (tiles of 32 to 64 tokens): an eight-group ring leaves more shared
@@ -622,6 +634,7 @@ TcPlan tc_plan_ntile_pair(int n_tile) {
   p.n_tile = n_tile;
   p.n_tiles = 1;
   p.sbreg = false;
+  p.gps = 2;
   const size_t kWStageBytes = (size_t)wstage_bytes(false);
   p.tmem = 256;
   const size_t stage = 2 * (size_t)n_tile * 128;
@@ -657,32 +670,44 @@ int tc_launch(const TcArgs& a, const TcPlan& p, dim3 grid, cudaStream_t stream) 
   if (p.tmem == 256) {
     switch (p.wring) {
       case 4:
-        return go(qgemm_tc_kernel<4, 256, false>);
+        return go(qgemm_tc_kernel<4, 256, false, 2>);
       default:
-        return go(qgemm_tc_kernel<2, 256, false>);
+        return go(qgemm_tc_kernel<2, 256, false, 2>);
     }
   }
   if (p.sbreg) {
     switch (p.wring) {
       case 16:
-        return go(qgemm_tc_kernel<16, 512, true>);
+        return go(qgemm_tc_kernel<16, 512, true, 2>);
       case 8:
-        return go(qgemm_tc_kernel<8, 512, true>);
+        return go(qgemm_tc_kernel<8, 512, true, 2>);
       case 4:
-        return go(qgemm_tc_kernel<4, 512, true>);
+        return go(qgemm_tc_kernel<4, 512, true, 2>);
       default:
-        return go(qgemm_tc_kernel<2, 512, true>);
+        return go(qgemm_tc_kernel<2, 512, true, 2>);
+    }
+  }
+  if (p.gps == 4) {
+    switch (p.wring) {
+      case 16:
+        return go(qgemm_tc_kernel<16, 512, false, 4>);
+      case 8:
+        return go(qgemm_tc_kernel<8, 512, false, 4>);
+      case 4:
+        return go(qgemm_tc_kernel<4, 512, false, 4>);
+      default:
+        return go(qgemm_tc_kernel<2, 512, false, 4>);
     }
   }
   switch (p.wring) {
     case 16:
-      return go(qgemm_tc_kernel<16, 512, false>);
+      return go(qgemm_tc_kernel<16, 512, false, 2>);
     case 8:
-      return go(qgemm_tc_kernel<8, 512, false>);
+      return go(qgemm_tc_kernel<8, 512, false, 2>);
     case 4:
-      return go(qgemm_tc_kernel<4, 512, false>);
+      return go(qgemm_tc_kernel<4, 512, false, 2>);
     default:
-      return go(qgemm_tc_kernel<2, 512, false>);
+      return go(qgemm_tc_kernel<2, 512, false, 2>);
   }
 }
 
