@@ -86,6 +86,8 @@ def _L():
             lib.orc_quantize_rows.restype = I
             lib.orc_rmsnorm.argtypes = [P, I, P, I64, ctypes.c_double, P]
             lib.orc_rmsnorm.restype = I
+            lib.orc_gated_rmsnorm.argtypes = [P, P, I, P, I64, I64, ctypes.c_double, P]
+            lib.orc_gated_rmsnorm.restype = I
             lib.orc_sigmoid.argtypes = [ctypes.c_double]
             lib.orc_sigmoid.restype = ctypes.c_double
             lib.orc_sigmoid_scalar_fma.argtypes = [ctypes.c_double, P, P, P, I64, P, P]
@@ -240,6 +242,26 @@ def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
 def rmsnorm_qgemv(packed, scales, biases, x, gamma, eps: float, group_size: int = 64):
     """y, absref of W rmsnorm(x): the norm in float64, then the GEMV of the normalised vector."""
     return qgemv_f64x(packed, scales, biases, rmsnorm(x, gamma, eps), group_size)
+
+
+def gated_rmsnorm(y: np.ndarray, z: np.ndarray, gamma: np.ndarray, eps: float, head_dim: int) -> np.ndarray:
+    """out = silu(z) * gamma * y / sqrt(mean over the head of y^2 + eps), heads of head_dim
+    consecutive elements, float64 (y, z: bf16 bits or float32, the same type; gamma bf16 bits)."""
+    y = np.ascontiguousarray(y)
+    z = np.ascontiguousarray(z, dtype=y.dtype)
+    gamma = np.ascontiguousarray(gamma, dtype=np.uint16)
+    if gamma.size != y.size or z.size != y.size:
+        raise ValueError("y, z and gamma differ in length")
+    out = np.empty(y.size, dtype=np.float64)
+    rc = _L().orc_gated_rmsnorm(_p(y), _p(z), _xtype(y), _p(gamma), y.size, int(head_dim), float(eps), _p(out))
+    if rc != 0:
+        raise ValueError("orc_gated_rmsnorm rejected the arguments")
+    return out
+
+
+def gated_rmsnorm_qgemv(packed, scales, biases, y, z, gamma, eps: float, head_dim: int, group_size: int = 64):
+    """out, absref of W gated_rmsnorm(y, z): the norm in float64, then the GEMV of the result."""
+    return qgemv_f64x(packed, scales, biases, gated_rmsnorm(y, z, gamma, eps, head_dim), group_size)
 
 
 def code2(packed, in_dim: int, row: int, j: int) -> int:

@@ -290,6 +290,36 @@ int orc_rmsnorm(const void *x, int xtype, const uint16_t *gamma, int64_t n, doub
 }
 
 /* ---------------------------------------------------------------------------------------
+ * Gated RMSNorm ([FFAI#14] "gatedRmsNormQgemvInt4Fast": the Mamba2-style gated norm of the GDN
+ * mixer's output, silu(z) * w * rmsnorm(y), before its out-projection; heads of head_dim
+ * consecutive elements, "Hv*Dv" of them in all):
+ *   for head h (elements j = h*head_dim .. (h+1)*head_dim - 1):
+ *     r_h = sqrt( (1/head_dim) sum_{i in h} y[i]^2 + eps )
+ *     out[j] = silu(z[j]) * gamma[j] * y[j] / r_h,      silu(t) = t / (1 + exp(-t))
+ * head_dim = n is the norm over the whole vector.  y, z bf16 or fp32 (the same type) [n]; gamma
+ * bf16 [n]; out double [n].  Sums in index order.
+ * ------------------------------------------------------------------------------------- */
+int orc_gated_rmsnorm(const void *y, const void *z, int xtype, const uint16_t *gamma, int64_t n, int64_t head_dim,
+                      double eps, double *out) {
+  if (n <= 0 || head_dim <= 0 || n % head_dim != 0 || eps < 0.0) return ORC_EINVAL;
+  for (int64_t h0 = 0; h0 < n; h0 += head_dim) {
+    double ss = 0.0;
+    for (int64_t i = h0; i < h0 + head_dim; ++i) {
+      double v = load_x(y, xtype, i);
+      ss += v * v;
+    }
+    double r = sqrt(ss / (double)head_dim + eps);
+    if (!(r > 0.0)) return ORC_EINVAL; /* an all-zero head with eps = 0 has no norm */
+    for (int64_t j = h0; j < h0 + head_dim; ++j) {
+      double t = load_x(z, xtype, j);
+      double silu = t / (1.0 + exp(-t));
+      out[j] = silu * orc_bf16_to_f64(gamma[j]) * (load_x(y, xtype, j) / r);
+    }
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------------------
  * Sigmoid-gated scalar FMA with the residual folded in ([FFAI#14] scalar-FMA commit:
  * "sigmoidScalarFMAResidual(gate, value, base, residual, into:) -- sigmoid-gated FMA with the
  * post-MoE residual add folded in"; "out[i] = base[i] + scalar[0] * value[i]"; the shared-expert

@@ -707,3 +707,53 @@ def test_moe2_equals_4bit_moe_on_repacked_codes():
     np.testing.assert_array_equal(y2, y4)
     np.testing.assert_array_equal(a2, a4)
     assert f2 == f4 == 0
+
+
+# ---------------------------------------------------------------- gated RMSNorm (Mamba2-style, GDN tail)
+def _bf(vals):
+    """bf16 bits of values exactly representable in bf16."""
+    v = np.asarray(vals, dtype=np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_gated_rmsnorm_large_gate_is_rmsnorm_times_gate():
+    """silu(t) = t exactly in binary64 for t = 64 (1 / (1 + e^-64) rounds to 1): with z = 64 everywhere
+    and one head, the gated norm is 64 times the plain RMSNorm, which is pinned on its own."""
+    y = I.bf16_normal(21, I.TID_X, 256)
+    g = I.bf16_normal(22, I.TID_RESID, 256)
+    z = _bf(np.full(256, 64.0))
+    out = oracle.gated_rmsnorm(y, z, g, 1e-6, 256)
+    np.testing.assert_allclose(out, 64.0 * oracle.rmsnorm(y, g, 1e-6), rtol=1e-15, atol=0)
+
+
+def test_gated_rmsnorm_zero_gate_and_silu_values():
+    """z = 0 gives 0 (silu(0) = 0); z = +-1 gives silu(1) = 1/(1+e^-1) and silu(-1) = -1/(1+e)."""
+    y = _bf([1.0, -2.0, 3.0, 0.5])
+    g = _bf([1.0, 1.0, 1.0, 1.0])
+    r = math.sqrt((1 + 4 + 9 + 0.25) / 4)
+    out = oracle.gated_rmsnorm(y, _bf([0.0, 1.0, -1.0, 0.0]), g, 0.0, 4)
+    assert out[0] == 0.0 and out[3] == 0.0
+    assert abs(out[1] - (1 / (1 + math.exp(-1))) * (-2.0 / r)) < 1e-15
+    assert abs(out[2] - (-1 / (1 + math.e)) * (3.0 / r)) < 1e-15
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_gated_rmsnorm_heads_are_independent(head_dim):
+    """Per head, with gamma = 1 and z = 64: the output over 64 has mean square 1 (eps = 0), and
+    scaling one head's y by 8 changes no output anywhere."""
+    n = 512
+    y = I.f32_normal(23, I.TID_X, n)
+    z = np.full(n, 64.0, np.float32)
+    g = _bf(np.ones(n))
+    out = oracle.gated_rmsnorm(y, z, g, 0.0, head_dim) / 64.0
+    ms = (out.reshape(-1, head_dim) ** 2).mean(axis=1)
+    np.testing.assert_allclose(ms, 1.0, rtol=1e-13)
+    y2 = y.copy()
+    y2[head_dim:2 * head_dim] *= np.float32(8.0)
+    np.testing.assert_allclose(oracle.gated_rmsnorm(y2, z, g, 0.0, head_dim) / 64.0, out, rtol=1e-14, atol=0)
+
+
+def test_gated_rmsnorm_rejects_bad_heads():
+    y = I.f32_normal(24, I.TID_X, 96)
+    with pytest.raises(ValueError):
+        oracle.gated_rmsnorm(y, y, _bf(np.ones(96)), 1e-6, 64)
