@@ -457,6 +457,23 @@ def measure_configs(qg, I, dev, stream):
     nbytes = weight_bytes(SD_OUT, SD_IN) + SD_IN * 4 + 4 + SD_OUT * (4 + 2 + 4)
     res["n1_shared_down_sigmoid_fma_2048x768"] = dict(gb(nbytes, us), call="qgemv_int4_sigmoid_fma",
                                                       l2="weights rotate over 192 copies (170 MB, larger than L2)")
+
+    # ... and the gated RMSNorm before the GDN mixer's out-projection: 32 heads of 128 into 2048
+    GN_OUT, GN_IN, GN_HD = 2048, 4096, 128
+    gn = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_W, GN_OUT, GN_IN), dev)
+    gns = copies(gn, 36)
+    gy = qg.to_device(I.bf16_normal(0, I.TID_X, GN_IN), dev)
+    gz = qg.to_device(I.bf16_normal(1, I.TID_X, GN_IN), dev)
+    gg = qg.to_device(I.bf16_normal(0, I.TID_RESID, GN_IN), dev)
+    go = torch.empty(GN_OUT, dtype=torch.float32, device=dev)
+    gws = torch.empty(qg.qg_workspace_bytes(qg.QG_OP_GATED_NORM, gn, 0), dtype=torch.uint8, device=dev)
+    us = tl(lambda i: lib.gated_rmsnorm_qgemv_int4(byref(gns[i % 36].struct), P(gy.data_ptr()), P(gz.data_ptr()),
+                                                   qg.QG_X_BF16, P(gg.data_ptr()), ctypes.c_float(1e-6), GN_HD,
+                                                   P(go.data_ptr()), P(gws.data_ptr()), gws.numel(), s), 200)
+    nbytes = weight_bytes(GN_OUT, GN_IN) + GN_IN * 2 * 3 + GN_IN * 4 * 2 + GN_OUT * 4
+    res["n1_gated_rmsnorm_2048x4096_heads128"] = dict(gb(nbytes, us), call="gated_rmsnorm_qgemv_int4", launches=2,
+                                                      l2="weights rotate over 36 copies (170 MB)")
+    del gn, gns
     del sd, sds
 
     # next row N3: the affine encoder over the FFN gate's shape (bf16 weights in, Q4_64A / Q2_64A out)

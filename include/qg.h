@@ -207,6 +207,20 @@ int moe_layer_int4(const float *logits, int renorm, const qg_int4_weight *gate, 
                    uint32_t *idx, float *p, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * gated_rmsnorm_qgemv_int4 -- the gated RMSNorm before a projection ([FFAI#14]
+ * "gatedRmsNormQgemvInt4Fast": the Mamba2-style silu(z) * w * rmsnorm(y) of the GDN mixer's output,
+ * then its out-projection), per head of head_dim consecutive elements:
+ *   x[j] = silu(z[j]) * gamma[j] * y[j] / sqrt(mean over j's head of y^2 + eps),   out = W x
+ * head_dim = w->in normalises over the whole vector.  y, z: bf16 or fp32 [in] (x_type, both);
+ * gamma: bf16 [in]; out: fp32 [w->out].  workspace: at least qg_workspace_bytes(QG_OP_GATED_NORM, w, 0)
+ * bytes; holds x (fp32 [in]) after the call.  Two launches (the norm, one block per head, then the
+ * GEMV with fp32 x).  Limits as qgemv_int4; head_dim >= 1 divides in; eps >= 0, finite.
+ */
+int gated_rmsnorm_qgemv_int4(const qg_int4_weight *w, const void *y, const void *z, int x_type,
+                             const uint16_t *gamma, float eps, int head_dim, float *out, void *workspace,
+                             size_t ws_bytes, void *stream);
+
+/*
  * moe_prefill_int4 -- the MoE layer for T tokens at once (prefill; [FFAI#9] "moeGatherDequantGemmInt4",
  * "mt_moe_gather_qmm_int4": rows sorted by expert with CSR expert offsets, for prefill):
  *   for token t: (idx[t], p[t]) = moe_router_topk(logits[t], renorm);
@@ -342,7 +356,8 @@ typedef enum {
   QG_OP_QGEMM = 3,
   QG_OP_LAYER = 4,     /* dense_layer_int4 */
   QG_OP_LAYER_HOST = 5, /* dense_layer_int4_host (T_or_k = hidden) */
-  QG_OP_MOE_PREFILL = 6 /* moe_prefill_int4 (the down weight, T_or_k = T; room for any k <= 8) */
+  QG_OP_MOE_PREFILL = 6, /* moe_prefill_int4 (the down weight, T_or_k = T; room for any k <= 8) */
+  QG_OP_GATED_NORM = 7   /* gated_rmsnorm_qgemv_int4 (T_or_k ignored) */
 } qg_op;
 
 /* Workspace bytes the call `op` needs for weight `w` and T (QG_OP_QGEMM) or k (QG_OP_MOE; pass

@@ -126,6 +126,25 @@ int rmsnorm_qgemv_int4(const qg_int4_weight* w, const void* x, int xt, const uin
   return gemv_dense_launch(&m, 1, x, xt, w->in, static_cast<cudaStream_t>(stream), ex);
 }
 
+int gated_rmsnorm_qgemv_int4(const qg_int4_weight* w, const void* y, const void* z, int xt, const uint16_t* gamma,
+                             float eps, int head_dim, float* out, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_weight(w, false);
+  if (rc) return rc;
+  if (!y || !z || !gamma || !out || (xt != QG_X_BF16 && xt != QG_X_F32) || !(eps >= 0.f) || !(eps < INFINITY))
+    return QG_EINVAL;
+  if (head_dim < 1 || w->in % head_dim != 0) return QG_EINVAL;
+  if (!aligned16(y) || !aligned16(z) || !aligned16(gamma) || !aligned16(out)) return QG_EALIGN;
+  const size_t need = qg_workspace_bytes(QG_OP_GATED_NORM, w, 0);
+  if (!workspace || ws_bytes < need) return QG_EWORKSPACE;
+  if (!aligned16(workspace)) return QG_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* x = static_cast<float*>(workspace);
+  rc = gated_norm_launch(y, z, xt, gamma, w->in, head_dim, eps, x, s);
+  if (rc) return rc;
+  GemvMatArg m{w->packed, w->scales, w->biases, out, w->out};
+  return gemv_dense_launch(&m, 1, x, QG_X_F32, w->in, s);
+}
+
 int rmsnorm_qgemv_int4_multi(int n, const qg_int4_weight* ws, const void* x, int xt, const uint16_t* gamma, float eps,
                              float* const* ys, int epi, void* stream) {
   if (!gamma || !(eps >= 0.f)) return QG_EINVAL;
@@ -365,6 +384,8 @@ size_t qg_workspace_bytes(int op, const qg_int4_weight* w, int T_or_k) {
       return round16((size_t)w->in * sizeof(float)) + (size_t)(T_or_k > 0 ? T_or_k : 0) * sizeof(float);
     case QG_OP_MOE_PREFILL:  // plan tables, grouped token tiles, G, U, h tiles, down outputs
       return moe_prefill_workspace_bytes(w, T_or_k);
+    case QG_OP_GATED_NORM:  // the normalised, gated vector x (fp32 [in])
+      return (size_t)w->in * sizeof(float);
     default:
       return 0;
   }

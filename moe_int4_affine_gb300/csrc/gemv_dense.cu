@@ -36,4 +36,49 @@ int ingest_launch(const void* src_dev_mapped, void* dst, size_t bytes, cudaStrea
                 static_cast<uint4*>(dst), (int)(bytes / 16));
 }
 
+// Gated RMSNorm, one head per block ([FFAI#14] "gatedRmsNormQgemvInt4Fast": the Mamba2-style
+// gated norm silu(z) * w * rmsnorm(y) before the GDN mixer's out-projection), written as fp32 into
+// the workspace for the GEMV that follows:
+//   x[j] = silu(z[j]) * gamma[j] * (y[j] / sqrt(mean over the head of y^2 + eps))
+template <bool F32>
+__global__ void __launch_bounds__(256) gated_norm_kernel(const void* __restrict__ y, const void* __restrict__ z,
+                                                         const uint16_t* __restrict__ gamma, int head_dim,
+                                                         float eps, float* __restrict__ x) {
+  __shared__ float red[8];
+  pdl_trigger();
+  pdl_wait();
+  const size_t h0 = (size_t)blockIdx.x * head_dim;
+  auto ld = [](const void* p, size_t i) {
+    return F32 ? __ldg(static_cast<const float*>(p) + i)
+               : __uint_as_float((uint32_t)__ldg(static_cast<const uint16_t*>(p) + i) << 16);
+  };
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < head_dim; i += 256) {
+    const float v = ld(y, h0 + i);
+    ss = fmaf(v, v, ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) t += red[w];
+  const float rn = 1.f / sqrtf(t / (float)head_dim + eps);
+  for (int i = threadIdx.x; i < head_dim; i += 256) {
+    const float zz = ld(z, h0 + i);
+    const float silu = zz / (1.f + expf(-zz));
+    const float g = __uint_as_float((uint32_t)__ldg(gamma + h0 + i) << 16);
+    x[h0 + i] = silu * g * (ld(y, h0 + i) * rn);
+  }
+}
+
+int gated_norm_launch(const void* y, const void* z, int xt, const uint16_t* gamma, int n, int head_dim, float eps,
+                      float* x, cudaStream_t stream) {
+  if (head_dim < 1 || n % head_dim != 0) return QG_EINVAL;
+  const dim3 grid((unsigned)(n / head_dim));
+  return xt == QG_X_F32 ? launch(gated_norm_kernel<true>, grid, dim3(256), 0, stream, y, z, gamma, head_dim, eps, x)
+                        : launch(gated_norm_kernel<false>, grid, dim3(256), 0, stream, y, z, gamma, head_dim, eps, x);
+}
+
 }  // namespace qg

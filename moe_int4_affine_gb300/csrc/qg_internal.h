@@ -79,6 +79,9 @@ int moe_gate_up_routed_launch(const float* logits, int n_logits, int renorm, con
 // Copy `bytes` (a multiple of 16) from device-mapped host memory to device memory, in the launch
 // chain (gemv_dense.cu).
 int ingest_launch(const void* src_dev_mapped, void* dst, size_t bytes, cudaStream_t stream);
+// Gated RMSNorm per head of head_dim elements (gemv_dense.cu): x = silu(z) * gamma * rmsnorm_head(y), fp32.
+int gated_norm_launch(const void* y, const void* z, int xt, const uint16_t* gamma, int n, int head_dim, float eps,
+                      float* x, cudaStream_t stream);
 // Affine group-64 encode (quant.cu): bits 4 or 2, w bf16 or fp32 [out][in].
 int quant_launch(const void* w, int wt, int out, int in, int bits, uint32_t* packed, uint16_t* scales,
                  uint16_t* biases, cudaStream_t stream);

@@ -23,7 +23,7 @@ QG_OK, QG_EINVAL, QG_EALIGN, QG_EWORKSPACE, QG_ELAUNCH, QG_ENOTSUP, QG_EDEVICE =
 QG_STATUS_BAD_EXPERT, QG_STATUS_TIMEOUT = 1, 2
 QG_X_BF16, QG_X_F32 = 0, 1
 QG_EPI_NONE, QG_EPI_SWIGLU = 0, 1
-QG_OP_QGEMV, QG_OP_MULTI, QG_OP_MOE, QG_OP_QGEMM, QG_OP_LAYER, QG_OP_LAYER_HOST, QG_OP_MOE_PREFILL = 0, 1, 2, 3, 4, 5, 6
+QG_OP_QGEMV, QG_OP_MULTI, QG_OP_MOE, QG_OP_QGEMM, QG_OP_LAYER, QG_OP_LAYER_HOST, QG_OP_MOE_PREFILL, QG_OP_GATED_NORM = 0, 1, 2, 3, 4, 5, 6, 7
 QG_NOALLOC_MOE_MAX_FLOATS = 32768
 
 
@@ -42,6 +42,7 @@ lib.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
 lib.moe_gather_qgemv_int4.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]
 lib.moe_layer_int4.argtypes = [_P, _I, _W, _W, _W, _I, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
 lib.moe_prefill_int4.argtypes = [_P, _I, _I, _W, _W, _W, _I, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+lib.gated_rmsnorm_qgemv_int4.argtypes = [_W, _P, _P, _I, _P, ctypes.c_float, _I, _P, _P, ctypes.c_size_t, _P]
 lib.qgemv_q2.argtypes = [_W, _P, _I, _P, _P]
 lib.moe_gather_qgemv_q2.argtypes = [_W, _W, _W, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]
 lib.moe_layer_q2.argtypes = [_P, _I, _W, _W, _W, _I, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
@@ -68,7 +69,7 @@ lib.qg_strerror.argtypes = [_I]
 lib.qg_strerror.restype = ctypes.c_char_p
 lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
-           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "moe_prefill_int4", "dense_layer_int4", "dense_layer_int4_host", "rmsnorm_qgemv_int4", "qgemv_q2", "qgemv_q2_multi", "moe_gather_qgemv_q2", "moe_layer_q2",
+           "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "moe_prefill_int4", "gated_rmsnorm_qgemv_int4", "dense_layer_int4", "dense_layer_int4_host", "rmsnorm_qgemv_int4", "qgemv_q2", "qgemv_q2_multi", "moe_gather_qgemv_q2", "moe_layer_q2",
            "rmsnorm_qgemv_int4_multi", "qgemv_int4_sigmoid_fma", "sigmoid_scalar_fma_residual",
            "scalar_fma_chain8_residual", "qgemm_int4", "qgemm_int4_multi", "quantize_affine_q64a", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
@@ -305,6 +306,21 @@ def moe_layer_int4(logits, gate: Int4Weight, up: Int4Weight, down: Int4Weight, x
               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_layer_int4" if bits == 4 else "moe_layer_q2")
     return y, idx, p
+
+
+def gated_rmsnorm_qgemv_int4(w: Int4Weight, y, z, gamma, eps: float, head_dim: int, out=None, workspace=None,
+                             stream=None):
+    """out = W (silu(z) * gamma * rmsnorm per head of y); y, z bf16 or fp32 (the same type)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(w.out, dtype=torch.float32, device=y.device)
+    if workspace is None:
+        workspace = torch.empty(qg_workspace_bytes(QG_OP_GATED_NORM, w, 0), dtype=torch.uint8, device=y.device)
+    _check(lib.gated_rmsnorm_qgemv_int4(ctypes.byref(w.struct), _ptr(y), _ptr(z), _xtype(y), _ptr(gamma), float(eps),
+                                        int(head_dim), _ptr(out), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream)),
+           "gated_rmsnorm_qgemv_int4")
+    return out
 
 
 def moe_prefill_int4(logits, gate: Int4Weight, up: Int4Weight, down: Int4Weight, X, residual=None, k: int = 8,

@@ -166,3 +166,37 @@ def test_sigmoid_scalar_fma_residual(qg, n, with_resid):
     y_ref, a = oracle.sigmoid_scalar_fma(float(gate[0]), v, base, resid)
     assert_within_bound(qg.to_numpy(out).astype(np.float64), y_ref, a)
     assert qg.qg_device_status() == 0
+
+
+# ---------------------------------------------------------------- gated RMSNorm before a projection
+@pytest.mark.parametrize("out,in_dim,head_dim", [(2048, 4096, 128), (256, 1024, 64), (500, 576, 576), (96, 512, 512)])
+@pytest.mark.parametrize("kind", ["bf16", "f32"])
+def test_gated_rmsnorm_qgemv_vs_oracle(qg, out, in_dim, head_dim, kind):
+    """W (silu(z) * gamma * rmsnorm per head of y): the GDN tail shape (32 heads of 128 into 2048)
+    and whole-vector norms; y and z of either type."""
+    d = I.int4_weight(out + head_dim, I.TID_W, out, in_dim)
+    y = _x(kind, in_dim + 1, in_dim)
+    z = _x(kind, in_dim + 2, in_dim)
+    gamma = I.bf16_normal(in_dim + 3, I.TID_RESID, in_dim)
+    o = qg.gated_rmsnorm_qgemv_int4(qg.Int4Weight.from_numpy(d), qg.to_device(y), qg.to_device(z),
+                                    qg.to_device(gamma), 1e-6, head_dim)
+    y_ref, a = oracle.gated_rmsnorm_qgemv(d["packed"], d["scales"], d["biases"], y, z, gamma, 1e-6, head_dim)
+    assert_within_bound(qg.to_numpy(o).astype(np.float64), y_ref, a)
+    assert qg.qg_device_status() == 0
+
+
+def test_gated_rmsnorm_qgemv_rejects_bad_heads_and_workspace(qg):
+    import torch
+
+    d = I.int4_weight(1, I.TID_W, 64, 256)
+    w = qg.Int4Weight.from_numpy(d)
+    y = qg.to_device(I.bf16_normal(1, I.TID_X, 256))
+    g = qg.to_device(I.bf16_normal(2, I.TID_RESID, 256))
+    for hd in (0, 96, 512):
+        with pytest.raises(qg.QGError) as e:
+            qg.gated_rmsnorm_qgemv_int4(w, y, y, g, 1e-6, hd)
+        assert e.value.code == qg.QG_EINVAL
+    with pytest.raises(qg.QGError) as e:
+        qg.gated_rmsnorm_qgemv_int4(w, y, y, g, 1e-6, 128, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.code == qg.QG_EWORKSPACE
+    assert qg.qg_device_status() == 0
