@@ -108,3 +108,59 @@ def test_workspace_and_strings(lib):
     assert lib.qg_strerror(-3) == b"workspace missing or too small"
     assert lib.qg_set_pdl(1) == 0 and lib.qg_set_pdl(0) == 1
     assert lib.qg_version() >> 16 == 1
+
+
+def test_host_validation_of_the_later_entry_points(lib):
+    """moe_prefill_int4, gated_rmsnorm_qgemv_int4 and quantize_affine_q64a reject bad arguments on
+    the host (every call here fails validation)."""
+    P = ctypes.c_void_p
+    lib.moe_prefill_int4.argtypes = [P, ctypes.c_int, ctypes.c_int] + [ctypes.POINTER(W)] * 3 + \
+        [ctypes.c_int, P, P, P, P, P, P, ctypes.c_size_t, P]
+    g, u, dn = _w(out=64, in_=128, n_mat=8), _w(out=64, in_=128, n_mat=8), _w(out=128, in_=64, n_mat=8)
+    pre = lambda T=4, k=2, ws=FAKE, nb=1 << 30, d=dn, renorm=1, res=FAKE: lib.moe_prefill_int4(
+        FAKE, T, renorm, ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), k, FAKE, res, FAKE, FAKE, FAKE, ws, nb, None)
+    assert pre(k=9) == -1
+    assert pre(k=0) == -1
+    assert pre(T=0) == -1
+    assert pre(T=70000) == -1
+    assert pre(renorm=2) == -1
+    assert pre(d=_w(out=128, in_=128, n_mat=8)) == -1  # down's in must be the intermediate size
+    assert pre(ws=None) == -3
+    assert pre(nb=1000) == -3
+    assert pre(res=FAKE + 8) == -2
+    lib.gated_rmsnorm_qgemv_int4.argtypes = [ctypes.POINTER(W), P, P, ctypes.c_int, P, ctypes.c_float, ctypes.c_int,
+                                             P, P, ctypes.c_size_t, P]
+    w = _w(out=8, in_=256)
+    gated = lambda hd=128, z=FAKE, eps=1e-6, ws=FAKE, nb=4096, xt=0: lib.gated_rmsnorm_qgemv_int4(
+        ctypes.byref(w), FAKE, z, xt, FAKE, eps, hd, FAKE, ws, nb, None)
+    assert gated(hd=0) == -1
+    assert gated(hd=96) == -1  # does not divide in
+    assert gated(hd=512) == -1
+    assert gated(z=None) == -1
+    assert gated(eps=-1.0) == -1
+    assert gated(xt=3) == -1
+    assert gated(nb=100) == -3
+    assert gated(z=FAKE + 4) == -2
+    lib.quantize_affine_q64a.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P]
+    q = lambda bits=4, out=8, in_=128, wt=0, w_=FAKE: lib.quantize_affine_q64a(w_, wt, out, in_, bits, FAKE, FAKE,
+                                                                              FAKE, None)
+    assert q(bits=3) == -1
+    assert q(in_=100) == -1
+    assert q(out=0) == -1
+    assert q(wt=5) == -1
+    assert q(w_=FAKE + 2) == -2
+
+
+def test_workspace_sizes_of_the_later_ops(lib):
+    lib.qg_workspace_bytes.argtypes = [ctypes.c_int, ctypes.POINTER(W), ctypes.c_int]
+    lib.qg_workspace_bytes.restype = ctypes.c_size_t
+    w = _w(out=2048, in_=4096)
+    assert lib.qg_workspace_bytes(7, ctypes.byref(w), 0) == 4096 * 4  # gated norm: x fp32 [in]
+    down = _w(out=2048, in_=768, n_mat=128)
+    sizes = [lib.qg_workspace_bytes(6, ctypes.byref(down), T) for T in (1, 32, 256, 512)]
+    # at least the grouped rows' token tiles, gate/up outputs, h tiles and down outputs for T k rows
+    for T, b in zip((1, 32, 256, 512), sizes):
+        rows = T * 8
+        assert b >= rows * (2048 * 2 + 768 * 4 * 2 + 768 * 2 + 2048 * 4)
+    assert sizes == sorted(sizes)
+    assert lib.qg_workspace_bytes(6, ctypes.byref(down), 0) == 0
