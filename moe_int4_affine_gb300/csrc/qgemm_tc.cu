@@ -6,21 +6,27 @@
 // A[128 x 16] * B[n_tile x 16]^T with A = the dequantized weights (fp16, in tensor memory, one
 // weight row per lane) and B = the tokens (fp16, K-major in shared memory with the 128-byte
 // swizzle), D fp32 in tensor memory.
-//   * A pipeline stage covers two 64-column quantization groups (K = 128).  Two producer warp
-//     groups (4 warps each, one thread per weight row) fill them: group h makes group 2 j + h of
-//     stage j.  (A tenth warp issues the stages' token-tile copies.)  A thread streams its row's
-//     packed codes, scale and bias through a
-//     per-thread cp.async ring (WRING of its groups ahead), dequantizes the 64 weights with packed
-//     half-precision arithmetic (w = s * q + b, one rounding to fp16) and writes them with one
-//     tensor-memory store (tcgen05.st, 32 columns of its row's lane) into its group's A columns.
+//   * A pipeline stage covers GPS 64-column quantization groups (GPS = 2, K = 128; GPS = 4, K = 256
+//     for tiles of at most 64 tokens, which halves the stage hand-overs that pace small tiles).
+//     Two producer warp groups (4 warps each, one thread per weight row) fill them: group h makes
+//     groups GPS j + 2 q + h of stage j.  (A tenth warp issues the stages' token-tile copies.)  A
+//     thread streams its row's packed codes through a per-thread cp.async ring (WRING of its
+//     groups ahead) -- with the scale and bias words (4-byte copies, through L1), or, for tiles of
+//     128 tokens and more, with the scales and biases as 16-byte chunks of 8 groups in registers --
+//     dequantizes the 64 weights of a group with packed half-precision arithmetic (w = s * q + b,
+//     one rounding to fp16) and writes them with one tensor-memory store (tcgen05.st, 32 columns of
+//     its row's lane) into the stage's A columns.
 //   * The token tile of a stage is one contiguous block of the workspace (written there, already
 //     swizzled, by the prep kernel) and arrives by a single bulk copy (TMA engine) on the stage's
 //     mbarrier.
-//   * One thread of the MMA warp issues eight K=16 MMAs per stage and commits them to the stage's
-//     "empty" mbarrier; a final commit releases the epilogue, which reads the accumulator from tensor
-//     memory (tcgen05.ld), applies each token's power-of-two input scale and writes Y.
+//   * One thread of the MMA warp issues four K=16 MMAs per group and commits each stage to the
+//     stage's "empty" mbarrier; a final commit releases the epilogue, which reads the accumulator
+//     from tensor memory (tcgen05.ld), applies each token's power-of-two input scale and writes Y.
 //   * Every mbarrier wait is bounded (2 s): on a timeout the CTA records QG_STATUS_TIMEOUT, stops
 //     issuing, drains what it has in flight and frees its tensor memory before returning.
+//   * Grouped (MoE) mode: token tile y belongs to expert tile_expert[y]; the CTA reads it first
+//     and takes that expert's slab of every matrix (unused tiles exit before any setup).  Tiles
+//     of at most 64 tokens there run two CTAs per SM (256 tensor-memory columns each).
 //
 // Numerics: each token row of X is scaled by a power of two 2^(14 - e_t) (e_t = floor(log2 max|x_t|))
 // so that it sits in fp16's range, then rounded to fp16 (exact for bf16 inputs within 2^10 of the
