@@ -213,8 +213,10 @@ int moe_layer_int4(const float *logits, int renorm, const qg_int4_weight *gate, 
  *   x[j] = silu(z[j]) * gamma[j] * y[j] / sqrt(mean over j's head of y^2 + eps),   out = W x
  * head_dim = w->in normalises over the whole vector.  y, z: bf16 or fp32 [in] (x_type, both);
  * gamma: bf16 [in]; out: fp32 [w->out].  workspace: at least qg_workspace_bytes(QG_OP_GATED_NORM, w, 0)
- * bytes; holds x (fp32 [in]) after the call.  Two launches (the norm, one block per head, then the
- * GEMV with fp32 x).  Limits as qgemv_int4; head_dim >= 1 divides in; eps >= 0, finite.
+ * bytes.  head_dim a multiple of 64: one launch, the norm in the GEMV's prologue (per-head roots
+ * applied to each 64-column group's x factors); otherwise two (a norm kernel, one block per head,
+ * writes x as fp32 into the workspace, then the GEMV).  Limits as qgemv_int4; head_dim >= 1
+ * divides in; eps >= 0, finite.
  */
 int gated_rmsnorm_qgemv_int4(const qg_int4_weight *w, const void *y, const void *z, int x_type,
                              const uint16_t *gamma, float eps, int head_dim, float *out, void *workspace,

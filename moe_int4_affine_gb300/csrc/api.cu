@@ -138,10 +138,18 @@ int gated_rmsnorm_qgemv_int4(const qg_int4_weight* w, const void* y, const void*
   if (!workspace || ws_bytes < need) return QG_EWORKSPACE;
   if (!aligned16(workspace)) return QG_EALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* x = static_cast<float*>(workspace);
+  GemvMatArg m{w->packed, w->scales, w->biases, out, w->out};
+  if (head_dim % 64 == 0) {  // heads of whole groups: the norm inside the GEMV's prologue, one launch
+    GemvExtras ex{};
+    ex.gamma = gamma;
+    ex.eps = eps;
+    ex.gz = z;
+    ex.head_dim = head_dim;
+    return gemv_dense_launch(&m, 1, y, xt, w->in, s, ex);
+  }
+  float* x = static_cast<float*>(workspace);  // otherwise: the norm kernel, then the GEMV of its x
   rc = gated_norm_launch(y, z, xt, gamma, w->in, head_dim, eps, x, s);
   if (rc) return rc;
-  GemvMatArg m{w->packed, w->scales, w->biases, out, w->out};
   return gemv_dense_launch(&m, 1, x, QG_X_F32, w->in, s);
 }
 

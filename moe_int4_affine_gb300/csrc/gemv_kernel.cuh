@@ -44,6 +44,7 @@
 namespace qg {
 
 constexpr int kMaxMats = 8;
+constexpr int kMaxXGroups = 512;  // groups of x: in <= 32768
 enum GemvMode { kDense = 0, kPair = 1, kSeg = 2 };
 constexpr int kThreads = 512;       // 16 warps per CTA, one CTA per SM
 constexpr int kGroupsPerUnit = 32;  // groups of one work unit (one per lane)
@@ -95,6 +96,11 @@ struct GemvArgs {
   // x * gamma is what gets quantized, and the finisher multiplies by the root (y is linear in x).
   const uint16_t* gamma;  // bf16 [in]
   float eps;
+  // Gated RMSNorm (NORM kernels, dense, gz set): x * gamma * silu(z) is quantized, and every group's
+  // x factors are scaled by its head's 1 / sqrt(mean over the head of x^2 + eps) before the main
+  // loop (heads of head_dim columns, a multiple of 64).
+  const void* gz;  // z, the type of x [in]
+  int head_dim;
   // Gated epilogue (dense): y = ebase + sigmoid(*sgate) * (W x), then + resid when set.
   const float* sgate;
   const float* ebase;
@@ -276,6 +282,8 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
 template <int MODE, int RN, bool STG, bool NORM, int BITS = 4>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float s_gss[NORM ? kMaxXGroups : 1];  // gated: each group's sum of x^2, then
+  __shared__ float s_hrn[NORM ? kMaxXGroups : 1];  // each head's 1 / root
   __shared__ uint32_t s_idx[kMaxMats];  // the in-kernel router's selection
   __shared__ float s_p[kMaxMats];
   __shared__ float s_ss[kThreads / 32];  // NORM: per-warp sums of x^2
@@ -389,15 +397,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     float ss = 0.f;  // NORM: this thread's sum of x^2
     // NORM: accumulate x^2 (live groups only), then x *= gamma (eight bf16 in gw)
     auto apply_norm = [&](int g, float (&v)[8], const uint4& gw) {
+      float pg = 0.f;  // this lane's part of group g's sum of x^2
       if (g < G) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
+        for (int j = 0; j < 8; ++j) pg = fmaf(v[j], v[j], pg);
       }
+      ss += pg;
       const uint32_t w[4] = {gw.x, gw.y, gw.z, gw.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         v[2 * j] *= __uint_as_float(w[j] << 16);
         v[2 * j + 1] *= __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+      if (a.gz) {  // gated (uniform): times silu(z), and the group's sum of x^2 for its head
+        float zf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (g < G) {
+          if (a.xf32) {
+            const float4* zp = reinterpret_cast<const float4*>(static_cast<const float*>(a.gz) + (size_t)g * 64) + 2 * sub;
+            const float4 z0 = __ldg(zp), z1 = __ldg(zp + 1);
+            zf[0] = z0.x; zf[1] = z0.y; zf[2] = z0.z; zf[3] = z0.w;
+            zf[4] = z1.x; zf[5] = z1.y; zf[6] = z1.z; zf[7] = z1.w;
+          } else {
+            const uint4 zr = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.gz) + (size_t)g * 64) + sub);
+            const uint32_t zw[4] = {zr.x, zr.y, zr.z, zr.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              zf[2 * j] = __uint_as_float(zw[j] << 16);
+              zf[2 * j + 1] = __uint_as_float(zw[j] & 0xFFFF0000u);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] *= zf[j] / (1.f + expf(-zf[j]));
+        pg += __shfl_xor_sync(0xffffffffu, pg, 1);
+        pg += __shfl_xor_sync(0xffffffffu, pg, 2);
+        pg += __shfl_xor_sync(0xffffffffu, pg, 4);
+        if (sub == 0 && g < G) s_gss[g] = pg;
       }
     };
     auto quant = [&](int g, const float (&v)[8]) {
@@ -541,6 +576,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     if (idxp[threadIdx.x] >= (uint32_t)a.n_experts) set_status(QG_STATUS_BAD_EXPERT);
   }
   __syncthreads();
+  if constexpr (NORM) {
+    if (a.gz) {  // gated: each head's root, then every group's x factors scaled by its head's
+      const int hg = a.head_dim / 64, nh = G / hg;
+      for (int h = threadIdx.x; h < nh; h += kThreads) {
+        float t = 0.f;
+        for (int q = 0; q < hg; ++q) t += s_gss[h * hg + q];
+        s_hrn[h] = 1.f / sqrtf(t / (float)a.head_dim + a.eps);
+      }
+      __syncthreads();
+      for (int g = threadIdx.x; g < G; g += kThreads) {
+        const float r = s_hrn[g / hg];
+        gsx[g] = make_float2(gsx[g].x * r, gsx[g].y * r);
+      }
+      __syncthreads();
+    }
+  }
 
   // --- main loop: this warp's units u = warp, warp + NW, ...; two buffers in turn, the next unit's
   // codes in flight while one is computed ---
@@ -613,12 +664,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   __syncthreads();
 
   // --- finish: sum each row's K chunks in order, epilogue, write ---
-  float rn = 1.f;  // NORM: 1 / sqrt(mean(x^2) + eps)
+  float rn = 1.f;  // NORM: 1 / sqrt(mean(x^2) + eps) (gated: applied per head above)
   if constexpr (NORM) {
+    if (!a.gz) {
     float t = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) t += s_ss[w];
     rn = 1.f / sqrtf(t / (float)a.in + a.eps);
+    }
   }
   const float sig = a.sgate ? 1.f / (1.f + expf(-__ldg(a.sgate))) : 0.f;
   for (int lr = threadIdx.x; lr < ve - vb; lr += kThreads) {
@@ -739,6 +792,8 @@ inline void apply_extras(GemvArgs& a, const GemvExtras& ex) {
   a.bits = ex.bits ? ex.bits : 4;
   a.gamma = ex.gamma;
   a.eps = ex.eps;
+  a.gz = ex.gz;
+  a.head_dim = ex.head_dim;
   a.sgate = ex.sgate;
   a.ebase = ex.ebase;
   a.resid = ex.resid;

@@ -56,6 +56,8 @@ struct GemvMatArg {
 struct GemvExtras {
   const uint16_t* gamma;
   float eps;
+  const void* gz;  // gated RMSNorm: z (the type of x), per head of head_dim columns (needs gamma)
+  int head_dim;
   const float* sgate;
   const float* ebase;
   const uint16_t* resid;
