@@ -120,3 +120,20 @@ def test_moe_prefill_rejects_bad_arguments(qg):
         qg.moe_prefill_int4(logits, G, U, D, X, k=2, workspace=small)
     assert e.value.code == qg.QG_EWORKSPACE
     assert qg.qg_device_status() == 0
+
+
+def test_moe_prefill_is_deterministic(qg, moe_full):
+    """The plan places rows within an expert's group in atomic order, which may differ from call to
+    call; every row is computed independently of its neighbours, so y, indices and weights are bit
+    for bit the same over repeated calls."""
+    T = 64
+    logits = qg.to_device(I.f32_normal(3, I.TID_LOGITS, (T, 128)))
+    X = qg.to_device(I.bf16_normal(3, I.TID_X, (T, 2048)))
+    R = qg.to_device(I.bf16_normal(3, I.TID_RESID, (T, 2048)))
+    G, U, D = (qg.Int4Weight.from_numpy(d) for d in moe_full)
+    first = [qg.to_numpy(a) for a in qg.moe_prefill_int4(logits, G, U, D, X, R, k=8)]
+    for _ in range(3):
+        again = [qg.to_numpy(a) for a in qg.moe_prefill_int4(logits, G, U, D, X, R, k=8)]
+        for a, b in zip(first, again):
+            np.testing.assert_array_equal(a, b)
+    assert qg.qg_device_status() == 0
