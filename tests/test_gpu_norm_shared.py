@@ -170,12 +170,12 @@ def test_sigmoid_scalar_fma_residual(qg, n, with_resid):
 
 # ---------------------------------------------------------------- gated RMSNorm before a projection
 @pytest.mark.parametrize("out,in_dim,head_dim", [(2048, 4096, 128), (256, 1024, 64), (500, 576, 576), (96, 512, 512),
-                                                  (300, 576, 96), (128, 1024, 32)])
+                                                  (300, 576, 96), (128, 1024, 32), (64, 8256, 192)])
 @pytest.mark.parametrize("kind", ["bf16", "f32"])
 def test_gated_rmsnorm_qgemv_vs_oracle(qg, out, in_dim, head_dim, kind):
     """W (silu(z) * gamma * rmsnorm per head of y): the GDN tail shape (32 heads of 128 into 2048),
-    whole-vector norms (both in the GEMV's prologue) and heads of 96 and 32 columns (the separate
-    norm kernel); y and z of either type."""
+    whole-vector norms (both in the GEMV's prologue; x of 129 groups is loaded by the threads, not
+    staged) and heads of 96 and 32 columns (the separate norm kernel); y and z of either type."""
     d = I.int4_weight(out + head_dim, I.TID_W, out, in_dim)
     y = _x(kind, in_dim + 1, in_dim)
     z = _x(kind, in_dim + 2, in_dim)
