@@ -228,7 +228,12 @@ def run_qg(args, rank, world, local_rank):
     us_down_nopdl = time_loop(down_bf16, n_loop)
     qg.qg_set_pdl(not args.no_pdl)
 
-    configs = measure_configs(qg, I, dev, stream) if rank == 0 and not args.no_configs else None
+    configs = None
+    if rank == 0 and not args.no_configs:
+        try:  # (a failing configuration is reported in the line, not allowed to drop the line)
+            configs = measure_configs(qg, I, dev, stream)
+        except Exception as e:  # noqa: BLE001
+            configs = {"error": f"{type(e).__name__}: {e}"}
     qg.qg_set_pdl(not args.no_pdl)
 
     # end to end through the host-buffer call: every step the GPU reads x from pinned host memory
@@ -635,7 +640,7 @@ def cpu_baseline(target_s: float = 12.0):
                       f"fp64 C oracle, {threads} host threads, {tot_t:.1f} s"}
 
 
-def run_reference(args):
+def run_reference(args, world=1):
     threads = os.cpu_count() or 1
     dt, nb = oracle_layer_sample(0.002, threads)
     frac = min(1.0, 0.002 * 4.0 / max(dt, 1e-3))  # each step about 4 s of oracle work
@@ -649,7 +654,7 @@ def run_reference(args):
     v = tot_b / tot_t / 1e9
     return {"impl": "reference", "metric": "int4 dequant-GEMV effective GB/s (dense decode layer M=1, hidden 5120, "
                                            "FFN 17408)",
-            "value": round(v, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "dense decode layer M=1: gate+up 17408x5120 -> down 5120x17408 (row sample)",
@@ -680,7 +685,7 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             if rank == 0:
-                print(json.dumps(run_reference(args)), flush=True)
+                print(json.dumps(run_reference(args, world)), flush=True)
             return 0
         line = run_qg(args, rank, world, local_rank)
         if rank == 0:
