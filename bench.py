@@ -621,6 +621,69 @@ def oracle_layer_sample(frac: float, threads: int):
     return dt, nbytes
 
 
+def oracle_config_times(threads: int, rows_per_sample: int = 192):
+    """The fp64 oracle timed per configuration, single-threaded and on `threads` host threads: a
+    sample of rows of each matrix (the oracle's cost per row depends only on the row length), scaled
+    to the call's rows; the MoE step (8 of 128 experts) in full, single-threaded (the oracle's MoE
+    routine is single-threaded).  Returns {config: {"ms_1": .., "ms_n": .., "threads": n, ...}}."""
+    import oracle
+    from moe_int4_affine_gb300 import inputs as I
+
+    rows_n = max(rows_per_sample, 64 * threads)  # (enough rows per thread for the split to pay)
+
+    def per_row(in_dim, T=1):
+        w = I.int4_weight(7, I.TID_W, rows_n, in_dim)
+        X = I.bf16_normal(7, I.TID_X, (T, in_dim))
+        out = {}
+        for n, rows in ((1, rows_per_sample), (threads, rows_n)):
+            t0 = time.perf_counter()
+            if T == 1:
+                oracle.qgemv(w["packed"], w["scales"], w["biases"], X[0], rows=(0, rows), threads=n)
+            else:
+                oracle.qgemm(w["packed"], w["scales"], w["biases"], X, rows=(0, rows), threads=n)
+            out[n] = (time.perf_counter() - t0) / rows
+        return out
+
+    res = {}
+    cache = {}
+
+    def call(name, mats, T=1):  # mats: [(out, in)]
+        ms = {1: 0.0, threads: 0.0}
+        for o, i in mats:
+            key = (i, T)
+            if key not in cache:
+                cache[key] = per_row(i, T)
+            for n in ms:
+                ms[n] += cache[key][n] * o * 1e3
+        res[name] = {"ms_1": round(ms[1], 3), "ms_n": round(ms[threads], 3), "threads": threads,
+                     "sample": f"{rows_per_sample} (one thread) or {rows_n} ({threads} threads) rows of each "
+                               f"row length, scaled to the call's rows"}
+
+    call("c0_gemv_256x1024", [(256, 1024)])
+    call("c1_gemv_gate_up_17408x5120", [(17408, 5120), (17408, 5120)])
+    call("c1_gemv_down_5120x17408", [(5120, 17408)])
+    call("c1_decode_layer", [(17408, 5120), (17408, 5120), (5120, 17408)])
+    call("c2_quartet_8192_4096_32_32", [(8192, 2048), (4096, 2048), (32, 2048), (32, 2048)])
+    call("c2_triple_4096_512_512", [(4096, 2048), (512, 2048), (512, 2048)])
+    for T in (8, 32, 256):
+        call(f"c4_qgemm_T{T}", [(17408, 5120)], T)
+    # MoE T = 1: router + 8 experts' gate/up and down (hidden 2048, intermediate 768), in full
+    E, HID, INTER = 8, 2048, 768  # the 8 selected of the 128: the oracle reads only those
+    g = I.int4_weight(0, I.TID_GATE, INTER, HID, n_mat=E)
+    u = I.int4_weight(0, I.TID_UP, INTER, HID, n_mat=E)
+    d = I.int4_weight(0, I.TID_DOWN, HID, INTER, n_mat=E)
+    x = I.bf16_normal(0, I.TID_X, HID)
+    r = I.bf16_normal(0, I.TID_RESID, HID)
+    logits = I.f32_normal(0, I.TID_LOGITS, 128)
+    t0 = time.perf_counter()
+    idx, pr = oracle.router_topk(logits, 8)
+    oracle.moe(tuple(g[k] for k in ("packed", "scales", "biases")), tuple(u[k] for k in ("packed", "scales", "biases")),
+               tuple(d[k] for k in ("packed", "scales", "biases")), np.arange(8, dtype=np.uint32), pr, x, r)
+    res["c3_moe_layer_T1"] = {"ms_1": round((time.perf_counter() - t0) * 1e3, 3), "threads": 1,
+                              "sample": "the full step (router + 8 experts), single-threaded"}
+    return res
+
+
 def cpu_baseline(target_s: float = 12.0):
     """The oracle on whole-layer row samples, repeated until about target_s seconds of CPU work."""
     threads = os.cpu_count() or 1
@@ -691,6 +754,10 @@ def main(argv=None):
         if rank == 0:
             if world == 1 and not args.no_cpu_baseline:
                 line["cpu_baseline"] = cpu_baseline()
+                try:  # (a reported baseline: a failure here must not drop the line)
+                    line["cpu_baseline"]["per_config"] = oracle_config_times(os.cpu_count() or 1)
+                except Exception as e:  # noqa: BLE001
+                    line["cpu_baseline"]["per_config"] = {"error": f"{type(e).__name__}: {e}"}
             print(json.dumps(line), flush=True)
         return 0
     finally:
