@@ -262,6 +262,41 @@ def run_qg(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
     assert qg.qg_device_status() == 0
+
+    # the same layer steps captured once in a CUDA graph and replayed: the host's per-launch work
+    # leaves the loop (reported beside the stream-launched number, not instead of it)
+    graph = None
+    if rank == 0:
+        try:
+            cap = torch.cuda.Stream(dev)
+            cs = int(cap.cuda_stream)
+            n_graph = 16  # layer steps per graph, over rotating weight copies
+            g = torch.cuda.CUDAGraph()
+            cap.wait_stream(stream)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+                for i in range(n_graph):
+                    _, _, dref, gref, uref = pairs[i % N_COPIES]
+                    rc = lib.dense_layer_int4(gref, uref, dref, xp, qg.QG_X_BF16, yp, wsp, ws_bytes, cs)
+                    if rc != 0:
+                        raise RuntimeError(f"dense_layer_int4 returned {rc} under capture")
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            reps = max(4, args.steps // n_graph)
+            cur = torch.cuda.current_stream(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            for _ in range(reps):
+                g.replay()
+            e1.record(cur)
+            torch.cuda.synchronize()
+            g_us = e0.elapsed_time(e1) * 1e3 / (reps * n_graph)
+            graph = {"us_per_layer": round(g_us, 3), "GBps": round(B_LAYER / (g_us * 1e-6) / 1e9, 1),
+                     "steps_per_graph": n_graph, "replays": reps, "pdl_edges": not args.no_pdl}
+            assert qg.qg_device_status() == 0
+        except Exception as e:  # noqa: BLE001  (reported, not allowed to drop the line)
+            graph = {"error": f"{type(e).__name__}: {e}"}
     qg.qg_set_pdl(False)
 
     if rank != 0:
@@ -311,6 +346,7 @@ def run_qg(args, rank, world, local_rank):
                 "transfer": "x read by a GPU copy kernel from pinned host memory, y written by the "
                             "down kernel into pinned host memory (NVLink-C2C), every step",
                 "gpu_launches_per_step": 3},
+        "graph": graph,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "configs": configs,
