@@ -97,7 +97,27 @@ def _torch():
 
 
 def _ptr(t) -> int:
-    return 0 if t is None else int(t.data_ptr())
+    """Address of a device tensor for the C ABI (None -> 0).  The calls read and write flat device
+    arrays, so a tensor on the host or a non-contiguous view is refused here, before any launch."""
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise QGError(QG_EINVAL, f"expected a CUDA tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise QGError(QG_EINVAL, "expected a contiguous tensor")
+    return int(t.data_ptr())
+
+
+def _hptr(t) -> int:
+    """Address of a host tensor for the host-buffer calls (the library checks that it is
+    page-locked)."""
+    if t is None:
+        return 0
+    if t.is_cuda:
+        raise QGError(QG_EINVAL, "expected a host tensor")
+    if not t.is_contiguous():
+        raise QGError(QG_EINVAL, "expected a contiguous tensor")
+    return int(t.data_ptr())
 
 
 def _stream(stream) -> int:
@@ -370,7 +390,7 @@ def dense_layer_int4_host(gate: Int4Weight, up: Int4Weight, down: Int4Weight, x_
         workspace = torch.empty(qg_workspace_bytes(QG_OP_LAYER_HOST, down, gate.in_dim), dtype=torch.uint8,
                                 device=device)
     _check(lib.dense_layer_int4_host(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
-                                     _ptr(x_host), _xtype(x_host), _ptr(y_host), _ptr(workspace),
+                                     _hptr(x_host), _xtype(x_host), _hptr(y_host), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream)),
            "dense_layer_int4_host")
     return y_host

@@ -164,3 +164,19 @@ def test_workspace_sizes_of_the_later_ops(lib):
         assert b >= rows * (2048 * 2 + 768 * 4 * 2 + 768 * 2 + 2048 * 4)
     assert sizes == sorted(sizes)
     assert lib.qg_workspace_bytes(6, ctypes.byref(down), 0) == 0
+
+
+def test_binding_refuses_host_and_strided_tensors():
+    """The Python binding passes flat device arrays to the C ABI: a host tensor or a strided view
+    where device memory is expected is refused before any call (QG_EINVAL)."""
+    torch = pytest.importorskip("torch")
+    from moe_int4_affine_gb300 import qg
+
+    with pytest.raises(qg.QGError) as e:
+        qg._ptr(torch.zeros(8))
+    assert e.value.code == qg.QG_EINVAL
+    t = torch.zeros(4, 4)
+    with pytest.raises(qg.QGError):
+        qg._hptr(t.t())  # a transposed (non-contiguous) view
+    assert qg._hptr(t) == t.data_ptr()
+    assert qg._ptr(None) == 0 and qg._hptr(None) == 0
