@@ -120,6 +120,14 @@ def _hptr(t) -> int:
     return int(t.data_ptr())
 
 
+def _need(what: str, n: int, *ts) -> None:
+    """The kernels read and write whole vectors through plain pointers: a tensor shorter than the
+    call needs is refused here (QG_EINVAL) instead of being read or written past its end."""
+    for t in ts:
+        if t is not None and t.numel() < n:
+            raise QGError(QG_EINVAL, f"{what}: {t.numel()} elements where the call needs {n}")
+
+
 def _stream(stream) -> int:
     if stream is None:
         return int(_torch().cuda.current_stream().cuda_stream)
@@ -187,6 +195,8 @@ def qgemv_int4(w: Int4Weight, x, y=None, stream=None):
     torch = _torch()
     if y is None:
         y = torch.empty(w.out, dtype=torch.float32, device=x.device)
+    _need("x", w.in_dim, x)
+    _need("y", w.out, y)
     _check(lib.qgemv_int4(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(y), _stream(stream)), "qgemv_int4")
     return y
 
@@ -199,6 +209,9 @@ def qgemv_int4_multi(ws, x, ys=None, epilogue: str = "none", stream=None):
         ys = [torch.empty(w.out, dtype=torch.float32, device=x.device) for w in ws]
         if epi == QG_EPI_SWIGLU:
             ys[1] = None
+    _need("x", ws[0].in_dim, x)
+    for w, y_ in zip(ws, ys):
+        _need("y", w.out, y_)
     arr = (qg_int4_weight * n)(*[w.struct for w in ws])
     yp = (_P * n)(*[_ptr(y) for y in ys])
     _check(lib.qgemv_int4_multi(n, arr, _ptr(x), _xtype(x), yp, epi, _stream(stream)), "qgemv_int4_multi")
@@ -210,6 +223,8 @@ def qgemv_q2(w: Int4Weight, x, y=None, stream=None):
     torch = _torch()
     if y is None:
         y = torch.empty(w.out, dtype=torch.float32, device=x.device)
+    _need("x", w.in_dim, x)
+    _need("y", w.out, y)
     _check(lib.qgemv_q2(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(y), _stream(stream)), "qgemv_q2")
     return y
 
@@ -222,6 +237,9 @@ def qgemv_q2_multi(ws, x, ys=None, epilogue: str = "none", stream=None):
         ys = [torch.empty(w.out, dtype=torch.float32, device=x.device) for w in ws]
         if epi == QG_EPI_SWIGLU:
             ys[1] = None
+    _need("x", ws[0].in_dim, x)
+    for w, y_ in zip(ws, ys):
+        _need("y", w.out, y_)
     arr = (qg_int4_weight * n)(*[w.struct for w in ws])
     yp = (_P * n)(*[_ptr(y) for y in ys])
     _check(lib.qgemv_q2_multi(n, arr, _ptr(x), _xtype(x), yp, epi, _stream(stream)), "qgemv_q2_multi")
@@ -233,6 +251,8 @@ def rmsnorm_qgemv_int4(w: Int4Weight, x, gamma, eps: float = 1e-6, y=None, strea
     torch = _torch()
     if y is None:
         y = torch.empty(w.out, dtype=torch.float32, device=x.device)
+    _need("x, gamma", w.in_dim, x, gamma)
+    _need("y", w.out, y)
     _check(lib.rmsnorm_qgemv_int4(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(gamma), float(eps), _ptr(y),
                                   _stream(stream)), "rmsnorm_qgemv_int4")
     return y
@@ -246,6 +266,9 @@ def rmsnorm_qgemv_int4_multi(ws, x, gamma, eps: float = 1e-6, ys=None, epilogue:
         ys = [torch.empty(w.out, dtype=torch.float32, device=x.device) for w in ws]
         if epi == QG_EPI_SWIGLU:
             ys[1] = None
+    _need("x, gamma", ws[0].in_dim, x, gamma)
+    for w, y_ in zip(ws, ys):
+        _need("y", w.out, y_)
     arr = (qg_int4_weight * n)(*[w.struct for w in ws])
     yp = (_P * n)(*[_ptr(y) for y in ys])
     _check(lib.rmsnorm_qgemv_int4_multi(n, arr, _ptr(x), _xtype(x), _ptr(gamma), float(eps), yp, epi,
@@ -258,6 +281,9 @@ def qgemv_int4_sigmoid_fma(w: Int4Weight, x, gate, base, residual=None, y=None, 
     torch = _torch()
     if y is None:
         y = torch.empty(w.out, dtype=torch.float32, device=x.device)
+    _need("x", w.in_dim, x)
+    _need("gate", 1, gate)
+    _need("base, residual, y", w.out, base, residual, y)
     _check(lib.qgemv_int4_sigmoid_fma(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(gate), _ptr(base),
                                       _ptr(residual), _ptr(y), _stream(stream)), "qgemv_int4_sigmoid_fma")
     return y
@@ -269,6 +295,8 @@ def sigmoid_scalar_fma_residual(gate, value, base, residual=None, out=None, stre
     n = value.numel()
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=value.device)
+    _need("gate", 1, gate)
+    _need("base, residual, out", n, base, residual, out)
     _check(lib.sigmoid_scalar_fma_residual(_ptr(gate), _ptr(value), _ptr(base), _ptr(residual), _ptr(out), n,
                                            _stream(stream)), "sigmoid_scalar_fma_residual")
     return out
@@ -280,6 +308,7 @@ def moe_router_topk(logits, k: int = 8, renorm: bool = True, idx=None, p=None, s
         idx = torch.empty(k, dtype=torch.int32, device=logits.device)
     if p is None:
         p = torch.empty(k, dtype=torch.float32, device=logits.device)
+    _need("idx, p", k, idx, p)
     _check(lib.moe_router_topk(_ptr(logits), logits.numel(), k, 1 if renorm else 0, _ptr(idx), _ptr(p),
                                _stream(stream)), "moe_router_topk")
     return idx, p
@@ -298,6 +327,9 @@ def moe_gather_qgemv_int4(gate: Int4Weight, up: Int4Weight, down: Int4Weight, id
     need = qg_workspace_bytes(QG_OP_MOE, down, k)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _need("p", k, p)
+    _need("x", gate.in_dim, x)
+    _need("residual, y", down.out, residual, y)
     fn = lib.moe_gather_qgemv_int4 if bits == 4 else lib.moe_gather_qgemv_q2
     _check(fn(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
               _ptr(idx), _ptr(p), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(workspace),
@@ -320,6 +352,10 @@ def moe_layer_int4(logits, gate: Int4Weight, up: Int4Weight, down: Int4Weight, x
     need = qg_workspace_bytes(QG_OP_MOE, down, k)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _need("logits", gate.n_mat, logits)
+    _need("x", gate.in_dim, x)
+    _need("residual, y", down.out, residual, y)
+    _need("idx, p", k, idx, p)
     fn = lib.moe_layer_int4 if bits == 4 else lib.moe_layer_q2
     _check(fn(_ptr(logits), 1 if renorm else 0, ctypes.byref(gate.struct), ctypes.byref(up.struct),
               ctypes.byref(down.struct), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(idx), _ptr(p),
@@ -336,6 +372,8 @@ def gated_rmsnorm_qgemv_int4(w: Int4Weight, y, z, gamma, eps: float, head_dim: i
         out = torch.empty(w.out, dtype=torch.float32, device=y.device)
     if workspace is None:
         workspace = torch.empty(qg_workspace_bytes(QG_OP_GATED_NORM, w, 0), dtype=torch.uint8, device=y.device)
+    _need("y, z, gamma", w.in_dim, y, z, gamma)
+    _need("out", w.out, out)
     _check(lib.gated_rmsnorm_qgemv_int4(ctypes.byref(w.struct), _ptr(y), _ptr(z), _xtype(y), _ptr(gamma), float(eps),
                                         int(head_dim), _ptr(out), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -358,6 +396,10 @@ def moe_prefill_int4(logits, gate: Int4Weight, up: Int4Weight, down: Int4Weight,
         p = torch.empty((T, k), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = torch.empty(max(qg_workspace_bytes(QG_OP_MOE_PREFILL, down, T), 16), dtype=torch.uint8, device=dev)
+    _need("logits", T * gate.n_mat, logits)
+    _need("X, residual", T * gate.in_dim, X, residual)
+    _need("Y", T * down.out, Y)
+    _need("idx, p", T * k, idx, p)
     _check(lib.moe_prefill_int4(_ptr(logits), T, 1 if renorm else 0, ctypes.byref(gate.struct), ctypes.byref(up.struct),
                                 ctypes.byref(down.struct), k, _ptr(X), _ptr(residual), _ptr(Y), _ptr(idx), _ptr(p),
                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -374,6 +416,8 @@ def dense_layer_int4(gate: Int4Weight, up: Int4Weight, down: Int4Weight, x, y=No
         y = torch.empty(down.out, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = torch.empty(qg_workspace_bytes(QG_OP_LAYER, down, 0), dtype=torch.uint8, device=dev)
+    _need("x", gate.in_dim, x)
+    _need("y", down.out, y)
     _check(lib.dense_layer_int4(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
                                 _ptr(x), _xtype(x), _ptr(y), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -389,6 +433,8 @@ def dense_layer_int4_host(gate: Int4Weight, up: Int4Weight, down: Int4Weight, x_
     if workspace is None:
         workspace = torch.empty(qg_workspace_bytes(QG_OP_LAYER_HOST, down, gate.in_dim), dtype=torch.uint8,
                                 device=device)
+    _need("x_host", gate.in_dim, x_host)
+    _need("y_host", down.out, y_host)
     _check(lib.dense_layer_int4_host(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
                                      _hptr(x_host), _xtype(x_host), _hptr(y_host), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -400,6 +446,9 @@ def moe_gather_qgemv_int4_noalloc(gate: Int4Weight, up: Int4Weight, down: Int4We
                                   stream=None):
     """moe_gather_qgemv_int4 with the library's fixed scratch; `y` must be supplied (nothing is
     allocated on this path)."""
+    _need("p", idx.numel(), p)
+    _need("x", gate.in_dim, x)
+    _need("residual, y", down.out, residual, y)
     _check(lib.moe_gather_qgemv_int4_noalloc(ctypes.byref(gate.struct), ctypes.byref(up.struct),
                                              ctypes.byref(down.struct), _ptr(idx), _ptr(p), idx.numel(), _ptr(x),
                                              _ptr(residual), _ptr(y), _stream(stream)),
@@ -412,6 +461,9 @@ def scalar_fma_chain8_residual(p, v, residual, out=None, stream=None):
     n = residual.numel()
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=v.device)
+    _need("p", 8, p)
+    _need("v", 8 * n, v)
+    _need("out", n, out)
     _check(lib.scalar_fma_chain8_residual(_ptr(p), _ptr(v), _ptr(residual), _ptr(out), n, _stream(stream)),
            "scalar_fma_chain8_residual")
     return out
@@ -440,6 +492,9 @@ def qgemm_int4_multi(ws, X, Ys=None, workspace=None, stream=None):
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _need("X", T * ws[0].in_dim, X)
+    for w, y_ in zip(ws, Ys):
+        _need("Y", T * w.out, y_)
     arr = (qg_int4_weight * n)(*[w.struct for w in ws])
     yp = (_P * n)(*[_ptr(y) for y in Ys])
     _check(lib.qgemm_int4_multi(n, arr, _ptr(X), T, yp, _ptr(workspace), nbytes, _stream(stream)), "qgemm_int4_multi")
@@ -455,6 +510,8 @@ def qgemm_int4(w: Int4Weight, X, Y=None, workspace=None, stream=None):
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _need("X", T * w.in_dim, X)
+    _need("Y", T * w.out, Y)
     _check(lib.qgemm_int4(ctypes.byref(w.struct), _ptr(X), T, _ptr(Y), _ptr(workspace), nbytes, _stream(stream)),
            "qgemm_int4")
     return Y

@@ -180,3 +180,15 @@ def test_binding_refuses_host_and_strided_tensors():
         qg._hptr(t.t())  # a transposed (non-contiguous) view
     assert qg._hptr(t) == t.data_ptr()
     assert qg._ptr(None) == 0 and qg._hptr(None) == 0
+
+
+def test_binding_refuses_short_vectors():
+    """A vector shorter than the call needs is refused before the call (QG_EINVAL), not read or
+    written past its end by a kernel."""
+    torch = pytest.importorskip("torch")
+    from moe_int4_affine_gb300 import qg
+
+    qg._need("x", 4, torch.zeros(4), None)
+    with pytest.raises(qg.QGError) as e:
+        qg._need("x", 5, torch.zeros(4))
+    assert e.value.code == qg.QG_EINVAL and "x" in str(e.value)
