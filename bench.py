@@ -356,7 +356,7 @@ def run_qg(args, rank, world, local_rank):
 
 def measure_configs(qg, I, dev, stream):
     """Every configuration of the workload set, timed back to back with CUDA events on `stream`
-    (median of 3 runs).  Weights rotate over enough copies to exceed L2 unless noted."""
+    (median of 5 runs of at least 50 calls).  Weights rotate over enough copies to exceed L2 unless noted."""
     import ctypes
 
     import torch
@@ -368,13 +368,14 @@ def measure_configs(qg, I, dev, stream):
     peak_tf = _peak_tflops()
     res = {}
 
-    def tl(fn, n):
+    def tl(fn, n):  # the median of 5 runs of at least 50 back-to-back calls
+        n = max(n, 50)
         for i in range(6):
             assert fn(i) == 0
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ts = []
-        for _ in range(3):
+        for _ in range(5):
             e0.record(stream)
             for i in range(n):
                 fn(i)
