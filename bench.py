@@ -386,7 +386,7 @@ def measure_configs(qg, I, dev, stream):
 
     def copies(w, n):
         return [w] + [qg.Int4Weight(w.packed.clone(), w.scales.clone(), w.biases.clone(), w.out, w.in_dim,
-                                    w.n_mat) for _ in range(n - 1)]
+                                    w.n_mat, bits=w.bits) for _ in range(n - 1)]
 
     def gb(nbytes, us):
         return {"us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
@@ -535,7 +535,7 @@ def measure_configs(qg, I, dev, stream):
     def q2w(seed, tid, out, in_dim):
         d = I.int2_weight(seed, tid, out, in_dim)
         t = lambda a: qg.to_device(a, dev)
-        return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim)
+        return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim, bits=2)
 
     def q2bytes(out, in_dim):
         return out * in_dim // 4 + 4 * out * (in_dim // 64)
@@ -561,7 +561,7 @@ def measure_configs(qg, I, dev, stream):
     def q2stack(tid, out, in_dim):
         d = I.int2_weight(0, tid, out, in_dim, n_mat=E2)
         t = lambda a: qg.to_device(a, dev)
-        return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim, n_mat=E2)
+        return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim, n_mat=E2, bits=2)
     g2, u2, d2 = q2stack(I.TID_GATE, I2, H2), q2stack(I.TID_UP, I2, H2), q2stack(I.TID_DOWN, H2, I2)
     lg2 = [qg.to_device(I.f32_normal(i, I.TID_LOGITS, E2), dev) for i in range(16)]
     x2 = qg.to_device(I.bf16_normal(0, I.TID_X, H2), dev)

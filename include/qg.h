@@ -13,8 +13,8 @@
  * Conventions for every call
  *   - All tensor pointers are DEVICE pointers, owned by the caller, 16-byte aligned.  The library
  *     never allocates, frees or retains them.  Scratch space, where a call needs it, is a
- *     caller-owned device workspace whose size qg_workspace_bytes() reports ([FFAI#14] two-pass
- *     decode commit: scratch buffers "are caller-owned so a decode loop can amortise them").
+ *     caller-owned device workspace whose size qg_workspace_bytes() reports ([FFAI#14], two-pass
+ *     decode attention commit: the caller owns the scratch, so a decode loop reuses it across steps).
  *   - bf16 values are passed as their raw 16-bit patterns (uint16_t).
  *   - `stream` is a cudaStream_t cast to void* (NULL = the legacy default stream).  Every call is
  *     asynchronous on that stream; none synchronises the host except qg_device_status().
@@ -23,9 +23,10 @@
  *     range, a wait that timed out) set bits in a device status word read by qg_device_status().
  *   - Outputs of calls in flight must not alias inputs or outputs of other calls in flight.
  *
- * Weight format ([FFAI#14] commit "moeRouterTopK / dequantGemvInt4ExpertIndexed": stacked
- * "[nExperts, outDim, inDim/8] u32"; [FFAI#14] "(weight, scales, biases, input, output)";
- * [FFAI#14] fast-path preconditions "group_size = 64"; [ds4#844] Q4_64A "BF16 scale/bias"):
+ * Weight format ([FFAI#14], commit moeRouterTopK / dequantGemvInt4ExpertIndexed: expert weights
+ * stacked as u32 words [experts][out][in/8]; the GEMV operands there are the packed weight, its
+ * scales and biases, the input and the output; every fast path there requires groups of 64;
+ * [ds4#844], Q4_64A: one bf16 scale and one bf16 bias per group):
  *   packed  uint32 [n_mat][out][in/8]; element j of a row is the nibble at bits 4*(j%8) of word
  *           j/8 (low nibble first), an unsigned code q in 0..15.
  *   scales  bf16   [n_mat][out][in/64]
@@ -85,12 +86,12 @@ int qgemv_int4(const qg_int4_weight *w, const void *x, int xt, float *y, void *s
 
 /*
  * qgemv_int4_multi -- n in {2,3,4} projections sharing one input vector, one launch ([FFAI#14]
- * "dequantGemvInt4Two/Three/Four", "ffai_batched_qkv_qgemv_fast", "ffai_batched_4_qgemv_fast":
- * x is read once for all projections; "explicit precondition that all packed widths match").
+ * dequantGemvInt4Two/Three/Four, ffai_batched_qkv_qgemv_fast, ffai_batched_4_qgemv_fast: x is
+ * read once for all projections, and the projections must all have the same packed width).
  *   epi = QG_EPI_NONE:   ys[i][r] = sum_j w_i[r][j] x[j]   for each i < n.
  *   epi = QG_EPI_SWIGLU: n must be 2 with ws[0].out == ws[1].out; ws[0] = gate, ws[1] = up and
  *                        ys[0][r] = silu(g[r]) * u[r], silu(g) = g / (1 + exp(-g)) (unclamped,
- *                        [ds4#844] "unclamped SwiGLU"); ys[1] is unused (may be NULL).
+ *                        [ds4#844]: no clamp); ys[1] is unused (may be NULL).
  * ws: host array of n weights, all with the same `in`, n_mat == 1.  ys: host array of n device
  * pointers.  Limits as qgemv_int4.
  */
@@ -122,9 +123,9 @@ int moe_layer_q2(const float *logits, int renorm, const qg_int4_weight *gate, co
                  uint32_t *idx, float *p, void *workspace, size_t ws_bytes, void *stream);
 
 /*
- * rmsnorm_qgemv_int4 -- RMSNorm fused into the GEMV prologue ([FFAI#14] commit wrapping
- * "ffai_rms_norm_qgemv_fast": the normalised activation goes straight into the int4 dequant-GEMV,
- * no round trip of the normalised vector through memory):
+ * rmsnorm_qgemv_int4 -- RMSNorm fused into the GEMV prologue ([FFAI#14], the commit that wraps
+ * ffai_rms_norm_qgemv_fast: the normalised activation feeds the int4 dequant-GEMV directly, and
+ * the normalised vector is never written to memory):
  *   y[r] = sum_j w[r][j] * x[j] * gamma[j] / sqrt( (1/in) sum_i x[i]^2 + eps )
  * (the page names the norm without writing it out; this is the usual RMSNorm with an epsilon
  * inside the root).  x: bf16 or fp32 [in]; gamma: bf16 [in] (device, 16-byte aligned); eps >= 0.
@@ -143,9 +144,9 @@ int rmsnorm_qgemv_int4_multi(int n, const qg_int4_weight *ws, const void *x, int
                              float eps, float *const *ys, int epi, void *stream);
 
 /*
- * qgemv_int4_sigmoid_fma -- the shared-expert step fused into its GEMV ([FFAI#14] scalar-FMA
- * commit, "sigmoidScalarFMAResidual(gate, value, base, residual) -- sigmoid-gated FMA with the
- * post-MoE residual add folded in"; the value is this GEMV's output):
+ * qgemv_int4_sigmoid_fma -- the shared-expert step fused into its GEMV ([FFAI#14], scalar-FMA
+ * commit: sigmoidScalarFMAResidual adds a sigmoid-gated value and the residual to a base in one
+ * pass after the MoE; here the value is this GEMV's output):
  *   y[r] = base[r] + sigmoid(gate[0]) * sum_j w[r][j] x[j]  (+ residual[r] when not NULL)
  * gate: fp32 [1]; base: fp32 [out]; residual: bf16 [out] or NULL; y: fp32 [out] (may equal
  * base); all device, 16-byte aligned.  Other arguments as qgemv_int4.
@@ -154,8 +155,8 @@ int qgemv_int4_sigmoid_fma(const qg_int4_weight *w, const void *x, int x_type, c
                            const uint16_t *residual, float *y, void *stream);
 
 /*
- * sigmoid_scalar_fma_residual -- the same step on its own ([FFAI#14] "sigmoidScalarFMAResidual";
- * with residual NULL, "sigmoidScalarFMA"):
+ * sigmoid_scalar_fma_residual -- the same step on its own ([FFAI#14] sigmoidScalarFMAResidual;
+ * with residual NULL, sigmoidScalarFMA):
  *   out[i] = base[i] + sigmoid(gate[0]) * value[i]  (+ residual[i])
  * gate: fp32 [1]; value, base, out: fp32 [n]; residual: bf16 [n] or NULL (all device). n >= 1.
  */
@@ -163,8 +164,9 @@ int sigmoid_scalar_fma_residual(const float *gate, const float *value, const flo
                                 float *out, int n, void *stream);
 
 /*
- * moe_router_topk -- GPU router ([FFAI#14] commit "moeRouterTopK": logits [nExperts] -> [k] u32
- * indices + [k] weights, no host readback; [FFAI#9] top-K order "(value desc, index asc)").
+ * moe_router_topk -- GPU router ([FFAI#14], commit moeRouterTopK: the logits of all experts in,
+ * k u32 indices and k weights out, nothing read back by the host; [FFAI#9], partial-sort commit:
+ * larger logits first, equal logits by smaller index).
  * Selects the k largest logits, ties to the lower index; slot s holds the s-th selected expert.
  *   renorm = 1: p = softmax over the k selected logits (sums to 1).
  *   renorm = 0: p = softmax over all n_experts logits, read at the selected experts.
@@ -174,8 +176,8 @@ int sigmoid_scalar_fma_residual(const float *gate, const float *value, const flo
 int moe_router_topk(const float *logits, int n_experts, int k, int renorm, uint32_t *idx, float *p, void *stream);
 
 /*
- * moe_gather_qgemv_int4 -- MoE top-K gather decode step ([FFAI#14] commits "moeRouterTopK /
- * dequantGemvInt4ExpertIndexed" and "ffai_moe_down_swiglu_accum_int4_chain8"):
+ * moe_gather_qgemv_int4 -- MoE top-K gather decode step ([FFAI#14], commits moeRouterTopK /
+ * dequantGemvInt4ExpertIndexed and ffai_moe_down_swiglu_accum_int4_chain8):
  *   for slot k: e = idx[k]; g = Wg[e] x; u = Wu[e] x; h_k = silu(g) * u; d_k = Wd[e] h_k
  *   y[i] = residual[i] + sum_k p[k] * d_k[i]
  * gate, up: n_mat = n_experts stacked [inter][hidden] weights; down: n_experts stacked
@@ -208,8 +210,8 @@ int moe_layer_int4(const float *logits, int renorm, const qg_int4_weight *gate, 
 
 /*
  * gated_rmsnorm_qgemv_int4 -- the gated RMSNorm before a projection ([FFAI#14]
- * "gatedRmsNormQgemvInt4Fast": the Mamba2-style silu(z) * w * rmsnorm(y) of the GDN mixer's output,
- * then its out-projection), per head of head_dim consecutive elements:
+ * gatedRmsNormQgemvInt4Fast: a Mamba2-style gated norm, silu(z) * w * rmsnorm(y), on the GDN
+ * mixer's output ahead of its out-projection), per head of head_dim consecutive elements:
  *   x[j] = silu(z[j]) * gamma[j] * y[j] / sqrt(mean over j's head of y^2 + eps),   out = W x
  * head_dim = w->in normalises over the whole vector.  y, z: bf16 or fp32 [in] (x_type, both);
  * gamma: bf16 [in]; out: fp32 [w->out].  workspace: at least qg_workspace_bytes(QG_OP_GATED_NORM, w, 0)
@@ -295,8 +297,9 @@ int moe_gather_qgemv_int4_noalloc(const qg_int4_weight *gate, const qg_int4_weig
 
 /*
  * scalar_fma_chain8_residual -- eight (scalar, vector) pairs accumulated in one pass with the
- * residual folded in ([FFAI#14] scalar-FMA commit: "scalarFMAChain8 ... exact 8-way fused
- * dispatch", "out[i] = base[i] + scalar[0] * value[i]"; "post-MoE residual add folded in"):
+ * residual folded in ([FFAI#14], scalar-FMA commit: scalarFMAChain8 does the eight
+ * scalar-times-vector accumulations of a top-8 MoE in one dispatch, each a base plus a device
+ * scalar times a vector; the residual add after the MoE is fused into the same pass):
  *   out[i] = residual[i] + sum_{k<8} p[k] * v[k][i]
  * p: fp32 [8]; v: fp32 [8][n]; residual: bf16 [n]; out: fp32 [n] (all device).  n >= 1.
  */
@@ -304,8 +307,9 @@ int scalar_fma_chain8_residual(const float *p, const float *v, const uint16_t *r
                                void *stream);
 
 /*
- * qgemm_int4 -- dequant-GEMM for T >= 1 token rows ([FFAI#9] "Ops.dequantGemmDynamicM":
- * "Pads T -> ceil(T/32)*32 with zero rows, dispatches, slices the first T rows back"):
+ * qgemm_int4 -- dequant-GEMM for T >= 1 token rows ([FFAI#9], Ops.dequantGemmDynamicM: the
+ * token count is rounded up to a multiple of 32 with zero rows for the MMA kernel and only the
+ * first T output rows are kept):
  *   Y[t][r] = sum_j w[r][j] * X[t][j],  0 <= t < T.
  * X: bf16 [T][in]; Y: fp32 [T][out].  The caller passes exactly T rows; padding is internal and
  * only the T real rows are written.  w->n_mat must be 1.
@@ -323,7 +327,7 @@ int qgemm_int4(const qg_int4_weight *w, const uint16_t *X, int T, float *Y, void
 
 /*
  * qgemm_int4_multi -- n in {2, 3, 4} projections of the same T tokens ([FFAI#14]
- * "ffai_batched_qkv_qmm_fast" / "ffai_batched_4_qmm_fast": the M > 1 prefill form of the fused
+ * ffai_batched_qkv_qmm_fast / ffai_batched_4_qmm_fast: the M > 1 prefill form of the fused
  * QKV / GDN-input projections, x read once for all of them):
  *   Ys[i][t][r] = sum_j w_i[r][j] * X[t][j]
  * ws[i]: single matrices with the same in; X: bf16 [T][in]; Ys[i]: fp32 [T][ws[i].out] (device).

@@ -36,8 +36,8 @@ int ingest_launch(const void* src_dev_mapped, void* dst, size_t bytes, cudaStrea
                 static_cast<uint4*>(dst), (int)(bytes / 16));
 }
 
-// Gated RMSNorm, one head per block ([FFAI#14] "gatedRmsNormQgemvInt4Fast": the Mamba2-style
-// gated norm silu(z) * w * rmsnorm(y) before the GDN mixer's out-projection), written as fp32 into
+// Gated RMSNorm, one head per block ([FFAI#14] gatedRmsNormQgemvInt4Fast: a Mamba2-style gated
+// norm, silu(z) * w * rmsnorm(y), ahead of the GDN mixer's out-projection), written as fp32 into
 // the workspace for the GEMV that follows:
 //   x[j] = silu(z[j]) * gamma[j] * (y[j] / sqrt(mean over the head of y^2 + eps))
 template <bool F32>

@@ -4,7 +4,7 @@
 //     "ffai_batched_4_qgemv_fast");
 //   * pair: gate/up matrices reduced with SwiGLU, h = silu(W_g x) * (W_u x) -- a dense gate/up
 //     pair, or the k selected experts' gate/up slabs picked on the device from the router's index
-//     array ([FFAI#14] commit "moeRouterTopK / dequantGemvInt4ExpertIndexed");
+//     array ([FFAI#14], commit moeRouterTopK / dequantGemvInt4ExpertIndexed);
 //   * seg (MoE down): one output row is the concatenation of the k selected experts' down rows,
 //     the input the concatenation of p_k * h_k, and the residual is added on the way out
 //     ([FFAI#14] commit "ffai_moe_down_swiglu_accum_int4_chain8").
@@ -16,9 +16,16 @@
 //   * Persistent grid, one CTA of 16 warps per SM.  A CTA owns a contiguous range of rows (one contiguous
 //     byte range of codes per matrix).  (An L2 bulk prefetch of the CTA's whole range at kernel start
 //     was measured slower: the flood of prefetch requests queued the x and code loads behind it.)
-//   * x is read once per CTA and stored in shared memory as 16-bit fixed point per 64-column group
-//     g: X_j = round(x_j * 2^k_g) with 2^k_g putting the group's largest |x| in [2^14, 2^15) (bf16
-//     x: exact for every element within 2^7 of the group's largest; else |X_j - x_j 2^k_g| <= 1/2).
+//   * x is read once per CTA and stored in shared memory as fixed point per 64-column group g, in two
+//     16-bit passes: X_j = round(x_j 2^k_g), 2^k_g putting the group's largest |x| in [2^14, 2^15),
+//     and L_j = round((x_j 2^k_g - X_j) 2^15).  The represented value is x~_j = X_j 2^-k_g (first
+//     pass) or (X_j + L_j 2^-15) 2^-k_g (both); |x~_j - x_j| <= 2^(E_g - 15) or 2^(E_g - 30) with
+//     2^E_g <= max|x_g| < 2^(E_g + 1), and bf16 x is exact for every element within 2^7 (2^22) of
+//     its group's largest.  A unit takes the second pass when one of its 32 groups has a largest |x|
+//     above 16 times its mean |x| (outlier channels), else the first alone.  The bias term uses the
+//     group's sum of the same x~, so a row is the fp32-rounded dot product of W with x~:
+//       |y - W x| <= sum_g eps_g sum_{j in g} |w_j|  (+ fp32 rounding, ~1e-6 relative),
+//     eps_g the pass's bound above.
 //   * Warps are independent.  A work unit is 4 rows (2 for gate/up pairs) x 32 consecutive groups
 //     (2048 columns): lane l handles group 32 c + l of each row, keeps that group of x in registers
 //     for the unit, and reads its 32 bytes of codes per row straight from global memory with two
@@ -26,9 +33,9 @@
 //     next unit's loads are issued before the current unit is computed (two register buffers in
 //     turn); a warp walks its units u = warp, warp + 16, ... without divisions.
 //   * Unpack + dot: two ANDs split a u32 word into the byte codes of its even and sixteen times its
-//     odd nibbles; integer dp2a instructions accumulate q_j * X_j exactly in int32, two products per
-//     instruction.  Per group and row the scale and bias are applied once in fp32:
-//     y += s * (acc * 2^-k_g) + b * sum_g x.
+//     odd nibbles; integer dp2a instructions accumulate q_j * X_j (and q_j * L_j) exactly in int32,
+//     two products per instruction.  Per group and row the scale and bias are applied once in fp32:
+//     y += s * (acc * 2^-k_g) + b * sum_g x~.
 //   * Each unit's row sums go to shared memory; after a CTA barrier they are added in a fixed
 //     order (deterministic), the epilogue (SwiGLU / residual) applied and the outputs written.
 //   * Programmatic dependent launch: the first unit's codes are loaded before griddepcontrol.wait;
@@ -36,6 +43,7 @@
 #pragma once
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 #include <utility>
 
 #include "qg_common.cuh"
@@ -48,6 +56,11 @@ constexpr int kMaxXGroups = 512;  // groups of x: in <= 32768
 enum GemvMode { kDense = 0, kPair = 1, kSeg = 2 };
 constexpr int kThreads = 512;       // 16 warps per CTA, one CTA per SM
 constexpr int kGroupsPerUnit = 32;  // groups of one work unit (one per lane)
+constexpr int kXBytesPerGroup = 272;  // shared memory per group of x: X (128), L (128), factors (16)
+// A group of x takes the second fixed-point pass when its largest |x| exceeds kLoRatio times its
+// mean |x| (sum |x| < (64 / kLoRatio) max |x|): outlier channels, where the first pass alone would
+// leave the group's small entries with a few bits.
+constexpr float kLoSumOverMax = 4.0f;  // 64 / kLoRatio, kLoRatio = 16
 
 // A weight operand: base pointers of a (possibly stacked) weight, and the expert slot whose slab to
 // use (-1: the base itself).
@@ -275,8 +288,9 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
 // Shared memory per CTA: x of group g as 32 u32 (64 int16 values paired for dp2a: per 8-column
 // word w, (X0, X2), (X4, X6), (X1, X3), (X5, X7)) stored at 16-byte slot (w + g) % 8 of the group's
 // 128 bytes -- the rotation keeps a warp's loads (one group per lane, 128 bytes apart) free of bank
-// conflicts; then (2^-k_g, sum of the group's x) per group; then the partial sums [row][NC][chunk];
-// then (STG) the staged copy of x.
+// conflicts; then the second fixed-point pass L in the same layout; then per group (2^-k_g / 16, sum
+// of the first-pass values, sum of the two-pass values, needs-the-second-pass flag); then the
+// partial sums [row][NC][chunk]; then (STG) the staged copy of x.
 // STG: x arrives through one bulk copy (a.stage set by the planner), else the threads load it.
 // BITS: 4 or 2 (the 2-bit variant is built without NORM).
 template <int MODE, int RN, bool STG, bool NORM, int BITS = 4>
@@ -300,9 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   constexpr int NW = kThreads / 32;
   const int G = a.groups;
   const int ngs = a.in / 64;  // groups per segment
-  uint32_t* xq = reinterpret_cast<uint32_t*>(smem);               // [G][32]
-  float2* gsx = reinterpret_cast<float2*>(smem + (size_t)G * 128);  // [G]
-  float* part = reinterpret_cast<float*>(smem + (size_t)G * 136);   // [rows][NC][nkc]
+  uint32_t* xq = reinterpret_cast<uint32_t*>(smem);                      // [G][32] first pass X
+  uint32_t* xl = reinterpret_cast<uint32_t*>(smem + (size_t)G * 128);    // [G][32] second pass L
+  float4* gsx = reinterpret_cast<float4*>(smem + (size_t)G * 256);       // [G]
+  float* part = reinterpret_cast<float*>(smem + (size_t)G * kXBytesPerGroup);  // [rows][NC][nkc]
 
   const int vb = (int)((long long)blockIdx.x * a.total_rows / gridDim.x);
   const int ve = (int)((long long)(blockIdx.x + 1) * a.total_rows / gridDim.x);
@@ -435,46 +450,68 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         if (sub == 0 && g < G) s_gss[g] = pg;
       }
     };
+    // Group g of x (eight values per lane, eight lanes) to fixed point: the first pass
+    // X_j = round(x_j 2^k) with 2^k putting the group's largest |x| in [2^14, 2^15), the second pass
+    // L_j = round((x_j 2^k - X_j) 2^15); x~_j = (X_j + L_j 2^-15) 2^-k.  The per-group sums of the
+    // represented values (first pass alone, and both passes) carry the bias term, so that the code
+    // and bias terms see the same x~ and the whole product is the exact W x~ up to fp32 rounding.
     auto quant = [&](int g, const float (&v)[8]) {
-      float m = 0.f, sx = 0.f;
+      float m = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      // E = floor(log2 max|x|), k = 14 - E: |x| 2^k < 2^15.  Groups whose largest |x| is below
+      // 2^-60 add less than 64 |w| 2^-60 to a row and are dropped (X = L = 0).
+      const bool live = m >= 8.673617e-19f;  // 2^-60
+      int E = max((int)((__float_as_uint(m) >> 23) & 0xFF) - 127, -60);
+      // When max|x| 2^k would round up to 2^15 (fp32 x only: a bf16 max is at most
+      // (2 - 2^-7) 2^14 after scaling), one bit less for this group, so every |X_j| <= 32767.
+      if (live && m * exp2i(14 - E) >= 32767.5f) ++E;
+      const float scale = live ? exp2i(14 - E) : 0.f;  // 14 - E in [-113, 74]
+      // X_j = the low 16 bits of the float x_j 2^k + 1.5 2^23 (the magic-number rule above); the
+      // remainder x_j 2^k - X_j (exact, |.| <= 1/2) scaled by 2^15 gives L_j the same way
+      uint32_t b[8], l[8];
+      float hs = 0.f, ls = 0.f, sa = 0.f;  // sums of X_j and L_j (exact integers), of |x_j|
+      bool lnz = false;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        m = fmaxf(m, fabsf(v[j]));
-        sx += v[j];
+        const float t = fmaf(v[j], scale, 12582912.0f);
+        b[j] = __float_as_uint(t);
+        const float xf = t - 12582912.0f;
+        const float u = fmaf(fmaf(v[j], scale, -xf), 32768.0f, 12582912.0f);
+        l[j] = __float_as_uint(u);
+        const float lf = u - 12582912.0f;
+        hs += xf;
+        ls += lf;
+        sa += fabsf(v[j]);
+        lnz |= lf != 0.f;
       }
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) {
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        sx += __shfl_xor_sync(0xffffffffu, sx, o);
+        hs += __shfl_xor_sync(0xffffffffu, hs, o);
+        ls += __shfl_xor_sync(0xffffffffu, ls, o);
+        sa += __shfl_xor_sync(0xffffffffu, sa, o);
       }
+      // the second pass is needed when it is not all zero and the group's largest |x| is more than
+      // 16 times its mean |x|
+      const bool need = ((__ballot_sync(0xffffffffu, lnz) >> (lane & 24)) & 0xFFu) != 0u && sa < kLoSumOverMax * m;
       if (g < G) {
-        // E = floor(log2 max|x|), k = 14 - E: |x| 2^k < 2^15.  Groups whose largest |x| is below
-        // 2^-60 contribute less than 1e-17 per weight through the code term and are dropped from
-        // it (the bias term keeps the exact sum).
-        const bool live = m >= 8.673617e-19f;  // 2^-60
-        int E = max((int)((__float_as_uint(m) >> 23) & 0xFF) - 127, -60);
-        // When max|x| 2^k would round up to 2^15 (fp32 x only: a bf16 max is at most
-        // (2 - 2^-7) 2^14 after scaling), one bit less for this group, so every |X_j| <= 32767.
-        if (live && m * exp2i(14 - E) >= 32767.5f) ++E;
-        const float scale = live ? exp2i(14 - E) : 0.f;  // 14 - E in [-114, 74]
-        // X_j = the low 16 bits of the float x_j 2^k + 1.5 2^23 (the magic-number rule above), paired
-        // for dp2a as (X0, X2), (X4, X6), (X1, X3), (X5, X7)
-        uint32_t b[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) b[j] = __float_as_uint(fmaf(v[j], scale, 12582912.0f));
-        uint4 pk;
+        // paired for dp2a as (X0, X2), (X4, X6), (X1, X3), (X5, X7); 2-bit: (X0, X4), (X1, X5), ...
+        uint4 pk, pl;
         if constexpr (BITS == 4) {
-          pk.x = __byte_perm(b[0], b[2], 0x5410);
-          pk.y = __byte_perm(b[4], b[6], 0x5410);
-          pk.z = __byte_perm(b[1], b[3], 0x5410);
-          pk.w = __byte_perm(b[5], b[7], 0x5410);
-        } else {  // 2-bit pairs: (X0, X4), (X1, X5), (X2, X6), (X3, X7) (see the main loop)
-          pk.x = __byte_perm(b[0], b[4], 0x5410);
-          pk.y = __byte_perm(b[1], b[5], 0x5410);
-          pk.z = __byte_perm(b[2], b[6], 0x5410);
-          pk.w = __byte_perm(b[3], b[7], 0x5410);
+          pk = make_uint4(__byte_perm(b[0], b[2], 0x5410), __byte_perm(b[4], b[6], 0x5410),
+                          __byte_perm(b[1], b[3], 0x5410), __byte_perm(b[5], b[7], 0x5410));
+          pl = make_uint4(__byte_perm(l[0], l[2], 0x5410), __byte_perm(l[4], l[6], 0x5410),
+                          __byte_perm(l[1], l[3], 0x5410), __byte_perm(l[5], l[7], 0x5410));
+        } else {
+          pk = make_uint4(__byte_perm(b[0], b[4], 0x5410), __byte_perm(b[1], b[5], 0x5410),
+                          __byte_perm(b[2], b[6], 0x5410), __byte_perm(b[3], b[7], 0x5410));
+          pl = make_uint4(__byte_perm(l[0], l[4], 0x5410), __byte_perm(l[1], l[5], 0x5410),
+                          __byte_perm(l[2], l[6], 0x5410), __byte_perm(l[3], l[7], 0x5410));
         }
         reinterpret_cast<uint4*>(xq + (size_t)g * 32)[(sub + g) & 7] = pk;
+        reinterpret_cast<uint4*>(xl + (size_t)g * 32)[(sub + g) & 7] = pl;
         if (sub == 0) {
           float wgt = 1.f;
           if (SEG) {
@@ -483,7 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             wgt = ok ? __ldg(a.p + g / ngs) : 0.f;
           }
           // (2^-k / 16: the odd codes are accumulated sixteen times over, see the main loop)
-          gsx[g] = make_float2(live ? exp2i(E - (BITS == 4 ? 18 : 20)) * wgt : 0.f, sx * wgt);
+          const float kinv = live ? exp2i(E - 14) * wgt : 0.f;
+          gsx[g] = make_float4(live ? exp2i(E - (BITS == 4 ? 18 : 20)) * wgt : 0.f, hs * kinv,
+                               fmaf(ls, 3.0517578125e-05f, hs) * kinv, need ? 1.f : 0.f);
         }
       }
     };
@@ -587,7 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       __syncthreads();
       for (int g = threadIdx.x; g < G; g += kThreads) {
         const float r = s_hrn[g / hg];
-        gsx[g] = make_float2(gsx[g].x * r, gsx[g].y * r);
+        const float4 f = gsx[g];
+        gsx[g] = make_float4(f.x * r, f.y * r, f.z * r, f.w);
       }
       __syncthreads();
     }
@@ -595,57 +635,114 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
   // --- main loop: this warp's units u = warp, warp + NW, ...; two buffers in turn, the next unit's
   // codes in flight while one is computed ---
-  const uint32_t xq_s = smem_u32(xq);
-  auto compute = [&](const UnitLoads<RN>& L, const UnitCursor& c) {
-    const int g = c.kc * kGroupsPerUnit + lane;
-    const int gc = min(g, G - 1);
-    // this lane's group of x, in registers for all RN entries of the unit
-    uint4 X[8];
+  const uint32_t xq_s = smem_u32(xq), xl_s = smem_u32(xl);
+  // The unit's dot products: per entry e the code sums of both passes in exact int32 arithmetic,
+  // word by word (word wd of this lane's group of x from shared memory, the codes in registers).
+  // LO: the second pass as well (taken by the whole warp when any of its 32 groups needs it).
+  auto dot = [&](const UnitLoads<RN>& L, uint32_t xo, auto lo_tag, float (&acc)[RN]) {
+    constexpr bool LO = decltype(lo_tag)::value;
+    if constexpr (BITS == 4 && !LO) {
+      int s0[RN], s1[RN];
 #pragma unroll
-    for (int wd = 0; wd < 8; ++wd) X[wd] = lds128(xq_s + (uint32_t)gc * 128u + (uint32_t)((wd + gc) & 7) * 16u);
-    const float2 gs = gsx[gc];
-    float yp[RN];
+      for (int e = 0; e < RN; ++e) s0[e] = s1[e] = 0;
 #pragma unroll
-    for (int e = 0; e < RN; ++e) {
-      float acc;
-      if constexpr (BITS == 4) {
-        int s0 = 0, s1 = 0;
+      for (int wd = 0; wd < 8; ++wd) {
+        const uint4 X = lds128(xq_s + xo + (uint32_t)((wd + (xo >> 7)) & 7) * 16u);
 #pragma unroll
-        for (int wd = 0; wd < 8; ++wd) {
+        for (int e = 0; e < RN; ++e) {
           const uint4& c4 = wd < 4 ? L.a[e] : L.b[e];
           const int k = wd & 3;
           const uint32_t w = k == 0 ? c4.x : k == 1 ? c4.y : k == 2 ? c4.z : c4.w;
           const uint32_t c0 = w & 0x0F0F0F0Fu;  // codes q0, q2, q4, q6 as bytes
           const uint32_t c1 = w & 0xF0F0F0F0u;  // 16 q1, 16 q3, 16 q5, 16 q7
-          s0 = dp2a_lo(X[wd].x, c0, s0);
-          s0 = dp2a_hi(X[wd].y, c0, s0);
-          s1 = dp2a_lo(X[wd].z, c1, s1);
-          s1 = dp2a_hi(X[wd].w, c1, s1);
+          s0[e] = dp2a_hi(X.y, c0, dp2a_lo(X.x, c0, s0[e]));
+          s1[e] = dp2a_hi(X.w, c1, dp2a_lo(X.z, c1, s1[e]));
         }
-        // |s0| <= 32 * 15 * 32767 and |s1| <= 16 times that: 16 s0 + s1 < 2^29, exact in int32
-        // (rounded once to float, relative error 2^-24); gs.x carries the matching 1/16
-        acc = (float)(s0 * 16 + s1);
-      } else {
-        // 2-bit: word k holds columns 16k .. 16k + 15 at bits 2i; masks 3 << 2m pick codes
-        // m, m + 4, m + 8, m + 12 as bytes (times 4^m), paired with (X_m, X_m+4) of x's word 2k
-        // and (X_m+8, X_m+12) of word 2k + 1
-        int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t w = k == 0 ? L.a[e].x : k == 1 ? L.a[e].y : k == 2 ? L.a[e].z : L.a[e].w;
-          const uint4& A = X[2 * k];
-          const uint4& B = X[2 * k + 1];
-          const uint32_t c0 = w & 0x03030303u, c1 = w & 0x0C0C0C0Cu, c2 = w & 0x30303030u, c3 = w & 0xC0C0C0C0u;
-          s0 = dp2a_hi(B.x, c0, dp2a_lo(A.x, c0, s0));
-          s1 = dp2a_hi(B.y, c1, dp2a_lo(A.y, c1, s1));
-          s2 = dp2a_hi(B.z, c2, dp2a_lo(A.z, c2, s2));
-          s3 = dp2a_hi(B.w, c3, dp2a_lo(A.w, c3, s3));
-        }
-        // |s_m| <= 4^m * 16 * 3 * 32767: 64 s0 + 16 s1 + 4 s2 + s3 < 2^29, exact; gs.x carries 1/64
-        acc = (float)(s0 * 64 + s1 * 16 + s2 * 4 + s3);
       }
-      yp[e] = fmaf(bf16_bits_to_f32(L.s[e]), acc * gs.x, bf16_bits_to_f32(L.t[e]) * gs.y);
+      // |s0| <= 32 * 15 * 32767 and |s1| <= 16 times that: 16 s0 + s1 < 2^29, exact in int32
+      // (rounded once to float, relative error 2^-24); the group factor carries the matching 1/16
+#pragma unroll
+      for (int e = 0; e < RN; ++e) acc[e] = (float)(s0[e] * 16 + s1[e]);
+    } else if constexpr (BITS == 4) {
+      // both passes; each pass in one accumulator, its even codes as bytes 16 q (one shift), so
+      // that both sums are 16 sum q X: |.| <= 64 * 240 * 32767 < 2^31 (second pass: half that)
+      int s[RN], t[RN];
+#pragma unroll
+      for (int e = 0; e < RN; ++e) s[e] = t[e] = 0;
+#pragma unroll
+      for (int wd = 0; wd < 8; ++wd) {
+        const uint32_t ofs = xo + (uint32_t)((wd + (xo >> 7)) & 7) * 16u;
+        const uint4 X = lds128(xq_s + ofs), Lw = lds128(xl_s + ofs);
+#pragma unroll
+        for (int e = 0; e < RN; ++e) {
+          const uint4& c4 = wd < 4 ? L.a[e] : L.b[e];
+          const int k = wd & 3;
+          const uint32_t w = k == 0 ? c4.x : k == 1 ? c4.y : k == 2 ? c4.z : c4.w;
+          const uint32_t c0 = (w & 0x0F0F0F0Fu) << 4;  // 16 q0, 16 q2, 16 q4, 16 q6
+          const uint32_t c1 = w & 0xF0F0F0F0u;         // 16 q1, 16 q3, 16 q5, 16 q7
+          s[e] = dp2a_hi(X.w, c1, dp2a_lo(X.z, c1, dp2a_hi(X.y, c0, dp2a_lo(X.x, c0, s[e]))));
+          t[e] = dp2a_hi(Lw.w, c1, dp2a_lo(Lw.z, c1, dp2a_hi(Lw.y, c0, dp2a_lo(Lw.x, c0, t[e]))));
+        }
+      }
+      // the second pass weighs 2^-15 (rounded once to float each, then one fused add)
+#pragma unroll
+      for (int e = 0; e < RN; ++e) acc[e] = fmaf((float)t[e], 3.0517578125e-05f, (float)s[e]);
+    } else {
+      // 2-bit: word k holds columns 16k .. 16k + 15 at bits 2i; masks 3 << 2m pick codes
+      // m, m + 4, m + 8, m + 12 as bytes (times 4^m), paired with (X_m, X_m+4) of x's word 2k
+      // and (X_m+8, X_m+12) of word 2k + 1
+      int s0[RN], s1[RN], s2[RN], s3[RN], t0[RN], t1[RN], t2[RN], t3[RN];
+#pragma unroll
+      for (int e = 0; e < RN; ++e) s0[e] = s1[e] = s2[e] = s3[e] = t0[e] = t1[e] = t2[e] = t3[e] = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t oa = xo + (uint32_t)((2 * k + (xo >> 7)) & 7) * 16u;
+        const uint32_t ob = xo + (uint32_t)((2 * k + 1 + (xo >> 7)) & 7) * 16u;
+        const uint4 A = lds128(xq_s + oa), B = lds128(xq_s + ob);
+        uint4 LA, LB;
+        if constexpr (LO) {
+          LA = lds128(xl_s + oa);
+          LB = lds128(xl_s + ob);
+        }
+#pragma unroll
+        for (int e = 0; e < RN; ++e) {
+          const uint32_t w = k == 0 ? L.a[e].x : k == 1 ? L.a[e].y : k == 2 ? L.a[e].z : L.a[e].w;
+          const uint32_t c0 = w & 0x03030303u, c1 = w & 0x0C0C0C0Cu, c2 = w & 0x30303030u, c3 = w & 0xC0C0C0C0u;
+          s0[e] = dp2a_hi(B.x, c0, dp2a_lo(A.x, c0, s0[e]));
+          s1[e] = dp2a_hi(B.y, c1, dp2a_lo(A.y, c1, s1[e]));
+          s2[e] = dp2a_hi(B.z, c2, dp2a_lo(A.z, c2, s2[e]));
+          s3[e] = dp2a_hi(B.w, c3, dp2a_lo(A.w, c3, s3[e]));
+          if constexpr (LO) {
+            t0[e] = dp2a_hi(LB.x, c0, dp2a_lo(LA.x, c0, t0[e]));
+            t1[e] = dp2a_hi(LB.y, c1, dp2a_lo(LA.y, c1, t1[e]));
+            t2[e] = dp2a_hi(LB.z, c2, dp2a_lo(LA.z, c2, t2[e]));
+            t3[e] = dp2a_hi(LB.w, c3, dp2a_lo(LA.w, c3, t3[e]));
+          }
+        }
+      }
+      // |s_m| <= 4^m * 16 * 3 * 32767: 64 s0 + 16 s1 + 4 s2 + s3 < 2^29, exact; gs.x carries 1/64
+#pragma unroll
+      for (int e = 0; e < RN; ++e) {
+        acc[e] = (float)(s0[e] * 64 + s1[e] * 16 + s2[e] * 4 + s3[e]);
+        if constexpr (LO)
+          acc[e] = fmaf((float)(t0[e] * 64 + t1[e] * 16 + t2[e] * 4 + t3[e]), 3.0517578125e-05f, acc[e]);
+      }
     }
+  };
+  auto compute = [&](const UnitLoads<RN>& L, const UnitCursor& c) {
+    const int g = c.kc * kGroupsPerUnit + lane;
+    const int gc = min(g, G - 1);
+    const float4 gs = gsx[gc];
+    const bool lo = __any_sync(0xffffffffu, gs.w != 0.f);
+    float acc[RN];
+    if (lo)
+      dot(L, (uint32_t)gc * 128u, std::true_type{}, acc);
+    else
+      dot(L, (uint32_t)gc * 128u, std::false_type{}, acc);
+    const float xsum = lo ? gs.z : gs.y;  // the group's sum of the represented x
+    float yp[RN];
+#pragma unroll
+    for (int e = 0; e < RN; ++e) yp[e] = fmaf(bf16_bits_to_f32(L.s[e]), acc[e] * gs.x, bf16_bits_to_f32(L.t[e]) * xsum);
     const float tot = warp_sum_rows<RN>(yp, lane);
     if ((lane & (32 / RN - 1)) == 0) {
       const int e = (lane * RN) >> 5;
@@ -807,7 +904,7 @@ extern GemvTune g_gemv_tune;
 
 inline size_t gemv_smem_bytes(int groups, int rows_per_cta, int nc) {
   const int nkc = (groups + kGroupsPerUnit - 1) / kGroupsPerUnit;
-  return (size_t)groups * 136 + (size_t)rows_per_cta * nc * nkc * 4;
+  return (size_t)groups * kXBytesPerGroup + (size_t)rows_per_cta * nc * nkc * 4;
 }
 
 // Shared memory with the x staging area after `base` bytes, or `base` alone (staging off).  Staging
@@ -822,7 +919,7 @@ inline size_t plan_stage(GemvArgs& a, size_t base, size_t limit) {
   a.stage_off = a.stage ? (int)off : 0;
   return a.stage ? total : base;
 }
-constexpr size_t kStaticSmemReserve = 1024;  // the kernels' static shared variables
+constexpr size_t kStaticSmemReserve = 8192;  // the kernels' static shared variables (NORM: 4.2 KB)
 
 template <int MODE, int RN, bool STG, bool NORM, int BITS = 4>
 int launch_gemv_variant(const GemvArgs& a, int grid, size_t smem, cudaStream_t stream) {
@@ -844,8 +941,8 @@ int plan_and_launch(GemvArgs& a, cudaStream_t stream) {
   a.groups = a.nseg * a.in / 64;
   const int cps = g_gemv_tune.ctas_per_sm ? g_gemv_tune.ctas_per_sm : 1;
   int grid = std::max(1, std::min(cps * dev.num_sms, a.total_rows));
-  // keep the partial-sum buffer within budget (more, smaller CTAs otherwise)
-  const size_t budget = 100 * 1024;
+  // keep x and the partial-sum buffer within the shared memory (more, smaller CTAs otherwise)
+  const size_t budget = (size_t)dev.max_smem_optin - kStaticSmemReserve;
   for (;;) {
     a.rows_per_cta = (a.total_rows + grid - 1) / grid;
     if (gemv_smem_bytes(a.groups, a.rows_per_cta, NC) <= budget || grid >= a.total_rows) break;

@@ -1,7 +1,7 @@
 // gemv_pair.cu -- gate/up pairs reduced with SwiGLU, h = silu(W_g x) * (W_u x): a dense pair, or the
-// k router-selected experts' gate/up slabs of stacked weights ([FFAI#14] "dequantGemvInt4Two --
-// per-expert MoE gate + up projections", commit "moeRouterTopK / dequantGemvInt4ExpertIndexed";
-// SwiGLU unclamped as in [ds4#844]).
+// k router-selected experts' gate/up slabs of stacked weights ([FFAI#14]: dequantGemvInt4Two
+// serves the gate and up projections of each selected expert; commit moeRouterTopK /
+// dequantGemvInt4ExpertIndexed; SwiGLU without a clamp, as in [ds4#844]).
 #include "gemv_kernel.cuh"
 
 namespace qg {

@@ -141,7 +141,7 @@ int chain8_launch(const float* p, const float* v, const uint16_t* residual, floa
   return launch(chain8_kernel, dim3(blocks), dim3(threads), 0, stream, p, v, residual, out, n);
 }
 
-// The shared-expert step ([FFAI#14] scalar-FMA commit, "sigmoidScalarFMAResidual"):
+// The shared-expert step ([FFAI#14], scalar-FMA commit, sigmoidScalarFMAResidual):
 //   out[i] = base[i] + sigmoid(gate) * value[i] (+ resid[i])
 // gate read once per thread from device memory; 16-byte vectors when n % 4 == 0.
 __global__ void __launch_bounds__(256) sigmoid_fma_kernel(const float* __restrict__ gate, const float* __restrict__ value,

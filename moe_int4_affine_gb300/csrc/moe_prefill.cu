@@ -13,7 +13,7 @@
 //   7. combine    y[t] = residual[t] + sum_s p[t][s] * D[row of (t, s)]      (slot order)
 // Each (token, slot) row is computed independently of the others, so the order of the rows within
 // an expert's group (set by atomics in the plan) does not change any result.
-// ([FFAI#9] "moeGatherDequantGemmInt4" / "mt_moe_gather_qmm_int4": the T*topK rows sorted by
+// ([FFAI#9] moeGatherDequantGemmInt4 / mt_moe_gather_qmm_int4: the T*topK rows sorted by
 // expert with CSR expert offsets, in row tiles of 8 to 64, built there from the top-K indices on
 // the host; it loses to per-expert dispatches at T = 1 and is meant for prefill.  Here the offsets
 // are built on the device, so no index readback precedes the expert GEMMs.)

@@ -18,25 +18,30 @@ static __device__ __align__(256) float g_noalloc_h[QG_NOALLOC_MOE_MAX_FLOATS];
 
 namespace {
 constexpr int kMaxDev = 64;
-float* g_h_ptr[kMaxDev];
-int g_h_err[kMaxDev];
-std::once_flag g_h_once[kMaxDev];
+float* g_h_ptr[kMaxDev];  // the array's device address per device, once resolved (null before)
+std::mutex g_h_mutex;
 
-// Device address of the scratch array on the current device, resolved once per device (with that
-// device current) on the first call made on it.
+// Device address of the scratch array on the current device, resolved with that device current on
+// the first call made on it.  Only a successful lookup is kept: after a failure (its error cleared
+// from the runtime's last-error state) the next call tries again.
 float* scratch_for_current_device(int* err) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    (void)cudaGetLastError();
     *err = QG_EDEVICE;
     return nullptr;
   }
-  std::call_once(g_h_once[dev], [dev]() {
+  std::lock_guard<std::mutex> lock(g_h_mutex);
+  if (!g_h_ptr[dev]) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_h);
-    g_h_err[dev] = e == cudaSuccess && p ? QG_OK : QG_EDEVICE;
+    if (cudaGetSymbolAddress(&p, g_noalloc_h) != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      *err = QG_EDEVICE;
+      return nullptr;
+    }
     g_h_ptr[dev] = static_cast<float*>(p);
-  });
-  *err = g_h_err[dev];
+  }
+  *err = QG_OK;
   return g_h_ptr[dev];
 }
 }  // namespace

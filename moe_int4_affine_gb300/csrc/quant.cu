@@ -1,5 +1,6 @@
-// quant.cu -- affine group-64 quantizer (encode) for the Q4_64A / Q2_64A formats ([ds4#844]:
-// "Q4_64A and Q2_64A codes are derived from the serialized BF16 scale/bias"):
+// quant.cu -- affine group-64 quantizer (encode) for the Q4_64A / Q2_64A formats ([ds4#844],
+// Q4_64A / Q2_64A commit: the codes are computed from the scale and bias after their rounding to
+// bf16, the values that are stored):
 //   per group of 64 weights: lo = min, hi = max (a zero of either sign taken as +0);
 //   scale = (hi - lo) / (2^bits - 1); bias = lo; s = bf16(scale), b = bf16(bias) (nearest, ties to even);
 //   q_j = clamp(rint((w_j - b) / s), 0, 2^bits - 1)   (0 when s = 0)

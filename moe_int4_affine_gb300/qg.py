@@ -120,11 +120,22 @@ def _hptr(t) -> int:
     return int(t.data_ptr())
 
 
-def _need(what: str, n: int, *ts) -> None:
-    """The kernels read and write whole vectors through plain pointers: a tensor shorter than the
-    call needs is refused here (QG_EINVAL) instead of being read or written past its end."""
+_DT_NAMES = {"f32": ("float32",), "bf16": ("bfloat16",), "i32": ("int32",), "x": ("bfloat16", "float32")}
+
+
+def _need(what: str, n: int, *ts, dt: str) -> None:
+    """The kernels read and write whole vectors of a fixed element type through plain pointers: a
+    tensor of another dtype, or shorter than the call needs, is refused here (QG_EINVAL) instead
+    of being read or written past its end.  dt: "f32", "bf16", "i32" (uint32 indices) or "x"
+    (bf16 or fp32, the type the call is told)."""
+    torch = _torch()
+    ok = tuple(getattr(torch, d) for d in _DT_NAMES[dt])
     for t in ts:
-        if t is not None and t.numel() < n:
+        if t is None:
+            continue
+        if t.dtype not in ok:
+            raise QGError(QG_EINVAL, f"{what}: dtype {t.dtype} where the call needs {' or '.join(_DT_NAMES[dt])}")
+        if t.numel() < n:
             raise QGError(QG_EINVAL, f"{what}: {t.numel()} elements where the call needs {n}")
 
 
@@ -160,9 +171,18 @@ def to_numpy(t) -> np.ndarray:
 class Int4Weight:
     """Device tensors of one int4 affine weight (or a stack of n_mat expert weights)."""
 
-    def __init__(self, packed, scales, biases, out: int, in_dim: int, n_mat: int = 1, group_size: int = 64):
+    def __init__(self, packed, scales, biases, out: int, in_dim: int, n_mat: int = 1, group_size: int = 64,
+                 bits: int = 4):
+        """bits: 4 (Q4_64A, packed [n_mat][out][in/8]) or 2 (Q2_64A, packed [n_mat][out][in/16])."""
         self.packed, self.scales, self.biases = packed, scales, biases
         self.out, self.in_dim, self.n_mat, self.group_size = int(out), int(in_dim), int(n_mat), int(group_size)
+        if bits not in (2, 4):
+            raise QGError(QG_EINVAL, f"bits must be 2 or 4, got {bits}")
+        self.bits = bits
+        if self.group_size == 64 and self.in_dim % 64 == 0 and self.out > 0 and self.n_mat > 0:
+            rows = self.n_mat * self.out
+            _need("packed", rows * self.in_dim * bits // 32, packed, dt="i32")
+            _need("scales, biases", rows * (self.in_dim // 64), scales, biases, dt="bf16")
         self._s = qg_int4_weight(_ptr(packed), _ptr(scales), _ptr(biases), self.out, self.in_dim,
                                  self.group_size, self.n_mat)
 
@@ -175,6 +195,10 @@ class Int4Weight:
             (out, w), n_mat = packed.shape, 1
         return cls(to_device(packed, device), to_device(d["scales"], device), to_device(d["biases"], device),
                    out, w * 8, n_mat)
+
+    def _bits(self, bits: int, where: str) -> None:
+        if self.bits != bits:
+            raise QGError(QG_EINVAL, f"{where}: a {self.bits}-bit weight where the call takes {bits}-bit codes")
 
     @property
     def struct(self) -> qg_int4_weight:
@@ -195,8 +219,9 @@ def qgemv_int4(w: Int4Weight, x, y=None, stream=None):
     torch = _torch()
     if y is None:
         y = torch.empty(w.out, dtype=torch.float32, device=x.device)
-    _need("x", w.in_dim, x)
-    _need("y", w.out, y)
+    _need("x", w.in_dim, x, dt="x")
+    _need("y", w.out, y, dt="f32")
+    w._bits(4, "qgemv_int4")
     _check(lib.qgemv_int4(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(y), _stream(stream)), "qgemv_int4")
     return y
 
@@ -209,11 +234,13 @@ def qgemv_int4_multi(ws, x, ys=None, epilogue: str = "none", stream=None):
         ys = [torch.empty(w.out, dtype=torch.float32, device=x.device) for w in ws]
         if epi == QG_EPI_SWIGLU:
             ys[1] = None
-    _need("x", ws[0].in_dim, x)
+    _need("x", ws[0].in_dim, x, dt="x")
     for w, y_ in zip(ws, ys):
-        _need("y", w.out, y_)
+        _need("y", w.out, y_, dt="f32")
     arr = (qg_int4_weight * n)(*[w.struct for w in ws])
     yp = (_P * n)(*[_ptr(y) for y in ys])
+    for w_ in ws:
+        w_._bits(4, "qgemv_int4_multi")
     _check(lib.qgemv_int4_multi(n, arr, _ptr(x), _xtype(x), yp, epi, _stream(stream)), "qgemv_int4_multi")
     return ys[0] if epi == QG_EPI_SWIGLU else ys
 
@@ -223,8 +250,9 @@ def qgemv_q2(w: Int4Weight, x, y=None, stream=None):
     torch = _torch()
     if y is None:
         y = torch.empty(w.out, dtype=torch.float32, device=x.device)
-    _need("x", w.in_dim, x)
-    _need("y", w.out, y)
+    _need("x", w.in_dim, x, dt="x")
+    _need("y", w.out, y, dt="f32")
+    w._bits(2, "qgemv_q2")
     _check(lib.qgemv_q2(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(y), _stream(stream)), "qgemv_q2")
     return y
 
@@ -237,11 +265,13 @@ def qgemv_q2_multi(ws, x, ys=None, epilogue: str = "none", stream=None):
         ys = [torch.empty(w.out, dtype=torch.float32, device=x.device) for w in ws]
         if epi == QG_EPI_SWIGLU:
             ys[1] = None
-    _need("x", ws[0].in_dim, x)
+    _need("x", ws[0].in_dim, x, dt="x")
     for w, y_ in zip(ws, ys):
-        _need("y", w.out, y_)
+        _need("y", w.out, y_, dt="f32")
     arr = (qg_int4_weight * n)(*[w.struct for w in ws])
     yp = (_P * n)(*[_ptr(y) for y in ys])
+    for w_ in ws:
+        w_._bits(2, "qgemv_q2_multi")
     _check(lib.qgemv_q2_multi(n, arr, _ptr(x), _xtype(x), yp, epi, _stream(stream)), "qgemv_q2_multi")
     return ys[0] if epi == QG_EPI_SWIGLU else ys
 
@@ -251,8 +281,10 @@ def rmsnorm_qgemv_int4(w: Int4Weight, x, gamma, eps: float = 1e-6, y=None, strea
     torch = _torch()
     if y is None:
         y = torch.empty(w.out, dtype=torch.float32, device=x.device)
-    _need("x, gamma", w.in_dim, x, gamma)
-    _need("y", w.out, y)
+    _need("x", w.in_dim, x, dt="x")
+    _need("gamma", w.in_dim, gamma, dt="bf16")
+    _need("y", w.out, y, dt="f32")
+    w._bits(4, "rmsnorm_qgemv_int4")
     _check(lib.rmsnorm_qgemv_int4(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(gamma), float(eps), _ptr(y),
                                   _stream(stream)), "rmsnorm_qgemv_int4")
     return y
@@ -266,11 +298,14 @@ def rmsnorm_qgemv_int4_multi(ws, x, gamma, eps: float = 1e-6, ys=None, epilogue:
         ys = [torch.empty(w.out, dtype=torch.float32, device=x.device) for w in ws]
         if epi == QG_EPI_SWIGLU:
             ys[1] = None
-    _need("x, gamma", ws[0].in_dim, x, gamma)
+    _need("x", ws[0].in_dim, x, dt="x")
+    _need("gamma", ws[0].in_dim, gamma, dt="bf16")
     for w, y_ in zip(ws, ys):
-        _need("y", w.out, y_)
+        _need("y", w.out, y_, dt="f32")
     arr = (qg_int4_weight * n)(*[w.struct for w in ws])
     yp = (_P * n)(*[_ptr(y) for y in ys])
+    for w_ in ws:
+        w_._bits(4, "rmsnorm_qgemv_int4_multi")
     _check(lib.rmsnorm_qgemv_int4_multi(n, arr, _ptr(x), _xtype(x), _ptr(gamma), float(eps), yp, epi,
                                         _stream(stream)), "rmsnorm_qgemv_int4_multi")
     return ys[0] if epi == QG_EPI_SWIGLU else ys
@@ -281,9 +316,11 @@ def qgemv_int4_sigmoid_fma(w: Int4Weight, x, gate, base, residual=None, y=None, 
     torch = _torch()
     if y is None:
         y = torch.empty(w.out, dtype=torch.float32, device=x.device)
-    _need("x", w.in_dim, x)
-    _need("gate", 1, gate)
-    _need("base, residual, y", w.out, base, residual, y)
+    _need("x", w.in_dim, x, dt="x")
+    _need("gate", 1, gate, dt="f32")
+    _need("base, y", w.out, base, y, dt="f32")
+    _need("residual", w.out, residual, dt="bf16")
+    w._bits(4, "qgemv_int4_sigmoid_fma")
     _check(lib.qgemv_int4_sigmoid_fma(ctypes.byref(w.struct), _ptr(x), _xtype(x), _ptr(gate), _ptr(base),
                                       _ptr(residual), _ptr(y), _stream(stream)), "qgemv_int4_sigmoid_fma")
     return y
@@ -295,8 +332,9 @@ def sigmoid_scalar_fma_residual(gate, value, base, residual=None, out=None, stre
     n = value.numel()
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=value.device)
-    _need("gate", 1, gate)
-    _need("base, residual, out", n, base, residual, out)
+    _need("gate", 1, gate, dt="f32")
+    _need("value, base, out", n, value, base, out, dt="f32")
+    _need("residual", n, residual, dt="bf16")
     _check(lib.sigmoid_scalar_fma_residual(_ptr(gate), _ptr(value), _ptr(base), _ptr(residual), _ptr(out), n,
                                            _stream(stream)), "sigmoid_scalar_fma_residual")
     return out
@@ -308,7 +346,9 @@ def moe_router_topk(logits, k: int = 8, renorm: bool = True, idx=None, p=None, s
         idx = torch.empty(k, dtype=torch.int32, device=logits.device)
     if p is None:
         p = torch.empty(k, dtype=torch.float32, device=logits.device)
-    _need("idx, p", k, idx, p)
+    _need("logits", 1, logits, dt="f32")
+    _need("idx", k, idx, dt="i32")
+    _need("p", k, p, dt="f32")
     _check(lib.moe_router_topk(_ptr(logits), logits.numel(), k, 1 if renorm else 0, _ptr(idx), _ptr(p),
                                _stream(stream)), "moe_router_topk")
     return idx, p
@@ -327,9 +367,13 @@ def moe_gather_qgemv_int4(gate: Int4Weight, up: Int4Weight, down: Int4Weight, id
     need = qg_workspace_bytes(QG_OP_MOE, down, k)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
-    _need("p", k, p)
-    _need("x", gate.in_dim, x)
-    _need("residual, y", down.out, residual, y)
+    _need("idx", k, idx, dt="i32")
+    _need("p", k, p, dt="f32")
+    _need("x", gate.in_dim, x, dt="bf16")
+    _need("residual", down.out, residual, dt="bf16")
+    _need("y", down.out, y, dt="f32")
+    for w_ in (gate, up, down):
+        w_._bits(bits, "moe_gather_qgemv")
     fn = lib.moe_gather_qgemv_int4 if bits == 4 else lib.moe_gather_qgemv_q2
     _check(fn(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
               _ptr(idx), _ptr(p), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(workspace),
@@ -352,10 +396,14 @@ def moe_layer_int4(logits, gate: Int4Weight, up: Int4Weight, down: Int4Weight, x
     need = qg_workspace_bytes(QG_OP_MOE, down, k)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-    _need("logits", gate.n_mat, logits)
-    _need("x", gate.in_dim, x)
-    _need("residual, y", down.out, residual, y)
-    _need("idx, p", k, idx, p)
+    _need("logits", gate.n_mat, logits, dt="f32")
+    _need("x", gate.in_dim, x, dt="bf16")
+    _need("residual", down.out, residual, dt="bf16")
+    _need("y", down.out, y, dt="f32")
+    _need("idx", k, idx, dt="i32")
+    _need("p", k, p, dt="f32")
+    for w_ in (gate, up, down):
+        w_._bits(bits, "moe_layer")
     fn = lib.moe_layer_int4 if bits == 4 else lib.moe_layer_q2
     _check(fn(_ptr(logits), 1 if renorm else 0, ctypes.byref(gate.struct), ctypes.byref(up.struct),
               ctypes.byref(down.struct), k, _ptr(x), _ptr(residual), _ptr(y), _ptr(idx), _ptr(p),
@@ -372,8 +420,12 @@ def gated_rmsnorm_qgemv_int4(w: Int4Weight, y, z, gamma, eps: float, head_dim: i
         out = torch.empty(w.out, dtype=torch.float32, device=y.device)
     if workspace is None:
         workspace = torch.empty(qg_workspace_bytes(QG_OP_GATED_NORM, w, 0), dtype=torch.uint8, device=y.device)
-    _need("y, z, gamma", w.in_dim, y, z, gamma)
-    _need("out", w.out, out)
+    _need("y, z", w.in_dim, y, z, dt="x")
+    if z.dtype != y.dtype:
+        raise QGError(QG_EINVAL, "y and z must have the same dtype")
+    _need("gamma", w.in_dim, gamma, dt="bf16")
+    _need("out", w.out, out, dt="f32")
+    w._bits(4, "gated_rmsnorm_qgemv_int4")
     _check(lib.gated_rmsnorm_qgemv_int4(ctypes.byref(w.struct), _ptr(y), _ptr(z), _xtype(y), _ptr(gamma), float(eps),
                                         int(head_dim), _ptr(out), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -396,10 +448,13 @@ def moe_prefill_int4(logits, gate: Int4Weight, up: Int4Weight, down: Int4Weight,
         p = torch.empty((T, k), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = torch.empty(max(qg_workspace_bytes(QG_OP_MOE_PREFILL, down, T), 16), dtype=torch.uint8, device=dev)
-    _need("logits", T * gate.n_mat, logits)
-    _need("X, residual", T * gate.in_dim, X, residual)
-    _need("Y", T * down.out, Y)
-    _need("idx, p", T * k, idx, p)
+    _need("logits", T * gate.n_mat, logits, dt="f32")
+    _need("X, residual", T * gate.in_dim, X, residual, dt="bf16")
+    _need("Y", T * down.out, Y, dt="f32")
+    _need("idx", T * k, idx, dt="i32")
+    _need("p", T * k, p, dt="f32")
+    for w_ in (gate, up, down):
+        w_._bits(4, "moe_prefill_int4")
     _check(lib.moe_prefill_int4(_ptr(logits), T, 1 if renorm else 0, ctypes.byref(gate.struct), ctypes.byref(up.struct),
                                 ctypes.byref(down.struct), k, _ptr(X), _ptr(residual), _ptr(Y), _ptr(idx), _ptr(p),
                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -416,8 +471,10 @@ def dense_layer_int4(gate: Int4Weight, up: Int4Weight, down: Int4Weight, x, y=No
         y = torch.empty(down.out, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = torch.empty(qg_workspace_bytes(QG_OP_LAYER, down, 0), dtype=torch.uint8, device=dev)
-    _need("x", gate.in_dim, x)
-    _need("y", down.out, y)
+    _need("x", gate.in_dim, x, dt="x")
+    _need("y", down.out, y, dt="f32")
+    for w_ in (gate, up, down):
+        w_._bits(4, "dense_layer_int4")
     _check(lib.dense_layer_int4(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
                                 _ptr(x), _xtype(x), _ptr(y), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -433,8 +490,10 @@ def dense_layer_int4_host(gate: Int4Weight, up: Int4Weight, down: Int4Weight, x_
     if workspace is None:
         workspace = torch.empty(qg_workspace_bytes(QG_OP_LAYER_HOST, down, gate.in_dim), dtype=torch.uint8,
                                 device=device)
-    _need("x_host", gate.in_dim, x_host)
-    _need("y_host", down.out, y_host)
+    _need("x_host", gate.in_dim, x_host, dt="x")
+    _need("y_host", down.out, y_host, dt="f32")
+    for w_ in (gate, up, down):
+        w_._bits(4, "dense_layer_int4_host")
     _check(lib.dense_layer_int4_host(ctypes.byref(gate.struct), ctypes.byref(up.struct), ctypes.byref(down.struct),
                                      _hptr(x_host), _xtype(x_host), _hptr(y_host), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -446,9 +505,13 @@ def moe_gather_qgemv_int4_noalloc(gate: Int4Weight, up: Int4Weight, down: Int4We
                                   stream=None):
     """moe_gather_qgemv_int4 with the library's fixed scratch; `y` must be supplied (nothing is
     allocated on this path)."""
-    _need("p", idx.numel(), p)
-    _need("x", gate.in_dim, x)
-    _need("residual, y", down.out, residual, y)
+    _need("idx", idx.numel(), idx, dt="i32")
+    _need("p", idx.numel(), p, dt="f32")
+    _need("x", gate.in_dim, x, dt="bf16")
+    _need("residual", down.out, residual, dt="bf16")
+    _need("y", down.out, y, dt="f32")
+    for w_ in (gate, up, down):
+        w_._bits(4, "moe_gather_qgemv_int4_noalloc")
     _check(lib.moe_gather_qgemv_int4_noalloc(ctypes.byref(gate.struct), ctypes.byref(up.struct),
                                              ctypes.byref(down.struct), _ptr(idx), _ptr(p), idx.numel(), _ptr(x),
                                              _ptr(residual), _ptr(y), _stream(stream)),
@@ -461,9 +524,10 @@ def scalar_fma_chain8_residual(p, v, residual, out=None, stream=None):
     n = residual.numel()
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=v.device)
-    _need("p", 8, p)
-    _need("v", 8 * n, v)
-    _need("out", n, out)
+    _need("p", 8, p, dt="f32")
+    _need("v", 8 * n, v, dt="f32")
+    _need("residual", n, residual, dt="bf16")
+    _need("out", n, out, dt="f32")
     _check(lib.scalar_fma_chain8_residual(_ptr(p), _ptr(v), _ptr(residual), _ptr(out), n, _stream(stream)),
            "scalar_fma_chain8_residual")
     return out
@@ -492,11 +556,13 @@ def qgemm_int4_multi(ws, X, Ys=None, workspace=None, stream=None):
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _need("X", T * ws[0].in_dim, X)
+    _need("X", T * ws[0].in_dim, X, dt="bf16")
     for w, y_ in zip(ws, Ys):
-        _need("Y", T * w.out, y_)
+        _need("Y", T * w.out, y_, dt="f32")
     arr = (qg_int4_weight * n)(*[w.struct for w in ws])
     yp = (_P * n)(*[_ptr(y) for y in Ys])
+    for w_ in ws:
+        w_._bits(4, "qgemm_int4_multi")
     _check(lib.qgemm_int4_multi(n, arr, _ptr(X), T, yp, _ptr(workspace), nbytes, _stream(stream)), "qgemm_int4_multi")
     return Ys
 
@@ -510,8 +576,9 @@ def qgemm_int4(w: Int4Weight, X, Y=None, workspace=None, stream=None):
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _need("X", T * w.in_dim, X)
-    _need("Y", T * w.out, Y)
+    _need("X", T * w.in_dim, X, dt="bf16")
+    _need("Y", T * w.out, Y, dt="f32")
+    w._bits(4, "qgemm_int4")
     _check(lib.qgemm_int4(ctypes.byref(w.struct), _ptr(X), T, _ptr(Y), _ptr(workspace), nbytes, _stream(stream)),
            "qgemm_int4")
     return Y

@@ -270,20 +270,28 @@ def code2(packed, in_dim: int, row: int, j: int) -> int:
     return int(_L().orc_code2(_p(packed), in_dim, row, j))
 
 
-def qgemv2(packed, scales, biases, x, rows=None):
-    """y, absref of the 2-bit affine GEMV (packed uint32 [out][in/16])."""
+def qgemv2(packed, scales, biases, x, rows=None, threads: int = 1):
+    """y, absref of the 2-bit affine GEMV (packed uint32 [out][in/16]); ``threads`` as qgemv."""
     packed = np.ascontiguousarray(packed, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    biases = np.ascontiguousarray(biases, dtype=np.uint16)
     x = np.ascontiguousarray(x)
     in_dim = x.shape[-1]
     out = packed.size // (in_dim // 16)
     r0, r1 = (0, out) if rows is None else (int(rows[0]), int(rows[1]))
     y = np.empty(r1 - r0, dtype=np.float64)
     a = np.empty(r1 - r0, dtype=np.float64)
-    rc = _L().orc_qgemv2_rows(_p(packed), _p(np.ascontiguousarray(scales, dtype=np.uint16)),
-                              _p(np.ascontiguousarray(biases, dtype=np.uint16)), out, in_dim, _p(x), _xtype(x), r0,
-                              r1, _p(y), _p(a))
-    if rc != 0:
-        raise ValueError("orc_qgemv2_rows rejected the shape")
+    xt = _xtype(x)
+    L = _L()
+
+    def part(lo, hi):
+        rc = L.orc_qgemv2_rows(_p(packed), _p(scales), _p(biases), out, in_dim, _p(x), xt, lo, hi,
+                               ctypes.c_void_p(y.ctypes.data + 8 * (lo - r0)),
+                               ctypes.c_void_p(a.ctypes.data + 8 * (lo - r0)))
+        if rc != 0:
+            raise ValueError("orc_qgemv2_rows rejected the shape")
+
+    _split(r0, r1, threads, part)
     return y, a
 
 

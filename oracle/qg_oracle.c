@@ -33,9 +33,9 @@
 /* ---------------------------------------------------------------------------------------
  * Stored-value decode.
  * bf16 is the upper 16 bits of an IEEE-754 binary32; widening to binary32 is exact, and
- * binary32 -> binary64 is exact.  Scales and biases are bf16 ([FFAI#9] "affine-quant ...
- * u32-packed ... the dtype must be derived from the scales tensor"; [ds4#844] Q4_64A commit:
- * "BF16 scale/bias").
+ * binary32 -> binary64 is exact.  Scales and biases are bf16 ([FFAI#9], loader commit: the
+ * affine-quantized weights are u32-packed and their float type is taken from the scales;
+ * [ds4#844], Q4_64A commit: bf16 scale and bias).
  * ------------------------------------------------------------------------------------- */
 double orc_bf16_to_f64(uint16_t bits) {
   uint32_t u = (uint32_t)bits << 16;
@@ -51,9 +51,9 @@ static double load_x(const void *x, int xtype, int64_t j) {
 
 /* ---------------------------------------------------------------------------------------
  * Nibble unpack.
- * Weight tensor is u32 words, [out][in/8] ([FFAI#14] commit "moeRouterTopK /
- * dequantGemvInt4ExpertIndexed": stacked "[nExperts, outDim, inDim/8] u32"; [FFAI#14]
- * "batchedQkvQ*Fast ... derive in_dim from wQ.shape[1] * 8").  Within a word, element
+ * Weight tensor is u32 words, [out][in/8] ([FFAI#14], commit moeRouterTopK /
+ * dequantGemvInt4ExpertIndexed: experts stacked as u32 [experts][out][in/8]; [FFAI#14], the
+ * batched-projection wrappers take the input width as eight times the packed width).  Within a word, element
  * 8*w + i sits in bits 4i..4i+3 (low nibble first).
  * ------------------------------------------------------------------------------------- */
 unsigned orc_nibble(const uint32_t *packed, int64_t in, int64_t row, int64_t j) {
@@ -68,9 +68,9 @@ void orc_unpack_rows(const uint32_t *packed, int64_t in, int64_t r0, int64_t r1,
 
 /* ---------------------------------------------------------------------------------------
  * Affine group dequantisation: w[r][j] = scale[r][j/gs] * q[r][j] + bias[r][j/gs].
- * Scales and biases are [out][in/gs] ([FFAI#14] "(weight, scales, biases, input, output)";
- * group_size = 64 in every fast-path precondition of [FFAI#14]).  No zero-point is
- * subtracted: the bias carries the offset ([ds4#844] Q4_64A "scale/bias").
+ * Scales and biases are [out][in/gs] ([FFAI#14]: the GEMV operands are the packed weight, its
+ * scales and biases, the input and the output; every fast path there requires groups of 64).  No
+ * zero-point is subtracted: the bias carries the offset ([ds4#844], Q4_64A: a scale and a bias).
  * ------------------------------------------------------------------------------------- */
 double orc_dequant(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases, int64_t in,
                    int64_t gs, int64_t row, int64_t j) {
@@ -82,8 +82,8 @@ double orc_dequant(const uint32_t *packed, const uint16_t *scales, const uint16_
 
 /* ---------------------------------------------------------------------------------------
  * Dequant-GEMV, M = 1:  y[r] = sum_j w[r][j] * x[j]  for rows r0 <= r < r1, summed in j
- * order in double ([FFAI#14] "dequant_gemv_int4_*", CPU-truth "build packed weights +
- * scales + biases + expected GEMV output").
+ * order in double ([FFAI#14] dequant_gemv_int4_*; its tests check every wrapper against a
+ * CPU reference built from the packed weights, scales and biases).
  * absref[r] = sum_j |w[r][j] * x[j]| is the scale of the acceptance bound.
  * y and absref are indexed r - r0.  absref may be NULL.
  * ------------------------------------------------------------------------------------- */
@@ -125,8 +125,8 @@ int orc_qgemv_rows_f64x(const uint32_t *packed, const uint16_t *scales, const ui
 }
 
 /* ---------------------------------------------------------------------------------------
- * SwiGLU: h = silu(g) * u = g / (1 + exp(-g)) * u, unclamped ([FFAI#14] fused MoE down
- * commit: "inner[k] = silu(gate[k]) * up[k]"; [ds4#844] "unclamped SwiGLU").
+ * SwiGLU: h = silu(g) * u = g / (1 + exp(-g)) * u, unclamped ([FFAI#14], fused MoE down
+ * commit: each slot's inner activation is silu of its gate times its up; [ds4#844]: no clamp).
  * ------------------------------------------------------------------------------------- */
 double orc_silu(double g) { return g / (1.0 + exp(-g)); }
 
@@ -135,9 +135,9 @@ void orc_swiglu(const double *g, const double *u, int64_t n, double *h) {
 }
 
 /* ---------------------------------------------------------------------------------------
- * Router top-K ([FFAI#14] commit "moeRouterTopK": logits [nExperts] -> k u32 indices + k
- * weights; test "top-K of (1, 5, 3, 4) at k=2 picks indices {1, 3}; weights sum to 1.0";
- * [FFAI#9] partial-sort commit: order is (value desc, index asc)).
+ * Router top-K ([FFAI#14], commit moeRouterTopK: the logits of all experts in, k u32 indices
+ * and k weights out; its test takes logits (1, 5, 3, 4) with k = 2, expects experts 1 and 3 and
+ * weights that add up to one; [FFAI#9], partial-sort commit: larger value first, ties by index).
  * Selection: k rounds of "take the not-yet-taken expert with the largest logit; on equal
  * logits the smaller index".  Weights: renorm=1 -> softmax over the k selected logits
  * (sums to 1); renorm=0 -> the full softmax over all n experts, read at the selected ones.
@@ -173,9 +173,9 @@ int orc_router_topk(const float *logits, int n, int k, int renorm, uint32_t *idx
 /* ---------------------------------------------------------------------------------------
  * Scalar-weighted chain accumulate with residual:
  *   y[i] = r[i] + sum_{k<K} p[k] * v[k][i]
- * ([FFAI#14] scalar-FMA commit: "scalarFMAChain8 ... exact 8-way fused dispatch",
- * "out[i] = base[i] + scalar[0] * value[i]"; residual folded in as in
- * "sigmoidScalarFMAResidual ... post-MoE residual add folded in").
+ * ([FFAI#14], scalar-FMA commit: scalarFMAChain8 fuses the eight base-plus-scalar-times-vector
+ * updates of a top-8 MoE into one dispatch; the residual is added in the same pass, as
+ * sigmoidScalarFMAResidual does after the MoE).
  * absref[i] = |r[i]| + sum_k |p[k] * v[k][i]|.  Indices i0 <= i < i1; outputs indexed i - i0.
  * r is bf16; v is fp32 [K][n].
  * ------------------------------------------------------------------------------------- */
@@ -195,8 +195,8 @@ void orc_chain_residual(const double *p, int K, const float *v, const uint16_t *
 }
 
 /* ---------------------------------------------------------------------------------------
- * MoE top-K gather decode step ([FFAI#14] commits "moeRouterTopK / dequantGemvInt4ExpertIndexed"
- * and "ffai_moe_down_swiglu_accum_int4_chain8"):
+ * MoE top-K gather decode step ([FFAI#14], commits moeRouterTopK / dequantGemvInt4ExpertIndexed
+ * and ffai_moe_down_swiglu_accum_int4_chain8):
  *   for each slot k:  e = idx[k];  g = Wg[e] x;  u = Wu[e] x;  h = silu(g) * u;  d = Wd[e] h
  *   y[i] = r[i] + sum_k p[k] * d_k[i]
  * The expert slab e of a stacked weight is the e-th [rows][in/8] block (and the e-th
@@ -320,10 +320,10 @@ int orc_gated_rmsnorm(const void *y, const void *z, int xtype, const uint16_t *g
 }
 
 /* ---------------------------------------------------------------------------------------
- * Sigmoid-gated scalar FMA with the residual folded in ([FFAI#14] scalar-FMA commit:
- * "sigmoidScalarFMAResidual(gate, value, base, residual, into:) -- sigmoid-gated FMA with the
- * post-MoE residual add folded in"; "out[i] = base[i] + scalar[0] * value[i]"; the shared-expert
- * step of a decode layer: y = routed + sigmoid(shared_gate . x) * shared_expert(x) + r):
+ * Sigmoid-gated scalar FMA with the residual folded in ([FFAI#14], scalar-FMA commit:
+ * sigmoidScalarFMAResidual takes a gate, a value, a base and a residual and adds the sigmoid-gated
+ * value and the residual to the base in one pass; the shared-expert step of a decode layer:
+ * y = routed + sigmoid(shared_gate . x) * shared_expert(x) + r):
  *   out[i] = base[i] + sigmoid(gate) * value[i] + residual[i]      (residual may be NULL)
  * sigmoid(g) = 1 / (1 + exp(-g)).  gate: one value; value, base fp32 [n]; residual bf16 [n].
  * absref[i] = |base[i]| + |sigmoid(gate) * value[i]| + |residual[i]|.
@@ -343,9 +343,10 @@ void orc_sigmoid_scalar_fma(double gate, const float *value, const float *base, 
 }
 
 /* ---------------------------------------------------------------------------------------
- * Affine group-64 quantizer (encode) for the Q4_64A / Q2_64A formats ([ds4#844]: "Q4_64A and
- * Q2_64A codes are derived from the serialized BF16 scale/bias"; the page gives no formula for
- * the scale and bias themselves -- the plain reading is min/max affine):
+ * Affine group-64 quantizer (encode) for the Q4_64A / Q2_64A formats ([ds4#844], Q4_64A /
+ * Q2_64A commit: the codes come from the scale and bias as stored, after their rounding to bf16;
+ * the page gives no formula for the scale and bias themselves -- the plain reading is min/max
+ * affine):
  *   lo = min of the group (-0 taken as +0), hi = max;  scale = (hi - lo) / (2^bits - 1);  bias = lo
  *   s = bf16(scale), b = bf16(bias)            (round to nearest, ties to even)
  *   q_j = clamp(round_to_nearest_even((w_j - b) / s), 0, 2^bits - 1);   q_j = 0 when s == 0

@@ -188,7 +188,52 @@ def test_binding_refuses_short_vectors():
     torch = pytest.importorskip("torch")
     from moe_int4_affine_gb300 import qg
 
-    qg._need("x", 4, torch.zeros(4), None)
+    qg._need("x", 4, torch.zeros(4), None, dt="f32")
     with pytest.raises(qg.QGError) as e:
-        qg._need("x", 5, torch.zeros(4))
+        qg._need("x", 5, torch.zeros(4), dt="f32")
     assert e.value.code == qg.QG_EINVAL and "x" in str(e.value)
+
+
+@pytest.mark.parametrize("dt,bad", [("f32", "bfloat16"), ("f32", "float16"), ("i32", "int8"), ("i32", "int16"),
+                                    ("i32", "int64"), ("bf16", "float16"), ("bf16", "float32"), ("x", "float16"),
+                                    ("x", "int32")])
+def test_binding_refuses_wrong_dtypes(dt, bad):
+    """A tensor of the right length but another element type (a bf16 y where the kernel writes
+    4-byte floats, an int8 idx where it reads 4-byte indices) is refused before the call: its
+    bytes would not cover what the kernel reads or writes."""
+    torch = pytest.importorskip("torch")
+    from moe_int4_affine_gb300 import qg
+
+    t = torch.zeros(64, dtype=getattr(torch, bad))
+    with pytest.raises(qg.QGError) as e:
+        qg._need("arg", 64, t, dt=dt)
+    assert e.value.code == qg.QG_EINVAL and "dtype" in str(e.value)
+    good = {"f32": torch.float32, "i32": torch.int32, "bf16": torch.bfloat16, "x": torch.bfloat16}[dt]
+    qg._need("arg", 64, torch.zeros(64, dtype=good), dt=dt)
+
+
+def test_binding_weight_checks_sizes_and_types():
+    """An Int4Weight whose packed codes are not int32, whose scales are not bf16, or whose arrays
+    are shorter than out x in (x n_mat) needs for its code width, is refused when it is made."""
+    torch = pytest.importorskip("torch")
+    from moe_int4_affine_gb300 import qg
+
+    def w(packed_n, sb_n, pdt=torch.int32, sdt=torch.bfloat16, bits=4, n_mat=1):
+        return qg.Int4Weight(torch.zeros(packed_n, dtype=pdt), torch.zeros(sb_n, dtype=sdt),
+                             torch.zeros(sb_n, dtype=sdt), 4, 128, n_mat=n_mat, bits=bits)
+
+    # (the binding refuses host tensors only when it takes their device address: pass checks first)
+    for bad in (dict(packed_n=63, sb_n=8), dict(packed_n=64, sb_n=7), dict(packed_n=64, sb_n=8, pdt=torch.float32),
+                dict(packed_n=64, sb_n=8, sdt=torch.float16), dict(packed_n=31, sb_n=8, bits=2),
+                dict(packed_n=64, sb_n=8, n_mat=2)):
+        with pytest.raises(qg.QGError) as e:
+            w(**bad)
+        assert e.value.code == qg.QG_EINVAL
+        assert "dtype" in str(e.value) or "elements" in str(e.value), str(e.value)
+    with pytest.raises(qg.QGError) as e:
+        w(packed_n=64, sb_n=8, bits=3)
+    assert "bits" in str(e.value)
+    # a well-formed weight gets past these checks (and is then refused only for being on the host)
+    with pytest.raises(qg.QGError) as e:
+        w(packed_n=64, sb_n=8)
+    assert "CUDA tensor" in str(e.value)

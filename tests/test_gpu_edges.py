@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 import oracle
-from conftest import assert_within_bound
+from conftest import assert_within, assert_within_bound, dense_layer_reference
 from moe_int4_affine_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -64,12 +64,9 @@ def test_layer_with_one_row_down(qg):
     x = I.bf16_normal(3, I.TID_X, 512)
     G, U, D = (qg.Int4Weight.from_numpy(w) for w in (g, u, d))
     y = qg.to_numpy(qg.dense_layer_int4(G, U, D, qg.to_device(x))).astype(np.float64)
-    gr, _ = oracle.qgemv(g["packed"], g["scales"], g["biases"], x)
-    ur, _ = oracle.qgemv(u["packed"], u["scales"], u["biases"], x)
-    h = oracle.swiglu(gr, ur)
-    y_ref, a = oracle.qgemv_f64x(d["packed"], d["scales"], d["biases"], h)
-    # h from the GPU differs from the fp64 h within its own bound; allow that on top of y's
-    assert_within_bound(y, y_ref, a * 3)
+    # against the fp64 chain, within the bound propagated through SwiGLU and the down projection
+    y_ref, y_bound, _, _ = dense_layer_reference(g, u, d, x)
+    assert_within(y, y_ref, y_bound)
 
 
 def test_router_n_equals_k(qg):

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
-from conftest import assert_within_bound
+from conftest import ABS, REL, assert_within, assert_within_bound, swiglu_bound
 from moe_int4_affine_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -30,13 +30,11 @@ def _expert(d, e):
     return tuple(np.ascontiguousarray(a[e]) for a in _t(d))
 
 
-def _silu_bound(g, u, ag, au):
-    s = 1.0 / (1.0 + np.exp(-g))
-    dsilu = s * (1.0 + g * (1.0 - s))
-    return np.abs(dsilu * u) * ag + np.abs(g * s) * au
-
-
 def _check_token(ws, logits_t, x_t, r_t, k, renorm, y_t, idx_t):
+    """One token: indices bit-exact; y against the oracle's MoE (h in fp64) within the bound of the
+    down GEMVs on the GPU's h (1e-3 sum |w h~| + 1e-6) plus the gate/up errors carried through
+    SwiGLU and the down weights: |y~ - y| <= 1e-3 (A + D) + 1e-6 + D, D = sum_s p_s sum_j
+    |W_d[e_s][i][j]| dh_s[j] (conftest.swiglu_bound; the route weights are exact inputs to both)."""
     gate, up, down = ws
     i_ref, p_ref = oracle.router_topk(logits_t, k, renorm)
     assert idx_t.tolist() == i_ref.tolist()
@@ -46,9 +44,9 @@ def _check_token(ws, logits_t, x_t, r_t, k, renorm, y_t, idx_t):
     for s, e in enumerate(i_ref.tolist()):
         g, ag = oracle.qgemv(*_expert(gate, e), x_t)
         u, au = oracle.qgemv(*_expert(up, e), x_t)
-        _, dab = oracle.qgemv_f64x(*_expert(down, e), _silu_bound(g, u, ag, au))
+        _, dab = oracle.qgemv_f64x(*_expert(down, e), swiglu_bound(g, u, REL * ag + ABS, REL * au + ABS))
         extra += abs(p_ref[s]) * dab
-    assert_within_bound(y_t, y_ref, a + extra)
+    assert_within(y_t, y_ref, REL * (a + extra) + ABS + extra)
 
 
 def _run(qg, ws, T, k, renorm=True, residual=True, seed=0):

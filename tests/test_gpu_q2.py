@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 import oracle
-from conftest import assert_within_bound
+from conftest import ORACLE_THREADS, assert_within_bound
 from moe_int4_affine_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 
 def _w(qg, d, out, in_dim):
     t = qg.to_device
-    return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim)
+    return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim, bits=2)
 
 
 @pytest.mark.parametrize("out,in_dim", [(3, 64), (256, 1024), (1000, 576), (700, 8256), (130, 2048)])
@@ -28,14 +28,12 @@ def test_qgemv_q2_vs_oracle(qg, out, in_dim, kind):
 
 
 @pytest.mark.parametrize("out,in_dim", [(17408, 5120), (5120, 17408)])
-def test_qgemv_q2_full_size_sampled(qg, out, in_dim):
+def test_qgemv_q2_full_size_every_row(qg, out, in_dim):
     d = I.int2_weight(0, I.TID_W, out, in_dim)
     x = I.bf16_normal(0, I.TID_X, in_dim)
     y = qg.to_numpy(qg.qgemv_q2(_w(qg, d, out, in_dim), qg.to_device(x))).astype(np.float64)
-    rng = np.random.default_rng(out)
-    for r in sorted(set([0, out - 1, out // 152] + list(rng.integers(0, out, 40)))):
-        yr, ar = oracle.qgemv2(d["packed"], d["scales"], d["biases"], x, rows=(r, r + 1))
-        assert_within_bound(y[r:r + 1], yr, ar, what=f"row {r}")
+    y_ref, a = oracle.qgemv2(d["packed"], d["scales"], d["biases"], x, threads=ORACLE_THREADS)
+    assert_within_bound(y, y_ref, a)
 
 
 def test_qgemv_q2_multi_and_swiglu(qg):
@@ -63,7 +61,7 @@ def test_q2_encoder_feeds_the_q2_gemv(qg):
     rng = np.random.default_rng(5)
     w = rng.normal(0, 0.02, (640, 1024)).astype(np.float32)
     p, s, b = qg.quantize_affine_q64a(qg.to_device(w), 2)
-    W = qg.Int4Weight(p, s, b, 640, 1024)
+    W = qg.Int4Weight(p, s, b, 640, 1024, bits=2)
     x = I.bf16_normal(5, I.TID_X, 1024)
     y = qg.to_numpy(qg.qgemv_q2(W, qg.to_device(x))).astype(np.float64)
     pr, sr, br = oracle.quantize(w, 2)
@@ -73,7 +71,7 @@ def test_q2_encoder_feeds_the_q2_gemv(qg):
 
 def _stack(qg, d, E, out, in_dim):
     t = qg.to_device
-    return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim, n_mat=E)
+    return qg.Int4Weight(t(d["packed"]), t(d["scales"]), t(d["biases"]), out, in_dim, n_mat=E, bits=2)
 
 
 @pytest.mark.parametrize("E,hidden,inter,k", [(128, 2048, 768, 8), (9, 576, 128, 8), (5, 256, 192, 3)])

@@ -63,16 +63,14 @@ def test_quantize_bit_exact_vs_oracle(qg, out, in_dim, bits, kind):
     assert qg.qg_device_status() == 0
 
 
-def test_quantize_full_size_sampled_rows(qg):
-    """17408 x 5120 bf16 weights (the FFN gate's shape), 40 rows compared bit for bit."""
+def test_quantize_full_size_every_row(qg):
+    """17408 x 5120 bf16 weights (the FFN gate's shape): every code, scale and bias bit for bit."""
     w = _weights(7, 17408, 5120, "bf16")
     p, s, b = _gpu(qg, w, 4)
-    rng = np.random.default_rng(3)
-    for r in sorted(set([0, 1, 2, 3, 17407] + list(rng.integers(0, 17408, 35)))):
-        pr, sr, br = oracle.quantize(w, 4, rows=(r, r + 1))
-        np.testing.assert_array_equal(p[r:r + 1].astype(np.uint32), pr, err_msg=f"row {r}")
-        np.testing.assert_array_equal(s[r:r + 1], sr)
-        np.testing.assert_array_equal(b[r:r + 1], br)
+    pr, sr, br = oracle.quantize(w, 4)
+    np.testing.assert_array_equal(s, sr)
+    np.testing.assert_array_equal(b, br)
+    np.testing.assert_array_equal(p.astype(np.uint32), pr)
 
 
 def test_quantized_weights_feed_the_gemv(qg):
