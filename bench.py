@@ -183,33 +183,44 @@ def run_qg(args, rank, world, local_rank):
         i += 1
         if i % 64 == 0:
             torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1)
-    barrier(world)
-    ms = max_over_ranks(ms, world)
+    # the timed region: exactly K steps between a barrier and a synchronize on both sides, repeated
+    # (at least 5 times and 250 steps in all) and reported as the median over the repeats, with the
+    # spread; each repeat's time is the max over ranks
+    reps = max(5, -(-250 // args.steps))
+    rep_ms = []
+    for r in range(reps):
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(r * args.steps + i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        rep_ms.append(max_over_ranks(ev0.elapsed_time(ev1), world))
     clocks = sampler.stop() if sampler else None
+    ms = statistics.median(rep_ms)
     ms_step = ms / args.steps
     value = world * B_LAYER / (ms_step * 1e-3) / 1e9
+    spread = {"repeats": reps, "steps_per_repeat": args.steps,
+              "ms_per_step_min": round(min(rep_ms) / args.steps, 5), "ms_per_step_max": round(max(rep_ms) / args.steps, 5)}
 
     # dominant kernel (fused gate/up SwiGLU GEMV), back to back on the same stream
-    def time_loop(fn, n):
+    def time_loop(fn, n):  # us per launch: the median of 5 runs of n back-to-back launches
         for i in range(8):
             fn(i)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(n):
-            fn(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1e3 / n  # us per launch
+        ts = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(n):
+                fn(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / n)
+        return statistics.median(ts)
 
     def gateup(i):
         arr, ys = pairs[i % N_COPIES][:2]
@@ -322,6 +333,8 @@ def run_qg(args, rank, world, local_rank):
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
         "us_per_layer": round(ms_step * 1e3, 3),
+        "timing": dict(spread, how="median over the repeats of exactly `steps` steps, each between a barrier "
+                                   "and a device synchronize, CUDA events on the launching stream"),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -581,7 +594,7 @@ def measure_configs(qg, I, dev, stream):
     # config 4: dequant-GEMM, W 17408 x 5120, X T x 5120
     w = qg.Int4Weight.from_numpy(I.int4_weight(0, I.TID_W, FFN, HIDDEN), dev)
     ws_ = copies(w, 12)
-    for T, tc_min, label in ((8, 0, "gemv_path"), (8, 1, "tensor_core_path"), (32, 0, "tensor_core_path"),
+    for T, tc_min, label in ((8, 9, "gemv_path"), (8, 0, "tensor_core_path"), (32, 0, "tensor_core_path"),
                              (256, 0, "tensor_core_path")):
         qg.qg_tune_qgemm(tc_min)
         X = qg.to_device(I.bf16_normal(0, I.TID_X, (T, HIDDEN)), dev)
@@ -589,11 +602,12 @@ def measure_configs(qg, I, dev, stream):
         need = qg.qg_workspace_bytes(qg.QG_OP_QGEMM, w, T)
         wsb = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         args = [(byref(c.struct), P(X.data_ptr()), T, P(Y.data_ptr()), P(wsb.data_ptr()), wsb.numel(), s) for c in ws_]
-        us = tl(lambda i: lib.qgemm_int4(*args[i % 12]), 30 if T == 8 and tc_min == 0 else 60)
+        gemv_path = T < (tc_min or 3)
+        us = tl(lambda i: lib.qgemm_int4(*args[i % 12]), 30 if gemv_path else 60)
         nbytes = weight_bytes(FFN, HIDDEN) + T * HIDDEN * 2 + T * FFN * 4
         tf = 2.0 * T * FFN * HIDDEN / us / 1e6
         e = dict(gb(nbytes, us), path=label, TFLOPs=round(tf, 1), frac_of_tensor_peak=round(tf / peak_tf, 4),
-                 launches=(T if tc_min == 0 and T < 32 else 2))
+                 launches=(T if gemv_path else 2))
         res[f"c4_qgemm_T{T}_{label}"] = e
     qg.qg_tune_qgemm(0)
 
@@ -764,6 +778,74 @@ def run_reference(args, world=1):
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_case(case: str, T: int, bits: int, kind: str) -> int:
+    """Small fixed invocations of the library's kernels for profilers (ncu): a case builds its seeded
+    synthetic inputs (a few hundred MB at most on the device), runs its calls three times and prints
+    "ok <device status>".  Nothing is timed.  Cases: layer (gate/up SwiGLU pair + down, 17408 x
+    5120), down_bf16 (the M = 1 GEMV 5120 x 17408, bf16 x), moe (router + MoE gather, 128 experts,
+    top 8), moe_layer (the same through moe_layer_int4), qgemm (17408 x 5120, T tokens), quant
+    (encode 17408 x 5120 weights of `kind` to `bits`), moe_prefill (128 experts, top 8, T tokens)."""
+    import torch
+
+    from moe_int4_affine_gb300 import build
+
+    build.build()
+    from moe_int4_affine_gb300 import inputs as I
+    from moe_int4_affine_gb300 import qg
+
+    qg.qg_set_pdl(True)
+    reps = 3
+    W = lambda seed, tid, out, in_dim, n_mat=None: qg.Int4Weight.from_numpy(  # noqa: E731
+        I.int4_weight(seed, tid, out, in_dim, n_mat=n_mat))
+    if case == "layer":
+        g, u, d = W(0, I.TID_GATE, 17408, 5120), W(0, I.TID_UP, 17408, 5120), W(0, I.TID_DOWN, 5120, 17408)
+        x = qg.to_device(I.bf16_normal(0, I.TID_X, 5120))
+        for _ in range(reps):
+            qg.dense_layer_int4(g, u, d, x)
+    elif case == "down_bf16":
+        d = W(0, I.TID_DOWN, 5120, 17408)
+        x = qg.to_device(I.bf16_normal(0, I.TID_X, 17408))
+        y = torch.empty(5120, device="cuda")
+        for _ in range(reps):
+            qg.qgemv_int4(d, x, y)
+    elif case in ("moe", "moe_layer"):
+        g, u = W(0, I.TID_GATE, 768, 2048, 128), W(0, I.TID_UP, 768, 2048, 128)
+        d = W(0, I.TID_DOWN, 2048, 768, 128)
+        x = qg.to_device(I.bf16_normal(0, I.TID_X, 2048))
+        r = qg.to_device(I.bf16_normal(0, I.TID_RESID, 2048))
+        for i in range(reps):
+            logits = qg.to_device(I.f32_normal(i, I.TID_LOGITS, 128))
+            if case == "moe":
+                idx, p = qg.moe_router_topk(logits, k=8)
+                qg.moe_gather_qgemv_int4(g, u, d, idx, p, x, r)
+            else:
+                qg.moe_layer_int4(logits, g, u, d, x, r, k=8)
+    elif case == "qgemm":
+        w = W(0, I.TID_W, 17408, 5120)
+        X = qg.to_device(I.bf16_normal(0, I.TID_X, (T, 5120)))
+        for _ in range(reps):
+            qg.qgemm_int4(w, X)
+    elif case == "quant":
+        shape = (17408, 5120)
+        w = qg.to_device(I.bf16_normal(0, I.TID_W, shape) if kind == "bf16" else I.f32_normal(0, I.TID_W, shape))
+        for _ in range(reps):
+            qg.quantize_affine_q64a(w, bits)
+    elif case == "moe_prefill":
+        g, u = W(0, I.TID_GATE, 768, 2048, 128), W(0, I.TID_UP, 768, 2048, 128)
+        d = W(0, I.TID_DOWN, 2048, 768, 128)
+        X = qg.to_device(I.bf16_normal(0, I.TID_X, (T, 2048)))
+        r = qg.to_device(I.bf16_normal(0, I.TID_RESID, (T, 2048)))
+        for i in range(reps):
+            qg.moe_prefill_int4(qg.to_device(I.f32_normal(i, I.TID_LOGITS, (T, 128))), g, u, d, X, r, k=8)
+    else:
+        print(f"unknown case {case!r}", file=sys.stderr)
+        return 2
+    torch.cuda.synchronize()
+    status = qg.qg_device_status()
+    print("ok", status)
+    return 0 if status == 0 else 1
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -774,7 +856,13 @@ def main(argv=None):
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration section")
+    ap.add_argument("--case", default=None, help="run one fixed, untimed invocation for a profiler (see run_case)")
+    ap.add_argument("--T", type=int, default=256, help="--case qgemm / moe_prefill: tokens")
+    ap.add_argument("--bits", type=int, default=4, help="--case quant: code width")
+    ap.add_argument("--kind", default="bf16", choices=["bf16", "f32"], help="--case quant: weight type")
     args = ap.parse_args(argv)
+    if args.case:
+        return run_case(args.case, args.T, args.bits, args.kind)
     args.warmup = max(3, args.warmup)
     rank, world, local_rank = dist_env()
     if world > 1:

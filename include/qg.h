@@ -313,10 +313,16 @@ int scalar_fma_chain8_residual(const float *p, const float *v, const uint16_t *r
  *   Y[t][r] = sum_j w[r][j] * X[t][j],  0 <= t < T.
  * X: bf16 [T][in]; Y: fp32 [T][out].  The caller passes exactly T rows; padding is internal and
  * only the T real rows are written.  w->n_mat must be 1.
- * T >= 32 (see qg_tune_qgemm) runs on the tensor cores (tcgen05): the weights are dequantized to
- * fp16 in shared memory, each token row is scaled by a power of two into fp16's range, products
- * accumulate in fp32.  That path needs every dequantized weight s*q + b within fp16's range
- * (|w| < 65504; scales and biases of typical models are far inside it).  Smaller T runs the
+ * T >= 3 (see qg_tune_qgemm) runs on the tensor cores (tcgen05): the weights are dequantized to
+ * fp16 in tensor memory, each token row is scaled by a power of two into fp16's range, products
+ * accumulate in fp32.  Error: a bf16 token element within 2^31 of its row's largest converts to
+ * fp16 exactly; a weight rounds once to fp16 (relative 2^-11 when |w| >= 2^-14, else 2^-25
+ * absolute); the tensor cores add 16 exact products per MMA and round the running fp32 sum once
+ * per MMA (assumed: relative 2^-23 of the magnitudes involved; undocumented hardware behaviour,
+ * checked by the tests at K = 5120, 17408 and 32768).  So |Y - Y_exact| <= (2^-11 + (K/16 + 1)
+ * 2^-23) sum |w x| (+ the 2^-25 and out-of-range terms): 6.2e-4 at K = 17408 and 7.3e-4 at
+ * K = 32768, inside the 1e-3 bound.  That path needs every scale and bias within fp16's normal
+ * range (2^-14 <= |s|, |b| < 65504, or zero; typical models are far inside it).  T < 3 runs the
  * CUDA-core GEMV once per token row.
  * workspace: at least qg_workspace_bytes(QG_OP_QGEMM, w, T) bytes (0 means none is needed): the
  * tensor-core path stages the converted tokens there.
@@ -391,7 +397,7 @@ int qg_tune_gemv(int ctas_per_sm);
 
 /*
  * qg_tune_qgemm -- smallest T that qgemm_int4 runs on the tensor cores (1..4096; 0 restores the
- * default, 32); smaller T runs the CUDA-core GEMV once per token row.  Process-wide, not thread-safe;
+ * default, 3); smaller T runs the CUDA-core GEMV once per token row.  Process-wide, not thread-safe;
  * query qg_workspace_bytes(QG_OP_QGEMM, ...) after changing it.  Returns QG_EINVAL outside that range.
  */
 int qg_tune_qgemm(int tc_min_T);

@@ -20,7 +20,9 @@ LIB = os.path.join(BUILD, "libqg.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["gemv_dense.cu", "gemv_pair.cu", "gemv_seg.cu", "moe.cu", "moe_prefill.cu", "qgemm.cu", "qgemm_tc.cu", "quant.cu", "api.cu", "noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-rdc=true", "-Xcompiler", "-fPIC", "-I", INCLUDE]
+# -fno-gnu-unique: function-local statics of templates stay private to this library (GCC would
+# otherwise merge them with those of any other loaded copy of it)
+FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-rdc=true", "-Xcompiler", "-fPIC,-fno-gnu-unique", "-I", INCLUDE]
 
 
 def nvcc() -> str:

@@ -21,9 +21,9 @@
 //     and L_j = round((x_j 2^k_g - X_j) 2^15).  The represented value is x~_j = X_j 2^-k_g (first
 //     pass) or (X_j + L_j 2^-15) 2^-k_g (both); |x~_j - x_j| <= 2^(E_g - 15) or 2^(E_g - 30) with
 //     2^E_g <= max|x_g| < 2^(E_g + 1), and bf16 x is exact for every element within 2^7 (2^22) of
-//     its group's largest.  A unit takes the second pass when one of its 32 groups has a largest |x|
-//     above 16 times its mean |x| (outlier channels), else the first alone.  The bias term uses the
-//     group's sum of the same x~, so a row is the fp32-rounded dot product of W with x~:
+//     its group's largest.  A group takes the second pass when its largest |x| is above 32 times its
+//     mean |x| (outlier channels), else the first alone.  The bias term uses the group's sum of the
+//     same x~, so a row is the fp32-rounded dot product of W with x~:
 //       |y - W x| <= sum_g eps_g sum_{j in g} |w_j|  (+ fp32 rounding, ~1e-6 relative),
 //     eps_g the pass's bound above.
 //   * Warps are independent.  A work unit is 4 rows (2 for gate/up pairs) x 32 consecutive groups
@@ -56,11 +56,13 @@ constexpr int kMaxXGroups = 512;  // groups of x: in <= 32768
 enum GemvMode { kDense = 0, kPair = 1, kSeg = 2 };
 constexpr int kThreads = 512;       // 16 warps per CTA, one CTA per SM
 constexpr int kGroupsPerUnit = 32;  // groups of one work unit (one per lane)
-constexpr int kXBytesPerGroup = 272;  // shared memory per group of x: X (128), L (128), factors (16)
-// A group of x takes the second fixed-point pass when its largest |x| exceeds kLoRatio times its
-// mean |x| (sum |x| < (64 / kLoRatio) max |x|): outlier channels, where the first pass alone would
-// leave the group's small entries with a few bits.
-constexpr float kLoSumOverMax = 4.0f;  // 64 / kLoRatio, kLoRatio = 16
+constexpr int kXBytesPerGroup = 265;  // shared memory per group of x: X (128), L (128), factors (8), flag (1)
+// A group of x takes the second fixed-point pass when its largest |x| exceeds 32 times its mean |x|
+// (sum |x| < 2 max |x|): outlier channels, where the first pass alone would leave the group's small
+// entries with a few bits.  Below the ratio the first pass's error, 2^-15 max|x_g| sum |w| at most,
+// is under 32 2^-15 = 0.98e-3 times mean|x_g| sum |w|.  (The SwiGLU output of the dense layer here
+// peaks at 25 times its group mean, so it never takes the second pass; N(0, 1) inputs at 7.)
+constexpr float kLoSumOverMax = 2.0f;
 
 // A weight operand: base pointers of a (possibly stacked) weight, and the expert slot whose slab to
 // use (-1: the base itself).
@@ -288,9 +290,9 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
 // Shared memory per CTA: x of group g as 32 u32 (64 int16 values paired for dp2a: per 8-column
 // word w, (X0, X2), (X4, X6), (X1, X3), (X5, X7)) stored at 16-byte slot (w + g) % 8 of the group's
 // 128 bytes -- the rotation keeps a warp's loads (one group per lane, 128 bytes apart) free of bank
-// conflicts; then the second fixed-point pass L in the same layout; then per group (2^-k_g / 16, sum
-// of the first-pass values, sum of the two-pass values, needs-the-second-pass flag); then the
-// partial sums [row][NC][chunk]; then (STG) the staged copy of x.
+// conflicts; then the second fixed-point pass L in the same layout (written for the groups that
+// take it); then per group (2^-k_g / 16, the sum of its represented values, -, takes-the-second-pass
+// flag); then the partial sums [row][NC][chunk]; then (STG) the staged copy of x.
 // STG: x arrives through one bulk copy (a.stage set by the planner), else the threads load it.
 // BITS: 4 or 2 (the 2-bit variant is built without NORM).
 template <int MODE, int RN, bool STG, bool NORM, int BITS = 4>
@@ -316,8 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const int ngs = a.in / 64;  // groups per segment
   uint32_t* xq = reinterpret_cast<uint32_t*>(smem);                      // [G][32] first pass X
   uint32_t* xl = reinterpret_cast<uint32_t*>(smem + (size_t)G * 128);    // [G][32] second pass L
-  float4* gsx = reinterpret_cast<float4*>(smem + (size_t)G * 256);       // [G]
-  float* part = reinterpret_cast<float*>(smem + (size_t)G * kXBytesPerGroup);  // [rows][NC][nkc]
+  float2* gsx = reinterpret_cast<float2*>(smem + (size_t)G * 256);       // [G]
+  uint8_t* gflag = smem + (size_t)G * 264;                                // [G] takes the second pass
+  float* part = reinterpret_cast<float*>(smem + (((size_t)G * 265 + 15) & ~(size_t)15));  // [rows][NC][nkc]
 
   const int vb = (int)((long long)blockIdx.x * a.total_rows / gridDim.x);
   const int ve = (int)((long long)(blockIdx.x + 1) * a.total_rows / gridDim.x);
@@ -469,49 +472,49 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       // (2 - 2^-7) 2^14 after scaling), one bit less for this group, so every |X_j| <= 32767.
       if (live && m * exp2i(14 - E) >= 32767.5f) ++E;
       const float scale = live ? exp2i(14 - E) : 0.f;  // 14 - E in [-113, 74]
-      // X_j = the low 16 bits of the float x_j 2^k + 1.5 2^23 (the magic-number rule above); the
-      // remainder x_j 2^k - X_j (exact, |.| <= 1/2) scaled by 2^15 gives L_j the same way
-      uint32_t b[8], l[8];
-      float hs = 0.f, ls = 0.f, sa = 0.f;  // sums of X_j and L_j (exact integers), of |x_j|
-      bool lnz = false;
+      // X_j = the low 16 bits of the float x_j 2^k + 1.5 2^23 (the magic-number rule above)
+      uint32_t b[8];
+      float sa = 0.f;  // sum of |x_j|
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float t = fmaf(v[j], scale, 12582912.0f);
-        b[j] = __float_as_uint(t);
-        const float xf = t - 12582912.0f;
-        const float u = fmaf(fmaf(v[j], scale, -xf), 32768.0f, 12582912.0f);
-        l[j] = __float_as_uint(u);
-        const float lf = u - 12582912.0f;
-        hs += xf;
-        ls += lf;
+        b[j] = __float_as_uint(fmaf(v[j], scale, 12582912.0f));
         sa += fabsf(v[j]);
-        lnz |= lf != 0.f;
       }
+      // sum of X_j, exact: dp2a of the packed int16 pairs with byte weights (1, 1)
+      int hsi = 0;
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) hsi = dp2a_lo(__byte_perm(b[j], b[j + 1], 0x5410), 0x0101u, hsi);
+      float hs = (float)hsi;
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) {
         hs += __shfl_xor_sync(0xffffffffu, hs, o);
-        ls += __shfl_xor_sync(0xffffffffu, ls, o);
         sa += __shfl_xor_sync(0xffffffffu, sa, o);
       }
-      // the second pass is needed when it is not all zero and the group's largest |x| is more than
-      // 16 times its mean |x|
-      const bool need = ((__ballot_sync(0xffffffffu, lnz) >> (lane & 24)) & 0xFFu) != 0u && sa < kLoSumOverMax * m;
+      const bool need = sa < kLoSumOverMax * m;  // (false for an all-zero group)
+      float ls = 0.f;                            // sum of L_j (exact integers)
+      uint32_t l[8];
+      if (__any_sync(0xffffffffu, need)) {  // (uniform per warp) the second pass: the remainder
+        // x_j 2^k - X_j (exact, |.| <= 1/2) scaled by 2^15, rounded by the same rule
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float u = fmaf(fmaf(v[j], scale, 12582912.0f - __uint_as_float(b[j])), 32768.0f, 12582912.0f);
+          l[j] = __float_as_uint(u);
+          ls += u - 12582912.0f;
+        }
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+      }
       if (g < G) {
         // paired for dp2a as (X0, X2), (X4, X6), (X1, X3), (X5, X7); 2-bit: (X0, X4), (X1, X5), ...
-        uint4 pk, pl;
-        if constexpr (BITS == 4) {
-          pk = make_uint4(__byte_perm(b[0], b[2], 0x5410), __byte_perm(b[4], b[6], 0x5410),
-                          __byte_perm(b[1], b[3], 0x5410), __byte_perm(b[5], b[7], 0x5410));
-          pl = make_uint4(__byte_perm(l[0], l[2], 0x5410), __byte_perm(l[4], l[6], 0x5410),
-                          __byte_perm(l[1], l[3], 0x5410), __byte_perm(l[5], l[7], 0x5410));
-        } else {
-          pk = make_uint4(__byte_perm(b[0], b[4], 0x5410), __byte_perm(b[1], b[5], 0x5410),
-                          __byte_perm(b[2], b[6], 0x5410), __byte_perm(b[3], b[7], 0x5410));
-          pl = make_uint4(__byte_perm(l[0], l[4], 0x5410), __byte_perm(l[1], l[5], 0x5410),
-                          __byte_perm(l[2], l[6], 0x5410), __byte_perm(l[3], l[7], 0x5410));
-        }
-        reinterpret_cast<uint4*>(xq + (size_t)g * 32)[(sub + g) & 7] = pk;
-        reinterpret_cast<uint4*>(xl + (size_t)g * 32)[(sub + g) & 7] = pl;
+        constexpr int P0 = BITS == 4 ? 0 : 0, P1 = BITS == 4 ? 2 : 4, P2 = BITS == 4 ? 4 : 1, P3 = BITS == 4 ? 6 : 5;
+        constexpr int P4 = BITS == 4 ? 1 : 2, P5 = BITS == 4 ? 3 : 6, P6 = BITS == 4 ? 5 : 3, P7 = BITS == 4 ? 7 : 7;
+        reinterpret_cast<uint4*>(xq + (size_t)g * 32)[(sub + g) & 7] =
+            make_uint4(__byte_perm(b[P0], b[P1], 0x5410), __byte_perm(b[P2], b[P3], 0x5410),
+                       __byte_perm(b[P4], b[P5], 0x5410), __byte_perm(b[P6], b[P7], 0x5410));
+        if (need)
+          reinterpret_cast<uint4*>(xl + (size_t)g * 32)[(sub + g) & 7] =
+              make_uint4(__byte_perm(l[P0], l[P1], 0x5410), __byte_perm(l[P2], l[P3], 0x5410),
+                         __byte_perm(l[P4], l[P5], 0x5410), __byte_perm(l[P6], l[P7], 0x5410));
         if (sub == 0) {
           float wgt = 1.f;
           if (SEG) {
@@ -519,10 +522,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             resolve(a, idxp, WRef{a.seg.packed, a.seg.scales, a.seg.biases, g / ngs}, ok);
             wgt = ok ? __ldg(a.p + g / ngs) : 0.f;
           }
-          // (2^-k / 16: the odd codes are accumulated sixteen times over, see the main loop)
+          // (2^-k / 16: the odd codes are accumulated sixteen times over, see the main loop); the
+          // group's sum of its represented values x~ (both passes when it takes the second)
           const float kinv = live ? exp2i(E - 14) * wgt : 0.f;
-          gsx[g] = make_float4(live ? exp2i(E - (BITS == 4 ? 18 : 20)) * wgt : 0.f, hs * kinv,
-                               fmaf(ls, 3.0517578125e-05f, hs) * kinv, need ? 1.f : 0.f);
+          gsx[g] = make_float2(live ? exp2i(E - (BITS == 4 ? 18 : 20)) * wgt : 0.f,
+                               (need ? fmaf(ls, 3.0517578125e-05f, hs) : hs) * kinv);
+          gflag[g] = need ? 1 : 0;
         }
       }
     };
@@ -626,8 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       __syncthreads();
       for (int g = threadIdx.x; g < G; g += kThreads) {
         const float r = s_hrn[g / hg];
-        const float4 f = gsx[g];
-        gsx[g] = make_float4(f.x * r, f.y * r, f.z * r, f.w);
+        gsx[g] = make_float2(gsx[g].x * r, gsx[g].y * r);
       }
       __syncthreads();
     }
@@ -636,10 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   // --- main loop: this warp's units u = warp, warp + NW, ...; two buffers in turn, the next unit's
   // codes in flight while one is computed ---
   const uint32_t xq_s = smem_u32(xq), xl_s = smem_u32(xl);
-  // The unit's dot products: per entry e the code sums of both passes in exact int32 arithmetic,
-  // word by word (word wd of this lane's group of x from shared memory, the codes in registers).
-  // LO: the second pass as well (taken by the whole warp when any of its 32 groups needs it).
-  auto dot = [&](const UnitLoads<RN>& L, uint32_t xo, auto lo_tag, float (&acc)[RN]) {
+  // The unit's RN dot products in exact int32 arithmetic, word by word (word wd of this lane's group
+  // of x from shared memory, the codes in registers).  LO: the second pass too (the warp takes it
+  // when one of its 32 groups does; the other lanes' L reads as zero).
+  auto dot = [&](const UnitLoads<RN>& L, uint32_t xo, bool own_lo, auto lo_tag, float (&acc)[RN]) {
     constexpr bool LO = decltype(lo_tag)::value;
     if constexpr (BITS == 4 && !LO) {
       int s0[RN], s1[RN];
@@ -672,7 +676,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
       for (int wd = 0; wd < 8; ++wd) {
         const uint32_t ofs = xo + (uint32_t)((wd + (xo >> 7)) & 7) * 16u;
-        const uint4 X = lds128(xq_s + ofs), Lw = lds128(xl_s + ofs);
+        const uint4 X = lds128(xq_s + ofs);
+        const uint4 Lw = own_lo ? lds128(xl_s + ofs) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int e = 0; e < RN; ++e) {
           const uint4& c4 = wd < 4 ? L.a[e] : L.b[e];
@@ -684,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           t[e] = dp2a_hi(Lw.w, c1, dp2a_lo(Lw.z, c1, dp2a_hi(Lw.y, c0, dp2a_lo(Lw.x, c0, t[e]))));
         }
       }
-      // the second pass weighs 2^-15 (rounded once to float each, then one fused add)
+      // the second pass weighs 2^-15 (each sum rounded once to float, then one fused add)
 #pragma unroll
       for (int e = 0; e < RN; ++e) acc[e] = fmaf((float)t[e], 3.0517578125e-05f, (float)s[e]);
     } else {
@@ -699,8 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         const uint32_t oa = xo + (uint32_t)((2 * k + (xo >> 7)) & 7) * 16u;
         const uint32_t ob = xo + (uint32_t)((2 * k + 1 + (xo >> 7)) & 7) * 16u;
         const uint4 A = lds128(xq_s + oa), B = lds128(xq_s + ob);
-        uint4 LA, LB;
-        if constexpr (LO) {
+        uint4 LA = make_uint4(0u, 0u, 0u, 0u), LB = LA;
+        if (LO && own_lo) {
           LA = lds128(xl_s + oa);
           LB = lds128(xl_s + ob);
         }
@@ -729,20 +734,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       }
     }
   };
-  auto compute = [&](const UnitLoads<RN>& L, const UnitCursor& c) {
-    const int g = c.kc * kGroupsPerUnit + lane;
-    const int gc = min(g, G - 1);
-    const float4 gs = gsx[gc];
-    const bool lo = __any_sync(0xffffffffu, gs.w != 0.f);
-    float acc[RN];
-    if (lo)
-      dot(L, (uint32_t)gc * 128u, std::true_type{}, acc);
-    else
-      dot(L, (uint32_t)gc * 128u, std::false_type{}, acc);
-    const float xsum = lo ? gs.z : gs.y;  // the group's sum of the represented x
-    float yp[RN];
-#pragma unroll
-    for (int e = 0; e < RN; ++e) yp[e] = fmaf(bf16_bits_to_f32(L.s[e]), acc[e] * gs.x, bf16_bits_to_f32(L.t[e]) * xsum);
+  // The unit's row sums into the partial-sum buffer.
+  auto store_rows = [&](const float (&yp)[RN], const UnitCursor& c) {
     const float tot = warp_sum_rows<RN>(yp, lane);
     if ((lane & (32 / RN - 1)) == 0) {
       const int e = (lane * RN) >> 5;
@@ -750,6 +743,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       block_rows<RB>(a, vb, ve, c.blk, m, rf, nr, l0);
       if (e / NC < nr) part[((l0 + e / NC) * NC + e % NC) * nkc + c.kc] = tot;
     }
+  };
+  auto compute = [&](const UnitLoads<RN>& L, const UnitCursor& c) {
+    const int gc = min(c.kc * kGroupsPerUnit + lane, G - 1);
+    // (gc past the last group: its scale and bias were loaded as zero, whatever it reads here)
+    const bool own_lo = gflag[gc] != 0;
+    float acc[RN];
+    if (__builtin_expect(__any_sync(0xffffffffu, own_lo), 0))
+      dot(L, (uint32_t)gc * 128u, own_lo, std::true_type{}, acc);
+    else
+      dot(L, (uint32_t)gc * 128u, false, std::false_type{}, acc);
+    const float2 gs = gsx[gc];  // the bias term takes the group's sum of its represented x
+    float yp[RN];
+#pragma unroll
+    for (int e = 0; e < RN; ++e) yp[e] = fmaf(bf16_bits_to_f32(L.s[e]), acc[e] * gs.x, bf16_bits_to_f32(L.t[e]) * gs.y);
+    store_rows(yp, c);
   };
   for (; u < nunits; u += NW) {
     const UnitCursor un = advance(uc);
@@ -904,7 +912,7 @@ extern GemvTune g_gemv_tune;
 
 inline size_t gemv_smem_bytes(int groups, int rows_per_cta, int nc) {
   const int nkc = (groups + kGroupsPerUnit - 1) / kGroupsPerUnit;
-  return (size_t)groups * kXBytesPerGroup + (size_t)rows_per_cta * nc * nkc * 4;
+  return (((size_t)groups * kXBytesPerGroup + 15) & ~(size_t)15) + (size_t)rows_per_cta * nc * nkc * 4;
 }
 
 // Shared memory with the x staging area after `base` bytes, or `base` alone (staging off).  Staging
@@ -921,14 +929,19 @@ inline size_t plan_stage(GemvArgs& a, size_t base, size_t limit) {
 }
 constexpr size_t kStaticSmemReserve = 8192;  // the kernels' static shared variables (NORM: 4.2 KB)
 
+// The kernel's dynamic shared-memory limit is raised once per device (an attribute of the function
+// in that device's context), to the largest size launched there so far.
 template <int MODE, int RN, bool STG, bool NORM, int BITS = 4>
 int launch_gemv_variant(const GemvArgs& a, int grid, size_t smem, cudaStream_t stream) {
   auto k = gemv_kernel<MODE, RN, STG, NORM, BITS>;
-  static std::atomic<int> smem_set{0};
-  if ((int)smem > smem_set.load(std::memory_order_relaxed)) {
+  constexpr int kDevs = 64;
+  static std::atomic<int> smem_set[kDevs];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return QG_EDEVICE;
+  if ((int)smem > smem_set[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return QG_ELAUNCH;
-    smem_set.store((int)smem, std::memory_order_relaxed);
+    smem_set[dev].store((int)smem, std::memory_order_relaxed);
   }
   return launch(k, dim3(grid), dim3(kThreads), smem, stream, a);
 }

@@ -1,6 +1,6 @@
 // qgemm.cu -- dequant-GEMM for T token rows ([FFAI#9] "Ops.dequantGemmDynamicM"):
 //   Y[t][r] = sum_j w[r][j] * X[t][j]
-// Dispatch: T >= the tensor-core threshold (32 unless tuned) runs the tcgen05 kernel of qgemm_tc.cu
+// Dispatch: T >= the tensor-core threshold (3 unless tuned) runs the tcgen05 kernel of qgemm_tc.cu
 // (the tokens padded to a multiple of 16 inside the kernel's tiles); smaller T runs the streaming
 // CUDA-core GEMV once per token row.
 #include "qg_common.cuh"
@@ -8,11 +8,14 @@
 
 namespace qg {
 
-static int g_tc_min_T = 32;
+// The tensor-core path from this many tokens on: its one 16-token tile (30 us at 17408 x 5120)
+// beats the per-token GEMV launches (about 12 us each) from T = 3 (measured on the GB300).
+constexpr int kTcMinTDefault = 3;
+static int g_tc_min_T = kTcMinTDefault;
 
 int qgemm_tune(int tc_min_T) {
   if (tc_min_T < 0 || tc_min_T > 4096) return QG_EINVAL;
-  g_tc_min_T = tc_min_T ? tc_min_T : 32;
+  g_tc_min_T = tc_min_T ? tc_min_T : kTcMinTDefault;
   return QG_OK;
 }
 

@@ -28,11 +28,21 @@
 //     and takes that expert's slab of every matrix (unused tiles exit before any setup).  Tiles
 //     of at most 64 tokens there run two CTAs per SM (256 tensor-memory columns each).
 //
-// Numerics: each token row of X is scaled by a power of two 2^(14 - e_t) (e_t = floor(log2 max|x_t|))
-// so that it sits in fp16's range, then rounded to fp16 (exact for bf16 inputs within 2^10 of the
-// row's largest magnitude); the weights are rounded to fp16 once (relative error <= 2^-11); products
-// accumulate in fp32.  |y - y_exact| <= (2^-11 + 2^-11 + K 2^-23) * sum |w x| roughly, below the
-// 1e-3 * sum |w x| acceptance bound.  Scales and biases must lie within fp16's range (|w| < 65504).
+// Numerics: each token row of X is scaled by a power of two 2^(14 - e_t) (e_t = floor(log2 max|x_t|)),
+// putting its largest magnitude in [2^14, 2^15), then rounded to fp16.  A bf16 value (8 significant
+// bits) is exact in fp16 down to 2^-17 after scaling (fp16's subnormal step is 2^-24), i.e. for every
+// element within 2^31 of its row's largest; smaller ones are off by at most 2^-25 (scaled).  Scales
+// and biases convert to fp16 exactly when they lie in fp16's normal range (2^-14 <= |v| < 65504, or
+// zero: required); the dequantized weight w~ = fl16(s q + b) is one fp16 rounding, |w~ - w| <=
+// 2^-11 |w| (|w| >= 2^-14) or 2^-25.  The products of fp16 operands are exact in fp32; each MMA of
+// K = 16 adds its 16 products to the fp32 accumulator with one rounding, taken here as at most
+// 2^-23 relative to the magnitudes involved (the tensor cores' internal alignment and rounding are
+// undocumented; this allows for truncation).  Over K: |y - y_exact| <= (2^-11 + (K / 16 + 1) 2^-23)
+// sum |w x| plus the 2^-25 terms: 5.3e-4 at K = 5120, 6.2e-4 at K = 17408, 7.3e-4 at K = 32768 --
+// inside the 1e-3 sum |w x| acceptance bound at every supported K.  Excluded inputs: token elements
+// more than 2^31 below their row's largest, and weights below 2^-14 in magnitude, where the
+// absolute terms above apply instead (the 1e-6 absolute part of the bound covers them only for
+// rows of small magnitude).
 #include <algorithm>
 
 #include "qg_common.cuh"

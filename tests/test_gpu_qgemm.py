@@ -78,12 +78,12 @@ def test_qgemm_t8_tensor_core_matches_gemv_path(qg):
     """T = 8 padded onto the tensor cores equals the CUDA-core GEMV path within the bound."""
     d = I.int4_weight(8, I.TID_W, 640, 1024)
     X = I.bf16_normal(8, I.TID_X, (8, 1024))
-    y_gemv = _run(qg, d, X)
-    qg.qg_tune_qgemm(1)
+    qg.qg_tune_qgemm(9)  # T = 8 below the threshold: the per-token GEMV path
     try:
-        y_tc = _run(qg, d, X)
+        y_gemv = _run(qg, d, X)
     finally:
         qg.qg_tune_qgemm(0)
+    y_tc = _run(qg, d, X)  # the default for T = 8: the tensor cores
     Y_ref, A = oracle.qgemm(d["packed"], d["scales"], d["biases"], X)
     assert_within_bound(y_gemv, Y_ref, A, what="gemv path")
     assert_within_bound(y_tc, Y_ref, A, what="tensor-core path")
