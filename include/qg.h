@@ -396,6 +396,17 @@ int qg_set_pdl(int enable);
 int qg_tune_gemv(int ctas_per_sm);
 
 /*
+ * qg_tune_gemv_split -- the GEMV planner's split of K across a thread-block cluster: 0 (default)
+ * lets the planner choose per shape, 1 never splits, 2..4 splits K across clusters of that many CTAs
+ * wherever a split is allowed (no norm prologue, at least one 32-group chunk of K per CTA).  The
+ * CTAs of a cluster share one row range, each converts and streams its own slice of K, and their
+ * row sums are added through distributed shared memory in rank order (deterministic).  Process-wide,
+ * not thread-safe; for tests and sweeps.  Returns QG_EINVAL outside 0..4.  QG_DEBUG_PLAN=1 in the
+ * environment prints each distinct shape's plan (grid, split, shared memory) once, on stderr.
+ */
+int qg_tune_gemv_split(int kcl);
+
+/*
  * qg_tune_qgemm -- smallest T that qgemm_int4 runs on the tensor cores (1..4096; 0 restores the
  * default, 3); smaller T runs the CUDA-core GEMV once per token row.  Process-wide, not thread-safe;
  * query qg_workspace_bytes(QG_OP_QGEMM, ...) after changing it.  Returns QG_EINVAL outside that range.

@@ -70,6 +70,7 @@ const DeviceInfo& device_info() {
     cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
     cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (d.num_sms <= 0) d.num_sms = 1;
+    d.id = dev;
     g_dev[dev] = d;
   });
   return g_dev[dev];
@@ -402,6 +403,8 @@ size_t qg_workspace_bytes(int op, const qg_int4_weight* w, int T_or_k) {
 int qg_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
 int qg_tune_gemv(int ctas_per_sm) { return gemv_tune(ctas_per_sm); }
+
+int qg_tune_gemv_split(int kcl) { return gemv_tune_split(kcl); }
 
 int qg_tune_qgemm(int tc_min_T) { return qgemm_tune(tc_min_T); }
 

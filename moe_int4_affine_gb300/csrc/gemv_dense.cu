@@ -1,15 +1,70 @@
 // gemv_dense.cu -- dense dequant-GEMV launches: one matrix, or n in {2,3,4} matrices sharing x
 // ([FFAI#14] "dequant_gemv_int4_*", "dequantGemvInt4Two/Three/Four", "ffai_batched_4_qgemv_fast").
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <set>
+#include <tuple>
+
 #include "gemv_kernel.cuh"
 
 namespace qg {
 
-GemvTune g_gemv_tune = {0};
+GemvTune g_gemv_tune = {0, 0};
 
 int gemv_tune(int ctas_per_sm) {
   if (ctas_per_sm < 0 || ctas_per_sm > 4) return QG_EINVAL;
-  g_gemv_tune = GemvTune{ctas_per_sm};
+  g_gemv_tune.ctas_per_sm = ctas_per_sm;
   return QG_OK;
+}
+
+int gemv_tune_split(int kcl) {
+  if (kcl < 0 || kcl > 4) return QG_EINVAL;
+  g_gemv_tune.kcl = kcl;
+  return QG_OK;
+}
+
+int gemv_max_clusters(int dev, int C) {
+  static std::atomic<int> cache[kGemvDevs][5];  // value + 1 once known
+  if (C < 2 || C > 4 || dev < 0 || dev >= kGemvDevs) return 0;
+  const int known = cache[dev][C].load(std::memory_order_relaxed);
+  if (known) return known - 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(C * 16));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;  // (one CTA per SM whatever its shared memory: the registers decide)
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)C;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel<kDense, 4, false, false, 4>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache[dev][C].store(n + 1, std::memory_order_relaxed);
+  return n;
+}
+
+// QG_DEBUG_PLAN=1 in the environment (read once): each distinct GEMV shape's plan on stderr, once.
+void gemv_debug_plan(int mode, const GemvArgs& a, int grid, size_t smem) {
+  static const bool on = [] {
+    const char* e = std::getenv("QG_DEBUG_PLAN");
+    return e && e[0] && e[0] != '0';
+  }();
+  if (!on) return;
+  static std::mutex mu;
+  static std::set<std::tuple<int, int, int, int, int, int, int>> seen;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!seen.insert({mode, a.total_rows, a.groups, a.nmat, a.nseg, a.xf32, a.bits}).second) return;
+  std::fprintf(stderr,
+               "qg plan: gemv mode %d rows %d groups %d (mats %d, segments %d, %s x, %d-bit): grid %d, K split %d "
+               "(slice %d groups), rows per CTA %d, shared memory %zu B, x %s\n",
+               mode, a.total_rows, a.groups, a.nmat, a.nseg, a.xf32 ? "fp32" : "bf16", a.bits, grid, a.kcl,
+               a.slice_groups, a.rows_per_cta, smem, a.stage ? "staged by one bulk copy" : "loaded by the threads");
 }
 
 int gemv_dense_launch(const GemvMatArg* mats, int n, const void* x, int xt, int in, cudaStream_t stream,

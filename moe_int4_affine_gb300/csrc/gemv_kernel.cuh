@@ -120,6 +120,11 @@ struct GemvArgs {
   const float* sgate;
   const float* ebase;
   int bits;  // code width: 4 (Q4_64A, 8 codes per u32) or 2 (Q2_64A, 16 per u32)
+  // Split K across a thread-block cluster of kcl CTAs (1: no split).  The CTAs of a cluster share
+  // one row range; CTA rank r takes the r-th contiguous slice of the K chunks, converts only that
+  // slice of x, and the slices' row sums are added through distributed shared memory in rank order.
+  int kcl;
+  int slice_groups;  // groups of x in the largest slice (sizes shared memory)
 };
 
 struct WPtr {
@@ -287,6 +292,26 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
   }
 }
 
+// ------------------------------------------------------------------ thread-block cluster helpers
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// All threads of all CTAs of the cluster: shared-memory writes before it are visible to the
+// cluster's CTAs after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A float in CTA `rank`'s shared memory at the address this CTA's `p` has in its own.
+__device__ __forceinline__ float ld_peer_f32(const float* p, uint32_t rank) {
+  uint32_t ra;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
 // Shared memory per CTA: x of group g as 32 u32 (64 int16 values paired for dp2a: per 8-column
 // word w, (X0, X2), (X4, X6), (X1, X3), (X5, X7)) stored at 16-byte slot (w + g) % 8 of the group's
 // 128 bytes -- the rotation keeps a warp's loads (one group per lane, 128 bytes apart) free of bank
@@ -295,7 +320,7 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
 // flag); then the partial sums [row][NC][chunk]; then (STG) the staged copy of x.
 // STG: x arrives through one bulk copy (a.stage set by the planner), else the threads load it.
 // BITS: 4 or 2 (the 2-bit variant is built without NORM).
-template <int MODE, int RN, bool STG, bool NORM, int BITS = 4>
+template <int MODE, int RN, bool STG, bool NORM, int BITS = 4, bool KS = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float s_gss[NORM ? kMaxXGroups : 1];  // gated: each group's sum of x^2, then
@@ -314,17 +339,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   constexpr int RB = RN / NC;       // rows per work unit
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int NW = kThreads / 32;
-  const int G = a.groups;
   const int ngs = a.in / 64;  // groups per segment
+  // This CTA's K slice: chunks [kc0, kc0 + nkc) of the row's chunks of 32 groups, i.e. groups
+  // [gb0, gend) of x (all of them without a split); rows [vb, ve), its cluster's.
+  // (KS: the kernel built for a K split; without it, one CTA per row range and all of K)
+  const int C = KS ? a.kcl : 1;
+  const int rank = KS ? (int)cluster_rank() : 0;
+  const int ncl = KS ? (int)gridDim.x / C : (int)gridDim.x, cid = KS ? (int)blockIdx.x / C : (int)blockIdx.x;
+  const int nkc_all = (a.groups + kGroupsPerUnit - 1) / kGroupsPerUnit;
+  const int kc0 = KS ? rank * nkc_all / C : 0;
+  const int nkc = KS ? (rank + 1) * nkc_all / C - kc0 : nkc_all;  // K chunks per row in this CTA
+  const int gb0 = kc0 * kGroupsPerUnit;
+  const int gend = KS ? min(a.groups, gb0 + nkc * kGroupsPerUnit) : a.groups;
+  const int G = gend - gb0;  // groups of x in this CTA (local index g - gb0)
+  const int GS = KS ? a.slice_groups : a.groups;  // (layout: every CTA of the launch uses the same offsets)
   uint32_t* xq = reinterpret_cast<uint32_t*>(smem);                      // [G][32] first pass X
-  uint32_t* xl = reinterpret_cast<uint32_t*>(smem + (size_t)G * 128);    // [G][32] second pass L
-  float2* gsx = reinterpret_cast<float2*>(smem + (size_t)G * 256);       // [G]
-  uint8_t* gflag = smem + (size_t)G * 264;                                // [G] takes the second pass
-  float* part = reinterpret_cast<float*>(smem + (((size_t)G * 265 + 15) & ~(size_t)15));  // [rows][NC][nkc]
+  uint32_t* xl = reinterpret_cast<uint32_t*>(smem + (size_t)GS * 128);   // [G][32] second pass L
+  float2* gsx = reinterpret_cast<float2*>(smem + (size_t)GS * 256);      // [G]
+  uint8_t* gflag = smem + (size_t)GS * 264;                               // [G] takes the second pass
+  float* part = reinterpret_cast<float*>(smem + (((size_t)GS * 265 + 15) & ~(size_t)15));  // [rows][NC][nkc]
 
-  const int vb = (int)((long long)blockIdx.x * a.total_rows / gridDim.x);
-  const int ve = (int)((long long)(blockIdx.x + 1) * a.total_rows / gridDim.x);
-  const int nkc = (G + kGroupsPerUnit - 1) / kGroupsPerUnit;  // K chunks per row
+  const int vb = (int)((long long)cid * a.total_rows / ncl);
+  const int ve = (int)((long long)(cid + 1) * a.total_rows / ncl);
 
   const bool indexed = a.idx != nullptr || a.logits != nullptr;  // slots resolved through indices
   const uint32_t* idxp = a.logits ? s_idx : a.idx;
@@ -340,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   auto issue = [&](const UnitCursor& uc, UnitLoads<RN>& L) {
     int m = 0, rf = 0, nr = 0, l0 = 0;
     block_rows<RB>(a, vb, ve, uc.blk, m, rf, nr, l0);
-    const int g = uc.kc * kGroupsPerUnit + lane;  // this lane's group (across segments)
-    const bool gv = g < G;
-    const int gl = gv ? g : G - 1;  // (a valid group to load from; its terms are zeroed below)
+    const int g = gb0 + uc.kc * kGroupsPerUnit + lane;  // this lane's group (across segments)
+    const bool gv = g < gend;
+    const int gl = gv ? g : gend - 1;  // (a valid group to load from; its terms are zeroed below)
     const int sg = SEG ? gl / ngs : 0;
     const int lg = SEG ? gl - sg * ngs : gl;
 #pragma unroll
@@ -383,6 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   if (u < nunits && !indexed) issue(uc, b0);  // before the dependency wait: weights only
 
   // --- x: 16-bit fixed point per group, into shared memory ---
+  bool xok = true;   // (false: x never arrived)
+  bool tlo = false;  // one of this thread's groups takes the second pass
   pdl_wait();
   uint8_t* stage = smem + a.stage_off;
   if (STG && threadIdx.x == 0) {
@@ -393,11 +431,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const uint32_t gbytes = NORM ? (uint32_t)G * 128u : 0u;  // gamma after x
     mbar_arrive_expect_tx(&xbar, xbytes + gbytes);
     for (uint32_t off = 0; off < xbytes; off += kChunk)
-      bulk_g2s_bytes(stage + off, static_cast<const uint8_t*>(a.x) + off, min(kChunk, xbytes - off), &xbar);
+      bulk_g2s_bytes(stage + off, static_cast<const uint8_t*>(a.x) + (size_t)gb0 * (a.xf32 ? 256u : 128u) + off,
+                     min(kChunk, xbytes - off), &xbar);
     if constexpr (NORM) {
       for (uint32_t off = 0; off < gbytes; off += kChunk)
-        bulk_g2s_bytes(stage + xbytes + off, reinterpret_cast<const uint8_t*>(a.gamma) + off, min(kChunk, gbytes - off),
-                       &xbar);
+        bulk_g2s_bytes(stage + xbytes + off, reinterpret_cast<const uint8_t*>(a.gamma) + (size_t)gb0 * 128u + off,
+                       min(kChunk, gbytes - off), &xbar);
     }
   }
   if (a.logits) {  // the router, in every CTA
@@ -431,12 +470,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         float zf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (g < G) {
           if (a.xf32) {
-            const float4* zp = reinterpret_cast<const float4*>(static_cast<const float*>(a.gz) + (size_t)g * 64) + 2 * sub;
+            const float4* zp = reinterpret_cast<const float4*>(static_cast<const float*>(a.gz) + (size_t)(gb0 + g) * 64) + 2 * sub;
             const float4 z0 = __ldg(zp), z1 = __ldg(zp + 1);
             zf[0] = z0.x; zf[1] = z0.y; zf[2] = z0.z; zf[3] = z0.w;
             zf[4] = z1.x; zf[5] = z1.y; zf[6] = z1.z; zf[7] = z1.w;
           } else {
-            const uint4 zr = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.gz) + (size_t)g * 64) + sub);
+            const uint4 zr = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.gz) + (size_t)(gb0 + g) * 64) + sub);
             const uint32_t zw[4] = {zr.x, zr.y, zr.z, zr.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -458,10 +497,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // L_j = round((x_j 2^k - X_j) 2^15); x~_j = (X_j + L_j 2^-15) 2^-k.  The per-group sums of the
     // represented values (first pass alone, and both passes) carry the bias term, so that the code
     // and bias terms see the same x~ and the whole product is the exact W x~ up to fp32 rounding.
+    // The first pass of group g (eight values per lane in v, eight lanes): X_j = round(x_j 2^k),
+    // the group's factor and the sum of its represented values, and whether it takes the second
+    // pass (computed after the prologue's barrier, only where some group takes it).
     auto quant = [&](int g, const float (&v)[8]) {
-      float m = 0.f;
+      float m = 0.f, sa = 0.f;  // largest |x_j|, sum of |x_j|
 #pragma unroll
-      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+      for (int j = 0; j < 8; ++j) {
+        m = fmaxf(m, fabsf(v[j]));
+        sa += fabsf(v[j]);
+      }
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       // E = floor(log2 max|x|), k = 14 - E: |x| 2^k < 2^15.  Groups whose largest |x| is below
@@ -472,15 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       // (2 - 2^-7) 2^14 after scaling), one bit less for this group, so every |X_j| <= 32767.
       if (live && m * exp2i(14 - E) >= 32767.5f) ++E;
       const float scale = live ? exp2i(14 - E) : 0.f;  // 14 - E in [-113, 74]
-      // X_j = the low 16 bits of the float x_j 2^k + 1.5 2^23 (the magic-number rule above)
+      // X_j = the low 16 bits of the float x_j 2^k + 1.5 2^23 (the magic-number rule above); their
+      // sum, exact, by dp2a of the packed int16 pairs with byte weights (1, 1)
       uint32_t b[8];
-      float sa = 0.f;  // sum of |x_j|
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        b[j] = __float_as_uint(fmaf(v[j], scale, 12582912.0f));
-        sa += fabsf(v[j]);
-      }
-      // sum of X_j, exact: dp2a of the packed int16 pairs with byte weights (1, 1)
+      for (int j = 0; j < 8; ++j) b[j] = __float_as_uint(fmaf(v[j], scale, 12582912.0f));
       int hsi = 0;
 #pragma unroll
       for (int j = 0; j < 8; j += 2) hsi = dp2a_lo(__byte_perm(b[j], b[j + 1], 0x5410), 0x0101u, hsi);
@@ -491,42 +532,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         sa += __shfl_xor_sync(0xffffffffu, sa, o);
       }
       const bool need = sa < kLoSumOverMax * m;  // (false for an all-zero group)
-      float ls = 0.f;                            // sum of L_j (exact integers)
-      uint32_t l[8];
-      if (__any_sync(0xffffffffu, need)) {  // (uniform per warp) the second pass: the remainder
-        // x_j 2^k - X_j (exact, |.| <= 1/2) scaled by 2^15, rounded by the same rule
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float u = fmaf(fmaf(v[j], scale, 12582912.0f - __uint_as_float(b[j])), 32768.0f, 12582912.0f);
-          l[j] = __float_as_uint(u);
-          ls += u - 12582912.0f;
-        }
-#pragma unroll
-        for (int o = 4; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-      }
+      tlo |= need && g < G;
       if (g < G) {
         // paired for dp2a as (X0, X2), (X4, X6), (X1, X3), (X5, X7); 2-bit: (X0, X4), (X1, X5), ...
-        constexpr int P0 = BITS == 4 ? 0 : 0, P1 = BITS == 4 ? 2 : 4, P2 = BITS == 4 ? 4 : 1, P3 = BITS == 4 ? 6 : 5;
-        constexpr int P4 = BITS == 4 ? 1 : 2, P5 = BITS == 4 ? 3 : 6, P6 = BITS == 4 ? 5 : 3, P7 = BITS == 4 ? 7 : 7;
-        reinterpret_cast<uint4*>(xq + (size_t)g * 32)[(sub + g) & 7] =
-            make_uint4(__byte_perm(b[P0], b[P1], 0x5410), __byte_perm(b[P2], b[P3], 0x5410),
-                       __byte_perm(b[P4], b[P5], 0x5410), __byte_perm(b[P6], b[P7], 0x5410));
-        if (need)
-          reinterpret_cast<uint4*>(xl + (size_t)g * 32)[(sub + g) & 7] =
-              make_uint4(__byte_perm(l[P0], l[P1], 0x5410), __byte_perm(l[P2], l[P3], 0x5410),
-                         __byte_perm(l[P4], l[P5], 0x5410), __byte_perm(l[P6], l[P7], 0x5410));
+        uint4 pk;
+        if constexpr (BITS == 4) {
+          pk.x = __byte_perm(b[0], b[2], 0x5410);
+          pk.y = __byte_perm(b[4], b[6], 0x5410);
+          pk.z = __byte_perm(b[1], b[3], 0x5410);
+          pk.w = __byte_perm(b[5], b[7], 0x5410);
+        } else {
+          pk.x = __byte_perm(b[0], b[4], 0x5410);
+          pk.y = __byte_perm(b[1], b[5], 0x5410);
+          pk.z = __byte_perm(b[2], b[6], 0x5410);
+          pk.w = __byte_perm(b[3], b[7], 0x5410);
+        }
+        reinterpret_cast<uint4*>(xq + (size_t)g * 32)[(sub + g) & 7] = pk;
         if (sub == 0) {
           float wgt = 1.f;
           if (SEG) {
             bool ok;
-            resolve(a, idxp, WRef{a.seg.packed, a.seg.scales, a.seg.biases, g / ngs}, ok);
-            wgt = ok ? __ldg(a.p + g / ngs) : 0.f;
+            resolve(a, idxp, WRef{a.seg.packed, a.seg.scales, a.seg.biases, (gb0 + g) / ngs}, ok);
+            wgt = ok ? __ldg(a.p + (gb0 + g) / ngs) : 0.f;
           }
           // (2^-k / 16: the odd codes are accumulated sixteen times over, see the main loop); the
-          // group's sum of its represented values x~ (both passes when it takes the second)
-          const float kinv = live ? exp2i(E - 14) * wgt : 0.f;
+          // group's sum of its represented values (the second pass adds its part later)
           gsx[g] = make_float2(live ? exp2i(E - (BITS == 4 ? 18 : 20)) * wgt : 0.f,
-                               (need ? fmaf(ls, 3.0517578125e-05f, hs) : hs) * kinv);
+                               live ? hs * exp2i(E - 14) * wgt : 0.f);
           gflag[g] = need ? 1 : 0;
         }
       }
@@ -534,9 +566,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     if constexpr (STG) {
       // one group per 8 lanes, four groups per warp and step, read from the staged copy
       __syncthreads();  // (the barrier's initialisation, by thread 0, before anyone waits on it)
-      if (!__syncthreads_and(mbar_wait(&xbar, 0))) return;
+      // a copy that never lands (bounded wait, QG_STATUS_TIMEOUT set): nothing is converted and no
+      // output is written, but the CTA still reaches its cluster's barriers
+      xok = __syncthreads_and(mbar_wait(&xbar, 0));
       const uint32_t st = smem_u32(stage);
-      for (int g0 = warp * 4; g0 < G; g0 += NW * 4) {
+      for (int g0 = warp * 4; xok && g0 < G; g0 += NW * 4) {
         const int g = g0 + (lane >> 3);
         const int gs = g < G ? g : G - 1;  // (in range; its results are not stored)
         float v[8];
@@ -568,10 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
         for (int i = 0; i < XB; ++i) {
           const int g = gb + i * NW * 4 + (lane >> 3);
-          raw[i] = g < G ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)g * 64) + sub)
+          raw[i] = g < G ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)(gb0 + g) * 64) + sub)
                          : make_uint4(0u, 0u, 0u, 0u);
           if constexpr (NORM)
-            graw[i] = g < G ? __ldg(reinterpret_cast<const uint4*>(a.gamma + (size_t)g * 64) + sub) : make_uint4(0u, 0u, 0u, 0u);
+            graw[i] = g < G ? __ldg(reinterpret_cast<const uint4*>(a.gamma + (size_t)(gb0 + g) * 64) + sub) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int i = 0; i < XB; ++i) {
@@ -595,11 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
         for (int i = 0; i < XB; ++i) {
           const int g = gb + i * NW * 4 + (lane >> 3);
-          const float4* p4 = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)g * 64) + 2 * sub;
+          const float4* p4 = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)(gb0 + g) * 64) + 2 * sub;
           r0[i] = g < G ? __ldg(p4) : make_float4(0.f, 0.f, 0.f, 0.f);
           r1[i] = g < G ? __ldg(p4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
           if constexpr (NORM)
-            graw[i] = g < G ? __ldg(reinterpret_cast<const uint4*>(a.gamma + (size_t)g * 64) + sub) : make_uint4(0u, 0u, 0u, 0u);
+            graw[i] = g < G ? __ldg(reinterpret_cast<const uint4*>(a.gamma + (size_t)(gb0 + g) * 64) + sub) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int i = 0; i < XB; ++i) {
@@ -619,7 +653,115 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   if (a.idx && blockIdx.x == 0 && (int)threadIdx.x < (SEG ? a.nseg : a.nmat)) {
     if (idxp[threadIdx.x] >= (uint32_t)a.n_experts) set_status(QG_STATUS_BAD_EXPERT);
   }
-  __syncthreads();
+  // some group of this CTA's x takes the second pass: the main loop with it, else the one without
+  const bool anylo = __syncthreads_or(tlo);
+  if (__builtin_expect(anylo, 0)) {
+    // The second pass, for the groups that take it (rare: outlier channels), after the barrier so
+    // that the common prologue stays short: each such group's eight lanes load its x again (with
+    // the norm's factors), L_j = round((x_j 2^k - X_j) 2^15) with the first pass's k and X, and the
+    // group's sum of represented values gains (sum L) 2^-15 2^-k.
+    const int sub = lane & 7;
+    const uint32_t st = smem_u32(smem + a.stage_off);
+    for (int g0 = warp * 4; g0 < G; g0 += NW * 4) {
+      const int g = g0 + (lane >> 3);
+      if (g >= G || !gflag[g]) continue;  // (uniform per 8 lanes; the shuffles below name those 8)
+      const uint32_t m8 = 0xFFu << (lane & 24);
+      float v[8];
+      const size_t gx = (size_t)(gb0 + g) * 64 + (size_t)sub * 8;  // this lane's first element
+      if (STG && !a.xf32) {
+        const uint4 r = lds128(st + (uint32_t)g * 128u + (uint32_t)sub * 16u);
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[2 * j] = __uint_as_float(w[j] << 16);
+          v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      } else if (STG) {
+        const uint4 r0 = lds128(st + (uint32_t)g * 256u + (uint32_t)sub * 32u);
+        const uint4 r1 = lds128(st + (uint32_t)g * 256u + (uint32_t)sub * 32u + 16u);
+        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(w[j]);
+      } else if (!a.xf32) {
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + gx));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[2 * j] = __uint_as_float(w[j] << 16);
+          v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      } else {
+        const float4* p4 = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + gx);
+        const float4 r0 = __ldg(p4), r1 = __ldg(p4 + 1);
+        v[0] = r0.x; v[1] = r0.y; v[2] = r0.z; v[3] = r0.w;
+        v[4] = r1.x; v[5] = r1.y; v[6] = r1.z; v[7] = r1.w;
+      }
+      if constexpr (NORM) {  // x * gamma (* silu(z)): the values the first pass quantized
+        const uint4 gw = STG ? lds128(st + (uint32_t)G * (a.xf32 ? 256u : 128u) + (uint32_t)g * 128u + (uint32_t)sub * 16u)
+                             : __ldg(reinterpret_cast<const uint4*>(a.gamma + gx));
+        const uint32_t w[4] = {gw.x, gw.y, gw.z, gw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[2 * j] *= __uint_as_float(w[j] << 16);
+          v[2 * j + 1] *= __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+        if (a.gz) {
+          float zf[8];
+          if (a.xf32) {
+            const float4* zp = reinterpret_cast<const float4*>(static_cast<const float*>(a.gz) + gx);
+            const float4 z0 = __ldg(zp), z1 = __ldg(zp + 1);
+            zf[0] = z0.x; zf[1] = z0.y; zf[2] = z0.z; zf[3] = z0.w;
+            zf[4] = z1.x; zf[5] = z1.y; zf[6] = z1.z; zf[7] = z1.w;
+          } else {
+            const uint4 zr = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.gz) + gx));
+            const uint32_t zw[4] = {zr.x, zr.y, zr.z, zr.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              zf[2 * j] = __uint_as_float(zw[j] << 16);
+              zf[2 * j + 1] = __uint_as_float(zw[j] & 0xFFFF0000u);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] *= zf[j] / (1.f + expf(-zf[j]));
+        }
+      }
+      float m = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(m8, m, o));
+      const bool live = m >= 8.673617e-19f;  // (the first pass's rule, step for step)
+      int E = max((int)((__float_as_uint(m) >> 23) & 0xFF) - 127, -60);
+      if (live && m * exp2i(14 - E) >= 32767.5f) ++E;
+      const float scale = live ? exp2i(14 - E) : 0.f;
+      // the remainder x_j 2^k - X_j (exact, |.| <= 1/2) scaled by 2^15, rounded by the magic rule
+      uint32_t l[8];
+      float ls = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float t = fmaf(v[j], scale, 12582912.0f);  // (1.5 2^23 + X_j)
+        const float u = fmaf(fmaf(v[j], scale, 12582912.0f - t), 32768.0f, 12582912.0f);
+        l[j] = __float_as_uint(u);
+        ls += u - 12582912.0f;
+      }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) ls += __shfl_xor_sync(m8, ls, o);
+      uint4 pl;
+      if constexpr (BITS == 4) {
+        pl = make_uint4(__byte_perm(l[0], l[2], 0x5410), __byte_perm(l[4], l[6], 0x5410),
+                        __byte_perm(l[1], l[3], 0x5410), __byte_perm(l[5], l[7], 0x5410));
+      } else {
+        pl = make_uint4(__byte_perm(l[0], l[4], 0x5410), __byte_perm(l[1], l[5], 0x5410),
+                        __byte_perm(l[2], l[6], 0x5410), __byte_perm(l[3], l[7], 0x5410));
+      }
+      reinterpret_cast<uint4*>(xl + (size_t)g * 32)[(sub + g) & 7] = pl;
+      if (sub == 0) {  // 2^-k (times the slot weight) is the group factor times 16 (2-bit: 64)
+        const float2 f = gsx[g];
+        gsx[g] = make_float2(f.x, fmaf(ls * 3.0517578125e-05f, f.x * (BITS == 4 ? 16.f : 64.f), f.y));
+      }
+    }
+    __syncthreads();
+  }
   if constexpr (NORM) {
     if (a.gz) {  // gated: each head's root, then every group's x factors scaled by its head's
       const int hg = a.head_dim / 64, nh = G / hg;
@@ -744,28 +886,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       if (e / NC < nr) part[((l0 + e / NC) * NC + e % NC) * nkc + c.kc] = tot;
     }
   };
-  auto compute = [&](const UnitLoads<RN>& L, const UnitCursor& c) {
+  auto compute = [&](const UnitLoads<RN>& L, const UnitCursor& c, auto lo_tag) {
+    constexpr bool LOK = decltype(lo_tag)::value;  // (the loop where some group takes the second pass)
     const int gc = min(c.kc * kGroupsPerUnit + lane, G - 1);
     // (gc past the last group: its scale and bias were loaded as zero, whatever it reads here)
-    const bool own_lo = gflag[gc] != 0;
     float acc[RN];
-    if (__builtin_expect(__any_sync(0xffffffffu, own_lo), 0))
-      dot(L, (uint32_t)gc * 128u, own_lo, std::true_type{}, acc);
-    else
+    if constexpr (LOK) {
+      const bool own_lo = gflag[gc] != 0;
+      if (__any_sync(0xffffffffu, own_lo))
+        dot(L, (uint32_t)gc * 128u, own_lo, std::true_type{}, acc);
+      else
+        dot(L, (uint32_t)gc * 128u, false, std::false_type{}, acc);
+    } else {
       dot(L, (uint32_t)gc * 128u, false, std::false_type{}, acc);
+    }
     const float2 gs = gsx[gc];  // the bias term takes the group's sum of its represented x
     float yp[RN];
 #pragma unroll
     for (int e = 0; e < RN; ++e) yp[e] = fmaf(bf16_bits_to_f32(L.s[e]), acc[e] * gs.x, bf16_bits_to_f32(L.t[e]) * gs.y);
     store_rows(yp, c);
   };
-  for (; u < nunits; u += NW) {
-    const UnitCursor un = advance(uc);
-    if (u + NW < nunits) issue(un, b1);
-    compute(b0, uc);
-    b0 = b1;
-    uc = un;
-  }
+  auto main_loop = [&](auto lo_tag) {
+    for (; xok && u < nunits; u += NW) {
+      const UnitCursor un = advance(uc);
+      if (u + NW < nunits) issue(un, b1);
+      compute(b0, uc, lo_tag);
+      b0 = b1;
+      uc = un;
+    }
+  };
+  if (__builtin_expect(anylo, 0))
+    main_loop(std::true_type{});
+  else
+    main_loop(std::false_type{});
   __syncthreads();
 
   // --- finish: sum each row's K chunks in order, epilogue, write ---
@@ -779,18 +932,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
   }
   const float sig = a.sgate ? 1.f / (1.f + expf(-__ldg(a.sgate))) : 0.f;
-  for (int lr = threadIdx.x; lr < ve - vb; lr += kThreads) {
+  // K split: each CTA's row sums over its own chunks, then (after the cluster barrier) rank r
+  // finishes its share of the cluster's rows, adding the C slices' sums in rank order.
+  // (at the same offset in every CTA of the cluster: after the partial sums of the widest slice)
+  float* rsum = part + (size_t)a.rows_per_cta * NC * ((nkc_all + C - 1) / C);  // [rows][NC], KS only
+  int lr0 = 0, lr1 = ve - vb;
+  if constexpr (KS) {
+    for (int i = threadIdx.x; i < (ve - vb) * NC; i += kThreads) {
+      float t = 0.f;
+      for (int kc = 0; kc < nkc; ++kc) t += part[i * nkc + kc];
+      rsum[i] = t;
+    }
+    cluster_sync();
+    lr0 = rank * (ve - vb) / C;
+    lr1 = (rank + 1) * (ve - vb) / C;
+  }
+  for (int lr = lr0 + (int)threadIdx.x; xok && lr < lr1; lr += kThreads) {
     const int v = vb + lr;
     int m = 0;
     while (m + 1 < a.nmat && v >= a.mat[m + 1].row0) ++m;
     const GemvMat& mt = a.mat[m];
     const int row = v - mt.row0;
-    float acc = 0.f;
-    for (int kc = 0; kc < nkc; ++kc) acc += part[(lr * NC) * nkc + kc];
+    float acc = 0.f, up = 0.f;
+    if constexpr (KS) {
+      for (int c = 0; c < C; ++c) {
+        acc += ld_peer_f32(rsum + lr * NC, (uint32_t)c);
+        if (PAIR) up += ld_peer_f32(rsum + lr * NC + 1, (uint32_t)c);
+      }
+    } else {
+      for (int kc = 0; kc < nkc; ++kc) acc += part[(lr * NC) * nkc + kc];
+      if (PAIR)
+        for (int kc = 0; kc < nkc; ++kc) up += part[(lr * NC + 1) * nkc + kc];
+    }
     if (NORM) acc *= rn;
     if (PAIR) {
-      float up = 0.f;
-      for (int kc = 0; kc < nkc; ++kc) up += part[(lr * NC + 1) * nkc + kc];
       if (NORM) up *= rn;
       bool ok = true;
       if (mt.w[0].slot >= 0) resolve(a, idxp, mt.w[0], ok);
@@ -800,6 +975,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     if (a.resid) acc += bf16_bits_to_f32(a.resid[row]);
     mt.y[row] = acc;
   }
+  if constexpr (KS) cluster_sync();  // (no CTA leaves while a peer may still read its row sums)
 }
 
 // ------------------------------------------------------------------ host side: arguments
@@ -907,69 +1083,135 @@ inline void apply_extras(GemvArgs& a, const GemvExtras& ex) {
 // ------------------------------------------------------------------ host side: planning
 struct GemvTune {
   int ctas_per_sm;  // 0: automatic
+  int kcl;          // K split (cluster size): 0 automatic, 1 none, 2..8 forced where allowed
 };
 extern GemvTune g_gemv_tune;
 
-inline size_t gemv_smem_bytes(int groups, int rows_per_cta, int nc) {
-  const int nkc = (groups + kGroupsPerUnit - 1) / kGroupsPerUnit;
-  return (((size_t)groups * kXBytesPerGroup + 15) & ~(size_t)15) + (size_t)rows_per_cta * nc * nkc * 4;
+// x of GS groups (the widest K slice), the partial sums of rows x NC components x the slice's chunks,
+// and (K split) the row sums the cluster's CTAs read from each other.
+inline size_t gemv_smem_bytes(int GS, int rows_per_cta, int nc, int kcl) {
+  const int nkc = (GS + kGroupsPerUnit - 1) / kGroupsPerUnit;
+  return (((size_t)GS * kXBytesPerGroup + 15) & ~(size_t)15) + (size_t)rows_per_cta * nc * nkc * 4 +
+         (kcl > 1 ? (size_t)rows_per_cta * nc * 4 : 0);
 }
 
-// Shared memory with the x staging area after `base` bytes, or `base` alone (staging off).  Staging
-// is used for short x only: measured on the decode shapes, the bulk copy beat the threads' own loads
-// for x of up to 128 groups (gate/up 5120 bf16: 20.7 -> 20.1 us; MoE 2048 bf16 and 8 x 768 fp32:
-// 16.0 -> 14.9 us per layer) and lost for the 17408-wide down x (12.37 -> 12.54 us).
+// Shared memory with the x staging area after `base` bytes, or `base` alone (staging off).  Staged:
+// x of up to 128 groups, and fp32 x of any length (the activations a previous kernel of the chain
+// produced); long bf16 x is loaded by the threads.  Measured on the decode shapes: the bulk copy beat
+// the threads' own loads for short x (gate/up 5120 bf16: 20.7 -> 20.1 us; MoE 2048 bf16 and 8 x 768
+// fp32: 16.0 -> 14.9 us per layer); for the 17408-wide down x it loses standalone (bf16 12.9 -> 13.3
+// us) but wins in the dense layer, where x is the gate/up kernel's fresh output (36.6 -> 34.9 us).
 constexpr int kStageMaxGroups = 128;
 inline size_t plan_stage(GemvArgs& a, size_t base, size_t limit) {
   const size_t off = (base + 127) & ~(size_t)127;
-  const size_t total = off + (size_t)a.groups * ((a.xf32 ? 256 : 128) + (a.gamma ? 128 : 0));
-  a.stage = total <= limit && a.groups <= kStageMaxGroups ? 1 : 0;
+  const size_t total = off + (size_t)a.slice_groups * ((a.xf32 ? 256 : 128) + (a.gamma ? 128 : 0));
+  a.stage = total <= limit && (a.slice_groups <= kStageMaxGroups || a.xf32) ? 1 : 0;
   a.stage_off = a.stage ? (int)off : 0;
   return a.stage ? total : base;
 }
 constexpr size_t kStaticSmemReserve = 8192;  // the kernels' static shared variables (NORM: 4.2 KB)
+constexpr int kGemvDevs = 64;
+
+// How many clusters of C CTAs of the GEMV kernel (512 threads, one CTA per SM) can be resident at
+// once on the current device (cudaOccupancyMaxActiveClusters), cached per device and C.  A K-split
+// grid never asks for more, so no cluster waits for a second wave.
+int gemv_max_clusters(int dev, int C);
 
 // The kernel's dynamic shared-memory limit is raised once per device (an attribute of the function
 // in that device's context), to the largest size launched there so far.
-template <int MODE, int RN, bool STG, bool NORM, int BITS = 4>
+template <int MODE, int RN, bool STG, bool NORM, int BITS = 4, bool KS = false>
 int launch_gemv_variant(const GemvArgs& a, int grid, size_t smem, cudaStream_t stream) {
-  auto k = gemv_kernel<MODE, RN, STG, NORM, BITS>;
-  constexpr int kDevs = 64;
-  static std::atomic<int> smem_set[kDevs];
+  auto k = gemv_kernel<MODE, RN, STG, NORM, BITS, KS>;
+  static std::atomic<int> smem_set[kGemvDevs];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return QG_EDEVICE;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kGemvDevs) return QG_EDEVICE;
   if ((int)smem > smem_set[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return QG_ELAUNCH;
     smem_set[dev].store((int)smem, std::memory_order_relaxed);
   }
-  return launch(k, dim3(grid), dim3(kThreads), smem, stream, a);
+  return launch_cluster(k, dim3(grid), dim3(kThreads), smem, stream, KS ? a.kcl : 1, a);
 }
 
-// Plan (grid, shared memory) and launch.
+// The per-shape plan: the grid (one CTA per SM), the K split across a cluster of C CTAs and with
+// it each CTA's row range and K slice, and the shared memory.  Costs, in units of the time a warp
+// takes for one work unit (about 1.5 us on the decode shapes): the units of the busiest warp, the
+// x conversion of the widest slice (about a quarter unit per 64 groups of x on 512 threads), and
+// the cluster's start (its CTAs wait for as many free SMs of one GPC), two barriers and row-sum
+// exchange (about one unit: a forced split of the 5120 x 17408 GEMV cost 1.3 us).
+struct GemvPlan {
+  int grid, kcl, rows_per_cta, slice_groups;
+  double cost;
+};
+inline GemvPlan gemv_plan_for(int total_rows, int groups, int nc, int rb, int C, int num_sms, int max_cl) {
+  GemvPlan p{};
+  const int ncl = std::max(1, std::min(C > 1 ? max_cl : num_sms, std::min(num_sms / C, total_rows)));
+  p.grid = ncl * C;
+  p.kcl = C;
+  p.rows_per_cta = (total_rows + ncl - 1) / ncl;
+  const int nkc_all = (groups + kGroupsPerUnit - 1) / kGroupsPerUnit;
+  const int nkc_max = (nkc_all + C - 1) / C;
+  p.slice_groups = std::min(groups, nkc_max * kGroupsPerUnit);
+  const int units = (p.rows_per_cta + rb - 1) / rb * nkc_max;
+  p.cost = (double)((units + kThreads / 32 - 1) / (kThreads / 32)) + 0.25 * (p.slice_groups + 63) / 64 +
+           (C > 1 ? 1.0 : 0.0);
+  return p;
+}
+
+void gemv_debug_plan(int mode, const GemvArgs& a, int grid, size_t smem);
+
+// Plan (grid, K split, shared memory) and launch.
 template <int MODE>
 int plan_and_launch(GemvArgs& a, cudaStream_t stream) {
   const DeviceInfo& dev = device_info();
   constexpr int NC = MODE == kPair ? 2 : 1;
+  constexpr int RB = 4 / NC;
   a.groups = a.nseg * a.in / 64;
   const int cps = g_gemv_tune.ctas_per_sm ? g_gemv_tune.ctas_per_sm : 1;
-  int grid = std::max(1, std::min(cps * dev.num_sms, a.total_rows));
-  // keep x and the partial-sum buffer within the shared memory (more, smaller CTAs otherwise)
-  const size_t budget = (size_t)dev.max_smem_optin - kStaticSmemReserve;
-  for (;;) {
-    a.rows_per_cta = (a.total_rows + grid - 1) / grid;
-    if (gemv_smem_bytes(a.groups, a.rows_per_cta, NC) <= budget || grid >= a.total_rows) break;
-    grid = std::min(a.total_rows, grid * 2);
-  }
   const size_t limit = (size_t)dev.max_smem_optin - kStaticSmemReserve;
-  const size_t smem = plan_stage(a, gemv_smem_bytes(a.groups, a.rows_per_cta, NC), limit);
+  // K split: not with a norm prologue (its sums of squares and per-head roots span all of x), and
+  // only when every CTA of the cluster gets at least one chunk of K
+  const int nkc_all = (a.groups + kGroupsPerUnit - 1) / kGroupsPerUnit;
+  int best_c = 1;
+  GemvPlan best = gemv_plan_for(a.total_rows, a.groups, NC, RB, 1, cps * dev.num_sms, 0);
+  const int forced = g_gemv_tune.kcl;
+  if (!a.gamma && cps == 1 && nkc_all >= 2 && forced != 1) {
+    for (int C = 2; C <= 4; ++C) {
+      if (C > nkc_all || (forced && forced != C)) continue;
+      const int mc = gemv_max_clusters(dev.id, C);
+      if (mc < 1) continue;
+      const GemvPlan p = gemv_plan_for(a.total_rows, a.groups, NC, RB, C, dev.num_sms, mc);
+      if (forced == C || p.cost < best.cost) {
+        best = p;
+        best_c = C;
+      }
+    }
+  }
+  int grid = best.grid;
+  a.kcl = best_c;
+  a.slice_groups = best.slice_groups;
+  a.rows_per_cta = best.rows_per_cta;
+  // keep x and the partial-sum buffer within the shared memory (more, smaller CTAs otherwise;
+  // unsplit only)
+  while (a.kcl == 1 && gemv_smem_bytes(a.slice_groups, a.rows_per_cta, NC, 1) > limit && grid < a.total_rows) {
+    grid = std::min(a.total_rows, grid * 2);
+    a.rows_per_cta = (a.total_rows + grid - 1) / grid;
+  }
+  const size_t smem = plan_stage(a, gemv_smem_bytes(a.slice_groups, a.rows_per_cta, NC, a.kcl), limit);
   if (smem > limit) return QG_ENOTSUP;
+  gemv_debug_plan(MODE, a, grid, smem);
   // rows x components per work unit: 4 (dense and seg: four rows; pair: two rows, gate and up)
   if (a.bits == 2) {
     if (a.gamma) return QG_ENOTSUP;
+    if (a.kcl > 1)
+      return a.stage ? launch_gemv_variant<MODE, 4, true, false, 2, true>(a, grid, smem, stream)
+                     : launch_gemv_variant<MODE, 4, false, false, 2, true>(a, grid, smem, stream);
     return a.stage ? launch_gemv_variant<MODE, 4, true, false, 2>(a, grid, smem, stream)
                    : launch_gemv_variant<MODE, 4, false, false, 2>(a, grid, smem, stream);
   }
+  if (a.kcl > 1)  // (never with a norm prologue)
+    return a.stage ? launch_gemv_variant<MODE, 4, true, false, 4, true>(a, grid, smem, stream)
+                   : launch_gemv_variant<MODE, 4, false, false, 4, true>(a, grid, smem, stream);
   if constexpr (MODE != kSeg) {
     if (a.gamma)
       return a.stage ? launch_gemv_variant<MODE, 4, true, true>(a, grid, smem, stream)

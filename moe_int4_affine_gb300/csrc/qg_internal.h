@@ -14,6 +14,7 @@ namespace qg {
 struct DeviceInfo {
   int num_sms;
   int max_smem_optin;
+  int id;  // the device's ordinal
 };
 const DeviceInfo& device_info();
 
@@ -33,6 +34,39 @@ int launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStr
   if (pdl_enabled()) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return QG_ELAUNCH;
+  e = cudaGetLastError();
+  return e == cudaSuccess ? QG_OK : QG_ELAUNCH;
+}
+
+// The same with the kernel's CTAs grouped into clusters of `cluster` along x (1: no cluster); the
+// grid must be a multiple of it.
+template <typename... KArgs, typename... Args>
+int launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster,
+                   Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (cluster > 1) {
+    if (grid.x % (unsigned)cluster != 0) return QG_EINVAL;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
     ++na;
   }
   cfg.attrs = attr;
@@ -73,6 +107,7 @@ int gemv_pair_launch(const GemvMatArg& gate, const GemvMatArg& up, const void* x
 int sigmoid_fma_launch(const float* gate, const float* value, const float* base, const uint16_t* resid, float* out,
                        int n, cudaStream_t stream);
 int gemv_tune(int ctas_per_sm);
+int gemv_tune_split(int kcl);
 int moe_gate_up_launch(const qg_int4_weight* gate, const qg_int4_weight* up, const uint32_t* idx, int k,
                        const uint16_t* x, float* h, cudaStream_t stream, int bits = 4);
 int moe_gate_up_routed_launch(const float* logits, int n_logits, int renorm, const qg_int4_weight* gate,

@@ -62,6 +62,7 @@ lib.qg_workspace_bytes.argtypes = [_I, _W, _I]
 lib.qg_workspace_bytes.restype = ctypes.c_size_t
 lib.qg_set_pdl.argtypes = [_I]
 lib.qg_tune_gemv.argtypes = [_I]
+lib.qg_tune_gemv_split.argtypes = [_I]
 lib.qg_tune_qgemm.argtypes = [_I]
 lib.qg_selftest_wait_timeout.argtypes = [_I, _P]
 lib.qg_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
@@ -71,7 +72,7 @@ lib.qg_version.argtypes = []
 for _f in ("qgemv_int4", "qgemv_int4_multi", "moe_router_topk", "moe_gather_qgemv_int4",
            "moe_gather_qgemv_int4_noalloc", "moe_layer_int4", "moe_prefill_int4", "gated_rmsnorm_qgemv_int4", "dense_layer_int4", "dense_layer_int4_host", "rmsnorm_qgemv_int4", "qgemv_q2", "qgemv_q2_multi", "moe_gather_qgemv_q2", "moe_layer_q2",
            "rmsnorm_qgemv_int4_multi", "qgemv_int4_sigmoid_fma", "sigmoid_scalar_fma_residual",
-           "scalar_fma_chain8_residual", "qgemm_int4", "qgemm_int4_multi", "quantize_affine_q64a", "qg_set_pdl", "qg_tune_gemv", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
+           "scalar_fma_chain8_residual", "qgemm_int4", "qgemm_int4_multi", "quantize_affine_q64a", "qg_set_pdl", "qg_tune_gemv", "qg_tune_gemv_split", "qg_tune_qgemm", "qg_selftest_wait_timeout", "qg_device_status", "qg_version"):
     getattr(lib, _f).restype = ctypes.c_int
 
 
@@ -590,6 +591,11 @@ def qg_set_pdl(enable: bool) -> bool:
 
 def qg_tune_gemv(ctas_per_sm: int = 0) -> None:
     _check(lib.qg_tune_gemv(ctas_per_sm), "qg_tune_gemv")
+
+
+def qg_tune_gemv_split(kcl: int = 0) -> None:
+    """K split of the GEMV across a thread-block cluster: 0 automatic, 1 never, 2..4 forced."""
+    _check(lib.qg_tune_gemv_split(kcl), "qg_tune_gemv_split")
 
 
 def qg_selftest_wait_timeout(limit_us: int = 1000, stream=None) -> None:

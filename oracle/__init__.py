@@ -295,6 +295,22 @@ def qgemv2(packed, scales, biases, x, rows=None, threads: int = 1):
     return y, a
 
 
+def qgemv2_f64x(packed, scales, biases, x64: np.ndarray):
+    """y, absref of the 2-bit GEMV of an input given in float64 (the 2-bit MoE down's h)."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint32)
+    x64 = np.ascontiguousarray(x64, dtype=np.float64)
+    in_dim = x64.shape[-1]
+    out = packed.size // (in_dim // 16)
+    y = np.empty(out, dtype=np.float64)
+    a = np.empty(out, dtype=np.float64)
+    rc = _L().orc_qgemv2_rows_f64x(_p(packed), _p(np.ascontiguousarray(scales, dtype=np.uint16)),
+                                   _p(np.ascontiguousarray(biases, dtype=np.uint16)), out, in_dim, _p(x64), 0, out,
+                                   _p(y), _p(a))
+    if rc != 0:
+        raise ValueError("orc_qgemv2_rows_f64x rejected the shape")
+    return y, a
+
+
 def moe2(gate, up, down, idx, p, x, residual):
     """The MoE decode step with 2-bit experts (gate/up packed [E][inter][hidden/16], down
     [E][hidden][inter/16]); returns y, absref and the invalid-slot flag bits, as moe()."""
