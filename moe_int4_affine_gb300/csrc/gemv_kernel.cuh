@@ -53,7 +53,10 @@ namespace qg {
 
 constexpr int kMaxMats = 8;
 constexpr int kMaxXGroups = 512;  // groups of x: in <= 32768
-enum GemvMode { kDense = 0, kPair = 1, kSeg = 2 };
+// kPairRouted: the MoE gate/up kernel that selects the experts from the logits itself (built
+// apart, so that the other kernels carry none of the router's code).
+enum GemvMode { kDense = 0, kPair = 1, kSeg = 2, kPairRouted = 3 };
+__host__ __device__ constexpr bool mode_pair(int m) { return m == kPair || m == kPairRouted; }
 constexpr int kThreads = 512;       // 16 warps per CTA, one CTA per SM
 constexpr int kGroupsPerUnit = 32;  // groups of one work unit (one per lane)
 constexpr int kXBytesPerGroup = 265;  // shared memory per group of x: X (128), L (128), factors (8), flag (1)
@@ -96,8 +99,8 @@ struct GemvArgs {
   int groups;                         // nseg * in / 64
   int total_rows;
   int rows_per_cta;  // upper bound of a CTA's row count (sizes the partial-sum buffer)
-  // Router in the kernel (pair mode, MoE gate/up): with `logits` set, every CTA selects the top
-  // nmat of n_logits logits itself (instead of reading idx), and CTA 0 writes the selection to
+  // Router in the kernel (the routed gate/up mode): with `logits` set, every CTA selects the top
+  // nmat of n_logits logits itself instead of reading idx, and CTA 0 writes the selection to
   // idx_out / p_out for the kernels that follow.
   const float* logits;
   int n_logits, renorm;
@@ -238,34 +241,46 @@ __device__ __forceinline__ uint32_t router_float_key(float f) {
 
 // Top-k of n logits by one warp ([FFAI#14] commit "moeRouterTopK"; order (value desc, index asc)
 // as in [FFAI#9]): a candidate is the 64-bit key (float key << 32) | ~index, unique per expert, so
-// round s takes the warp's largest key below round s - 1's.  Weights: softmax over the k selected
-// logits (renorm) or over all n read at the selected ones.  Results for slot s go to idx[s] / p[s]
-// (shared memory) and, when given, to gidx[s] / gp[s] (global).  k <= 32, n <= 1024.
-__device__ __forceinline__ void route_topk_warp(const float* logits, int n, int k, int renorm, uint32_t* idx,
-                                                float* p, uint32_t* gidx, float* gp) {
-  const int lane = threadIdx.x & 31;
-  // up to 128 experts: the lane's keys stay in registers; beyond, they are re-read each round
+// round s takes the warp's largest key not yet taken.  Two steps, so that the logits' loads can be
+// in flight beside other loads: router_load issues them (the first 128 experts' keys stay in
+// registers, the rest are re-read each round), router_select runs the k rounds (the warp's largest
+// key as the largest upper half, then the largest lower half among the lanes holding it: two warp
+// reductions per round) and the weights: softmax over the k selected logits (renorm) or over all n
+// read at the selected ones.  Results for slot s go to idx[s] / p[s] and, when given, to
+// gidx[s] / gp[s].  k <= 32, n <= 1024.  The logits are read through L2 (ld.global.cg).
+struct RouterKeys {
   unsigned long long kr[4];
+};
+__device__ __forceinline__ unsigned long long router_key(float f, int e) {
+  return ((unsigned long long)router_float_key(f) << 32) | (uint32_t)~(uint32_t)e;
+}
+__device__ __forceinline__ RouterKeys router_load(const float* logits, int n) {
+  const int lane = threadIdx.x & 31;
+  RouterKeys r;
+  float v[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int e = lane + 32 * j;
-    kr[j] = e < n ? ((unsigned long long)router_float_key(__ldg(logits + e)) << 32) | (uint32_t)~(uint32_t)e : 0ull;
-  }
+  for (int j = 0; j < 4; ++j) v[j] = lane + 32 * j < n ? __ldcg(logits + lane + 32 * j) : 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) r.kr[j] = lane + 32 * j < n ? router_key(v[j], lane + 32 * j) : 0ull;
+  return r;
+}
+__device__ __forceinline__ void router_select(RouterKeys r, const float* logits, int n, int k, int renorm,
+                                              uint32_t* idx, float* p, uint32_t* gidx, float* gp) {
+  const int lane = threadIdx.x & 31;
   unsigned long long prev = ~0ull, mine = 0;
   for (int s = 0; s < k; ++s) {
-    unsigned long long best = 0;
+    unsigned long long best = 0;  // (taken register keys are zeroed; no key is 0)
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (kr[j] < prev && kr[j] > best) best = kr[j];
+    for (int j = 0; j < 4; ++j) best = r.kr[j] > best ? r.kr[j] : best;
     for (int e = lane + 128; e < n; e += 32) {
-      const unsigned long long key = ((unsigned long long)router_float_key(__ldg(logits + e)) << 32) | (uint32_t)~(uint32_t)e;
+      const unsigned long long key = router_key(__ldcg(logits + e), e);
       if (key < prev && key > best) best = key;
     }
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
+    best = ((unsigned long long)hi << 32) | lo;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
-      best = o > best ? o : best;
-    }
+    for (int j = 0; j < 4; ++j) r.kr[j] = r.kr[j] == best ? 0ull : r.kr[j];
     if (lane == s) mine = best;
     prev = best;
   }
@@ -277,7 +292,7 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
   if (renorm) {
     z = lane < k ? expf(my_v - m) : 0.f;
   } else {
-    for (int e = lane; e < n; e += 32) z += expf(__ldg(logits + e) - m);
+    for (int e = lane; e < n; e += 32) z += expf(__ldcg(logits + e) - m);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
@@ -290,6 +305,62 @@ __device__ __forceinline__ void route_topk_warp(const float* logits, int n, int 
       gp[lane] = pv;
     }
   }
+  __syncwarp();
+}
+
+// The logit a key was made from (-0 comes back as +0).
+__device__ __forceinline__ float router_key_value(unsigned long long key) {
+  const uint32_t kv = (uint32_t)(key >> 32);
+  return __uint_as_float((kv & 0x80000000u) ? (kv & 0x7FFFFFFFu) : ~kv);
+}
+
+// CTA-wide top-k for n <= kRankExperts experts, all threads of the CTA: the expert of rank r (the
+// number of keys above its own) goes to sel[r] for r < k.  Thread t counts the keys above expert
+// t / 4's among every fourth expert from t % 4 (the four lanes' loads of one step fall in distinct
+// banks), and the four counts are added by shuffles.  keys[0, n) (keys as in router_select) is
+// complete before the call; the caller places a barrier before sel is read.
+constexpr int kRankExperts = kThreads / 4;
+__device__ __forceinline__ void router_rank(const unsigned long long* keys, int n, int k, uint32_t* sel) {
+  const int e = threadIdx.x >> 2, q = threadIdx.x & 3;
+  int c = 0;
+  if (e < n) {
+    const unsigned long long ke = keys[e];
+#pragma unroll 8
+    for (int j = q; j < n; j += 4) c += keys[j] > ke ? 1 : 0;
+  }
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  if (e < n && q == 0 && c < k) sel[c] = (uint32_t)e;
+}
+
+// The weights of the selection sel[0, k) by one warp: softmax over the k selected logits (renorm)
+// or over all n, from the keys; slot s's expert and weight to idx[s] / p[s] and, when given,
+// gidx[s] / gp[s].
+__device__ __forceinline__ void router_weights(const unsigned long long* keys, int n, int k, int renorm,
+                                               const uint32_t* sel, uint32_t* idx, float* p, uint32_t* gidx,
+                                               float* gp) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t my_idx = lane < k ? sel[lane] : sel[0];
+  const float my_v = router_key_value(keys[my_idx]);
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);  // rank 0: the largest logit
+  float z = 0.f;
+  if (renorm) {
+    z = lane < k ? expf(my_v - m) : 0.f;
+  } else {
+    for (int e = lane; e < n; e += 32) z += expf(router_key_value(keys[e]) - m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+  if (lane < k) {
+    const float pv = expf(my_v - m) / z;
+    idx[lane] = my_idx;
+    p[lane] = pv;
+    if (gidx) {
+      gidx[lane] = my_idx;
+      gp[lane] = pv;
+    }
+  }
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ thread-block cluster helpers
@@ -325,8 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float s_gss[NORM ? kMaxXGroups : 1];  // gated: each group's sum of x^2, then
   __shared__ float s_hrn[NORM ? kMaxXGroups : 1];  // each head's 1 / root
-  __shared__ uint32_t s_idx[kMaxMats];  // the in-kernel router's selection
-  __shared__ float s_p[kMaxMats];
+  constexpr bool PAIR = mode_pair(MODE), SEG = MODE == kSeg;
+  constexpr bool ROUTED = MODE == kPairRouted;  // a.logits set
+  constexpr int NRW = ROUTED ? kThreads / 32 : 1;
+  __shared__ uint32_t s_idx[NRW][kMaxMats];  // the router's selection, per warp
+  __shared__ float s_p[NRW][kMaxMats];
+  __shared__ unsigned long long s_key[ROUTED ? kRankExperts : 1];  // the router's keys
+  __shared__ uint32_t s_sel[kMaxMats];
   __shared__ float s_ss[kThreads / 32];  // NORM: per-warp sums of x^2
   __shared__ __align__(8) uint64_t xbar;  // the x copy's completion
   pdl_trigger();
@@ -334,7 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     mbar_init(&xbar, 1);
     mbar_fence_init();
   }
-  constexpr bool PAIR = MODE == kPair, SEG = MODE == kSeg;
   constexpr int NC = PAIR ? 2 : 1;  // components per row
   constexpr int RB = RN / NC;       // rows per work unit
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -362,8 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const int vb = (int)((long long)cid * a.total_rows / ncl);
   const int ve = (int)((long long)(cid + 1) * a.total_rows / ncl);
 
-  const bool indexed = a.idx != nullptr || a.logits != nullptr;  // slots resolved through indices
-  const uint32_t* idxp = a.logits ? s_idx : a.idx;
+  const bool indexed = ROUTED || a.idx != nullptr;  // slots resolved through indices
+  // Routed: the selection, made after the dependency wait, from each warp's own copy.
+  const uint32_t* idxp = ROUTED ? s_idx[ROUTED ? warp : 0] : a.idx;
 
   int nblocks = 0;
   for (int mi = 0; mi < a.nmat; ++mi) {
@@ -416,7 +492,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   UnitLoads<RN> b0, b1;
   int u = warp;
   UnitCursor uc{warp / nkc, warp % nkc};
+  // The router (logits set), every thread of the CTA (uniform; barriers inside): up to
+  // kRankExperts experts ranked by the whole CTA, more by each warp on its own.  w0: the warp that
+  // writes the selection to idx_out / p_out.
+  auto route = [&](bool w0) {
+    if constexpr (ROUTED) {
+      const int k = a.nmat, n = a.n_logits;
+      uint32_t* gi = w0 ? a.idx_out : nullptr;
+      float* gp = w0 ? a.p_out : nullptr;
+      if (n <= kRankExperts) {
+        if ((int)threadIdx.x < n) s_key[threadIdx.x] = router_key(__ldcg(a.logits + threadIdx.x), (int)threadIdx.x);
+        __syncthreads();
+        router_rank(s_key, n, k, s_sel);
+        __syncthreads();
+        router_weights(s_key, n, k, a.renorm, s_sel, s_idx[warp], s_p[warp], gi, gp);
+      } else {
+        router_select(router_load(a.logits, n), a.logits, n, k, a.renorm, s_idx[warp], s_p[warp], gi, gp);
+      }
+    }
+  };
   if (u < nunits && !indexed) issue(uc, b0);  // before the dependency wait: weights only
+  // Before the wait, the lines that the first steps after it read (the logits, or the indices and
+  // slot weights, and this CTA's slice of a staged x) are asked into L2 with their address
+  // translations: the values may still change, but L2 is where the writes land, so the reads after
+  // the wait see them.
+  if constexpr (MODE == kPairRouted) {
+    if ((int)threadIdx.x * 32 < a.n_logits) prefetch_l2(a.logits + threadIdx.x * 32);
+  } else {
+    if (threadIdx.x == 0 && a.idx) prefetch_l2(a.idx);
+    if (threadIdx.x == 32 && a.p) prefetch_l2(a.p);
+  }
+  if constexpr (STG) {
+    const int nl = G * (a.xf32 ? 2 : 1);
+    const uint8_t* xb = static_cast<const uint8_t*>(a.x) + (size_t)gb0 * (a.xf32 ? 256u : 128u);
+    for (int i = threadIdx.x; i < nl; i += kThreads) prefetch_l2(xb + (size_t)i * 128);
+  }
 
   // --- x: 16-bit fixed point per group, into shared memory ---
   bool xok = true;   // (false: x never arrived)
@@ -439,12 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                        min(kChunk, gbytes - off), &xbar);
     }
   }
-  if (a.logits) {  // the router, in every CTA
-    if (warp == 0) route_topk_warp(a.logits, a.n_logits, a.nmat, a.renorm, s_idx, s_p, blockIdx.x == 0 ? a.idx_out : nullptr,
-                                   blockIdx.x == 0 ? a.p_out : nullptr);
-    __syncthreads();
+  if constexpr (MODE == kPairRouted) {  // the router, then the weights, then x (staged meanwhile)
+    route(blockIdx.x == 0 && warp == 0);
+    if (u < nunits) issue(uc, b0);
+  } else if constexpr (!ROUTED) {
+    if (u < nunits && indexed) issue(uc, b0);  // indices from the previous kernel
   }
-  if (u < nunits && indexed) issue(uc, b0);
   {
     // 8 lanes per group, 8 values (one 8-column word) per lane.  All of a thread's loads (up to 8
     // groups of bf16 or 5 of fp32: one round for every in <= 32768 bf16 / 20480 fp32) are issued
@@ -1164,7 +1274,7 @@ void gemv_debug_plan(int mode, const GemvArgs& a, int grid, size_t smem);
 template <int MODE>
 int plan_and_launch(GemvArgs& a, cudaStream_t stream) {
   const DeviceInfo& dev = device_info();
-  constexpr int NC = MODE == kPair ? 2 : 1;
+  constexpr int NC = mode_pair(MODE) ? 2 : 1;
   constexpr int RB = 4 / NC;
   a.groups = a.nseg * a.in / 64;
   const int cps = g_gemv_tune.ctas_per_sm ? g_gemv_tune.ctas_per_sm : 1;
@@ -1212,7 +1322,7 @@ int plan_and_launch(GemvArgs& a, cudaStream_t stream) {
   if (a.kcl > 1)  // (never with a norm prologue)
     return a.stage ? launch_gemv_variant<MODE, 4, true, false, 4, true>(a, grid, smem, stream)
                    : launch_gemv_variant<MODE, 4, false, false, 4, true>(a, grid, smem, stream);
-  if constexpr (MODE != kSeg) {
+  if constexpr (MODE == kDense || MODE == kPair) {
     if (a.gamma)
       return a.stage ? launch_gemv_variant<MODE, 4, true, true>(a, grid, smem, stream)
                      : launch_gemv_variant<MODE, 4, false, true>(a, grid, smem, stream);

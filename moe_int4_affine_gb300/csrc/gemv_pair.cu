@@ -32,7 +32,7 @@ int moe_gate_up_routed_launch(const float* logits, int n_logits, int renorm, con
   a.renorm = renorm;
   a.idx_out = idx_out;
   a.p_out = p_out;
-  return plan_and_launch<kPair>(a, stream);
+  return plan_and_launch<kPairRouted>(a, stream);
 }
 
 }  // namespace qg

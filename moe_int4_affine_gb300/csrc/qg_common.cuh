@@ -76,6 +76,11 @@ __device__ __forceinline__ void bulk_g2s_bytes(void* dst, const void* src, uint3
                : "memory");
 }
 
+// The line holding p into L2 (no value returned; also brings its address translation along).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Wait until the preceding kernel in the stream has completed and its writes are visible.  A
 // no-op when the kernel was launched without the programmatic-serialization attribute.

@@ -178,8 +178,10 @@ def test_moe_layer_fused_router_matches_oracle_and_two_calls(qg, moe_full, seed,
     assert qg.qg_device_status() == 0
 
 
-@pytest.mark.parametrize("E,hidden,inter,k", [(4, 128, 64, 2), (9, 576, 128, 8), (37, 256, 192, 5)])
+@pytest.mark.parametrize("E,hidden,inter,k", [(4, 128, 64, 2), (9, 576, 128, 8), (37, 256, 192, 5),
+                                           (300, 256, 64, 8), (1024, 128, 64, 7)])
 def test_moe_layer_fused_small_shapes(qg, E, hidden, inter, k):
+    """Both kernels select the experts themselves (more than 128 experts: keys re-read per round)."""
     gate, up, down = _moe_weights(E, hidden, inter, seed=E + 100)
     logits = I.f32_normal(E, I.TID_LOGITS, E)
     x = I.bf16_normal(E, I.TID_X, hidden)
@@ -190,3 +192,22 @@ def test_moe_layer_fused_small_shapes(qg, E, hidden, inter, k):
     assert qg.to_numpy(idx).astype(np.uint32).tolist() == i_ref.tolist()
     y_ref, a, _ = oracle.moe(_t(gate), _t(up), _t(down), i_ref, p_ref, x, r)
     assert_within_bound(qg.to_numpy(y).astype(np.float64), y_ref, a)
+
+
+@pytest.mark.parametrize("E", [128, 200])
+def test_moe_layer_fused_router_ties(qg, E):
+    """Logits on a coarse grid (many ties): both kernels of the layer take the lower index first,
+    as the oracle does, and agree with each other (y within the bound for the oracle's selection)."""
+    hidden, inter, k = 256, 128, 8
+    gate, up, down = _moe_weights(E, hidden, inter, seed=E + 7)
+    logits = np.round(I.f32_normal(E + 7, I.TID_LOGITS, E) * 2.0).astype(np.float32) / 2.0
+    x = I.bf16_normal(E + 7, I.TID_X, hidden)
+    r = I.bf16_normal(E + 7, I.TID_RESID, hidden)
+    G, U, D = (qg.Int4Weight.from_numpy(d) for d in (gate, up, down))
+    y, idx, p = qg.moe_layer_int4(qg.to_device(logits), G, U, D, qg.to_device(x), qg.to_device(r), k=k)
+    i_ref, p_ref = oracle.router_topk(logits, k)
+    assert len(set(logits[i_ref].tolist())) < k  # (the selection crosses a tie)
+    assert qg.to_numpy(idx).astype(np.uint32).tolist() == i_ref.tolist()
+    y_ref, a, _ = oracle.moe(_t(gate), _t(up), _t(down), i_ref, p_ref, x, r)
+    assert_within_bound(qg.to_numpy(y).astype(np.float64), y_ref, a)
+    assert qg.qg_device_status() == 0
