@@ -43,7 +43,11 @@
 // more than 2^31 below their row's largest, and weights below 2^-14 in magnitude, where the
 // absolute terms above apply instead (the 1e-6 absolute part of the bound covers them only for
 // rows of small magnitude).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <mutex>
 
 #include "qg_common.cuh"
 #include "qg_internal.h"
@@ -59,6 +63,16 @@ constexpr int kProducers = kProducerWarps * 32;
 constexpr int kMmaWarp = kProducerWarps;      // the MMA / tensor-memory warp
 constexpr int kLoadWarp = kProducerWarps + 1; // the token-tile loader
 constexpr int kThreads = kProducers + 64;
+constexpr int kCodeWarp = kProducerWarps + 2;  // CTMA: the weight-chunk loader
+constexpr int kThreadsC = kProducers + 96;
+// CTMA (token tiles of at most 64 rows): the weights arrive by TMA tensor copies in chunks of eight
+// groups for the CTA's 128 rows -- the codes as two 128-row x 128-byte boxes (128-byte swizzle),
+// then the scales and the biases as 128-row x 16-byte boxes -- instead of one cp.async per thread,
+// group and word.  Each thread owns a weight row, so a warp's per-thread copies touch 32 rows'
+// lines at once; the copy engine issues a box's lines without that per-request cost.
+constexpr uint32_t kCodeBox = 128 * 128;            // one codes box (four groups of 128 rows)
+constexpr uint32_t kSbBox = 128 * 16;               // one scales (or biases) box (eight groups)
+constexpr uint32_t kCSlot = 2 * kCodeBox + 2 * kSbBox;  // one chunk: 36 KB (a multiple of 1024)
 constexpr int kMaxStages = 4;
 constexpr int kAccCols = 256;                // tensor memory: columns 0..255 accumulator, then per stage
 constexpr int kACols = kGK / 2;              //   32 columns (64 fp16 per lane) of A per group,
@@ -80,6 +94,9 @@ struct TcMat {
 constexpr int kTcMaxMats = 4;
 
 struct TcArgs {
+  // CTMA: per matrix, tensor maps of the codes ([n_mat][out][in / 8] u32, box 32 x 128 x 1, 128-byte
+  // swizzle), scales and biases ([n_mat][out][in / 64] u16, box 8 x 128 x 1)
+  CUtensorMap tm_codes[kTcMaxMats], tm_scales[kTcMaxMats], tm_biases[kTcMaxMats];
   TcMat mat[kTcMaxMats];  // matrices sharing the tokens (same in)
   int nmat;
   // grouped (MoE) mode: token tile y belongs to expert tile_expert[y] (< 0: no tile, the CTA
@@ -89,7 +106,8 @@ struct TcArgs {
   const float* xs;    // [n_tiles * n_tile] per-token output scale
   int in, T;
   int n_tile;
-  int stages;
+  int stages;   // A stages (tensor memory)
+  int tstages;  // token-tile slots (shared memory; at least stages): loaded that many stages ahead
   uint32_t idesc;
 };
 
@@ -129,16 +147,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 // Both barriers' phases complete?  The two tests are issued together (one latency, not two).
-__device__ __forceinline__ bool test_wait2(uint64_t* b0, uint64_t* b1, uint32_t parity) {
+__device__ __forceinline__ bool test_wait2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %3;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q, [%2], %3;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q, [%2], %4;\n\t"
       "and.pred p, p, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(b0)), "r"(smem_u32(b1)), "r"(parity)
+      : "r"(smem_u32(b0)), "r"(smem_u32(b1)), "r"(p0), "r"(p1)
       : "memory");
   return ok != 0;
 }
@@ -150,6 +168,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
+}
+// One box of a 3-D tensor map into shared memory, completion counted on bar in bytes.
+__device__ __forceinline__ void tma3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
 }
 __device__ __forceinline__ void cp16(uint32_t dst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
@@ -209,36 +235,47 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2, uint32_t b2) 
 // GPS: quantization groups per pipeline stage (K = 64 GPS).  Four halve the number of stage
 // hand-overs for small token tiles (accumulator N <= 64 in columns 0-63, up to three A stages of 128
 // columns from column 64); two otherwise.
-template <int WRING, int TMEMC, bool SBREG, int GPS>
-__global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kernel(const __grid_constant__ TcArgs a) {
+// CTMA: the weights by TMA tensor copies (kCSlot chunks, a ring of WRING of them; see kCodeBox).
+template <int WRING, int TMEMC, bool SBREG, int GPS, bool CTMA = false>
+__global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 : 1)
+    qgemm_tc_kernel(const __grid_constant__ TcArgs a) {
   static_assert(GPS == 2 || (GPS == 4 && TMEMC == 512), "four groups per stage: one-CTA kernel only");
+  static_assert(!CTMA || (GPS == 4 && TMEMC == 512 && !SBREG), "tensor copies: the small-tile kernel only");
   constexpr uint32_t kABase = (TMEMC == 512 && GPS == 2) ? (uint32_t)kAccCols : 64u;
   constexpr uint32_t kAStageT = (uint32_t)(GPS * kACols);  // A columns of one stage
   constexpr int kWStageBytes = wstage_bytes(SBREG);
+  constexpr size_t kRingBytes = CTMA ? (size_t)WRING * kCSlot : (size_t)WRING * kWStageBytes;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* basep = smem_raw + (base - raw);
-  const int S = a.stages;
+  const int S = a.stages, D = a.tstages;
   const uint32_t btile = (uint32_t)a.n_tile * 128u;  // token tile of one group (the stage)
   const uint32_t stage_bytes = GPS * btile;  // the token tiles of a stage's groups
-  const uint32_t wring = base + (uint32_t)S * stage_bytes;  // weight staging ring
-  // full[s]: the producers' A columns; bfull[s]: the token tile's bytes; empty[s]: the stage's MMAs done
-  uint64_t* full = reinterpret_cast<uint64_t*>(basep + (size_t)S * stage_bytes + (size_t)WRING * kWStageBytes);
-  uint64_t* bfull = full + S;
-  uint64_t* empty = bfull + S;
-  uint64_t* done = empty + S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  const uint32_t wring = base + (uint32_t)D * stage_bytes;  // weight staging ring (CTMA: chunks, 1024-aligned)
+  // full[s] / empty[s]: A stage s written by the producers / its MMAs done; bfull[t] / tempty[t]:
+  // token slot t's bytes landed / the MMAs that read it done
+  uint64_t* full = reinterpret_cast<uint64_t*>(basep + (size_t)D * stage_bytes + kRingBytes);
+  uint64_t* empty = full + S;
+  uint64_t* bfull = empty + S;
+  uint64_t* tempty = bfull + D;
+  uint64_t* done = tempty + D;
+  // CTMA: cfull[c]: chunk slot c's bytes landed; cempty[c]: every producer warp has read it
+  uint64_t* cfull = done + 1;
+  uint64_t* cempty = cfull + (CTMA ? WRING : 0);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + (CTMA ? WRING : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int mi = 0;  // this CTA's matrix: the last one whose first tile is at or before blockIdx.x
   while (mi + 1 < a.nmat && (int)blockIdx.x >= a.mat[mi + 1].tile0) ++mi;
   TcMat mt = a.mat[mi];
+  int ez = 0;  // the expert (the tensor maps' third coordinate)
   if (a.tile_expert) {  // grouped: the tile table is the previous kernel's output
     pdl_wait();
     const int e = a.tile_expert[blockIdx.y];
     if (e < 0) return;  // (before any barrier, tensor memory or copy: the whole CTA leaves)
+    ez = e;
     mt.packed += (size_t)e * (size_t)mt.ew;
     mt.scales += (size_t)e * (size_t)mt.esb;
     mt.biases += (size_t)e * (size_t)mt.esb;
@@ -252,10 +289,19 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
     if (lane == 0) {
       for (int s = 0; s < S; ++s) {
         mbar_init(full + s, kProducerWarps);
-        mbar_init(bfull + s, 1);
         mbar_init(empty + s, 1);
       }
+      for (int t = 0; t < D; ++t) {
+        mbar_init(bfull + t, 1);
+        mbar_init(tempty + t, 1);
+      }
       mbar_init(done, 1);
+      if constexpr (CTMA) {
+        for (int c = 0; c < WRING; ++c) {
+          mbar_init(cfull + c, 1);
+          mbar_init(cempty + c, kProducerWarps);
+        }
+      }
       *abort_flag = 0;
       mbar_fence_init();
     }
@@ -270,8 +316,9 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Only the token tiles and their scales come from the previous kernel (the staging kernel): the
+  // token loader and the epilogue wait for it; the weights start streaming at once.
   pdl_trigger();
-  pdl_wait();
 
   if (warp < kProducerWarps) {
     // ---------------- producers: thread (row r, warp group h) makes group 2 j + h of every stage j
@@ -335,8 +382,11 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
       ld_chunk(qc, s_cur, b_cur);
       ld_chunk(qc + 1, s_nxt, b_nxt);
     }
+    if constexpr (!CTMA) {
 #pragma unroll 1
-    for (int jj = 0; jj < WRING - 1; ++jj) wissue(jj);
+      for (int jj = 0; jj < WRING - 1; ++jj) wissue(jj);
+    }
+    uint32_t csl = 0;  // CTMA: the current chunk's slot
 
     for (int j = 0; j < nst; ++j) {  // stage j: groups GPS j + 2 q + h, q < GPS / 2 (thread group jj)
       const int s = j % S;
@@ -346,13 +396,36 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
 #pragma unroll
       for (int q = 0; q < GPS / 2; ++q) {
         const int jj = (GPS / 2) * j + q;  // this thread's group 2 jj + h (its jj-th)
-        wissue(jj + WRING - 1);
-        cp_wait<WRING - 1>();  // group jj of this thread has landed
-        if (2 * jj + h < nk) {  // (uniform per warp)
-          const uint32_t g = (uint32_t)(jj % WRING) * kWStageBytes;
-          const uint4 c0 = lds128(wcode + g), c1 = lds128(wcode + g + kProducers * 16);
+        if constexpr (CTMA) {
+          if ((jj & 3) == 0) {  // chunk jj / 4 (groups 8 (jj / 4) ..): its bytes, then this row's scales and biases
+            const int c = jj >> 2;
+            csl = wring + (uint32_t)(c % WRING) * kCSlot;
+            if (!mbar_wait(cfull + c % WRING, (uint32_t)(c / WRING) & 1u)) *abort_flag = 1;
+            s_cur = lds128(csl + 2 * kCodeBox + (uint32_t)r * 16u);
+            b_cur = lds128(csl + 2 * kCodeBox + kSbBox + (uint32_t)r * 16u);
+          }
+        } else {
+          wissue(jj + WRING - 1);
+          cp_wait<WRING - 1>();  // group jj of this thread has landed
+        }
+        const bool live = 2 * jj + h < nk && !(CTMA && __any_sync(0xffffffffu, *abort_flag != 0));
+        if (live) {  // (uniform per warp: tcgen05.st is a warp-wide instruction)
+          uint4 c0, c1;
           uint32_t s2, b2;
-          if constexpr (SBREG) {
+          if constexpr (CTMA) {
+            // group o of the chunk: codes box o / 4, 16-byte pieces 2 (o % 4) and 2 (o % 4) + 1 of
+            // row r, each at its swizzled place (piece i of row r at i ^ (r % 8))
+            const int o = (2 * jj + h) & 7;
+            const uint32_t ra = csl + (uint32_t)(o >> 2) * kCodeBox + (uint32_t)r * 128u;
+            const uint32_t sw = (uint32_t)(r & 7);
+            c0 = lds128(ra + (((uint32_t)(2 * (o & 3)) ^ sw) << 4));
+            c1 = lds128(ra + (((uint32_t)(2 * (o & 3) + 1) ^ sw) << 4));
+            s2 = bf16_to_f16x2(pick16(s_cur, o));
+            b2 = bf16_to_f16x2(pick16(b_cur, o));
+          } else if constexpr (SBREG) {
+            const uint32_t g = (uint32_t)(jj % WRING) * kWStageBytes;
+            c0 = lds128(wcode + g);
+            c1 = lds128(wcode + g + kProducers * 16);
             const size_t e = e0 + 2 * (size_t)jj;  // (advances 2 per group: at most one chunk)
             if ((e >> 3) != qc) {
               s_cur = s_nxt;
@@ -363,6 +436,9 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
             s2 = bf16_to_f16x2(pick16(s_cur, (int)(e & 7)));
             b2 = bf16_to_f16x2(pick16(b_cur, (int)(e & 7)));
           } else {
+            const uint32_t g = (uint32_t)(jj % WRING) * kWStageBytes;
+            c0 = lds128(wcode + g);
+            c1 = lds128(wcode + g + kProducers * 16);
             const uint32_t sw = lds32(wsb + g), bw = lds32(wsb + g + 4);
             s2 = bf16_to_f16x2(odd ? sw >> 16 : sw & 0xFFFFu);
             b2 = bf16_to_f16x2(odd ? bw >> 16 : bw & 0xFFFFu);
@@ -381,6 +457,12 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
                         (kABase + kAStageT * (uint32_t)s + (uint32_t)(kACols * (2 * q + h))),
                     v);
         }
+        if constexpr (CTMA) {
+          if ((jj & 3) == 3) {  // this warp has read the chunk
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cempty + (jj >> 2) % WRING);
+          }
+        }
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
@@ -392,37 +474,60 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
     // ---------------- token-tile loader: stage j's tiles (contiguous in the workspace), one bulk
     // copy each, issued as soon as the stage is free
     if (lane == 0) {
+      pdl_wait();
       int issued = 0;
       for (int j = 0; j < nst; ++j) {
-        const int s = j % S;
-        if (j >= S && !mbar_wait(empty + s, (uint32_t)(j / S - 1) & 1u)) *abort_flag = 1;
+        const int t = j % D;
+        if (j >= D && !mbar_wait(tempty + t, (uint32_t)(j / D - 1) & 1u)) *abort_flag = 1;
         if (*abort_flag) break;
         const uint32_t bytes = (uint32_t)min(GPS, nk - GPS * j) * btile;
-        mbar_arrive_expect_tx(bfull + s, bytes);
-        bulk_g2s(base + (uint32_t)s * stage_bytes, a.xt + ((size_t)tile * nk + (size_t)GPS * j) * btile, bytes,
-                 bfull + s);
+        mbar_arrive_expect_tx(bfull + t, bytes);
+        bulk_g2s(base + (uint32_t)t * stage_bytes, a.xt + ((size_t)tile * nk + (size_t)GPS * j) * btile, bytes,
+                 bfull + t);
         ++issued;
       }
       // every bulk copy issued here has landed before the CTA can exit (normally long since: the MMA
-      // thread waited for it); the latest use of each stage may be outstanding
-      for (int j = max(0, issued - S); j < issued; ++j) mbar_wait(bfull + j % S, (uint32_t)(j / S) & 1u);
+      // thread waited for it); the latest use of each slot may be outstanding
+      for (int j = max(0, issued - D); j < issued; ++j) mbar_wait(bfull + j % D, (uint32_t)(j / D) & 1u);
     }
-  } else if (lane == 0) {  // (warp kMmaWarp)
+  } else if (CTMA && warp == kCodeWarp) {
+    // ---------------- weight-chunk loader: chunk c (groups 8c .. 8c + 7 of the CTA's 128 rows) into
+    // slot c % WRING as soon as every producer warp has read the chunk before it there
+    if (lane == 0) {
+      const int nch = (nk + 7) / 8;
+      const int y0 = m0;  // first row within the matrix
+      int issued = 0;
+      for (int c = 0; c < nch; ++c) {
+        const int sl = c % WRING;
+        if (c >= WRING && !mbar_wait(cempty + sl, (uint32_t)(c / WRING - 1) & 1u)) *abort_flag = 1;
+        if (*abort_flag) break;
+        const uint32_t d = wring + (uint32_t)sl * kCSlot;
+        mbar_arrive_expect_tx(cfull + sl, kCSlot);
+        tma3d(d, &a.tm_codes[mi], 64 * c, y0, ez, cfull + sl);
+        tma3d(d + kCodeBox, &a.tm_codes[mi], 64 * c + 32, y0, ez, cfull + sl);
+        tma3d(d + 2 * kCodeBox, &a.tm_scales[mi], 8 * c, y0, ez, cfull + sl);
+        tma3d(d + 2 * kCodeBox + kSbBox, &a.tm_biases[mi], 8 * c, y0, ez, cfull + sl);
+        ++issued;
+      }
+      // every copy issued here has landed before the CTA can exit
+      for (int c = max(0, issued - WRING); c < issued; ++c) mbar_wait(cfull + c % WRING, (uint32_t)(c / WRING) & 1u);
+    }
+  } else if (warp == kMmaWarp && lane == 0) {
     // ---------------- MMA issuer
-    // B descriptors: stage s and K step k add (s * stage_bytes + 32 k) / 16 to the start address
-    // field (bits 0-13: shared addresses stay below 2^18, so the field never carries).
+    // B descriptors: token slot t and K step k add (t * stage_bytes + 32 k) / 16 to the start
+    // address field (bits 0-13: shared addresses stay below 2^18, so the field never carries).
     const uint64_t db0 = smem_desc(base);
     const uint32_t dstage = stage_bytes >> 4;
-    int s = 0;
-    uint32_t ph = 0;  // parity of stage s's current use
+    int s = 0, t = 0;
+    uint32_t ph = 0, pt = 0;  // parities of A stage s's and token slot t's current uses
     for (int j = 0; j < nst; ++j) {
       // (fast path: both already complete; else the bounded waits, which also watch the flag)
-      if (!test_wait2(full + s, bfull + s, ph)) {
-        if (!mbar_wait(full + s, ph) || !mbar_wait(bfull + s, ph)) *abort_flag = 1;
+      if (!test_wait2(full + s, ph, bfull + t, pt)) {
+        if (!mbar_wait(full + s, ph) || !mbar_wait(bfull + t, pt)) *abort_flag = 1;
         if (*abort_flag) break;
       }
       tc_fence_after();  // the producers' tensor-memory stores are complete
-      const uint64_t db = db0 + (uint64_t)(s * dstage);
+      const uint64_t db = db0 + (uint64_t)(t * dstage);
       const uint32_t ta = tmem + kABase + kAStageT * (uint32_t)s;
       const int ng = min(GPS, nk - GPS * j);
       for (int gi = 0; gi < ng; ++gi) {
@@ -432,9 +537,14 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
                      (j | gi | k) != 0 ? 1u : 0u);
       }
       mma_commit(empty + s);
+      mma_commit(tempty + t);
       if (++s == S) {
         s = 0;
         ph ^= 1u;
+      }
+      if (++t == D) {
+        t = 0;
+        pt ^= 1u;
       }
     }
     mma_commit(done);  // arrives once every MMA issued above has completed
@@ -442,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, TMEMC == 256 ? 2 : 1) qgemm_tc_kerne
 
   // ---------------- epilogue: warps w and w + 4 read lanes 32 (w % 4) .. + 31, half of the columns each
   if (warp < kProducerWarps) {
+    pdl_wait();  // (the token scales; and Y is written only after the kernels before this one are done)
     const bool ok = mbar_wait(done, 0);
     tc_fence_after();
     if (ok && !*abort_flag) {
@@ -610,8 +721,10 @@ __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_swiglu_kernel(const f
 }
 
 struct TcPlan {
-  int n_tile, n_tiles, stages, wring;
+  int n_tile, n_tiles, stages, wring;  // (ctma: wring = chunks in the ring)
   size_t smem;
+  bool ctma;   // weights by TMA tensor copies (tiles of at most 64 tokens)
+  int tstages;  // token-tile slots (>= stages)
   int tmem;    // tensor-memory columns per CTA (512, or 256 for two CTAs per SM)
   bool sbreg;  // scales and biases in registers (token tiles of 128 and more, one CTA per SM)
   int gps;     // quantization groups per pipeline stage (4 for tiles of at most 64 tokens)
@@ -638,6 +751,7 @@ TcPlan tc_plan_ntile(int n_tile) {
   // sixteen: T = 8 39.3 us against 47.1 with eight)
   if (!p.sbreg && n_tile >= 32 && p.wring > 8) p.wring = 8;
   p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
+  p.tstages = p.stages;
   p.tmem = 512;
   return p;
 }
@@ -661,15 +775,76 @@ TcPlan tc_plan_ntile_pair(int n_tile) {
   // than eight groups: MoE prefill T = 256, 232.7 -> 219.0 us)
   p.wring = left >= 4 * (size_t)kWStageBytes ? 4 : 2;
   p.smem = fixed + (size_t)p.stages * stage + (size_t)p.wring * kWStageBytes;
+  p.tstages = p.stages;
   return p;
 }
 
+// The weights by tensor copies: tiles of at most 64 tokens, and scale rows a multiple of 16 bytes
+// (in a multiple of 512, which the tensor maps' strides need).  Three A stages (tensor memory); a
+// ring of three weight chunks (108 KB); the rest of the shared memory to token-tile slots (up to
+// twelve), so that the token tiles load well ahead of the A stages.
+TcPlan tc_plan_ctma(int n_tile) {
+  TcPlan p = tc_plan_ntile(n_tile);
+  const size_t stage = (size_t)p.gps * p.n_tile * 128;
+  const size_t fixed = 1024 + 16 + 8 * (2 * 3 + 2 * 12 + 1 + 2 * 3);  // alignment slack, slot and flag, barriers
+  p.ctma = true;
+  p.sbreg = false;
+  p.stages = 3;
+  p.wring = 3;
+  p.tstages = (int)std::min<size_t>(12, (kSmemBudget - fixed - (size_t)p.wring * kCSlot) / stage);
+  p.smem = fixed + (size_t)p.tstages * stage + (size_t)p.wring * kCSlot;
+  return p;
+}
+
+bool g_tc_ctma = true;  // (the tensor-copy kernel where it applies)
+
 TcPlan tc_plan(int out, int in, int T) {
   (void)out;
-  (void)in;
-  TcPlan p = tc_plan_ntile(std::min(kMaxN, (T + 15) / 16 * 16));
+  const int n_tile = std::min(kMaxN, (T + 15) / 16 * 16);
+  TcPlan p = g_tc_ctma && n_tile <= 64 && in % 512 == 0 ? tc_plan_ctma(n_tile) : tc_plan_ntile(n_tile);
   p.n_tiles = (T + p.n_tile - 1) / p.n_tile;
   return p;
+}
+
+// cuTensorMapEncodeTiled from the driver (no link against it: the runtime hands out its address).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// The three tensor maps of a weight (stack) for the tensor-copy kernel: codes [n_mat][out][in / 8]
+// u32 in boxes of 32 x 128 x 1 with the 128-byte swizzle; scales and biases [n_mat][out][in / 64] u16
+// in boxes of 8 x 128 x 1.  Rows and columns past the ends read as zero.
+bool encode_weight_maps(const qg_int4_weight& w, CUtensorMap* codes, CUtensorMap* scales, CUtensorMap* biases) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || w.in % 512 != 0) return false;
+  const cuuint64_t nm = (cuuint64_t)w.n_mat, out = (cuuint64_t)w.out;
+  const cuuint32_t es[3] = {1, 1, 1};
+  const cuuint64_t dc[3] = {(cuuint64_t)w.in / 8, out, nm};
+  const cuuint64_t sc[2] = {(cuuint64_t)w.in / 2, out * (cuuint64_t)(w.in / 2)};
+  const cuuint32_t bc[3] = {32, 128, 1};
+  if (enc(codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(w.packed), dc, sc, bc, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const cuuint64_t ds[3] = {(cuuint64_t)w.in / 64, out, nm};
+  const cuuint64_t ss[2] = {(cuuint64_t)w.in / 32, out * (cuuint64_t)(w.in / 32)};
+  const cuuint32_t bs[3] = {8, 128, 1};
+  for (int i = 0; i < 2; ++i) {
+    if (enc(i ? biases : scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(i ? w.biases : w.scales), ds,
+            ss, bs, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
 }
 
 int tc_launch(const TcArgs& a, const TcPlan& p, dim3 grid, cudaStream_t stream) {
@@ -681,8 +856,20 @@ int tc_launch(const TcArgs& a, const TcPlan& p, dim3 grid, cudaStream_t stream) 
     const int carve = (int)std::min<size_t>(100, (2 * p.smem + 2048) * 100 / (228 * 1024) + 1);
     if (p.tmem == 256 && cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, carve) != cudaSuccess)
       return (int)QG_ELAUNCH;
-    return launch(k, grid, dim3(kThreads), p.smem, stream, a);
+    return launch(k, grid, dim3(p.ctma ? kThreadsC : kThreads), p.smem, stream, a);
   };
+  if (p.ctma) {
+    switch (p.wring) {
+      case 5:
+        return go(qgemm_tc_kernel<5, 512, false, 4, true>);
+      case 4:
+        return go(qgemm_tc_kernel<4, 512, false, 4, true>);
+      case 3:
+        return go(qgemm_tc_kernel<3, 512, false, 4, true>);
+      default:
+        return go(qgemm_tc_kernel<2, 512, false, 4, true>);
+    }
+  }
   if (p.tmem == 256) {
     switch (p.wring) {
       case 4:
@@ -757,6 +944,7 @@ int qgemm_tc_launch_multi(const qg_int4_weight* w, int n, const uint16_t* X, int
   for (int i = 0; i < n; ++i) {
     a.mat[i] = TcMat{w[i].packed, w[i].scales, w[i].biases, Y[i], w[i].out, tiles, 0, 0};
     tiles += (w[i].out + kBM - 1) / kBM;
+    if (p.ctma && !encode_weight_maps(w[i], &a.tm_codes[i], &a.tm_scales[i], &a.tm_biases[i])) return QG_ELAUNCH;
   }
   a.nmat = n;
   a.xt = xt;
@@ -765,6 +953,7 @@ int qgemm_tc_launch_multi(const qg_int4_weight* w, int n, const uint16_t* X, int
   a.T = T;
   a.n_tile = p.n_tile;
   a.stages = p.stages;
+  a.tstages = p.tstages;
   a.idesc = tc_idesc(p.n_tile);
   return tc_launch(a, p, dim3((unsigned)tiles, (unsigned)p.n_tiles), stream);
 }
@@ -807,6 +996,7 @@ int qgemm_tc_grouped_launch(const qg_int4_weight* w, int n, const uint8_t* xt, c
   a.T = n_tiles * n_tile;
   a.n_tile = n_tile;
   a.stages = p.stages;
+  a.tstages = p.tstages;
   a.idesc = tc_idesc(n_tile);
   return tc_launch(a, p, dim3((unsigned)tiles, (unsigned)n_tiles), stream);
 }
