@@ -16,12 +16,21 @@
 //     dequantizes the 64 weights of a group with packed half-precision arithmetic (w = s * q + b,
 //     one rounding to fp16) and writes them with one tensor-memory store (tcgen05.st, 32 columns of
 //     its row's lane) into the stage's A columns.
+//     For tiles of at most 64 tokens (and in a multiple of 512) the weights come instead by TMA
+//     tensor copies, eight groups of the 128 rows at a time (see kCodeBox), issued by a weight
+//     loader warp into a ring of chunks; the producers read their row's codes from the swizzled
+//     boxes.  The weights do not depend on the previous kernel, so they start streaming before the
+//     dependency wait, which only the token loader and the epilogue take.
 //   * The token tile of a stage is one contiguous block of the workspace (written there, already
-//     swizzled, by the prep kernel) and arrives by a single bulk copy (TMA engine) on the stage's
-//     mbarrier.
+//     swizzled, by the prep kernel) and arrives by a single bulk copy (TMA engine) into a ring of
+//     token slots of its own (deeper than the A stages where shared memory allows).
 //   * One thread of the MMA warp issues four K=16 MMAs per group and commits each stage to the
-//     stage's "empty" mbarrier; a final commit releases the epilogue, which reads the accumulator
-//     from tensor memory (tcgen05.ld), applies each token's power-of-two input scale and writes Y.
+//     stage's "empty" mbarrier and to its token slot's; a final commit releases the epilogue, which
+//     reads the accumulator from tensor memory (tcgen05.ld), applies each token's power-of-two
+//     input scale and writes Y.
+//   * Small token tiles are paced by the MMA instructions themselves: measured on this part, an
+//     M = 128, K = 16 MMA takes about 70 ns for N = 16 to 64 (about 110 ns at N = 256 in this
+//     pipeline), so a 128-row tile of K = 5120 (320 MMAs) needs about 22 us at any T <= 64.
 //   * Every mbarrier wait is bounded (2 s): on a timeout the CTA records QG_STATUS_TIMEOUT, stops
 //     issuing, drains what it has in flight and frees its tensor memory before returning.
 //   * Grouped (MoE) mode: token tile y belongs to expert tile_expert[y]; the CTA reads it first
