@@ -325,7 +325,9 @@ int scalar_fma_chain8_residual(const float *p, const float *v, const uint16_t *r
  * range (2^-14 <= |s|, |b| < 65504, or zero; typical models are far inside it).  T < 3 runs the
  * CUDA-core GEMV once per token row.
  * workspace: at least qg_workspace_bytes(QG_OP_QGEMM, w, T) bytes (0 means none is needed): the
- * tensor-core path stages the converted tokens there.
+ * tensor-core path stages the converted tokens there.  For up to 64 tokens and in a multiple of
+ * 512 the weights are read by tensor-map copies (encoded on the host for each call through the
+ * driver entry point the CUDA runtime provides); QG_ELAUNCH if that encoding fails.
  * Limits: 1 <= T <= 4096; in % 64 == 0, 64 <= in <= 32768.
  */
 int qgemm_int4(const qg_int4_weight *w, const uint16_t *X, int T, float *Y, void *workspace, size_t ws_bytes,
@@ -337,8 +339,8 @@ int qgemm_int4(const qg_int4_weight *w, const uint16_t *X, int T, float *Y, void
  * QKV / GDN-input projections, x read once for all of them):
  *   Ys[i][t][r] = sum_j w_i[r][j] * X[t][j]
  * ws[i]: single matrices with the same in; X: bf16 [T][in]; Ys[i]: fp32 [T][ws[i].out] (device).
- * For T >= 32 one tensor-core launch covers the row tiles of all n matrices (the tokens staged
- * once); below that, one GEMV launch per token covers all n.  workspace: at least
+ * For T >= 3 (see qg_tune_qgemm) one tensor-core launch covers the row tiles of all n matrices
+ * (the tokens staged once); below that, one GEMV launch per token covers all n.  workspace: at least
  * qg_workspace_bytes(QG_OP_QGEMM, &ws[0], T) bytes.  Limits as qgemm_int4.
  */
 int qgemm_int4_multi(int n, const qg_int4_weight *ws, const uint16_t *X, int T, float *const *Ys, void *workspace,
