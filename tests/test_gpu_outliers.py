@@ -145,6 +145,19 @@ def test_moe_outlier_channels(qg):
     assert_within(qg.to_numpy(y).astype(np.float64), y_ref, REL * (a + extra) + ABS + extra)
 
 
+@pytest.mark.parametrize("T", [2, 5, 8])
+def test_qgemm_small_t_outlier_channels(qg, T):
+    """Small T with outlier channels in the token rows (one row without): T = 2 on the per-token
+    GEMV (flagged groups take the second pass), T = 5 and 8 on the tensor cores."""
+    d = _w_with_zeros(72, I.TID_W, 1000, 4096)
+    X = np.stack([_x_with_outliers(72 + t, 4096) for t in range(T)])
+    X[1 % T] = I.bf16_normal(73, I.TID_X, 4096)  # one token without outliers
+    Y = qg.to_numpy(qg.qgemm_int4(qg.Int4Weight.from_numpy(d), qg.to_device(X))).astype(np.float64)
+    Y_ref, A = oracle.qgemm(d["packed"], d["scales"], d["biases"], X, threads=ORACLE_THREADS)
+    assert_within_bound(Y, Y_ref, A)
+    assert qg.qg_device_status() == 0
+
+
 @pytest.mark.parametrize("T", [32, 40])
 def test_qgemm_tensor_core_outlier_channels(qg, T):
     """The tensor-core GEMM with outlier channels in every token row (each row scaled by its own
