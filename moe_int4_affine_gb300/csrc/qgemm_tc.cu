@@ -16,7 +16,8 @@
 //     dequantizes the 64 weights of a group with packed half-precision arithmetic (w = s * q + b,
 //     one rounding to fp16) and writes them with one tensor-memory store (tcgen05.st, 32 columns of
 //     its row's lane) into the stage's A columns.
-//     For tiles of at most 64 tokens (and in a multiple of 512) the weights come instead by TMA
+//     For tiles of at most 64 or at least 128 tokens (and in a multiple of 512; not in grouped
+//     mode) the weights come instead by TMA
 //     tensor copies, eight groups of the 128 rows at a time (see kCodeBox), issued by a weight
 //     loader warp into a ring of chunks; the producers read their row's codes from the swizzled
 //     boxes.  The weights do not depend on the previous kernel, so they start streaming before the
@@ -74,7 +75,7 @@ constexpr int kLoadWarp = kProducerWarps + 1; // the token-tile loader
 constexpr int kThreads = kProducers + 64;
 constexpr int kCodeWarp = kProducerWarps + 2;  // CTMA: the weight-chunk loader
 constexpr int kThreadsC = kProducers + 96;
-// CTMA (token tiles of at most 64 rows): the weights arrive by TMA tensor copies in chunks of eight
+// CTMA (the one-CTA kernel): the weights arrive by TMA tensor copies in chunks of eight
 // groups for the CTA's 128 rows -- the codes as two 128-row x 128-byte boxes (128-byte swizzle),
 // then the scales and the biases as 128-row x 16-byte boxes -- instead of one cp.async per thread,
 // group and word.  Each thread owns a weight row, so a warp's per-thread copies touch 32 rows'
@@ -249,7 +250,7 @@ template <int WRING, int TMEMC, bool SBREG, int GPS, bool CTMA = false>
 __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 : 1)
     qgemm_tc_kernel(const __grid_constant__ TcArgs a) {
   static_assert(GPS == 2 || (GPS == 4 && TMEMC == 512), "four groups per stage: one-CTA kernel only");
-  static_assert(!CTMA || (GPS == 4 && TMEMC == 512 && !SBREG), "tensor copies: the small-tile kernel only");
+  static_assert(!CTMA || (TMEMC == 512 && !SBREG), "tensor copies: the one-CTA kernel with ring scales only");
   constexpr uint32_t kABase = (TMEMC == 512 && GPS == 2) ? (uint32_t)kAccCols : 64u;
   constexpr uint32_t kAStageT = (uint32_t)(GPS * kACols);  // A columns of one stage
   constexpr int kWStageBytes = wstage_bytes(SBREG);
@@ -788,18 +789,20 @@ TcPlan tc_plan_ntile_pair(int n_tile) {
   return p;
 }
 
-// The weights by tensor copies: tiles of at most 64 tokens, and scale rows a multiple of 16 bytes
-// (in a multiple of 512, which the tensor maps' strides need).  Three A stages (tensor memory); a
-// ring of three weight chunks (108 KB); the rest of the shared memory to token-tile slots (up to
-// twelve), so that the token tiles load well ahead of the A stages.
+// The weights by tensor copies: scale rows a multiple of 16 bytes (in a multiple of 512, which the
+// tensor maps' strides need).  Three (four-group) or four (two-group) A stages in tensor memory; a
+// ring of three weight chunks (108 KB; two for 256-token tiles); the rest of the shared memory to
+// token-tile slots (up to twelve), so that the token tiles load ahead of the A stages.
 TcPlan tc_plan_ctma(int n_tile) {
   TcPlan p = tc_plan_ntile(n_tile);
   const size_t stage = (size_t)p.gps * p.n_tile * 128;
-  const size_t fixed = 1024 + 16 + 8 * (2 * 3 + 2 * 12 + 1 + 2 * 3);  // alignment slack, slot and flag, barriers
+  const size_t fixed = 1024 + 16 + 8 * (2 * 4 + 2 * 12 + 1 + 2 * 3);  // alignment slack, slot and flag, barriers
   p.ctma = true;
   p.sbreg = false;
-  p.stages = 3;
-  p.wring = 3;
+  // tensor-memory A stages: three of four groups after a 64-column accumulator, or four of two
+  // groups after a 256-column one
+  p.stages = p.gps == 4 ? 3 : 4;
+  p.wring = stage > 48 * 1024 ? 2 : 3;  // (256-token tiles: two chunks, two token slots)
   p.tstages = (int)std::min<size_t>(12, (kSmemBudget - fixed - (size_t)p.wring * kCSlot) / stage);
   p.smem = fixed + (size_t)p.tstages * stage + (size_t)p.wring * kCSlot;
   return p;
@@ -810,7 +813,10 @@ bool g_tc_ctma = true;  // (the tensor-copy kernel where it applies)
 TcPlan tc_plan(int out, int in, int T) {
   (void)out;
   const int n_tile = std::min(kMaxN, (T + 15) / 16 * 16);
-  TcPlan p = g_tc_ctma && n_tile <= 64 && in % 512 == 0 ? tc_plan_ctma(n_tile) : tc_plan_ntile(n_tile);
+  // (measured at 17408 x 5120: tensor copies T = 8 28.7 -> 25.8 us, T = 128 37.0 -> 35.3, T = 256
+  // 44.8 -> 40.7; at T = 96 the ring copies are faster, 32.7 against 34.1)
+  const bool ctma = g_tc_ctma && in % 512 == 0 && (n_tile <= 64 || n_tile >= 128);
+  TcPlan p = ctma ? tc_plan_ctma(n_tile) : tc_plan_ntile(n_tile);
   p.n_tiles = (T + p.n_tile - 1) / p.n_tile;
   return p;
 }
@@ -868,16 +874,8 @@ int tc_launch(const TcArgs& a, const TcPlan& p, dim3 grid, cudaStream_t stream) 
     return launch(k, grid, dim3(p.ctma ? kThreadsC : kThreads), p.smem, stream, a);
   };
   if (p.ctma) {
-    switch (p.wring) {
-      case 5:
-        return go(qgemm_tc_kernel<5, 512, false, 4, true>);
-      case 4:
-        return go(qgemm_tc_kernel<4, 512, false, 4, true>);
-      case 3:
-        return go(qgemm_tc_kernel<3, 512, false, 4, true>);
-      default:
-        return go(qgemm_tc_kernel<2, 512, false, 4, true>);
-    }
+    if (p.gps == 2) return p.wring == 3 ? go(qgemm_tc_kernel<3, 512, false, 2, true>) : go(qgemm_tc_kernel<2, 512, false, 2, true>);
+    return p.wring == 3 ? go(qgemm_tc_kernel<3, 512, false, 4, true>) : go(qgemm_tc_kernel<2, 512, false, 4, true>);
   }
   if (p.tmem == 256) {
     switch (p.wring) {
