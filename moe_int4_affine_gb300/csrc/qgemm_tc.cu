@@ -808,7 +808,7 @@ TcPlan tc_plan_ctma(int n_tile) {
   return p;
 }
 
-bool g_tc_ctma = true;  // (the tensor-copy kernel where it applies)
+constexpr bool g_tc_ctma = true;  // (the tensor-copy kernel where it applies)
 
 TcPlan tc_plan(int out, int in, int T) {
   (void)out;
