@@ -128,9 +128,10 @@ int moe_down_launch(const qg_int4_weight* down, const uint32_t* idx, const float
 // ---------------------------------------------------------------- MoE (moe.cu)
 int router_batch_launch(const float* logits, int T, int n_experts, int k, int renorm, uint32_t* idx, float* p,
                         cudaStream_t stream);
-// Grouped (MoE prefill) tensor-core pieces (qgemm_tc.cu): token tiles of grouped rows (pair i's X
-// row i / k, or the SwiGLU of the grouped gate/up outputs, into row rowpos[i]), and the GEMM over
-// expert stacks whose token tile y belongs to expert tile_expert[y] (< 0: none).
+// Grouped (MoE prefill) tensor-core pieces (qgemm_tc.cu): token tiles of grouped rows (token t's X
+// row, converted once, into rows rowpos[t k + s] for its k slots; or the SwiGLU of the grouped
+// gate/up outputs, pair i into row rowpos[i]), and the GEMM over expert stacks whose token tile y
+// belongs to expert tile_expert[y] (< 0: none).
 int qgemm_prep_pairs_launch(const uint16_t* X, int T, int in, const int* rowpos, int npairs, int k, int n_tile,
                             uint8_t* xt, float* xs, cudaStream_t stream);
 int qgemm_prep_swiglu_launch(const float* G, const float* U, int in, const int* rowpos, int npairs, int n_tile,

@@ -598,11 +598,13 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
 // ((tile * nk + kc) * n_tile + n % n_tile) * 128, the 16-byte chunk j (columns 8j .. 8j + 7 of the
 // group) at position j ^ (n % 8), its eight values in the column order 0, 4, 1, 5, 2, 6, 3, 7 (the
 // order the dequantized weights use).  Rows n >= T are zero.  Grouped mode (rowpos != null): block
-// i writes row rowpos[i] (< 0: nothing) from X row i / kdiv -- the (token, slot) pairs placed in
-// their experts' tiles; the tiles' padding rows are left unwritten (each MMA output column depends
-// on its own token row only, and padding outputs are never read).
+// t converts X row t once and writes it as rows rowpos[t kdiv + s], s < kdiv (< 0: none) -- the
+// token's (token, slot) pairs placed in their experts' tiles; the tiles' padding rows are left
+// unwritten (each MMA output column depends on its own token row only, and padding outputs are
+// never read).
 constexpr int kPrepThreads = 256;
 constexpr int kPrepMaxChunks = 16;  // 16-byte chunks per thread: in <= 16 * 256 * 8 = 32768
+constexpr int kPrepMaxFan = 8;      // grouped rows per token (top k <= 8)
 
 __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_kernel(const uint16_t* __restrict__ X, int T, int in,
                                                                    int n_tile, const int* __restrict__ rowpos,
@@ -612,9 +614,16 @@ __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_kernel(const uint16_t
   const int nk = in / 64, nch = in / 8;
   pdl_trigger();
   pdl_wait();
-  const int n = rowpos ? rowpos[blockIdx.x] : (int)blockIdx.x;
-  if (n < 0) return;  // (uniform per block)
-  const int src = rowpos ? (int)blockIdx.x / kdiv : n;
+  const int src = (int)blockIdx.x;
+  const int nfan = rowpos ? min(kdiv, kPrepMaxFan) : 1;
+  int dn[kPrepMaxFan];  // the rows this block writes (< 0: none)
+  bool any = false;
+#pragma unroll
+  for (int s = 0; s < kPrepMaxFan; ++s) {
+    dn[s] = s < nfan ? (rowpos ? rowpos[(size_t)src * kdiv + s] : src) : -1;
+    any |= dn[s] >= 0;
+  }
+  if (!any) return;  // (uniform per block)
   const bool live = src < T;
   const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? src : 0) * in);
   // one round of loads; the largest |x| from the bit patterns (|bf16| bits are ordered like values)
@@ -640,8 +649,9 @@ __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_kernel(const uint16_t
   // 2^(14 - e) with e = floor(log2 m): the row's largest magnitude lands in [2^14, 2^15)
   const int e = m > 0.f ? (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
   const float sc = live && m > 0.f ? exp2i(min(max(14 - e, -126), 127)) : 0.f;
-  if (threadIdx.x == 0) xs[n] = live && m > 0.f ? exp2i(min(max(e - 14, -126), 127)) : 0.f;
-  const int tile = n / n_tile, nl = n % n_tile;
+#pragma unroll
+  for (int s = 0; s < kPrepMaxFan; ++s)
+    if ((int)threadIdx.x == s && dn[s] >= 0) xs[dn[s]] = live && m > 0.f ? exp2i(min(max(e - 14, -126), 127)) : 0.f;
 #pragma unroll
   for (int i = 0; i < kPrepMaxChunks; ++i) {
     const int ch = (int)threadIdx.x + i * kPrepThreads;
@@ -660,8 +670,13 @@ __global__ void __launch_bounds__(kPrepThreads) qgemm_prep_kernel(const uint16_t
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.y) : "f"(f[5]), "f"(f[1]));
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.z) : "f"(f[6]), "f"(f[2]));
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o.w) : "f"(f[7]), "f"(f[3]));
-    uint8_t* dst = xt + (((size_t)tile * nk + kc) * n_tile + nl) * 128 + (size_t)((j ^ (nl & 7)) << 4);
-    *reinterpret_cast<uint4*>(dst) = o;
+#pragma unroll
+    for (int s = 0; s < kPrepMaxFan; ++s) {
+      if (dn[s] < 0) continue;
+      const int tile = dn[s] / n_tile, nl = dn[s] % n_tile;
+      uint8_t* dst = xt + (((size_t)tile * nk + kc) * n_tile + nl) * 128 + (size_t)((j ^ (nl & 7)) << 4);
+      *reinterpret_cast<uint4*>(dst) = o;
+    }
   }
 }
 
@@ -974,7 +989,8 @@ constexpr bool g_tc_pair = true;  // grouped mode: two CTAs per SM for token til
 
 int qgemm_prep_pairs_launch(const uint16_t* X, int T, int in, const int* rowpos, int npairs, int k, int n_tile,
                             uint8_t* xt, float* xs, cudaStream_t stream) {
-  return launch(qgemm_prep_kernel, dim3((unsigned)npairs), dim3(kPrepThreads), 0, stream, X, T, in, n_tile, rowpos, k,
+  if (k < 1 || k > kPrepMaxFan || npairs != T * k) return QG_EINVAL;
+  return launch(qgemm_prep_kernel, dim3((unsigned)T), dim3(kPrepThreads), 0, stream, X, T, in, n_tile, rowpos, k,
                 xt, xs);
 }
 
