@@ -16,8 +16,8 @@
 //     dequantizes the 64 weights of a group with packed half-precision arithmetic (w = s * q + b,
 //     one rounding to fp16) and writes them with one tensor-memory store (tcgen05.st, 32 columns of
 //     its row's lane) into the stage's A columns.
-//     For tiles of at most 64 or at least 128 tokens (and in a multiple of 512; not in grouped
-//     mode) the weights come instead by TMA
+//     For tiles of at most 64 or at least 128 tokens (and in a multiple of 512; in grouped mode
+//     with two CTAs per SM too) the weights come instead by TMA
 //     tensor copies, eight groups of the 128 rows at a time (see kCodeBox), issued by a weight
 //     loader warp into a ring of chunks; the producers read their row's codes from the swizzled
 //     boxes.  The weights do not depend on the previous kernel, so they start streaming before the
@@ -250,7 +250,7 @@ template <int WRING, int TMEMC, bool SBREG, int GPS, bool CTMA = false>
 __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 : 1)
     qgemm_tc_kernel(const __grid_constant__ TcArgs a) {
   static_assert(GPS == 2 || (GPS == 4 && TMEMC == 512), "four groups per stage: one-CTA kernel only");
-  static_assert(!CTMA || (TMEMC == 512 && !SBREG), "tensor copies: the one-CTA kernel with ring scales only");
+  static_assert(!CTMA || !SBREG, "tensor copies: ring scales only");
   constexpr uint32_t kABase = (TMEMC == 512 && GPS == 2) ? (uint32_t)kAccCols : 64u;
   constexpr uint32_t kAStageT = (uint32_t)(GPS * kACols);  // A columns of one stage
   constexpr int kWStageBytes = wstage_bytes(SBREG);
@@ -825,6 +825,20 @@ TcPlan tc_plan_ctma(int n_tile) {
 
 constexpr bool g_tc_ctma = true;  // (the tensor-copy kernel where it applies)
 
+// The grouped two-CTAs-per-SM kernel with the weights by tensor copies: three A stages (two for
+// 64-token tiles) and two weight chunks in half the shared memory each.
+TcPlan tc_plan_ntile_pair_ctma(int n_tile) {
+  TcPlan p = tc_plan_ntile_pair(n_tile);
+  const size_t stage = 2 * (size_t)n_tile * 128;
+  const size_t fixed = 1024 + 16 + 8 * (2 * 3 + 2 * 3 + 1 + 2 * 2);
+  p.ctma = true;
+  p.wring = 2;
+  p.stages = (int)std::min<size_t>(3, (kSmemHalf - fixed - 2 * (size_t)kCSlot) / stage);
+  p.tstages = p.stages;
+  p.smem = fixed + (size_t)p.stages * stage + 2 * (size_t)kCSlot;
+  return p;
+}
+
 TcPlan tc_plan(int out, int in, int T) {
   (void)out;
   const int n_tile = std::min(kMaxN, (T + 15) / 16 * 16);
@@ -889,6 +903,7 @@ int tc_launch(const TcArgs& a, const TcPlan& p, dim3 grid, cudaStream_t stream) 
     return launch(k, grid, dim3(p.ctma ? kThreadsC : kThreads), p.smem, stream, a);
   };
   if (p.ctma) {
+    if (p.tmem == 256) return go(qgemm_tc_kernel<2, 256, false, 2, true>);
     if (p.gps == 2) return p.wring == 3 ? go(qgemm_tc_kernel<3, 512, false, 2, true>) : go(qgemm_tc_kernel<2, 512, false, 2, true>);
     return p.wring == 3 ? go(qgemm_tc_kernel<3, 512, false, 4, true>) : go(qgemm_tc_kernel<2, 512, false, 4, true>);
   }
@@ -1003,13 +1018,16 @@ int qgemm_prep_swiglu_launch(const float* G, const float* U, int in, const int* 
 int qgemm_tc_grouped_launch(const qg_int4_weight* w, int n, const uint8_t* xt, const float* xs, int n_tiles,
                             int n_tile, const int* tile_expert, float* const* Y, cudaStream_t stream) {
   if (n < 1 || n > kTcMaxMats || n_tile < 16 || n_tile > kMaxN || n_tile % 16 != 0 || n_tiles < 1) return QG_EINVAL;
-  const TcPlan p = n_tile <= 64 && g_tc_pair ? tc_plan_ntile_pair(n_tile) : tc_plan_ntile(n_tile);
+  const bool pair = n_tile <= 64 && g_tc_pair;
+  const TcPlan p = pair ? (w[0].in % 512 == 0 ? tc_plan_ntile_pair_ctma(n_tile) : tc_plan_ntile_pair(n_tile))
+                        : tc_plan_ntile(n_tile);
   TcArgs a{};
   int tiles = 0;
   for (int i = 0; i < n; ++i) {
     a.mat[i] = TcMat{w[i].packed, w[i].scales, w[i].biases, Y[i], w[i].out, tiles,
                      (long long)w[i].out * (w[i].in / 8), (long long)w[i].out * (w[i].in / 64)};
     tiles += (w[i].out + kBM - 1) / kBM;
+    if (p.ctma && !encode_weight_maps(w[i], &a.tm_codes[i], &a.tm_scales[i], &a.tm_biases[i])) return QG_ELAUNCH;
   }
   a.nmat = n;
   a.tile_expert = tile_expert;
