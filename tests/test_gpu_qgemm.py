@@ -61,7 +61,7 @@ def test_qgemm_tensor_core_long_k(qg, in_dim, T):
 @pytest.mark.parametrize("T,out,in_dim", [(16, 128, 64), (32, 128, 128), (48, 130, 1088), (256, 384, 2048),
                                           (300, 200, 512), (257, 129, 192)])
 def test_qgemm_tensor_core_shapes(qg, T, out, in_dim):
-    """T >= 32 (and a forced 16) on the tensor-core path: one and several token tiles, ragged rows."""
+    """The tensor-core path (the threshold forced to 16): one and several token tiles, ragged rows."""
     qg.qg_tune_qgemm(16)
     try:
         d = I.int4_weight(T + 7, I.TID_W, out, in_dim)
