@@ -58,6 +58,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "qg_common.cuh"
 #include "qg_internal.h"
@@ -74,7 +75,6 @@ constexpr int kMmaWarp = kProducerWarps;      // the MMA / tensor-memory warp
 constexpr int kLoadWarp = kProducerWarps + 1; // the token-tile loader
 constexpr int kThreads = kProducers + 64;
 constexpr int kCodeWarp = kProducerWarps + 2;  // CTMA: the weight-chunk loader
-constexpr int kThreadsC = kProducers + 96;
 // CTMA (the one-CTA kernel): the weights arrive by TMA tensor copies in chunks of eight
 // groups for the CTA's 128 rows -- the codes as two 128-row x 128-byte boxes (128-byte swizzle),
 // then the scales and the biases as 128-row x 16-byte boxes -- instead of one cp.async per thread,
@@ -155,6 +155,30 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
+}
+// 32 lanes x 8 / 16 / 32 consecutive fp32 columns of tensor memory into registers (no wait).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* v) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
 }
 // Both barriers' phases complete?  The two tests are issued together (one latency, not two).
 __device__ __forceinline__ bool test_wait2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
@@ -246,11 +270,25 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2, uint32_t b2) 
 // hand-overs for small token tiles (accumulator N <= 64 in columns 0-63, up to three A stages of 128
 // columns from column 64); two otherwise.
 // CTMA: the weights by TMA tensor copies (kCSlot chunks, a ring of WRING of them; see kCodeBox).
-template <int WRING, int TMEMC, bool SBREG, int GPS, bool CTMA = false>
-__global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 : 1)
+// MW: MMA-issuing warps.  An MMA instruction occupies its issuing thread for about 65 cycles
+// whatever N is (measured), so small token tiles are issue-bound with one: with MW = 2 (four-group
+// stages, N <= 64) a second MMA warp (the one after the weight loader) issues groups 2 and 3 of
+// every stage into a second accumulator in the last 64 tensor-memory columns, and the epilogue adds
+// the two.
+// PG: producer warp groups (4 with the tensor copies and four-group stages: one group per thread
+// and stage; warps 8 .. 15 then make groups 2, 3 and do not take part in the epilogue).
+template <int WRING, int TMEMC, bool SBREG, int GPS, bool CTMA = false, int MW = 1, int PG = 2>
+__global__ void __launch_bounds__((CTMA ? 128 * PG + 96 : kThreads) + (MW - 1) * 32, TMEMC == 256 ? 2 : 1)
     qgemm_tc_kernel(const __grid_constant__ TcArgs a) {
   static_assert(GPS == 2 || (GPS == 4 && TMEMC == 512), "four groups per stage: one-CTA kernel only");
   static_assert(!CTMA || !SBREG, "tensor copies: ring scales only");
+  static_assert(MW == 1 || (MW == 2 && CTMA && GPS == 4 && TMEMC == 512), "two MMA warps: the small-tile kernel");
+  static_assert(PG == 2 || (PG == 4 && CTMA && GPS == 4), "four producer groups: tensor copies, four-group stages");
+  constexpr uint32_t kAcc2 = 448;  // MW = 2: the second accumulator's first column
+  constexpr int kPW = 4 * PG;       // producer warps; then the MMA, token-loader, weight-loader warps
+  constexpr int kWMma = kPW, kWLoad = kPW + 1, kWCode = kPW + 2;
+  constexpr int kQS = GPS / PG;     // groups per producer thread and stage
+  constexpr int kJC = 8 / PG;       // a thread's groups per weight chunk (eight groups)
   constexpr uint32_t kABase = (TMEMC == 512 && GPS == 2) ? (uint32_t)kAccCols : 64u;
   constexpr uint32_t kAStageT = (uint32_t)(GPS * kACols);  // A columns of one stage
   constexpr int kWStageBytes = wstage_bytes(SBREG);
@@ -295,21 +333,21 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
   const int nk = a.in / kGK;         // groups
   const int nst = (nk + GPS - 1) / GPS;  // pipeline stages (GPS groups each)
 
-  if (warp == kMmaWarp) {
+  if (warp == kWMma) {
     if (lane == 0) {
       for (int s = 0; s < S; ++s) {
-        mbar_init(full + s, kProducerWarps);
-        mbar_init(empty + s, 1);
+        mbar_init(full + s, kPW);
+        mbar_init(empty + s, MW);  // (one commit from each MMA warp)
       }
       for (int t = 0; t < D; ++t) {
         mbar_init(bfull + t, 1);
-        mbar_init(tempty + t, 1);
+        mbar_init(tempty + t, MW);
       }
-      mbar_init(done, 1);
+      mbar_init(done, MW);
       if constexpr (CTMA) {
         for (int c = 0; c < WRING; ++c) {
           mbar_init(cfull + c, 1);
-          mbar_init(cempty + c, kProducerWarps);
+          mbar_init(cempty + c, kPW);
         }
       }
       *abort_flag = 0;
@@ -330,7 +368,7 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
   // token loader and the epilogue wait for it; the weights start streaming at once.
   pdl_trigger();
 
-  if (warp < kProducerWarps) {
+  if (warp < kPW) {
     // ---------------- producers: thread (row r, warp group h) makes group 2 j + h of every stage j
     const int r = tid & (kBM - 1), h = tid >> 7;
     const int row = m0 + r;
@@ -404,11 +442,11 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
       if (*abort_flag) break;
       tc_fence_after();  // the MMAs that read this stage's A columns have completed
 #pragma unroll
-      for (int q = 0; q < GPS / 2; ++q) {
-        const int jj = (GPS / 2) * j + q;  // this thread's group 2 jj + h (its jj-th)
+      for (int q = 0; q < kQS; ++q) {
+        const int jj = kQS * j + q;  // this thread's group PG jj + h (its jj-th)
         if constexpr (CTMA) {
-          if ((jj & 3) == 0) {  // chunk jj / 4 (groups 8 (jj / 4) ..): its bytes, then this row's scales and biases
-            const int c = jj >> 2;
+          if (jj % kJC == 0) {  // chunk jj / kJC (groups 8 c ..): its bytes, then this row's scales and biases
+            const int c = jj / kJC;
             csl = wring + (uint32_t)(c % WRING) * kCSlot;
             if (!mbar_wait(cfull + c % WRING, (uint32_t)(c / WRING) & 1u)) *abort_flag = 1;
             s_cur = lds128(csl + 2 * kCodeBox + (uint32_t)r * 16u);
@@ -418,14 +456,14 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
           wissue(jj + WRING - 1);
           cp_wait<WRING - 1>();  // group jj of this thread has landed
         }
-        const bool live = 2 * jj + h < nk && !(CTMA && __any_sync(0xffffffffu, *abort_flag != 0));
+        const bool live = PG * jj + h < nk && !(CTMA && __any_sync(0xffffffffu, *abort_flag != 0));
         if (live) {  // (uniform per warp: tcgen05.st is a warp-wide instruction)
           uint4 c0, c1;
           uint32_t s2, b2;
           if constexpr (CTMA) {
             // group o of the chunk: codes box o / 4, 16-byte pieces 2 (o % 4) and 2 (o % 4) + 1 of
             // row r, each at its swizzled place (piece i of row r at i ^ (r % 8))
-            const int o = (2 * jj + h) & 7;
+            const int o = (PG * jj + h) & 7;
             const uint32_t ra = csl + (uint32_t)(o >> 2) * kCodeBox + (uint32_t)r * 128u;
             const uint32_t sw = (uint32_t)(r & 7);
             c0 = lds128(ra + (((uint32_t)(2 * (o & 3)) ^ sw) << 4));
@@ -464,13 +502,13 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
             v[4 * ch + 3] = d.w;
           }
           tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) +
-                        (kABase + kAStageT * (uint32_t)s + (uint32_t)(kACols * (2 * q + h))),
+                        (kABase + kAStageT * (uint32_t)s + (uint32_t)(kACols * (PG * q + h))),
                     v);
         }
         if constexpr (CTMA) {
-          if ((jj & 3) == 3) {  // this warp has read the chunk
+          if (jj % kJC == kJC - 1) {  // this warp has read the chunk
             __syncwarp();
-            if (lane == 0) mbar_arrive(cempty + (jj >> 2) % WRING);
+            if (lane == 0) mbar_arrive(cempty + (jj / kJC) % WRING);
           }
         }
       }
@@ -480,7 +518,7 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
       if (lane == 0) mbar_arrive(full + s);
     }
     cp_wait<0>();
-  } else if (warp == kLoadWarp) {
+  } else if (warp == kWLoad) {
     // ---------------- token-tile loader: stage j's tiles (contiguous in the workspace), one bulk
     // copy each, issued as soon as the stage is free
     if (lane == 0) {
@@ -500,7 +538,7 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
       // thread waited for it); the latest use of each slot may be outstanding
       for (int j = max(0, issued - D); j < issued; ++j) mbar_wait(bfull + j % D, (uint32_t)(j / D) & 1u);
     }
-  } else if (CTMA && warp == kCodeWarp) {
+  } else if (CTMA && warp == kWCode) {
     // ---------------- weight-chunk loader: chunk c (groups 8c .. 8c + 7 of the CTA's 128 rows) into
     // slot c % WRING as soon as every producer warp has read the chunk before it there
     if (lane == 0) {
@@ -522,8 +560,12 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
       // every copy issued here has landed before the CTA can exit
       for (int c = max(0, issued - WRING); c < issued; ++c) mbar_wait(cfull + c % WRING, (uint32_t)(c / WRING) & 1u);
     }
-  } else if (warp == kMmaWarp && lane == 0) {
-    // ---------------- MMA issuer
+  } else if ((warp == kWMma || (MW == 2 && warp == kPW + 3)) && lane == 0) {
+    // ---------------- MMA issuer (MW = 2: issuer m takes groups 2 m, 2 m + 1 of each stage into
+    // its own accumulator)
+    const int m = warp == kWMma ? 0 : 1;
+    const uint32_t dacc = tmem + (m ? kAcc2 : 0u);
+    const int gi0 = MW == 2 ? 2 * m : 0, gi1 = MW == 2 ? 2 * m + 2 : GPS;
     // B descriptors: token slot t and K step k add (t * stage_bytes + 32 k) / 16 to the start
     // address field (bits 0-13: shared addresses stay below 2^18, so the field never carries).
     const uint64_t db0 = smem_desc(base);
@@ -539,12 +581,12 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
       tc_fence_after();  // the producers' tensor-memory stores are complete
       const uint64_t db = db0 + (uint64_t)(t * dstage);
       const uint32_t ta = tmem + kABase + kAStageT * (uint32_t)s;
-      const int ng = min(GPS, nk - GPS * j);
-      for (int gi = 0; gi < ng; ++gi) {
+      const int ng = min(gi1, nk - GPS * j);
+      for (int gi = gi0; gi < ng; ++gi) {
 #pragma unroll
         for (int k = 0; k < kGK / 16; ++k)
-          mma_f16_ta(tmem, ta + kACols * gi + 8 * k, db + (uint64_t)(gi * (btile >> 4)) + 2 * k, a.idesc,
-                     (j | gi | k) != 0 ? 1u : 0u);
+          mma_f16_ta(dacc, ta + kACols * gi + 8 * k, db + (uint64_t)(gi * (btile >> 4)) + 2 * k, a.idesc,
+                     (j | (gi - gi0) | k) != 0 ? 1u : 0u);
       }
       mma_commit(empty + s);
       mma_commit(tempty + t);
@@ -561,7 +603,7 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
   }
 
   // ---------------- epilogue: warps w and w + 4 read lanes 32 (w % 4) .. + 31, half of the columns each
-  if (warp < kProducerWarps) {
+  if (warp < 8) {
     pdl_wait();  // (the token scales; and Y is written only after the kernels before this one are done)
     const bool ok = mbar_wait(done, 0);
     tc_fence_after();
@@ -570,24 +612,45 @@ __global__ void __launch_bounds__(CTMA ? kThreadsC : kThreads, TMEMC == 256 ? 2 
       const int row = m0 + q * 32 + lane;
       const int half = a.n_tile / 2;  // multiple of 8
       const int c0 = (warp >> 2) * half;
-      for (int cc = 0; cc < half; cc += 8) {
-        uint32_t v[8];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
-            : "r"(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c0 + cc)));
+      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
+      // W columns from cc: one wait per load (32 columns at a time where they fit, 16 with two
+      // accumulators); the token scales loaded one per lane before it and passed round by shuffles
+      // (17408 x 5120, T = 256: 42.0 -> 39.6 us against eight columns per wait)
+      auto emit = [&](int cc, auto wc) {
+        constexpr int W = decltype(wc)::value;
+        const int tq = n0 + c0 + cc + (lane & (W - 1));
+        const float xsl = tq < a.T ? __ldg(a.xs + tq) : 0.f;
+        uint32_t v[W];
+        auto ld = [](uint32_t ta, uint32_t* r) {
+          if constexpr (W == 32) tmem_ld32(ta, r); else if constexpr (W == 16) tmem_ld16(ta, r); else tmem_ld8(ta, r);
+        };
+        ld(tl + (uint32_t)cc, v);
+        if (MW == 2 && nk > 2) {  // (the second issuer's partial sum: groups 2, 3 of each stage)
+          uint32_t w2[W];
+          ld(tl + kAcc2 + (uint32_t)cc, w2);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int j = 0; j < W; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(w2[j]));
+        }
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < W; ++j) {
           const int t = n0 + c0 + cc + j;
-          if (row < mt.out && t < a.T) mt.y[(size_t)t * mt.out + row] = __uint_as_float(v[j]) * __ldg(a.xs + t);
+          const float xv = __shfl_sync(0xffffffffu, xsl, j);
+          if (row < mt.out && t < a.T) mt.y[(size_t)t * mt.out + row] = __uint_as_float(v[j]) * xv;
         }
-      }
+      };
+      int cc = 0;
+      // (two CTAs per SM: eight, the other CTA's main loop hides the latency and the registers
+      // stay fewer)
+      constexpr int kW = MW == 2 ? 16 : TMEMC == 256 ? 8 : 32;
+      for (; cc + kW <= half; cc += kW) emit(cc, std::integral_constant<int, kW>{});
+      for (; cc < half; cc += 8) emit(cc, std::integral_constant<int, 8>{});
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kWMma) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEMC) : "memory");
   }
@@ -749,6 +812,8 @@ struct TcPlan {
   int n_tile, n_tiles, stages, wring;  // (ctma: wring = chunks in the ring)
   size_t smem;
   bool ctma;   // weights by TMA tensor copies (tiles of at most 64 tokens)
+  int mw = 1;  // MMA-issuing warps
+  int pg = 2;  // producer warp groups
   int tstages;  // token-tile slots (>= stages)
   int tmem;    // tensor-memory columns per CTA (512, or 256 for two CTAs per SM)
   bool sbreg;  // scales and biases in registers (token tiles of 128 and more, one CTA per SM)
@@ -818,6 +883,10 @@ TcPlan tc_plan_ctma(int n_tile) {
   // groups after a 256-column one
   p.stages = p.gps == 4 ? 3 : 4;
   p.wring = stage > 48 * 1024 ? 2 : 3;  // (256-token tiles: two chunks, two token slots)
+  // small tiles: two MMA issuers (their accumulators fit beside three A stages) and four producer
+  // warp groups
+  p.mw = p.gps == 4 ? 2 : 1;
+  p.pg = p.gps == 4 ? 4 : 2;
   p.tstages = (int)std::min<size_t>(12, (kSmemBudget - fixed - (size_t)p.wring * kCSlot) / stage);
   p.smem = fixed + (size_t)p.tstages * stage + (size_t)p.wring * kCSlot;
   return p;
@@ -900,11 +969,14 @@ int tc_launch(const TcArgs& a, const TcPlan& p, dim3 grid, cudaStream_t stream) 
     const int carve = (int)std::min<size_t>(100, (2 * p.smem + 2048) * 100 / (228 * 1024) + 1);
     if (p.tmem == 256 && cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, carve) != cudaSuccess)
       return (int)QG_ELAUNCH;
-    return launch(k, grid, dim3(p.ctma ? kThreadsC : kThreads), p.smem, stream, a);
+    return launch(k, grid, dim3((unsigned)((p.ctma ? 128 * p.pg + 96 : kThreads) + (p.mw - 1) * 32)), p.smem, stream, a);
   };
   if (p.ctma) {
     if (p.tmem == 256) return go(qgemm_tc_kernel<2, 256, false, 2, true>);
     if (p.gps == 2) return p.wring == 3 ? go(qgemm_tc_kernel<3, 512, false, 2, true>) : go(qgemm_tc_kernel<2, 512, false, 2, true>);
+    if (p.wring == 3 && p.mw == 2)
+      return p.pg == 4 ? go(qgemm_tc_kernel<3, 512, false, 4, true, 2, 4>) : go(qgemm_tc_kernel<3, 512, false, 4, true, 2>);
+    if (p.wring == 3 && p.pg == 4) return go(qgemm_tc_kernel<3, 512, false, 4, true, 1, 4>);
     return p.wring == 3 ? go(qgemm_tc_kernel<3, 512, false, 4, true>) : go(qgemm_tc_kernel<2, 512, false, 4, true>);
   }
   if (p.tmem == 256) {
