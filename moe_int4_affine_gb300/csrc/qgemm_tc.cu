@@ -9,7 +9,8 @@
 //   * A pipeline stage covers GPS 64-column quantization groups (GPS = 2, K = 128; GPS = 4, K = 256
 //     for tiles of at most 64 tokens, which halves the stage hand-overs that pace small tiles).
 //     Two producer warp groups (4 warps each, one thread per weight row) fill them: group h makes
-//     groups GPS j + 2 q + h of stage j.  (A tenth warp issues the stages' token-tile copies.)  A
+//     groups GPS j + 2 q + h of stage j (four groups, one group each, for the small tiles).  (The
+//     warp after the MMA warp issues the stages' token-tile copies.)  A
 //     thread streams its row's packed codes through a per-thread cp.async ring (WRING of its
 //     groups ahead) -- with the scale and bias words (4-byte copies, through L1), or, for tiles of
 //     128 tokens and more, with the scales and biases as 16-byte chunks of 8 groups in registers --
@@ -29,9 +30,11 @@
 //     stage's "empty" mbarrier and to its token slot's; a final commit releases the epilogue, which
 //     reads the accumulator from tensor memory (tcgen05.ld), applies each token's power-of-two
 //     input scale and writes Y.
-//   * Small token tiles are paced by the MMA instructions themselves: measured on this part, an
-//     M = 128, K = 16 MMA takes about 70 ns for N = 16 to 64 (about 110 ns at N = 256 in this
-//     pipeline), so a 128-row tile of K = 5120 (320 MMAs) needs about 22 us at any T <= 64.
+//   * Small token tiles are paced by the MMA instructions themselves: an M = 128, K = 16 MMA
+//     occupies its issuing thread for 65-100 SM cycles whatever N is (measured), so a 128-row tile
+//     of K = 5120 (320 MMAs) needs about 16 us from one thread.  Tiles of at most 64 tokens
+//     therefore run four producer warp groups (one group per thread and stage) and two issuing
+//     threads, each on its own accumulator, added in the epilogue (see MW and PG below).
 //   * Every mbarrier wait is bounded (2 s): on a timeout the CTA records QG_STATUS_TIMEOUT, stops
 //     issuing, drains what it has in flight and frees its tensor memory before returning.
 //   * Grouped (MoE) mode: token tile y belongs to expert tile_expert[y]; the CTA reads it first
