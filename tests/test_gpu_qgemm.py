@@ -15,8 +15,10 @@ def _run(qg, d, X):
 
 
 @pytest.mark.parametrize("T,out,in_dim", [(1, 64, 128), (3, 100, 576), (8, 300, 1024), (33, 256, 2048),
-                                          (40, 130, 1088)])
+                                          (40, 130, 1088), (20, 129, 512), (57, 140, 1536), (64, 200, 1024)])
 def test_qgemm_small(qg, T, out, in_dim):
+    """Ragged rows and token counts; in a multiple of 512 with T <= 64 is the small-tile tensor-copy
+    kernel (two MMA-issuing threads, two accumulators) at every tile height from 16 to 64."""
     d = I.int4_weight(T, I.TID_W, out, in_dim)
     X = I.bf16_normal(T, I.TID_X, (T, in_dim))
     Y = _run(qg, d, X)
