@@ -325,8 +325,8 @@ int scalar_fma_chain8_residual(const float *p, const float *v, const uint16_t *r
  * range (2^-14 <= |s|, |b| < 65504, or zero; typical models are far inside it).  T < 3 runs the
  * CUDA-core GEMV once per token row.
  * workspace: at least qg_workspace_bytes(QG_OP_QGEMM, w, T) bytes (0 means none is needed): the
- * tensor-core path stages the converted tokens there.  For up to 64 tokens and in a multiple of
- * 512 the weights are read by tensor-map copies (encoded on the host for each call through the
+ * tensor-core path stages the converted tokens there.  With in a multiple of 512 and T outside
+ * 65..112 the weights are read by tensor-map copies (encoded on the host for each call through the
  * driver entry point the CUDA runtime provides); QG_ELAUNCH if that encoding fails.
  * Limits: 1 <= T <= 4096; in % 64 == 0, 64 <= in <= 32768.
  */
