@@ -74,10 +74,8 @@ constexpr int kGK = 64;                      // columns of one quantization grou
 constexpr int kMaxN = 256;                   // tokens per CTA (MMA N, tensor-memory columns)
 constexpr int kProducerWarps = 8;            // two warp groups of 4: one thread per weight row each
 constexpr int kProducers = kProducerWarps * 32;
-constexpr int kMmaWarp = kProducerWarps;      // the MMA / tensor-memory warp
-constexpr int kLoadWarp = kProducerWarps + 1; // the token-tile loader
-constexpr int kThreads = kProducers + 64;
-constexpr int kCodeWarp = kProducerWarps + 2;  // CTMA: the weight-chunk loader
+constexpr int kThreads = kProducers + 64;     // then the MMA warp and the token-tile loader (the
+                                              // kernel's kWMma, kWLoad; kWCode for the tensor copies)
 // CTMA (the one-CTA kernel): the weights arrive by TMA tensor copies in chunks of eight
 // groups for the CTA's 128 rows -- the codes as two 128-row x 128-byte boxes (128-byte swizzle),
 // then the scales and the biases as 128-row x 16-byte boxes -- instead of one cp.async per thread,
